@@ -1,0 +1,228 @@
+"""Thin ctypes binding over libsv.so (the C ABI in include/sv.h).
+
+Argument marshalling only: every step of the verify round runs in the
+library's CUDA kernels.  Tensors must be CUDA tensors of the stated dtype,
+contiguous; workspaces are allocated with torch when the caller passes none.
+There is no fallback: if the library is missing or fails to load, importing
+this module raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+from .build import LIB
+
+_P = ctypes.c_void_p
+_I32 = ctypes.c_int32
+_I64 = ctypes.c_int64
+_U64 = ctypes.c_uint64
+_F32 = ctypes.c_float
+_SZ = ctypes.c_size_t
+
+
+class SVError(RuntimeError):
+    def __init__(self, fn: str, status: int, msg: str):
+        super().__init__(f"{fn}: {msg} (status {status})")
+        self.status = status
+
+
+class _AttnShape(ctypes.Structure):
+    _fields_ = [("B", _I32), ("R", _I32), ("Hq", _I32), ("Hkv", _I32), ("D", _I32), ("T_cap", _I32)]
+
+
+def _load():
+    if not os.path.exists(LIB):
+        raise ImportError(f"libsv.so not built ({LIB}); run __graft_entry__.build() first")
+    L = ctypes.CDLL(LIB)
+    L.sv_version.restype = ctypes.c_int
+    L.sv_status_string.restype = ctypes.c_char_p
+    L.sv_status_string.argtypes = [ctypes.c_int]
+    L.sv_get_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32), _P]
+    L.sv_verify_attn_workspace.argtypes = [ctypes.POINTER(_AttnShape)]
+    L.sv_verify_attn_workspace.restype = _SZ
+    L.sv_verify_attn.argtypes = [ctypes.POINTER(_AttnShape), _P, _P, _P, _P, _P, _P, _P, _F32, _P, _P, _SZ, _P]
+    L.sv_lm_head.argtypes = [_P, _P, _P, _I32, _I32, _I32, _P]
+    L.sv_accept_greedy_workspace.argtypes = [_I32, _I32, _I32]
+    L.sv_accept_greedy_workspace.restype = _SZ
+    L.sv_accept_greedy.argtypes = [_P, _P, _P, _I32, _I32, _I32, _P, _P, _P, _P, _SZ, _P]
+    L.sv_accept_sample_workspace.argtypes = [_I32, _I32, _I32]
+    L.sv_accept_sample_workspace.restype = _SZ
+    L.sv_accept_sample.argtypes = [_P, _P, _I32, _P, _P, _I32, _I32, _I32, _F32, _U64, _U64, _P, _P, _P, _P, _P,
+                                   _SZ, _P]
+    L.sv_kv_commit.argtypes = [_P, _P, _P, _P, _I32, _I32, _I32, _I32, _I32, _I32, _P, _P, _P, _P]
+    L.sv_diag_exp.argtypes = [_P, _P, _I64, _P]
+    L.sv_diag_philox.argtypes = [_P, _P, _P, _I64, _P]
+    L.sv_diag_canon.argtypes = [_P, _I32, _I32, _P, _P, _P, _P]
+    for fn in ("sv_verify_attn", "sv_lm_head", "sv_accept_greedy", "sv_accept_sample", "sv_kv_commit",
+               "sv_diag_exp", "sv_diag_philox", "sv_diag_canon", "sv_get_device_error"):
+        getattr(L, fn).restype = ctypes.c_int
+    return L
+
+
+lib = _load()
+
+
+def _check(fn: str, status: int):
+    if status != 0:
+        raise SVError(fn, status, lib.sv_status_string(status).decode())
+
+
+def _ptr(t: Optional[torch.Tensor], dtype=None, name="tensor"):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _ws(nbytes: int, device, ws: Optional[torch.Tensor]):
+    if ws is not None:
+        if ws.numel() * ws.element_size() < nbytes:
+            raise ValueError("workspace too small")
+        return ws
+    return torch.empty(max(nbytes, 16), dtype=torch.uint8, device=device)
+
+
+# ---------------------------------------------------------------------------
+
+
+def attn_shape(q: torch.Tensor, k_cache: torch.Tensor) -> _AttnShape:
+    B, R, Hq, D = q.shape
+    _, Hkv, T_cap, _ = k_cache.shape
+    return _AttnShape(B, R, Hq, Hkv, D, T_cap)
+
+
+def verify_attn_workspace(B, R, Hq, Hkv, D, T_cap) -> int:
+    s = _AttnShape(B, R, Hq, Hkv, D, T_cap)
+    return int(lib.sv_verify_attn_workspace(ctypes.byref(s)))
+
+
+def verify_attn(q, k_cache, v_cache, length, k_blk, v_blk, parent=None, scale=None, out=None, ws=None,
+                stream=None):
+    """q [B,R,Hq,D]; caches [B,Hkv,T_cap,D]; blocks [B,Hkv,R,D] (bf16); length [B] int32;
+    parent None or [B,R] int32.  Returns out [B,R,Hq,D] bf16."""
+    s = attn_shape(q, k_cache)
+    if scale is None:
+        scale = q.shape[-1] ** -0.5
+    if out is None:
+        out = torch.empty_like(q)
+    nbytes = int(lib.sv_verify_attn_workspace(ctypes.byref(s)))
+    ws = _ws(nbytes, q.device, ws)
+    bf = torch.bfloat16
+    _check("sv_verify_attn", lib.sv_verify_attn(
+        ctypes.byref(s), _ptr(q, bf, "q"), _ptr(k_cache, bf, "k_cache"), _ptr(v_cache, bf, "v_cache"),
+        _ptr(length, torch.int32, "len"), _ptr(k_blk, bf, "k_blk"), _ptr(v_blk, bf, "v_blk"),
+        _ptr(parent, torch.int32, "parent"), float(scale), _ptr(out, bf, "out"), _ptr(ws), nbytes,
+        _stream(stream)))
+    return out
+
+
+def lm_head(hid, W, logits=None, stream=None):
+    """hid [N,H] bf16; W [H,V] bf16 -> logits [N,V] fp32."""
+    N, H = hid.shape
+    V = W.shape[1]
+    if logits is None:
+        logits = torch.empty(N, V, dtype=torch.float32, device=hid.device)
+    _check("sv_lm_head", lib.sv_lm_head(_ptr(hid, torch.bfloat16, "hid"), _ptr(W, torch.bfloat16, "W"),
+                                        _ptr(logits, torch.float32, "logits"), N, H, V, _stream(stream)))
+    return logits
+
+
+def _accept_outputs(B, R, device, n_acc, out_tok, path):
+    if n_acc is None:
+        n_acc = torch.empty(B, dtype=torch.int32, device=device)
+    if out_tok is None:
+        out_tok = torch.empty(B, dtype=torch.int32, device=device)
+    if path is None:
+        path = torch.empty(B, R, dtype=torch.int32, device=device)
+    return n_acc, out_tok, path
+
+
+def accept_greedy(logits, tok, parent=None, n_acc=None, out_tok=None, path=None, ws=None, stream=None):
+    """logits [B,R,V] fp32; tok [B,R] int32 -> (n_acc [B], out_tok [B], path [B,R])."""
+    B, R, V = logits.shape
+    n_acc, out_tok, path = _accept_outputs(B, R, logits.device, n_acc, out_tok, path)
+    nbytes = int(lib.sv_accept_greedy_workspace(B, R, V))
+    ws = _ws(nbytes, logits.device, ws)
+    i32 = torch.int32
+    _check("sv_accept_greedy", lib.sv_accept_greedy(
+        _ptr(logits, torch.float32, "logits"), _ptr(tok, i32, "tok"), _ptr(parent, i32, "parent"), B, R, V,
+        _ptr(n_acc, i32), _ptr(out_tok, i32), _ptr(path, i32), _ptr(ws), nbytes, _stream(stream)))
+    return n_acc, out_tok, path
+
+
+def accept_sample(logits, q, tok, parent=None, temperature=1.0, seed=0, step=0, uniforms=None, n_acc=None,
+                  out_tok=None, path=None, ws=None, stream=None):
+    """logits [B,R,V] fp32; q [B,R-1 (chain) or R (tree),Vq] fp32; tok [B,R] int32;
+    uniforms None (Philox) or [B,R,2] fp32."""
+    B, R, V = logits.shape
+    Vq = q.shape[-1]
+    n_acc, out_tok, path = _accept_outputs(B, R, logits.device, n_acc, out_tok, path)
+    nbytes = int(lib.sv_accept_sample_workspace(B, R, V))
+    ws = _ws(nbytes, logits.device, ws)
+    i32, f32 = torch.int32, torch.float32
+    _check("sv_accept_sample", lib.sv_accept_sample(
+        _ptr(logits, f32, "logits"), _ptr(q, f32, "q"), Vq, _ptr(tok, i32, "tok"), _ptr(parent, i32, "parent"),
+        B, R, V, float(temperature), int(seed) & (2 ** 64 - 1), int(step) & (2 ** 64 - 1),
+        _ptr(uniforms, f32, "uniforms"), _ptr(n_acc, i32), _ptr(out_tok, i32), _ptr(path, i32), _ptr(ws), nbytes,
+        _stream(stream)))
+    return n_acc, out_tok, path
+
+
+def kv_commit(k_cache, v_cache, k_blk, v_blk, path, n_acc, length, stream=None):
+    """caches [L,B,Hkv,T_cap,D]; blocks [L,B,Hkv,R,D] (bf16); path [B,R], n_acc [B], length [B] int32
+    (length updated in place)."""
+    L, B, Hkv, T_cap, D = k_cache.shape
+    R = k_blk.shape[3]
+    bf, i32 = torch.bfloat16, torch.int32
+    _check("sv_kv_commit", lib.sv_kv_commit(
+        _ptr(k_cache, bf, "k_cache"), _ptr(v_cache, bf, "v_cache"), _ptr(k_blk, bf, "k_blk"),
+        _ptr(v_blk, bf, "v_blk"), L, B, Hkv, D, T_cap, R, _ptr(path, i32, "path"), _ptr(n_acc, i32, "n_acc"),
+        _ptr(length, i32, "len"), _stream(stream)))
+
+
+def get_device_error(stream=None) -> int:
+    word = ctypes.c_uint32(0)
+    st = lib.sv_get_device_error(ctypes.byref(word), _stream(stream))
+    if st not in (0, 6):
+        _check("sv_get_device_error", st)
+    return int(word.value)
+
+
+def diag_exp(x: torch.Tensor, stream=None) -> torch.Tensor:
+    y = torch.empty_like(x)
+    _check("sv_diag_exp", lib.sv_diag_exp(_ptr(x, torch.float32), _ptr(y, torch.float32), x.numel(),
+                                          _stream(stream)))
+    return y
+
+
+def diag_philox(ctr: torch.Tensor, key: torch.Tensor, stream=None) -> torch.Tensor:
+    """ctr [n,4] int32 (bit patterns), key [n,2] int32 -> [n,4] int32."""
+    out = torch.empty_like(ctr)
+    _check("sv_diag_philox", lib.sv_diag_philox(_ptr(ctr, torch.int32), _ptr(key, torch.int32),
+                                                _ptr(out, torch.int32), ctr.shape[0], _stream(stream)))
+    return out
+
+
+def diag_canon(x: torch.Tensor, u: torch.Tensor, stream=None):
+    """x [m,n] fp32, u [m] fp32 -> (sums [m] fp32, draws [m] int32)."""
+    m, n = x.shape
+    sums = torch.empty(m, dtype=torch.float32, device=x.device)
+    draws = torch.empty(m, dtype=torch.int32, device=x.device)
+    _check("sv_diag_canon", lib.sv_diag_canon(_ptr(x, torch.float32), n, m, _ptr(u, torch.float32),
+                                              _ptr(sums), _ptr(draws), _stream(stream)))
+    return sums, draws

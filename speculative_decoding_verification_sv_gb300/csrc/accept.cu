@@ -1,0 +1,728 @@
+// accept.cu -- greedy and sampled acceptance of one verify round.
+//
+// Greedy ([SpecDec-Context-Scaling guide, sec. 3 and 3.1]): a vocab-parallel
+// argmax of every verify row, then a per-sequence walk that compares draft j
+// with the argmax of row j-1 (row 0 is saved_next), or walks a draft tree.
+//
+// Sampled ([wmrh.cn tutorial, sec. 2.2]; [mini-infer Phase 11, "Modified
+// Rejection Sampling"]; trees: [SubSpec summary, sec. 4.2]):
+//   1. sample_stats_kernel: one 8-CTA cluster per verify row pulls the row
+//      into shared memory with bulk copies, reduces the max of l/T across the
+//      cluster through distributed shared memory, and forms the canonical
+//      sum Z of exp(l/T - max).  The row is read from HBM exactly once.
+//   2. sample_finish_kernel: one 8-CTA cluster per sequence runs the
+//      acceptance walk (element-wise ratio tests from the row statistics),
+//      and the full-vocab passes it needs: the residual max(0, w - q) and its
+//      canonical sum, then inverse-CDF sampling by descending the summation
+//      tree (block level across the cluster, chunk level in shared memory,
+//      leaf level in one warp).
+// The summation tree: leaves = vocab entries zero-padded to 2^18; 4 leaves per
+// lane (level 2), 32 lanes per 128-leaf chunk (level 7), 32 chunks per
+// 4096-leaf block (level 12), 64 blocks (level 18).  Every level pairs
+// contiguous siblings, so the value of every node does not depend on the
+// launch shape.
+#include <cooperative_groups.h>
+#include <float.h>
+#include <limits.h>
+#include <stdlib.h>
+
+#include "sv_device.cuh"
+#include "sv_internal.h"
+
+namespace cg = cooperative_groups;
+
+namespace sv {
+namespace {
+
+constexpr int kBlk = 4096;            // leaves per block
+constexpr int kChunk = 128;           // leaves per chunk
+constexpr int kChunksPerBlk = kBlk / kChunk;
+constexpr int kMaxBlocks = 64;        // 2^18 / 4096
+constexpr int kCluster = 8;
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+constexpr int kMaxLocalBlocks = kMaxBlocks / kCluster;
+constexpr int kMaxR = 128;
+
+// With SV_SYNC_EACH_KERNEL=1 in the environment the launchers synchronise
+// after every kernel so a failing kernel is reported by name.
+bool debug_sync() {
+    static const bool on = [] {
+        const char* e = getenv("SV_SYNC_EACH_KERNEL");
+        return e && e[0] == '1';
+    }();
+    return on;
+}
+
+// ==========================================================================
+// greedy
+// ==========================================================================
+
+constexpr int kGreedyChunk = 8192;
+constexpr int kGreedyThreads = 256;
+
+struct ArgMax {
+    float v;
+    int i;
+};
+
+__device__ __forceinline__ ArgMax pick(ArgMax a, ArgMax b) {
+    return (b.v > a.v || (b.v == a.v && b.i < a.i)) ? b : a;
+}
+
+__device__ __forceinline__ ArgMax warp_pick(ArgMax a) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        ArgMax o;
+        o.v = __shfl_xor_sync(0xffffffffu, a.v, off);
+        o.i = __shfl_xor_sync(0xffffffffu, a.i, off);
+        a = pick(a, o);
+    }
+    return a;
+}
+
+__global__ void __launch_bounds__(kGreedyThreads) greedy_partial_kernel(const float* __restrict__ logits, int V,
+                                                                         int nchunk, int2* __restrict__ part,
+                                                                         unsigned int* err) {
+    const int row = blockIdx.y;
+    const int c0 = blockIdx.x * kGreedyChunk;
+    const int c1 = min(c0 + kGreedyChunk, V);
+    const float* L = logits + static_cast<size_t>(row) * V;
+    ArgMax best{-INFINITY, INT_MAX};
+    bool bad = false;
+    if ((V & 3) == 0) {
+        for (int i = c0 + 4 * threadIdx.x; i < c1; i += 4 * kGreedyThreads) {
+            const float4 x = __ldg(reinterpret_cast<const float4*>(L + i));
+            const float xs[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                if (xs[e] != xs[e]) { bad = true; continue; }
+                if (xs[e] > best.v || (xs[e] == best.v && i + e < best.i)) best = ArgMax{xs[e], i + e};
+            }
+        }
+    } else {
+        for (int i = c0 + threadIdx.x; i < c1; i += kGreedyThreads) {
+            const float x = __ldg(L + i);
+            if (x != x) { bad = true; continue; }
+            if (x > best.v || (x == best.v && i < best.i)) best = ArgMax{x, i};
+        }
+    }
+    if (bad) raise_error(err, SV_DEVERR_NONFINITE);
+    best = warp_pick(best);
+    __shared__ ArgMax red[kGreedyThreads / 32];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (lane == 0) red[warp] = best;
+    __syncthreads();
+    if (warp == 0) {
+        best = lane < kGreedyThreads / 32 ? red[lane] : ArgMax{-INFINITY, INT_MAX};
+        best = warp_pick(best);
+        if (lane == 0) part[static_cast<size_t>(row) * nchunk + blockIdx.x] = make_int2(__float_as_int(best.v), best.i);
+    }
+}
+
+// Children of node u in index order, for a chain (parent == nullptr: the only
+// child of u is u+1) or a tree.
+__device__ __forceinline__ int next_child(const int* par, int R, int u, int after) {
+    if (par == nullptr) return (after < 0 && u + 1 < R) ? u + 1 : -1;
+    for (int c = (after < 0 ? u + 1 : after + 1); c < R; ++c)
+        if (par[c] == u) return c;
+    return -1;
+}
+
+// Loads and validates the tree of sequence b into shared memory; returns
+// false (and raises SV_DEVERR_TREE) if it is malformed.
+__device__ bool load_tree(const int32_t* parent, int b, int R, int* par_s, unsigned int* err) {
+    __shared__ int bad;
+    if (threadIdx.x == 0) bad = 0;
+    __syncthreads();
+    for (int j = threadIdx.x; j < R; j += blockDim.x) {
+        const int p = parent[static_cast<size_t>(b) * R + j];
+        par_s[j] = p;
+        if ((j == 0 && p != -1) || (j > 0 && (p < 0 || p >= j))) bad = 1;
+    }
+    __syncthreads();
+    const bool ok = bad == 0;
+    if (!ok && threadIdx.x == 0) raise_error(err, SV_DEVERR_TREE);
+    return ok;
+}
+
+__global__ void __launch_bounds__(128) greedy_finish_kernel(const int2* __restrict__ part, int nchunk,
+                                                             const int32_t* __restrict__ tok,
+                                                             const int32_t* __restrict__ parent, int R, int V,
+                                                             int32_t* n_acc, int32_t* out_tok, int32_t* path,
+                                                             unsigned int* err) {
+    __shared__ int g[kMaxR];
+    __shared__ int par_s[kMaxR];
+    const int b = blockIdx.x;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int j = warp; j < R; j += 4) {
+        ArgMax best{-INFINITY, INT_MAX};
+        const int2* pr = part + (static_cast<size_t>(b) * R + j) * nchunk;
+        for (int c = lane; c < nchunk; c += 32) {
+            const int2 x = pr[c];
+            best = pick(best, ArgMax{__int_as_float(x.x), x.y});
+        }
+        best = warp_pick(best);
+        if (lane == 0) g[j] = (best.i == INT_MAX) ? 0 : best.i;
+    }
+    bool tree_ok = true;
+    if (parent) tree_ok = load_tree(parent, b, R, par_s, err);
+    __syncthreads();
+    if (threadIdx.x != 0) return;
+    const int32_t* tk = tok + static_cast<size_t>(b) * R;
+    int32_t* pth = path + static_cast<size_t>(b) * R;
+    for (int j = 1; j < R; ++j)
+        if (tk[j] < 0 || tk[j] >= V) raise_error(err, SV_DEVERR_TOKEN);
+    const int* par = parent ? par_s : nullptr;
+    int u = 0, depth = 0;
+    pth[0] = 0;
+    if (tree_ok) {
+        for (int guard = 0; guard < R; ++guard) {
+            int next = -1;
+            for (int c = next_child(par, R, u, -1); c >= 0; c = next_child(par, R, u, c))
+                if (tk[c] == g[u]) { next = c; break; }
+            if (next < 0) break;
+            u = next;
+            pth[++depth] = u;
+        }
+    }
+    for (int j = depth + 1; j < R; ++j) pth[j] = -1;
+    n_acc[b] = depth;
+    out_tok[b] = g[u];
+}
+
+// ==========================================================================
+// sampled: row statistics
+// ==========================================================================
+
+__global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads)
+    sample_stats_kernel(const float* __restrict__ logits, int V, float T, int nblk, int smem_blocks,
+                        float2* __restrict__ stats, unsigned int* err) {
+    extern __shared__ __align__(128) float srow[];   // [local blocks][4096]
+    __shared__ float cmax[kCluster];
+    __shared__ float bsum[kMaxBlocks];
+    __shared__ float csum[kMaxLocalBlocks * kChunksPerBlk];
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ float wred[kWarps];
+
+    cg::cluster_group cluster = cg::this_cluster();
+    const int rank = static_cast<int>(cluster.block_rank());
+    const int row = blockIdx.x / kCluster;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const float* L = logits + static_cast<size_t>(row) * V;
+    const int nlocal = rank < nblk ? (nblk - rank + kCluster - 1) / kCluster : 0;
+
+    if (tid == 0) {
+        mbar_init(&bar, 1);
+        fence_mbar_init();
+    }
+    if (tid < kMaxBlocks) bsum[tid] = 0.0f;
+    __syncthreads();
+    cluster_arrive_relaxed();   // paired with cluster_wait() before the first remote store
+    if (tid == 0 && nlocal > 0) {
+        uint32_t total = 0;
+        for (int lb = 0; lb < nlocal; ++lb) {
+            const int gb = rank + lb * kCluster;
+            total += static_cast<uint32_t>(min(kBlk, V - gb * kBlk)) * 4u;
+        }
+        mbar_arrive_expect_tx(&bar, total);
+        for (int lb = 0; lb < nlocal; ++lb) {
+            const int gb = rank + lb * kCluster;
+            const int n = min(kBlk, V - gb * kBlk);
+            if (!SV_CHECK(n > 0 && (n & 3) == 0 && lb < smem_blocks, err, 3)) continue;
+            bulk_g2s(srow + lb * kBlk, L + static_cast<size_t>(gb) * kBlk, static_cast<uint32_t>(n) * 4u, &bar);
+        }
+    }
+    if (nlocal > 0) mbar_wait(&bar, 0, err);
+
+    // local max of z = l / T (z stored back when T != 1)
+    float m = -INFINITY;
+    bool bad = false;
+    for (int lb = 0; lb < nlocal; ++lb) {
+        const int gb = rank + lb * kCluster;
+        const int n = min(kBlk, V - gb * kBlk);
+        float* s = srow + lb * kBlk;
+        for (int i = 4 * tid; i < n; i += 4 * kThreads) {
+            float4 x = *reinterpret_cast<float4*>(s + i);
+            if (T != 1.0f) {
+                x = make_float4(__fdiv_rn(x.x, T), __fdiv_rn(x.y, T), __fdiv_rn(x.z, T), __fdiv_rn(x.w, T));
+                *reinterpret_cast<float4*>(s + i) = x;
+            }
+            bad |= !(isfinite(x.x) && isfinite(x.y) && isfinite(x.z) && isfinite(x.w));
+            m = fmaxf(fmaxf(m, fmaxf(x.x, x.y)), fmaxf(x.z, x.w));
+        }
+    }
+    if (bad) raise_error(err, SV_DEVERR_NONFINITE);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+    if (lane == 0) wred[warp] = m;
+    __syncthreads();
+    cluster_wait();             // every CTA of the cluster has started
+    if (tid < kCluster) {
+        float mm = -INFINITY;
+        for (int w = 0; w < kWarps; ++w) mm = fmaxf(mm, wred[w]);
+        *cluster.map_shared_rank(&cmax[rank], tid) = mm;
+    }
+    cluster.sync();
+    float M = -INFINITY;
+#pragma unroll
+    for (int r = 0; r < kCluster; ++r) M = fmaxf(M, cmax[r]);
+
+    // chunk sums (level 7) of e = exp(z - M), zero beyond V
+    for (int cid = warp; cid < nlocal * kChunksPerBlk; cid += kWarps) {
+        const int lb = cid / kChunksPerBlk, c = cid % kChunksPerBlk;
+        const int gb = rank + lb * kCluster;
+        const int v = gb * kBlk + c * kChunk + 4 * lane;
+        float4 e = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (v < V) {
+            const float4 z = *reinterpret_cast<const float4*>(srow + lb * kBlk + c * kChunk + 4 * lane);
+            e = make_float4(sv_exp(__fsub_rn(z.x, M)), sv_exp(__fsub_rn(z.y, M)), sv_exp(__fsub_rn(z.z, M)),
+                            sv_exp(__fsub_rn(z.w, M)));
+        }
+        const float cs = warp_tree_sum(quad_sum(e));
+        if (lane == 0) csum[cid] = cs;
+    }
+    __syncthreads();
+    // block sums (level 12), pushed to rank 0
+    if (warp < nlocal) {
+        const float bs = warp_tree_sum(csum[warp * kChunksPerBlk + lane]);
+        if (lane == 0 && SV_CHECK(rank + warp * kCluster < kMaxBlocks, err, 4))
+            *cluster.map_shared_rank(&bsum[rank + warp * kCluster], 0) = bs;
+    }
+    cluster.sync();
+    if (rank == 0 && warp == 0) {
+        const float Z = warp_tree_sum(__fadd_rn(bsum[2 * lane], bsum[2 * lane + 1]));   // level 13 -> 18
+        if (lane == 0) {
+            if (!(Z > 0.0f) || !isfinite(Z)) raise_error(err, SV_DEVERR_NONFINITE);
+            stats[row] = make_float2(M, Z);
+        }
+    }
+}
+
+// ==========================================================================
+// sampled: acceptance walk and full-vocab passes
+// ==========================================================================
+
+struct SampleArgs {
+    const float* logits;
+    const float* q;
+    const int32_t* tok;
+    const int32_t* parent;
+    const float2* stats;
+    const float* uniforms;
+    int32_t* n_acc;
+    int32_t* out_tok;
+    int32_t* path;
+    unsigned int* err;
+    uint64_t seed, step;
+    int R, Rq, V, Vq, nblk;
+    float T;
+};
+
+// The working distribution at node u after `nsteps` rejected children:
+// w_0 = p_u;  w_i = max(0, w_{i-1} - q_u) / S_i if S_i > 0, else w_{i-1}.
+struct RowValues {
+    const float* L;     // logits row u
+    const float* Q;     // q row u (Vq entries); nullptr when no q row exists (a leaf)
+    int Vq;
+    float T, M, Z;
+    const float* S;     // S_1..S_nsteps
+    int nsteps;
+    bool residual;      // value = max(0, w_nsteps - q) instead of w_nsteps
+    int V;
+    unsigned int* err;
+
+    __device__ __forceinline__ float one(float l, float qv) const {
+        const float z = (T == 1.0f) ? l : __fdiv_rn(l, T);
+        float w = __fdiv_rn(sv_exp(__fsub_rn(z, M)), Z);
+        for (int s = 0; s < nsteps; ++s) {
+            const float d = __fsub_rn(w, qv);
+            const float rho = d > 0.0f ? d : 0.0f;
+            w = S[s] > 0.0f ? __fdiv_rn(rho, S[s]) : w;
+        }
+        if (residual) {
+            const float d = __fsub_rn(w, qv);
+            return d > 0.0f ? d : 0.0f;
+        }
+        return w;
+    }
+    __device__ __forceinline__ float at(int v) const {
+        if (!SV_CHECK(v >= 0 && v < V, err, 5)) return 0.0f;
+        const float qv = (Q != nullptr && v < Vq) ? __ldg(Q + v) : 0.0f;
+        return one(__ldg(L + v), qv);
+    }
+    // 4 consecutive entries starting at v (v % 4 == 0, v < V, V % 4 == 0)
+    __device__ __forceinline__ float4 at4(int v) const {
+        if (!SV_CHECK(v >= 0 && v + 3 < V && (v & 3) == 0, err, 6)) return make_float4(0.f, 0.f, 0.f, 0.f);
+        const float4 l = __ldg(reinterpret_cast<const float4*>(L + v));
+        float4 qv = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (Q != nullptr && v < Vq) qv = __ldg(reinterpret_cast<const float4*>(Q + v));
+        return make_float4(one(l.x, qv.x), one(l.y, qv.y), one(l.z, qv.z), one(l.w, qv.w));
+    }
+};
+
+// Raw values of a float array (diagnostic path).
+struct ArrayValues {
+    const float* x;
+    __device__ __forceinline__ float4 at4(int v) const { return __ldg(reinterpret_cast<const float4*>(x + v)); }
+};
+
+// Shared state of one cluster's full-vocab pass.
+struct PassSmem {
+    float csum[kMaxLocalBlocks * kChunksPerBlk];
+    float bsum[kMaxBlocks];
+    float tree[2 * kMaxBlocks];   // upper levels of the summation tree during a descent
+    int token;
+    int node;
+    float acc;
+};
+
+// Builds the levels above `n` leaves (n a power of two <= 64) in sm.tree by
+// warp 0: tree[0..n) = leaves, then each level follows the previous one.
+__device__ __forceinline__ void build_levels(const float* leaves, int n, float* tree) {
+    const int lane = threadIdx.x & 31;
+    for (int i = lane; i < n; i += 32) tree[i] = leaves[i];
+    __syncwarp();
+    int in = 0, out = n;
+    for (int m = n >> 1; m >= 1; m >>= 1) {
+        for (int i = lane; i < m; i += 32) tree[out + i] = __fadd_rn(tree[in + 2 * i], tree[in + 2 * i + 1]);
+        __syncwarp();
+        in = out;
+        out += m;
+    }
+}
+
+// Descends from the root of a tree built by build_levels over n leaves;
+// returns the leaf index and updates acc.
+__device__ __forceinline__ int descend_levels(const float* tree, int n, float tau, float& acc) {
+    // level offsets: leaves at 0, parents at n, ... ; root at 2n-2
+    int offs[8];
+    int lv = 0, off = 0;
+    for (int m = n; m >= 1; m >>= 1) { offs[lv++] = off; off += m; }
+    int node = 0;
+    for (int l = lv - 1; l >= 1; --l) {   // node at level l, children at level l-1
+        const float sl = tree[offs[l - 1] + 2 * node], sr = tree[offs[l - 1] + 2 * node + 1];
+        if (tau < __fadd_rn(acc, sl) || sr == 0.0f) {
+            node = 2 * node;
+        } else {
+            acc = __fadd_rn(acc, sl);
+            node = 2 * node + 1;
+        }
+    }
+    return node;
+}
+
+// Full pass over the vocab: chunk sums into csum (this CTA's blocks), block
+// sums into every CTA's bsum; returns the canonical total (identical in every
+// CTA).  All threads of all CTAs of the cluster must call it.
+template <class Vals>
+__device__ float full_pass(const Vals& vals, int V, int nblk, PassSmem& sm, cg::cluster_group& cluster) {
+    const int rank = static_cast<int>(cluster.block_rank());
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nlocal = rank < nblk ? (nblk - rank + kCluster - 1) / kCluster : 0;
+    cluster.sync();   // all CTAs started (first pass) / previous pass fully consumed everywhere
+    for (int cid = warp; cid < nlocal * kChunksPerBlk; cid += kWarps) {
+        const int lb = cid / kChunksPerBlk, c = cid % kChunksPerBlk;
+        const int v = (rank + lb * kCluster) * kBlk + c * kChunk + 4 * lane;
+        const float4 x = v < V ? vals.at4(v) : make_float4(0.f, 0.f, 0.f, 0.f);
+        const float cs = warp_tree_sum(quad_sum(x));
+        if (lane == 0) sm.csum[cid] = cs;
+    }
+    __syncthreads();
+    if (warp < nlocal) {
+        const float bs = warp_tree_sum(sm.csum[warp * kChunksPerBlk + lane]);
+        if (lane < kCluster) *cluster.map_shared_rank(&sm.bsum[rank + warp * kCluster], lane) = bs;
+    }
+    cluster.sync();
+    float lvl[kMaxBlocks / 2];
+#pragma unroll
+    for (int i = 0; i < kMaxBlocks / 2; ++i) lvl[i] = __fadd_rn(sm.bsum[2 * i], sm.bsum[2 * i + 1]);
+#pragma unroll
+    for (int n = kMaxBlocks / 4; n >= 1; n >>= 1)
+#pragma unroll
+        for (int i = 0; i < n; ++i) lvl[i] = __fadd_rn(lvl[2 * i], lvl[2 * i + 1]);
+    return lvl[0];
+}
+
+// One descent step: children sums sl, sr of the current node.
+__device__ __forceinline__ bool go_left(float tau, float acc, float sl, float sr) {
+    return tau < __fadd_rn(acc, sl) || sr == 0.0f;
+}
+
+// Inverse-CDF draw after full_pass(vals): returns the token in the CTA that
+// owns the chosen block (and -1 elsewhere).  All threads of all CTAs call it.
+template <class Vals>
+__device__ int tree_descent(const Vals& vals, int V, float total, float u, PassSmem& sm,
+                            cg::cluster_group& cluster, unsigned int* err) {
+    const int rank = static_cast<int>(cluster.block_rank());
+    const float tau = __fmul_rn(u, total);
+    // levels 18 -> 12 over the 64 block sums (every CTA reaches the same block)
+    if ((threadIdx.x >> 5) == 0) build_levels(sm.bsum, kMaxBlocks, sm.tree);
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float acc = 0.0f;
+        sm.node = descend_levels(sm.tree, kMaxBlocks, tau, acc);
+        sm.acc = acc;
+    }
+    __syncthreads();
+    const int blk = sm.node;
+    if (!SV_CHECK(blk >= 0 && blk < kMaxBlocks, err, 1)) return -1;
+    if (blk % kCluster != rank) return -1;
+    const int lb = blk / kCluster;
+    __syncthreads();
+    // levels 12 -> 7 over the block's 32 chunk sums
+    if ((threadIdx.x >> 5) == 0) build_levels(sm.csum + lb * kChunksPerBlk, kChunksPerBlk, sm.tree);
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float acc = sm.acc;
+        sm.node = descend_levels(sm.tree, kChunksPerBlk, tau, acc);
+        sm.acc = acc;
+    }
+    __syncthreads();
+    const int chunk = sm.node;
+    float acc = sm.acc;
+    if (!SV_CHECK(chunk >= 0 && chunk < kChunksPerBlk, err, 2)) return -1;
+    // levels 7 -> 0 inside the chunk: warp 0 recomputes its 128 leaves
+    if ((threadIdx.x >> 5) == 0) {
+        const int lane = threadIdx.x & 31;
+        const int v0 = blk * kBlk + chunk * kChunk;
+        const int v = v0 + 4 * lane;
+        const float4 x = v < V ? vals.at4(v) : make_float4(0.f, 0.f, 0.f, 0.f);
+        const float n1a = __fadd_rn(x.x, x.y), n1b = __fadd_rn(x.z, x.w);
+        float lvl[6];                      // lvl[k]: node at level k+2 containing this lane
+        lvl[0] = __fadd_rn(n1a, n1b);
+#pragma unroll
+        for (int k = 1; k < 6; ++k) lvl[k] = __fadd_rn(lvl[k - 1], __shfl_xor_sync(0xffffffffu, lvl[k - 1], 1 << (k - 1)));
+        int base = 0;                       // first lane of the current node
+#pragma unroll
+        for (int k = 5; k >= 1; --k) {      // node at level k+2 -> children at level k+1
+            const int half = 1 << (k - 1);
+            const float sl = __shfl_sync(0xffffffffu, lvl[k - 1], base);
+            const float sr = __shfl_sync(0xffffffffu, lvl[k - 1], base + half);
+            if (!go_left(tau, acc, sl, sr)) {
+                acc = __fadd_rn(acc, sl);
+                base += half;
+            }
+        }
+        // level 2 -> 1 -> 0 inside lane `base`
+        const float a = __shfl_sync(0xffffffffu, x.x, base), bb = __shfl_sync(0xffffffffu, x.y, base);
+        const float c = __shfl_sync(0xffffffffu, x.z, base), d = __shfl_sync(0xffffffffu, x.w, base);
+        const float s01 = __fadd_rn(a, bb), s23 = __fadd_rn(c, d);
+        int leaf;
+        if (go_left(tau, acc, s01, s23)) {
+            leaf = go_left(tau, acc, a, bb) ? 0 : 1;
+        } else {
+            acc = __fadd_rn(acc, s01);
+            leaf = go_left(tau, acc, c, d) ? 2 : 3;
+        }
+        if (lane == 0) sm.token = min(v0 + 4 * base + leaf, V - 1);
+    }
+    __syncthreads();
+    return sm.token;
+}
+
+__global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads)
+    sample_finish_kernel(SampleArgs a) {
+    __shared__ PassSmem sm;
+    __shared__ int par_s[kMaxR];
+    __shared__ float Schain[kMaxR];
+    cg::cluster_group cluster = cg::this_cluster();
+    const int rank = static_cast<int>(cluster.block_rank());
+    const int b = blockIdx.x / kCluster;
+    const int R = a.R, V = a.V, Vq = a.Vq;
+    if (threadIdx.x < kMaxBlocks) sm.bsum[threadIdx.x] = 0.0f;
+    bool tree_ok = true;
+    if (a.parent) tree_ok = load_tree(a.parent, b, R, par_s, a.err);
+    __syncthreads();
+    const int* par = a.parent ? par_s : nullptr;
+    const int32_t* tk = a.tok + static_cast<size_t>(b) * R;
+    const float* Lb = a.logits + static_cast<size_t>(b) * R * V;
+    const float* Qb = a.q + static_cast<size_t>(b) * a.Rq * Vq;
+    const float2* st = a.stats + static_cast<size_t>(b) * R;
+
+    int u = 0, depth = 0, token = -1;
+    int32_t* pth = a.path + static_cast<size_t>(b) * R;
+    for (int guard = 0; guard <= R && token < 0; ++guard) {
+        if (!SV_CHECK(u >= 0 && u < R, a.err, 7)) break;
+        const float2 ms = st[u];
+        RowValues rv{Lb + static_cast<size_t>(u) * V, Qb + static_cast<size_t>(u) * Vq, Vq, a.T, ms.x, ms.y, Schain,
+                     0, false, V, a.err};
+        int first = tree_ok ? next_child(par, R, u, -1) : -1;
+        if (first < 0) {   // leaf: bonus token from p_u
+            rv.Q = nullptr;
+            const float tot = full_pass(rv, V, a.nblk, sm, cluster);
+            token = tree_descent(rv, V, tot, node_uniforms(a.seed, a.step, b, u, a.uniforms, R).y, sm, cluster, a.err);
+            break;
+        }
+        int accepted = -1, nsteps = 0;
+        for (int c = first; c >= 0; c = next_child(par, R, u, c)) {
+            const int d = tk[c];
+            const bool tok_ok = d >= 0 && d < V;
+            if (!tok_ok && threadIdx.x == 0 && rank == 0) raise_error(a.err, SV_DEVERR_TOKEN);
+            bool accept = false;
+            if (tok_ok) {
+                const float qd = d < Vq ? __ldg(rv.Q + d) : 0.0f;
+                if (!(qd >= 0.0f) && threadIdx.x == 0 && rank == 0) raise_error(a.err, SV_DEVERR_QPROB);
+                rv.nsteps = nsteps;
+                rv.residual = false;
+                const float wd = rv.at(d);
+                const float ua = node_uniforms(a.seed, a.step, b, c, a.uniforms, R).x;
+                accept = (qd == 0.0f) || (ua < __fdiv_rn(wd, qd));
+            }
+            if (accept) { accepted = c; break; }
+            const bool last = next_child(par, R, u, c) < 0;
+            rv.nsteps = nsteps;
+            rv.residual = true;
+            const float S = full_pass(rv, V, a.nblk, sm, cluster);
+            if (last) {
+                const float ur = node_uniforms(a.seed, a.step, b, u, a.uniforms, R).y;
+                if (S > 0.0f) {
+                    token = tree_descent(rv, V, S, ur, sm, cluster, a.err);
+                } else {
+                    rv.residual = false;
+                    const float tot = full_pass(rv, V, a.nblk, sm, cluster);
+                    token = tree_descent(rv, V, tot, ur, sm, cluster, a.err);
+                }
+                break;
+            }
+            if (threadIdx.x == 0 && SV_CHECK(nsteps < kMaxR, a.err, 8)) Schain[nsteps] = S;
+            __syncthreads();
+            ++nsteps;
+        }
+        if (token >= 0 || accepted < 0) break;
+        u = accepted;
+        ++depth;
+        if (rank == 0 && threadIdx.x == 0 && SV_CHECK(depth < R, a.err, 9)) pth[depth] = u;
+    }
+    // The owner of the sampled block writes the token; rank 0 the walk.
+    if (token >= 0 && threadIdx.x == 0) a.out_tok[b] = token;
+    if (rank == 0 && threadIdx.x == 0) {
+        pth[0] = 0;
+        for (int j = depth + 1; j < R; ++j) pth[j] = -1;
+        a.n_acc[b] = depth;
+    }
+}
+
+// ==========================================================================
+// diagnostics
+// ==========================================================================
+
+__global__ void diag_exp_kernel(const float* x, float* y, int64_t n) {
+    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x)
+        y[i] = sv_exp(x[i]);
+}
+
+__global__ void diag_philox_kernel(const uint32_t* ctr, const uint32_t* key, uint32_t* out, int64_t n) {
+    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const uint4 c = make_uint4(ctr[4 * i], ctr[4 * i + 1], ctr[4 * i + 2], ctr[4 * i + 3]);
+        const uint4 r = philox4x32_10(c, make_uint2(key[2 * i], key[2 * i + 1]));
+        out[4 * i] = r.x;
+        out[4 * i + 1] = r.y;
+        out[4 * i + 2] = r.z;
+        out[4 * i + 3] = r.w;
+    }
+}
+
+__global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads)
+    diag_canon_kernel(const float* x, int n, int nblk, const float* u, float* sums, int32_t* draws) {
+    __shared__ PassSmem sm;
+    cg::cluster_group cluster = cg::this_cluster();
+    const int row = blockIdx.x / kCluster;
+    if (threadIdx.x < kMaxBlocks) sm.bsum[threadIdx.x] = 0.0f;
+    __syncthreads();
+    ArrayValues vals{x + static_cast<size_t>(row) * n};
+    const float tot = full_pass(vals, n, nblk, sm, cluster);
+    const int tok = tree_descent(vals, n, tot, u[row], sm, cluster, nullptr);
+    if (threadIdx.x == 0 && cluster.block_rank() == 0) sums[row] = tot;
+    if (threadIdx.x == 0 && tok >= 0) draws[row] = tok;
+}
+
+int blocks_for(int V) { return (V + kBlk - 1) / kBlk; }
+
+}  // namespace
+
+size_t greedy_workspace(int B, int R, int V) {
+    const int nchunk = (V + kGreedyChunk - 1) / kGreedyChunk;
+    return static_cast<size_t>(B) * R * nchunk * sizeof(int2);
+}
+
+cudaError_t launch_accept_greedy(const float* logits, const int32_t* tok, const int32_t* parent, int B, int R,
+                                 int V, int32_t* n_acc, int32_t* out_tok, int32_t* path, void* ws,
+                                 cudaStream_t st) {
+    const int nchunk = (V + kGreedyChunk - 1) / kGreedyChunk;
+    int2* part = static_cast<int2*>(ws);
+    unsigned int* err = device_error_word();
+    greedy_partial_kernel<<<dim3(nchunk, B * R), kGreedyThreads, 0, st>>>(logits, V, nchunk, part, err);
+    greedy_finish_kernel<<<B, 128, 0, st>>>(part, nchunk, tok, parent, R, V, n_acc, out_tok, path, err);
+    return cudaGetLastError();
+}
+
+size_t sample_workspace(int B, int R, int /*V*/) { return static_cast<size_t>(B) * R * sizeof(float2); }
+
+cudaError_t launch_accept_sample(const float* logits, const float* q, int Vq, const int32_t* tok,
+                                 const int32_t* parent, int B, int R, int V, float temperature, uint64_t seed,
+                                 uint64_t step, const float* uniforms, int32_t* n_acc, int32_t* out_tok,
+                                 int32_t* path, void* ws, cudaStream_t st) {
+    unsigned int* err = device_error_word();
+    const int nblk = blocks_for(V);
+    const int nlocal = (nblk + kCluster - 1) / kCluster;
+    const size_t smem = static_cast<size_t>(nlocal) * kBlk * sizeof(float);
+    cudaError_t e = cudaFuncSetAttribute(sample_stats_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    float2* stats = static_cast<float2*>(ws);
+    sample_stats_kernel<<<B * R * kCluster, kThreads, smem, st>>>(logits, V, temperature, nblk, nlocal, stats, err);
+    if (debug_sync()) {
+        e = cudaStreamSynchronize(st);
+        if (e != cudaSuccess) return e;
+    }
+    SampleArgs a;
+    a.logits = logits;
+    a.q = q;
+    a.tok = tok;
+    a.parent = parent;
+    a.stats = stats;
+    a.uniforms = uniforms;
+    a.n_acc = n_acc;
+    a.out_tok = out_tok;
+    a.path = path;
+    a.err = err;
+    a.seed = seed;
+    a.step = step;
+    a.R = R;
+    a.Rq = parent ? R : R - 1;
+    a.V = V;
+    a.Vq = Vq;
+    a.nblk = nblk;
+    a.T = temperature;
+    sample_finish_kernel<<<B * kCluster, kThreads, 0, st>>>(a);
+    if (debug_sync()) {
+        e = cudaStreamSynchronize(st);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_diag_exp(const float* x, float* y, int64_t n, cudaStream_t st) {
+    const int64_t blocks = (n + 255) / 256;
+    diag_exp_kernel<<<static_cast<int>(blocks > 65535 ? 65535 : (blocks < 1 ? 1 : blocks)), 256, 0, st>>>(x, y, n);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_diag_philox(const uint32_t* ctr, const uint32_t* key, uint32_t* out, int64_t n,
+                               cudaStream_t st) {
+    const int64_t blocks = (n + 255) / 256;
+    diag_philox_kernel<<<static_cast<int>(blocks > 65535 ? 65535 : (blocks < 1 ? 1 : blocks)), 256, 0, st>>>(
+        ctr, key, out, n);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_diag_canon(const float* x, int n, int m, const float* u, float* sums, int32_t* draws,
+                              cudaStream_t st) {
+    diag_canon_kernel<<<m * kCluster, kThreads, 0, st>>>(x, n, blocks_for(n), u, sums, draws);
+    return cudaGetLastError();
+}
+
+}  // namespace sv

@@ -1,0 +1,280 @@
+// sv_device.cuh -- device helpers shared by the sv kernels (sm_103a).
+//
+// PTX wrappers for mbarriers, bulk / tensor (TMA) copies, ldmatrix and the
+// bf16 mma; and the single-precision building blocks of the sampled
+// acceptance whose arithmetic is fixed so that a host implementation can
+// reproduce every decision bit for bit:
+//   * sv_exp      Cody-Waite reduction (Cody & Waite, "Software Manual for the
+//                 Elementary Functions", 1980) + degree-7 Taylor polynomial;
+//   * philox4x32_10  Salmon et al., "Parallel Random Numbers: As Easy as 1, 2,
+//                 3", SC'11;
+//   * canonical pairwise summation: leaves are the vocab entries zero-padded
+//                 to a power of two, each tree node is the float sum of its
+//                 two contiguous halves.
+// All float arithmetic that decides an integer uses the explicitly rounded
+// intrinsics (__fadd_rn, __fmul_rn, __fdiv_rn, __fmaf_rn) so the compiler
+// cannot contract or reassociate it.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "sv.h"
+
+namespace sv {
+
+// --------------------------------------------------------------------------
+// error word
+// --------------------------------------------------------------------------
+
+__device__ __forceinline__ void raise_error(unsigned int* err, unsigned int bit) {
+    if (err) atomicOr(err, bit);
+}
+
+// Self-checks compiled in with -DSV_DEBUG: a failed check sets bit 0x80 and
+// the check's code (bits 8..) in the error word, and the guarded access is
+// skipped.  Without SV_DEBUG the checks vanish.
+#ifdef SV_DEBUG
+__device__ __forceinline__ bool sv_check(bool ok, unsigned int* err, unsigned int code) {
+    if (!ok) raise_error(err, 0x80u | (1u << (8 + (code & 23))));
+    return ok;
+}
+#define SV_CHECK(cond, err, code) ::sv::sv_check((cond), (err), (code))
+#else
+#define SV_CHECK(cond, err, code) true
+#endif
+
+// --------------------------------------------------------------------------
+// addresses, timers
+// --------------------------------------------------------------------------
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// --------------------------------------------------------------------------
+// mbarrier + bulk copies
+// --------------------------------------------------------------------------
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait on an mbarrier phase: gives up after ~2 s of wall time (or a
+// large iteration count), raises SV_DEVERR_TIMEOUT and returns false.  The
+// copies these barriers track cannot fail short of a device fault, so the
+// bound only guarantees that no kernel of this library can spin forever.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsigned int* err) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t it = 0; it < (1u << 28); ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 255u) == 0 && global_timer_ns() - t0 > 2000000000ull) break;
+    }
+    raise_error(err, SV_DEVERR_TIMEOUT);
+    return false;
+}
+
+// 1-D bulk copy global -> this CTA's shared memory, completing on `bar`.
+// dst, src 16-byte aligned; bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// 2-D tiled tensor copy (TMA) global -> shared, completing on `bar`.
+// x (innermost coordinate) times the element size must be a multiple of 16 B.
+__device__ __forceinline__ void tma_load_2d(void* dst, const void* tmap, int32_t x, int32_t y, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+            smem_u32(dst)),
+        "l"(tmap), "r"(x), "r"(y), "r"(smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tmap(const void* tmap) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
+}
+
+// Split cluster barrier.  Every CTA of a cluster must have started before any
+// CTA touches another's shared memory: arrive early, wait right before the
+// first distributed-shared-memory access.
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.aligned;" ::: "memory"); }
+
+// Programmatic dependent launch: wait for the preceding kernel's results /
+// let the next kernel start its prologue.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// --------------------------------------------------------------------------
+// tensor-core fragments (mma.sync m16n8k16, bf16 in, fp32 accumulate)
+// --------------------------------------------------------------------------
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x2(uint32_t addr, uint32_t& r0, uint32_t& r1) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0,%1}, [%2];" : "=r"(r0), "=r"(r1) : "r"(addr));
+}
+
+__device__ __forceinline__ void mma_bf16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// 2^x via the SFU (attention softmax only; not used where bits must match).
+__device__ __forceinline__ float fast_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// Address of 16-byte chunk `chunk` (0..7) of row `row` inside a TMA box of
+// 128-byte rows written with CU_TENSOR_MAP_SWIZZLE_128B (box base 1024-aligned).
+__device__ __forceinline__ uint32_t swz128(uint32_t box_base, int row, int chunk) {
+    return box_base + row * 128 + (((chunk ^ (row & 7)) & 7) << 4);
+}
+
+// --------------------------------------------------------------------------
+// exponential with a fixed operation sequence
+// --------------------------------------------------------------------------
+
+__device__ __forceinline__ float sv_exp(float x) {
+    if (x != x) return x;
+    if (x < -104.0f) return 0.0f;                 // below half the least subnormal
+    if (x > 88.0f) return __int_as_float(0x7f800000);
+    const float kInvLn2 = 1.44269504088896340736f;
+    const float kLn2Head = 0.693145751953125f;    // 12 significant bits: n * head exact
+    const float kLn2Tail = 1.428606820309417232e-06f;
+    const float n = rintf(__fmul_rn(x, kInvLn2));
+    float r = __fmaf_rn(-n, kLn2Head, x);
+    r = __fmaf_rn(-n, kLn2Tail, r);
+    float s = 1.0f / 5040.0f;                      // Taylor coefficients 1/k!
+    s = __fmaf_rn(s, r, 1.0f / 720.0f);
+    s = __fmaf_rn(s, r, 1.0f / 120.0f);
+    s = __fmaf_rn(s, r, 1.0f / 24.0f);
+    s = __fmaf_rn(s, r, 1.0f / 6.0f);
+    s = __fmaf_rn(s, r, 0.5f);
+    s = __fmaf_rn(s, r, 1.0f);
+    s = __fmaf_rn(s, r, 1.0f);
+    const int k = static_cast<int>(n);
+    if (k >= -126) return __fmul_rn(s, __int_as_float((k + 127) << 23));
+    // 2^k subnormal: an exact scaling by 2^(k+64), then one rounding by 2^-64
+    return __fmul_rn(__fmul_rn(s, __int_as_float((k + 64 + 127) << 23)), __int_as_float((127 - 64) << 23));
+}
+
+// --------------------------------------------------------------------------
+// Philox4x32-10
+// --------------------------------------------------------------------------
+
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint2 k) {
+    const uint32_t kMulA = 0xD2511F53u, kMulB = 0xCD9E8D57u;
+    const uint32_t kWeylA = 0x9E3779B9u, kWeylB = 0xBB67AE85u;
+#pragma unroll
+    for (int round = 0; round < 10; ++round) {
+        const uint32_t hi_a = __umulhi(kMulA, c.x), lo_a = kMulA * c.x;
+        const uint32_t hi_b = __umulhi(kMulB, c.z), lo_b = kMulB * c.z;
+        c = make_uint4(hi_b ^ c.y ^ k.x, lo_b, hi_a ^ c.w ^ k.y, lo_a);
+        k.x += kWeylA;
+        k.y += kWeylB;
+    }
+    return c;
+}
+
+__device__ __forceinline__ float uniform24(uint32_t w) {
+    return __fmul_rn(static_cast<float>(w >> 8), 5.9604644775390625e-08f);   // * 2^-24, exact
+}
+
+// The acceptance (word 0) and sampling (word 1) uniforms of tree node u.
+__device__ __forceinline__ float2 node_uniforms(uint64_t seed, uint64_t step, int b, int u, const float* uniforms,
+                                                int R) {
+    if (uniforms) {
+        const float* p = uniforms + (static_cast<size_t>(b) * R + u) * 2;
+        return make_float2(p[0], p[1]);
+    }
+    const uint4 w = philox4x32_10(
+        make_uint4(static_cast<uint32_t>(b), static_cast<uint32_t>(u), static_cast<uint32_t>(step),
+                   static_cast<uint32_t>(step >> 32)),
+        make_uint2(static_cast<uint32_t>(seed), static_cast<uint32_t>(seed >> 32)));
+    return make_float2(uniform24(w.x), uniform24(w.y));
+}
+
+// --------------------------------------------------------------------------
+// canonical pairwise summation pieces
+// --------------------------------------------------------------------------
+
+// Node over 4 contiguous leaves: (a+b) + (c+d).
+__device__ __forceinline__ float quad_sum(float4 v) {
+    return __fadd_rn(__fadd_rn(v.x, v.y), __fadd_rn(v.z, v.w));
+}
+
+// Lane i holds the node over leaves [i*s, (i+1)*s); returns (in every lane)
+// the node over all 32*s leaves.  Step `off` pairs lanes i and i^off, which
+// are adjacent siblings at that level, and float addition is commutative, so
+// both partners hold the same parent value.
+__device__ __forceinline__ float warp_tree_sum(float v) {
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, off));
+    return v;
+}
+
+}  // namespace sv

@@ -1,0 +1,62 @@
+// sv_internal.h -- launchers shared between the kernel translation units and
+// the C-ABI entry points (sv_api.cu).  Host-side only; not installed.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "sv.h"
+
+namespace sv {
+
+constexpr int kSmCount = 152;   // GB300; launch heuristics query the device when it differs
+
+unsigned int* device_error_word();          // per-device __device__ word (sv_api.cu)
+int device_sm_count();
+
+// accept.cu
+size_t greedy_workspace(int B, int R, int V);
+cudaError_t launch_accept_greedy(const float* logits, const int32_t* tok, const int32_t* parent, int B, int R,
+                                 int V, int32_t* n_acc, int32_t* out_tok, int32_t* path, void* ws,
+                                 cudaStream_t st);
+size_t sample_workspace(int B, int R, int V);
+cudaError_t launch_accept_sample(const float* logits, const float* q, int Vq, const int32_t* tok,
+                                 const int32_t* parent, int B, int R, int V, float temperature, uint64_t seed,
+                                 uint64_t step, const float* uniforms, int32_t* n_acc, int32_t* out_tok,
+                                 int32_t* path, void* ws, cudaStream_t st);
+cudaError_t launch_diag_exp(const float* x, float* y, int64_t n, cudaStream_t st);
+cudaError_t launch_diag_philox(const uint32_t* ctr, const uint32_t* key, uint32_t* out, int64_t n,
+                               cudaStream_t st);
+cudaError_t launch_diag_canon(const float* x, int n, int m, const float* u, float* sums, int32_t* draws,
+                              cudaStream_t st);
+
+// kv_commit.cu
+cudaError_t launch_kv_commit(uint16_t* k_cache, uint16_t* v_cache, const uint16_t* k_blk, const uint16_t* v_blk,
+                             int L, int B, int Hkv, int D, int T_cap, int R, const int32_t* path,
+                             const int32_t* n_acc, int32_t* len, cudaStream_t st);
+
+// lm_head.cu
+cudaError_t launch_lm_head(const uint16_t* hid, const uint16_t* W, float* logits, int N, int H, int V,
+                           cudaStream_t st);
+
+// verify_attn.cu
+struct AttnPlan {
+    int G;          // query heads per KV head
+    int rows;       // R * G query rows per (sequence, KV head)
+    int row_tiles;  // ceil(rows / 64)
+    int warps;      // warps per CTA (16 rows each)
+    int splits;     // context splits (the block rows get one extra split)
+};
+AttnPlan attn_plan(const sv_attn_shape& s);
+size_t attn_workspace(const sv_attn_shape& s);
+cudaError_t launch_verify_attn(const sv_attn_shape& s, const uint16_t* q, const uint16_t* k_cache,
+                               const uint16_t* v_cache, const int32_t* len, const uint16_t* k_blk,
+                               const uint16_t* v_blk, const int32_t* parent, float scale, uint16_t* out,
+                               void* ws, cudaStream_t st);
+
+// TMA descriptor encoding (driver entry point fetched through the runtime).
+bool encode_tmap_2d_bf16(void* tmap, const void* base, uint64_t inner, uint64_t outer, uint64_t row_stride_bytes,
+                         uint32_t box_inner, uint32_t box_outer);
+
+}  // namespace sv

@@ -267,8 +267,9 @@ def sample_inputs(B: int, k: int, V: int, wid: int = 2, device="cpu", Vq: Option
     tok = torch.zeros(B, R, dtype=torch.int32, device=device)
     tok[:, 0] = torch.randint(0, V, (B,), generator=g3, device=device, dtype=torch.int32)
     if parent is None:
-        draws = torch.multinomial(q.reshape(B * Rq, Vq), 1, generator=g3).reshape(B, Rq)
-        tok[:, 1:] = draws.to(torch.int32)
+        if Rq > 0:
+            draws = torch.multinomial(q.reshape(B * Rq, Vq), 1, generator=g3).reshape(B, Rq)
+            tok[:, 1:] = draws.to(torch.int32)
         par_t = None
     else:
         draws = torch.multinomial(q.reshape(B * Rq, Vq), R, replacement=True,

@@ -1,0 +1,83 @@
+"""The C-ABI library loads and exports every entry point include/sv.h
+declares; host-side argument validation rejects bad calls before any CUDA
+work is enqueued (no GPU needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "sv.h")).read()
+    return sorted(set(re.findall(r"^SV_API\s+[\w\s\*]+?\b(sv_\w+)\s*\(", src, flags=re.M)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from speculative_decoding_verification_sv_gb300 import build
+    build.build()
+    return ctypes.CDLL(build.LIB)
+
+
+def test_header_declares_the_five_calls():
+    names = _declared()
+    for fn in ("sv_verify_attn", "sv_lm_head", "sv_accept_greedy", "sv_accept_sample", "sv_kv_commit"):
+        assert fn in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = _declared()
+    assert len(names) >= 14
+    for fn in names:
+        assert hasattr(lib, fn), fn
+
+
+def test_binding_imports_without_gpu():
+    from speculative_decoding_verification_sv_gb300 import binding
+    assert binding.lib.sv_version() == 100
+    assert binding.lib.sv_status_string(3) == b"unsupported configuration"
+
+
+def test_host_validation_rejects_before_launch(lib):
+    from speculative_decoding_verification_sv_gb300 import binding as b
+    L = b.lib
+    P = ctypes.c_void_p
+    fake = ctypes.c_void_p(0x10000)          # never dereferenced: validation fails first
+    # NULL pointers
+    assert L.sv_lm_head(None, fake, fake, 5, 1536, 151936, None) == 1
+    # misaligned pointer
+    assert L.sv_lm_head(ctypes.c_void_p(0x10002), fake, fake, 5, 1536, 151936, None) == 1
+    # bad shapes
+    assert L.sv_lm_head(fake, fake, fake, 0, 1536, 151936, None) == 2
+    assert L.sv_lm_head(fake, fake, fake, 5, 1537, 151936, None) == 2
+    # head dim other than 128 is unsupported
+    s = b._AttnShape(1, 5, 12, 2, 64, 4096)
+    assert L.sv_verify_attn(ctypes.byref(s), fake, fake, fake, fake, fake, fake, None, ctypes.c_float(0.1), fake,
+                            fake, 1 << 30, None) == 3
+    s = b._AttnShape(1, 5, 12, 5, 128, 4096)   # Hq % Hkv != 0
+    assert L.sv_verify_attn(ctypes.byref(s), fake, fake, fake, fake, fake, fake, None, ctypes.c_float(0.1), fake,
+                            fake, 1 << 30, None) == 2
+    # short workspace
+    s = b._AttnShape(1, 5, 12, 2, 128, 4096)
+    assert L.sv_verify_attn_workspace(ctypes.byref(s)) > 0
+    assert L.sv_verify_attn(ctypes.byref(s), fake, fake, fake, fake, fake, fake, None, ctypes.c_float(0.1), fake,
+                            fake, 16, None) == 4
+    # temperature must be positive; vocab must be a multiple of 4
+    args = [fake, fake, 151936, fake, None, 64, 9, 151936, ctypes.c_float(0.0), 1, 0, None, fake, fake, fake, fake,
+            1 << 20, None]
+    assert L.sv_accept_sample(*args) == 1
+    args[8] = ctypes.c_float(1.0)
+    args[7] = 151937
+    assert L.sv_accept_sample(*args) == 2
+    # commit: R above 128
+    assert L.sv_kv_commit(fake, fake, fake, fake, 28, 1, 2, 128, 4224, 200, fake, fake, fake, None) == 2
+
+
+def test_workspace_queries(lib):
+    from speculative_decoding_verification_sv_gb300 import binding as b
+    assert b.lib.sv_accept_greedy_workspace(16, 9, 152064) == 16 * 9 * 19 * 8
+    assert b.lib.sv_accept_sample_workspace(64, 9, 151936) == 64 * 9 * 8
+    assert b.verify_attn_workspace(16, 9, 28, 4, 128, 8320) > 0

@@ -1,0 +1,193 @@
+"""GPU parity of sv_accept_greedy and sv_accept_sample against the oracle.
+
+Integer outputs (n_acc, out_tok, path) must be bit-exact, given identical
+logits, q and uniforms.  Inputs are seeded synthetic tensors from `synth`;
+no expected value comes from the GPU.
+"""
+import json
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from speculative_decoding_verification_sv_gb300 import synth
+
+from _helpers import assert_same
+
+pytestmark = pytest.mark.gpu
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+@pytest.fixture(scope="module")
+def sv():
+    from speculative_decoding_verification_sv_gb300 import binding
+    return binding
+
+
+def _greedy_inputs(B, R, V, seed, rate=0.6, ties=False):
+    rng = np.random.default_rng(seed)
+    logits = rng.standard_normal((B, R, V)).astype(np.float32)
+    if ties:   # quantised logits: many exact ties
+        logits = np.round(logits * 2).astype(np.float32)
+    g = np.stack([[oracle.accept_greedy(logits[b:b + 1, j:j + 1], np.zeros((1, 1), np.int32))[1][0]
+                   for j in range(R)] for b in range(B)])
+    tok = synth.plant_chain_drafts(g, rate, V, seed + 1)
+    return logits, tok
+
+
+@pytest.mark.parametrize("B,R,V", [(1, 5, 151936), (3, 9, 152064), (16, 9, 4000), (7, 1, 1000), (2, 3, 5),
+                                   (64, 9, 8192)])
+def test_greedy_chain(sv, B, R, V):
+    logits, tok = _greedy_inputs(B, R, V, seed=B * 1000 + R)
+    got = sv.accept_greedy(torch.from_numpy(logits).cuda(), torch.from_numpy(tok).cuda())
+    assert_same(got, oracle.accept_greedy(logits, tok), "greedy")
+    assert sv.get_device_error() == 0
+
+
+def test_greedy_ties_lowest_index(sv):
+    logits, tok = _greedy_inputs(8, 6, 3000, seed=5, ties=True)
+    got = sv.accept_greedy(torch.from_numpy(logits).cuda(), torch.from_numpy(tok).cuda())
+    assert_same(got, oracle.accept_greedy(logits, tok), "greedy ties")
+
+
+def test_greedy_golden_alignment(sv):
+    g = json.load(open(os.path.join(GOLDEN, "alignment.json")))
+    for case in g["cases"]:
+        logits = np.array(case["logits"], np.float32)[None]
+        tok = np.array(case["tok"], np.int32)[None]
+        n_acc, out_tok, path = sv.accept_greedy(torch.from_numpy(logits).cuda(), torch.from_numpy(tok).cuda())
+        assert int(n_acc[0]) == case["n_acc"], case["why"]
+        assert int(out_tok[0]) == case["out_tok"], case["why"]
+        assert path[0].tolist() == case["path"], case["why"]
+
+
+def _tree(n_nodes, depth, seed):
+    return synth.random_tree(n_nodes, depth, 3, seed)
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_greedy_tree(sv, seed):
+    B, V = 4, 20000
+    par = _tree(64, 8, seed)
+    R = len(par)
+    rng = np.random.default_rng(seed)
+    logits = rng.standard_normal((B, R, V)).astype(np.float32)
+    g = logits.argmax(-1)
+    parent = np.tile(par, (B, 1)).astype(np.int32)
+    tok = np.stack([synth.plant_tree_drafts(g[b:b + 1], par[None], 0.7, V, seed + b)[0] for b in range(B)])
+    got = sv.accept_greedy(torch.from_numpy(logits).cuda(), torch.from_numpy(tok).cuda(),
+                           torch.from_numpy(parent).cuda())
+    assert_same(got, oracle.accept_greedy(logits, tok, parent), "greedy tree")
+
+
+def test_greedy_errors_flagged(sv):
+    logits = np.zeros((1, 3, 64), np.float32)
+    logits[0, 1, 5] = np.nan
+    tok = np.array([[0, 99, 1]], np.int32)
+    sv.accept_greedy(torch.from_numpy(logits).cuda(), torch.from_numpy(tok).cuda())
+    word = sv.get_device_error()
+    assert word & 0x1 and word & 0x2
+    assert sv.get_device_error() == 0
+
+
+# ----------------------------------------------------------------------------
+# sampled
+# ----------------------------------------------------------------------------
+
+def _sample_case(B, k, V, Vq=None, seed=0, std=3.0, parent=None):
+    return synth.sample_inputs(B, k, V, wid=100 + seed, Vq=Vq, logit_std=std, parent=parent)
+
+
+@pytest.mark.parametrize("B,k,V,Vq,T", [(4, 4, 151936, None, 1.0), (8, 8, 152064, 151936, 1.0),
+                                          (5, 3, 1000, None, 0.7), (3, 0, 4096, None, 1.0),
+                                          (16, 8, 8192, None, 1.3), (2, 6, 4100, 4096, 0.5)])
+def test_sample_chain_philox(sv, B, k, V, Vq, T):
+    si = _sample_case(B, k, V, Vq, seed=B + k)
+    for step in (0, 1, 2 ** 40 + 3):
+        got = sv.accept_sample(si.logits.cuda(), si.q.cuda(), si.tok.cuda(), temperature=T, seed=0xDEADBEEF,
+                               step=step)
+        exp = oracle.accept_sample(si.logits.numpy(), si.q.numpy(), si.tok.numpy(), temperature=T,
+                                   seed=0xDEADBEEF, step=step)
+        assert_same(got, exp, f"sample chain step {step}")
+    assert sv.get_device_error() == 0
+
+
+def test_sample_chain_injected_uniforms(sv):
+    B, k, V = 32, 8, 20000
+    si = _sample_case(B, k, V, seed=3, std=1.0)
+    rng = np.random.default_rng(4)
+    for trial in range(3):
+        uni = (rng.integers(0, 2 ** 24, size=(B, k + 1, 2)) * 2.0 ** -24).astype(np.float32)
+        got = sv.accept_sample(si.logits.cuda(), si.q.cuda(), si.tok.cuda(), uniforms=torch.from_numpy(uni).cuda())
+        exp = oracle.accept_sample(si.logits.numpy(), si.q.numpy(), si.tok.numpy(), uniforms=uni)
+        assert_same(got, exp, "sample chain uniforms")
+
+
+def test_sample_full_size_b64_k8(sv):
+    """The sampled-acceptance workload at full size: 64 sequences, k = 8,
+    vocab 151936, T = 1, target logits ~ N(0, 3^2)."""
+    si = synth.sample_inputs(64, 8, 151936, wid=2)
+    got = sv.accept_sample(si.logits.cuda(), si.q.cuda(), si.tok.cuda(), seed=2024, step=7)
+    exp = oracle.accept_sample(si.logits.numpy(), si.q.numpy(), si.tok.numpy(), seed=2024, step=7)
+    assert_same(got, exp, "sample b64")
+    n_acc = exp[0]
+    assert 0 < n_acc.mean() < 8   # both rejections and acceptances occur
+
+
+@pytest.mark.parametrize("seed", [0, 1])
+def test_sample_tree(sv, seed):
+    V = 30000
+    par = _tree(64, 8, seed)
+    si = _sample_case(3, len(par) - 1, V, seed=10 + seed, std=1.5, parent=par)
+    for step in (0, 5):
+        got = sv.accept_sample(si.logits.cuda(), si.q.cuda(), si.tok.cuda(), si.parent.cuda(), seed=99, step=step)
+        exp = oracle.accept_sample(si.logits.numpy(), si.q.numpy(), si.tok.numpy(), si.parent.numpy(), seed=99,
+                                   step=step)
+        assert_same(got, exp, "sample tree")
+
+
+def test_sample_tree_with_rejected_siblings(sv):
+    # q far from p so that siblings are rejected and residuals chain
+    V = 8192
+    par = np.array([-1, 0, 0, 0, 1, 1, 4, 4, 4], np.int32)
+    B = 24
+    rng = np.random.default_rng(7)
+    logits = torch.from_numpy((rng.standard_normal((B, len(par), V)) * 2).astype(np.float32))
+    si = synth.sample_inputs(B, len(par) - 1, V, wid=120, parent=par,
+                             logits=logits, logit_std=2.0)
+    q = torch.softmax(torch.from_numpy(rng.standard_normal((B, len(par), V)).astype(np.float32) * 2), -1)
+    got = sv.accept_sample(logits.cuda(), q.contiguous().cuda(), si.tok.cuda(), si.parent.cuda(), seed=1, step=2)
+    exp = oracle.accept_sample(logits.numpy(), q.numpy(), si.tok.numpy(), si.parent.numpy(), seed=1, step=2)
+    assert_same(got, exp, "sample tree siblings")
+
+
+def test_sample_one_hot_equals_greedy(sv):
+    B, R, V = 40, 6, 4096
+    rng = np.random.default_rng(9)
+    g = rng.integers(0, V, size=(B, R))
+    logits = np.zeros((B, R, V), np.float32)
+    np.put_along_axis(logits, g[..., None], 200.0, axis=-1)
+    tok = rng.integers(0, V, size=(B, R)).astype(np.int32)
+    plant = rng.random((B, R)) < 0.7
+    tok[:, 1:] = np.where(plant[:, 1:], g[:, :-1], tok[:, 1:])
+    q = np.zeros((B, R - 1, V), np.float32)
+    np.put_along_axis(q, tok[:, 1:, None].astype(np.int64), 1.0, axis=-1)
+    gs = sv.accept_greedy(torch.from_numpy(logits).cuda(), torch.from_numpy(tok).cuda())
+    ss = sv.accept_sample(torch.from_numpy(logits).cuda(), torch.from_numpy(q).cuda(), torch.from_numpy(tok).cuda(),
+                          seed=3)
+    for a, b in zip(gs, ss):
+        assert torch.equal(a, b)
+
+
+def test_sample_errors_flagged(sv):
+    B, k, V = 2, 3, 1000
+    si = _sample_case(B, k, V, seed=50)
+    tok = si.tok.clone()
+    tok[0, 1] = V + 5
+    logits = si.logits.clone()
+    logits[1, 2, 17] = float("inf")
+    sv.accept_sample(logits.cuda(), si.q.cuda(), tok.cuda(), seed=1)
+    word = sv.get_device_error()
+    assert word & 0x2 and word & 0x1

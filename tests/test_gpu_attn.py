@@ -1,0 +1,102 @@
+"""GPU parity of sv_verify_attn against the oracle (double precision):
+max|err| <= 1e-2 max|ref| per call, over chain and tree masks, ragged and
+empty contexts, several key tiles and splits, and full-size layers of the
+Qwen2.5-1.5B / 7B workloads."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from speculative_decoding_verification_sv_gb300 import synth
+
+from _helpers import bits, within_tol
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def sv():
+    from speculative_decoding_verification_sv_gb300 import binding
+    return binding
+
+
+def _run(sv, B, R, Hq, Hkv, T_cap, lengths, parent=None, seed=0, scale=None):
+    D = 128
+    g = torch.Generator().manual_seed(seed)
+    mk = lambda *s: torch.randn(*s, generator=g).to(torch.bfloat16)
+    q, kc, vc, kb, vb = mk(B, R, Hq, D), mk(B, Hkv, T_cap, D), mk(B, Hkv, T_cap, D), mk(B, Hkv, R, D), mk(B, Hkv, R, D)
+    ln = torch.tensor(lengths, dtype=torch.int32)
+    par_t = None if parent is None else torch.from_numpy(np.ascontiguousarray(parent, np.int32))
+    out = sv.verify_attn(q.cuda(), kc.cuda(), vc.cuda(), ln.cuda(), kb.cuda(), vb.cuda(),
+                         None if par_t is None else par_t.cuda(), scale=scale)
+    ref = oracle.verify_attn(bits(q), bits(kc), bits(vc), ln.numpy(), bits(kb), bits(vb),
+                             None if par_t is None else par_t.numpy(), scale)
+    return out.float().cpu().numpy(), ref
+
+
+@pytest.mark.parametrize("B,R,Hq,Hkv,T_cap,lengths", [
+    (1, 5, 12, 2, 2112, [2048]),                 # 1.5B layout, t = 2048
+    (2, 5, 12, 2, 320, [0, 1]),                  # empty and single-key contexts
+    (3, 9, 28, 4, 256, [63, 64, 65]),            # 7B layout, tile edges
+    (2, 1, 8, 8, 200, [150, 7]),                 # R = 1, MHA
+    (4, 9, 28, 4, 1100, [1000, 513, 1024, 77]),  # ragged batch, multiple tiles and splits
+    (1, 17, 16, 2, 700, [600]),                  # 136 rows: 3 row tiles
+    (2, 3, 4, 1, 130, [130, 129]),               # full cache
+])
+def test_attn_chain(sv, B, R, Hq, Hkv, T_cap, lengths):
+    got, ref = _run(sv, B, R, Hq, Hkv, T_cap, lengths, seed=B * 31 + R)
+    ok, err, bound = within_tol(got, ref)
+    assert ok, (err, bound)
+    assert sv.get_device_error() == 0
+
+
+def test_attn_custom_scale(sv):
+    got, ref = _run(sv, 2, 5, 12, 2, 400, [300, 211], seed=3, scale=0.21)
+    ok, err, bound = within_tol(got, ref)
+    assert ok, (err, bound)
+
+
+@pytest.mark.parametrize("seed", [0, 1])
+def test_attn_tree_65_nodes(sv, seed):
+    par = synth.random_tree(64, 8, 3, seed)
+    B = 2
+    parent = np.tile(par, (B, 1))
+    got, ref = _run(sv, B, 65, 28, 4, 600, [513, 300], parent=parent, seed=seed + 50)
+    ok, err, bound = within_tol(got, ref)
+    assert ok, (err, bound)
+
+
+def test_attn_chain_equals_path_tree(sv):
+    B, R = 2, 9
+    parent = np.tile(np.arange(-1, R - 1, dtype=np.int32), (B, 1))
+    a, ref = _run(sv, B, R, 28, 4, 300, [250, 100], seed=77)
+    b, _ = _run(sv, B, R, 28, 4, 300, [250, 100], parent=parent, seed=77)
+    assert np.array_equal(a, b)
+    assert within_tol(a, ref)[0]
+
+
+def test_attn_bad_length_flagged(sv):
+    got, ref = _run(sv, 1, 3, 4, 1, 64, [64], seed=9)
+    assert within_tol(got, ref)[0]
+    D = 128
+    q = torch.randn(1, 3, 4, D).to(torch.bfloat16).cuda()
+    kc = torch.randn(1, 1, 64, D).to(torch.bfloat16).cuda()
+    sv.verify_attn(q, kc, kc, torch.tensor([65], dtype=torch.int32).cuda(), kc[:, :, :3].contiguous(),
+                   kc[:, :, :3].contiguous())
+    assert sv.get_device_error() & 0x4
+
+
+@pytest.mark.parametrize("wid,B,layer", [(0, 1, 0), (1, 1, 27), (3, 1, 5), (3, 16, 0)])
+def test_attn_full_layer(sv, wid, B, layer):
+    """A full-size layer of the 1.5B / 7B workloads, generated on the GPU; the
+    oracle checks every output row of sequences 0 and B-1."""
+    w = synth.workload(wid, B=B)
+    ai = synth.attn_inputs(w, device="cuda", layers=layer + 1)
+    L = layer
+    out = sv.verify_attn(ai.q[L], ai.k_cache[L], ai.v_cache[L], ai.length, ai.k_blk[L], ai.v_blk[L])
+    for b in sorted({0, B - 1}):
+        ref = oracle.verify_attn(bits(ai.q[L, b:b + 1]), bits(ai.k_cache[L, b:b + 1]), bits(ai.v_cache[L, b:b + 1]),
+                                 ai.length[b:b + 1].cpu().numpy(), bits(ai.k_blk[L, b:b + 1]),
+                                 bits(ai.v_blk[L, b:b + 1]))
+        ok, err, bound = within_tol(out[b:b + 1].float().cpu().numpy(), ref)
+        assert ok, (b, err, bound)
