@@ -1,0 +1,610 @@
+"""Benchmark of one speculative-decoding verify round on GB300.
+
+A step is one pass of the whole verify path over one batch of synthetic
+inputs: per-layer verify attention for every layer, the LM head over the k+1
+rows of every sequence, acceptance (greedy or sampled) and the KV commit of
+all layers (preceded by restoring the committed length so every step starts
+from the same cache state).  Inputs are resident in HBM; each step reads more
+than the 129 MB L2 (the KV cache of all layers plus the LM-head weights), so
+no L2 flush is needed between steps.
+
+Default workload: the 28-layer Qwen2.5-1.5B-shaped round (t = 4096, k = 4,
+batch 1, greedy).  `--workload` selects another (0, 1, 2, 3, 3b16, 3s, 3b16s).
+
+Timing: the step is captured into a CUDA graph through the library's C ABI;
+the timed region replays a graph of `chunk` steps (K steps in total) between
+CUDA events on the launching stream; per-kernel durations come from event
+nodes captured inside that graph (the last replay of the timed region).
+
+`--impl reference` times the CPU oracle instead (a bounded sample of the
+same workload on the host cores).  Multi-GPU (torchrun): independent replicas,
+one per GPU, no collective on the data path; value = all ranks' steps / the
+slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from speculative_decoding_verification_sv_gb300 import synth  # noqa: E402
+
+PEAKS_PATH = os.path.join(ROOT, "MEASURED_PEAKS.json")
+FALLBACK_HBM_GBS = 6800.0
+
+# DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) from an
+# ncu capture, keyed by kernel, with the hash of the source file it was taken
+# on; a different hash (the kernel changed) reports null.
+TRAFFIC = {
+    # ncu --set full, 28-layer 1.5B round, LM head N=5 H=1536 V=151936
+    "lm_head": {"bytes": 466805504 + 5640192, "src_hash": "014d4cc2603280a9"},
+}
+
+
+# ----------------------------------------------------------------------------
+# workloads
+# ----------------------------------------------------------------------------
+
+def workload_from_name(name: str):
+    table = {
+        "0": (0, {}, "greedy"), "1": (1, {}, "greedy"), "2": (2, {}, "sampled"),
+        "3": (3, {}, "greedy"), "3s": (3, {}, "sampled"),
+        "3b16": (3, {"B": 16}, "greedy"), "3b16s": (3, {"B": 16}, "sampled"),
+    }
+    wid, over, mode = table[name]
+    return synth.workload(wid, **over), mode
+
+
+def attn_bytes(w) -> int:
+    D, R = w.D, w.R
+    return w.B * (2 * w.t * w.Hkv * D * 2 + R * w.Hq * D * 2 * 2 + 2 * R * w.Hkv * D * 2)
+
+
+def lm_bytes(w) -> int:
+    N = w.B * w.R
+    return w.H * w.V * 2 + N * w.H * 2 + N * w.V * 4
+
+
+def greedy_bytes(w) -> int:
+    return w.B * w.R * w.V * 4
+
+
+def sample_bytes(w, n_acc: np.ndarray) -> int:
+    k = w.R - 1
+    rejected = int(np.sum(n_acc < k))
+    return w.B * w.R * w.V * 4 + rejected * w.draft_vocab * 4 + w.B * k * 8
+
+
+def commit_bytes(w, n_acc: np.ndarray) -> int:
+    return int(2 * w.L * np.sum(n_acc + 1) * w.Hkv * w.D * 2 * 2)
+
+
+def src_hash(*files) -> str:
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, "speculative_decoding_verification_sv_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def load_peaks():
+    try:
+        with open(PEAKS_PATH) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+# ----------------------------------------------------------------------------
+# GPU state for one workload
+# ----------------------------------------------------------------------------
+
+class Round:
+    """Device buffers and the sequence of C-ABI calls of one verify round."""
+
+    def __init__(self, w, mode, device):
+        from speculative_decoding_verification_sv_gb300 import binding as sv
+        self.sv, self.w, self.mode, self.dev = sv, w, mode, device
+        B, R, V = w.B, w.R, w.V
+        self.has_model = w.L > 0
+        if self.has_model:
+            ai = synth.attn_inputs(w, device=device)
+            self.q, self.kc, self.vc, self.kb, self.vb = ai.q, ai.k_cache, ai.v_cache, ai.k_blk, ai.v_blk
+            self.len0 = ai.length.clone()
+            self.length = ai.length.clone()
+            self.attn_out = torch.empty_like(self.q)
+            shape = (B, R, w.Hq, w.Hkv, w.D, w.T_cap)
+            self.attn_ws = torch.empty(sv.verify_attn_workspace(*shape), dtype=torch.uint8, device=device)
+            self.hid, self.W = synth.lm_inputs(w, device=device)
+            self.logits = torch.empty(B * R, V, dtype=torch.float32, device=device)
+            # planted drafts: argmax of every verify row of the synthetic logits
+            g = torch.argmax(self.hid.float() @ self.W.float(), dim=-1).reshape(B, R).cpu().numpy()
+            if mode == "greedy":
+                tok = synth.plant_chain_drafts(g, w.accept_rate, V, synth.seed_for(w.wid, 11))
+                self.tok = torch.from_numpy(tok).to(device)
+            else:
+                # draft distributions around the round's actual target logits
+                sv.lm_head(self.hid, self.W, logits=self.logits)
+                si = synth.sample_inputs(B, R - 1, V, wid=w.wid, device=device,
+                                         logits=self.logits.reshape(B, R, V).clone())
+                self.q_draft, self.tok = si.q, si.tok
+        else:
+            si = synth.sample_inputs(B, R - 1, V, wid=w.wid, device=device)
+            self.logits = si.logits.reshape(B * R, V)
+            self.q_draft, self.tok = si.q, si.tok
+        self.n_acc = torch.zeros(B, dtype=torch.int32, device=device)
+        self.out_tok = torch.zeros(B, dtype=torch.int32, device=device)
+        self.path = torch.zeros(B, R, dtype=torch.int32, device=device)
+        if mode == "greedy":
+            self.acc_ws = torch.empty(sv.lib.sv_accept_greedy_workspace(B, R, V), dtype=torch.uint8, device=device)
+        else:
+            self.acc_ws = torch.empty(sv.lib.sv_accept_sample_workspace(B, R, V), dtype=torch.uint8, device=device)
+        self.step_counter = 0
+
+    # kernel launches of one round (what gpu_launches counts)
+    def launches_per_step(self) -> int:
+        n = 0
+        if self.has_model:
+            n += 2 * self.w.L                        # split kernel + combine per layer
+            n += (self.w.B * self.w.R + 63) // 64    # LM head passes of <= 64 rows
+            n += 1                                   # commit
+        n += 2                                       # accept: two kernels
+        return n
+
+    def step(self, ev=None):
+        """Enqueues one round on the current stream.  ev: optional dict of
+        external events recorded around each kernel class."""
+        sv, w = self.sv, self.w
+        rec = (lambda k: ev[k].record()) if ev is not None else (lambda k: None)
+        if self.has_model:
+            self.length.copy_(self.len0, non_blocking=True)
+            rec("attn0")
+            for l in range(w.L):
+                sv.verify_attn(self.q[l], self.kc[l], self.vc[l], self.length, self.kb[l], self.vb[l],
+                               out=self.attn_out[l], ws=self.attn_ws)
+            rec("attn1")
+            sv.lm_head(self.hid, self.W, logits=self.logits)
+            rec("lm1")
+        else:
+            rec("attn0"); rec("attn1"); rec("lm1")
+        lg = self.logits.reshape(w.B, w.R, w.V)
+        if self.mode == "greedy":
+            sv.accept_greedy(lg, self.tok, n_acc=self.n_acc, out_tok=self.out_tok, path=self.path, ws=self.acc_ws)
+        else:
+            sv.accept_sample(lg, self.q_draft, self.tok, temperature=w.temperature, seed=0x5EED, step=0,
+                             n_acc=self.n_acc, out_tok=self.out_tok, path=self.path, ws=self.acc_ws)
+        rec("acc1")
+        if self.has_model:
+            sv.kv_commit(self.kc, self.vc, self.kb, self.vb, self.path, self.n_acc, self.length)
+        rec("commit1")
+
+    def step_inputs(self):
+        """The per-round inputs a caller would send from the host."""
+        if self.has_model:
+            return [self.q, self.kb, self.vb, self.hid, self.tok]
+        return [self.logits, self.q_draft, self.tok]
+
+    def step_outputs(self):
+        return [self.n_acc, self.out_tok, self.path]
+
+
+# ----------------------------------------------------------------------------
+# clocks
+# ----------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid: str):
+        self.uuid = uuid
+        self.proc = None
+        self.path = os.path.join("/tmp", f"sv_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-lms", "200"], stdout=self.fh, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.fh.close()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        rows = [[p.strip() for p in line.split(",")] for line in open(self.path)]
+        rows = [r for r in rows if len(r) >= 9]
+        uuids = {r[0] for r in rows}
+        mine = {u for u in uuids if self.uuid and self.uuid in u}
+        keep = mine if mine else (uuids if len(uuids) == 1 else set())
+        for parts in rows:
+            if parts[0] not in keep:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def device_uuid(dev) -> str:
+    try:
+        u = str(torch.cuda.get_device_properties(dev).uuid)
+        return u.replace("GPU-", "")
+    except Exception:
+        return ""
+
+
+# ----------------------------------------------------------------------------
+# CPU oracle: cpu_baseline and the reference arm
+# ----------------------------------------------------------------------------
+
+class OracleRound:
+    """The verify round of a workload as a list of equal-sized units of
+    oracle work: (layer, KV head, key chunk) attention slices paired with
+    LM-head column slices; the acceptance and commit ride on the last unit."""
+
+    KEY_CHUNK = 512
+
+    def __init__(self, w, mode):
+        import oracle
+        self.oracle, self.w, self.mode = oracle, w, mode
+        oracle.build()
+        B, R, V = w.B, w.R, w.V
+        if w.L > 0:
+            ai = synth.attn_inputs(w, device="cpu", layers=1)   # one layer's tensors stand for every layer
+            self.q = synth.bf16_bits(ai.q[0])
+            self.kc = synth.bf16_bits(ai.k_cache[0])
+            self.vc = synth.bf16_bits(ai.v_cache[0])
+            self.kb = synth.bf16_bits(ai.k_blk[0])
+            self.vb = synth.bf16_bits(ai.v_blk[0])
+            hid, Wt = synth.lm_inputs(w, device="cpu")
+            self.hid, self.W = synth.bf16_bits(hid), synth.bf16_bits(Wt)
+            G = w.Hq // w.Hkv
+            nch = max(1, -(-w.t // self.KEY_CHUNK))
+            self.attn_units = [(l, g, c) for l in range(w.L) for g in range(w.Hkv) for c in range(nch)]
+            n = len(self.attn_units)
+            edges = np.linspace(0, V, n + 1).astype(int)
+            self.lm_units = [(int(edges[i]), int(edges[i + 1])) for i in range(n)]
+            self.G = G
+            self.kc_sl = {}
+            self.logits = np.random.default_rng(1).standard_normal((B, R, V)).astype(np.float32)
+        else:
+            si = synth.sample_inputs(B, R - 1, V, wid=w.wid)
+            self.logits = si.logits.numpy()
+            self.attn_units = [None] * B
+            self.lm_units = [None] * B
+        if mode == "greedy":
+            self.tok = np.zeros((B, R), np.int32)
+        else:
+            si = synth.sample_inputs(B, R - 1, V, wid=w.wid, logits=torch.from_numpy(self.logits))
+            self.qd, self.tok = si.q.numpy(), si.tok.numpy()
+        self.units = len(self.attn_units)
+
+    def run_unit(self, i):
+        o, w = self.oracle, self.w
+        i %= self.units
+        if w.L > 0:
+            l, g, c = self.attn_units[i]
+            G = self.G
+            k0 = c * self.KEY_CHUNK
+            k1 = min(w.t, k0 + self.KEY_CHUNK)
+            q = np.ascontiguousarray(self.q[:, :, g * G:(g + 1) * G])
+            kc = np.ascontiguousarray(self.kc[:, g:g + 1, k0:k1])
+            vc = np.ascontiguousarray(self.vc[:, g:g + 1, k0:k1])
+            o.verify_attn(q, kc, vc, np.full(w.B, k1 - k0, np.int32), self.kb[:, g:g + 1], self.vb[:, g:g + 1])
+            v0, v1 = self.lm_units[i]
+            o.lm_head(self.hid, np.ascontiguousarray(self.W[:, v0:v1]))
+            if i == self.units - 1:
+                self._accept_commit()
+        else:
+            # sampled acceptance alone: one sequence per unit
+            b = i
+            if self.mode == "greedy":
+                o.accept_greedy(self.logits[b:b + 1], self.tok[b:b + 1])
+            else:
+                o.accept_sample(self.logits[b:b + 1], self.qd[b:b + 1], self.tok[b:b + 1], seed=0x5EED)
+
+    def _accept_commit(self):
+        o, w = self.oracle, self.w
+        if self.mode == "greedy":
+            n_acc, _, path = o.accept_greedy(self.logits, self.tok)
+        else:
+            n_acc, _, path = o.accept_sample(self.logits, self.qd, self.tok, seed=0x5EED)
+        # commit of every layer: the same per-layer copy, done L times
+        for _ in range(w.L):
+            o.kv_commit(self.kc[None], self.vc[None], self.kb[None], self.vb[None], path, n_acc,
+                        np.full(w.B, w.t, np.int32))
+
+
+def time_oracle(w, mode, units_total: int):
+    orc = OracleRound(w, mode)
+    orc.run_unit(0)   # warm the library and caches
+    t0 = time.perf_counter()
+    for i in range(units_total):
+        orc.run_unit(i)
+    dt = time.perf_counter() - t0
+    steps = units_total / orc.units
+    return steps / dt, orc, dt
+
+
+def cpu_baseline(w, mode, seconds=12.0):
+    orc = OracleRound(w, mode)
+    t0 = time.perf_counter()
+    orc.run_unit(0)
+    per_unit = max(time.perf_counter() - t0, 1e-4)
+    units = max(orc.units, int(seconds / per_unit))
+    units = min(units, 3 * orc.units)
+    value, orc, dt = time_oracle(w, mode, units)
+    return {"value": value, "unit": "steps/s", "cores": orc.oracle.num_threads(), "kind": "oracle",
+            "sample": f"{units} of the {orc.units} equal work units of one round "
+                      f"({units / orc.units:.2f} rounds, {dt:.1f} s of host time), scaled to rounds/s"}
+
+
+# ----------------------------------------------------------------------------
+# main
+# ----------------------------------------------------------------------------
+
+def dist_setup():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return ws, rank, local
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, ws: int, device) -> float:
+    if ws == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def config_dict(w, mode, ws, chunk):
+    return {"workload": w.name if mode == "greedy" or w.L == 0 else w.name.replace("greedy", "sampled"),
+            "layers": w.L, "batch": w.B, "k": w.R - 1, "context": w.t, "q_heads": w.Hq, "kv_heads": w.Hkv,
+            "head_dim": w.D, "hidden": w.H, "vocab": w.V, "acceptance": mode, "parallelism": f"replicas{ws}",
+            "l2": "inputs larger than L2 every step (no flush)", "graph_chunk": chunk}
+
+
+def run_reference(args, ws, rank):
+    if rank != 0:
+        return
+    w, mode = workload_from_name(args.workload)
+    orc = OracleRound(w, mode)
+    t0 = time.perf_counter()
+    orc.run_unit(0)
+    per_unit = max(time.perf_counter() - t0, 1e-4)
+    budget = 150.0
+    per_step_units = max(1, min(orc.units, int(budget / max(1, args.steps + args.warmup) / per_unit)))
+    for i in range(args.warmup):
+        for j in range(per_step_units):
+            orc.run_unit(i * per_step_units + j)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        for j in range(per_step_units):
+            orc.run_unit(i * per_step_units + j)
+    dt = time.perf_counter() - t0
+    rounds = args.steps * per_step_units / orc.units
+    value = rounds / dt
+    sample = (f"each step = {per_step_units} of the {orc.units} equal work units of one round; "
+              f"{rounds:.3f} rounds in {dt:.1f} s, scaled to rounds/s")
+    line = {"metric": "verify steps/s", "value": value, "unit": "steps/s", "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": 1000.0 * dt / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64 attention/LM head, f32 acceptance",
+            "data": "synthetic", "impl": "reference", "config": config_dict(w, mode, ws, 0),
+            "draft_tokens_per_s": value * w.B * (w.R - 1),
+            "cpu_baseline": {"value": value, "unit": "steps/s", "cores": orc.oracle.num_threads(),
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "steps/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="1")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=500)
+    args = ap.parse_args()
+    ws, rank, local = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, ws, rank)
+        if ws > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return
+    args.warmup = max(args.warmup, 3)
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    w, mode = workload_from_name(args.workload)
+    rnd = Round(w, mode, dev)
+
+    K = args.steps
+    chunk = max(d for d in range(1, min(100, K) + 1) if K % d == 0)
+    stream = torch.cuda.Stream(device=dev)
+    kinds = ["attn0", "attn1", "lm1", "acc1", "commit1"]
+    torch.cuda.synchronize()
+    # eager warm-up (library attributes, tensor-map driver entry point)
+    with torch.cuda.stream(stream):
+        rnd.step()
+    torch.cuda.synchronize()
+    g1 = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g1, stream=stream):
+        rnd.step()
+    try:
+        evs = [{k: torch.cuda.Event(enable_timing=True, external=True) for k in kinds} for _ in range(chunk)]
+        in_graph_events = True
+    except TypeError:   # torch without external (graph-node) events
+        evs = [{k: torch.cuda.Event(enable_timing=True) for k in kinds} for _ in range(chunk)]
+        in_graph_events = False
+    gC = torch.cuda.CUDAGraph()          # chunk rounds, no events
+    with torch.cuda.graph(gC, stream=stream):
+        for i in range(chunk):
+            rnd.step()
+    gE = gC
+    if in_graph_events:                  # the same chunk with event nodes (last replay only)
+        gE = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gE, stream=stream):
+            for i in range(chunk):
+                rnd.step(evs[i])
+    torch.cuda.synchronize()
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            g1.replay()
+    torch.cuda.synchronize()
+
+    clocks = ClockSampler(device_uuid(dev))
+    clocks.start()
+    time.sleep(0.3)
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    barrier(ws)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        t_start.record()
+        for _ in range(K // chunk - 1):
+            gC.replay()
+        gE.replay()
+        t_end.record()
+    torch.cuda.synchronize()
+    barrier(ws)
+    clk = clocks.stop()
+    ms_local = t_start.elapsed_time(t_end)
+    ms_total = max_over_ranks(ms_local, ws, dev)
+    ms_per_step = ms_total / K
+    value = ws * K / (ms_total / 1000.0)
+
+    # per-kernel durations from the event nodes of the last replay (or, without
+    # graph-node events, from `chunk` eager rounds timed the same way)
+    if not in_graph_events:
+        with torch.cuda.stream(stream):
+            for i in range(chunk):
+                rnd.step(evs[i])
+        torch.cuda.synchronize()
+
+    def avg(a, b):
+        return statistics.mean(evs[i][a].elapsed_time(evs[i][b]) for i in range(chunk)) / 1000.0
+    t_attn = avg("attn0", "attn1")
+    t_lm = avg("attn1", "lm1")
+    t_acc = avg("lm1", "acc1")
+    t_commit = avg("acc1", "commit1")
+    n_acc = rnd.n_acc.cpu().numpy()
+    hbm, peak_kind = load_peaks()
+    kern = {}
+    if w.L > 0:
+        kern["verify_attn"] = {"launches_per_step": w.L, "bytes_per_launch": attn_bytes(w),
+                               "us_per_launch": 1e6 * t_attn / w.L,
+                               "gbs": attn_bytes(w) * w.L / t_attn / 1e9}
+        kern["lm_head"] = {"launches_per_step": 1, "bytes_per_launch": lm_bytes(w), "us_per_launch": 1e6 * t_lm,
+                           "gbs": lm_bytes(w) / t_lm / 1e9}
+        kern["kv_commit"] = {"launches_per_step": 1, "bytes_per_launch": commit_bytes(w, n_acc),
+                             "us_per_launch": 1e6 * t_commit, "gbs": commit_bytes(w, n_acc) / t_commit / 1e9}
+    ab = greedy_bytes(w) if mode == "greedy" else sample_bytes(w, n_acc)
+    kern["accept_" + mode] = {"launches_per_step": 1, "bytes_per_launch": ab, "us_per_launch": 1e6 * t_acc,
+                              "gbs": ab / t_acc / 1e9}
+    for v in kern.values():
+        v["frac_of_peak"] = v["gbs"] / hbm
+    dom = max(kern, key=lambda k: kern[k]["bytes_per_launch"] * kern[k]["launches_per_step"])
+    dk = kern[dom]
+    src = {"lm_head": "lm_head.cu", "verify_attn": "verify_attn.cu", "accept_greedy": "accept.cu",
+           "accept_sampled": "accept.cu", "kv_commit": "kv_commit.cu"}[dom]
+    tr = TRAFFIC.get(dom)
+    traffic = tr["bytes"] if tr and tr["src_hash"] == src_hash(src) else None
+    roofline = {"kernel": dom, "bound": "hbm", "achieved": dk["gbs"], "peak": hbm, "unit": "GB/s",
+                "frac": dk["gbs"] / hbm, "traffic": traffic, "peak_source": f"hbm_gbs of {peak_kind}",
+                "bytes_per_launch": dk["bytes_per_launch"], "us_per_launch": dk["us_per_launch"],
+                "timing": "CUDA-event nodes inside the timed graph" if in_graph_events else "eager rounds with events"}
+
+    # end to end through the public API: pinned H2D of the round's inputs, one
+    # replay of the captured round, D2H of the accepted tokens, host sync
+    ins = rnd.step_inputs()
+    outs = rnd.step_outputs()
+    h_in = [t.detach().cpu().pin_memory() for t in ins]
+    h_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
+    h2d = sum(t.numel() * t.element_size() for t in ins)
+    d2h = sum(t.numel() * t.element_size() for t in outs)
+    E = args.e2e_steps
+    done = torch.cuda.Event()
+    for phase in ("warm", "timed"):
+        n = 5 if phase == "warm" else E
+        barrier(ws)
+        t0 = time.perf_counter()
+        for _ in range(n):
+            with torch.cuda.stream(stream):
+                for d, h in zip(ins, h_in):
+                    d.copy_(h, non_blocking=True)
+                g1.replay()
+                for h, d in zip(h_out, outs):
+                    h.copy_(d, non_blocking=True)
+                done.record()
+            done.synchronize()
+        e2e_s = time.perf_counter() - t0
+    e2e_s = max_over_ranks(e2e_s, ws, dev)
+    e2e = {"value": ws * E / e2e_s, "unit": "steps/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+           "steps": E, "how": "pinned H2D of the round's inputs + CUDA-graph replay of the C-ABI calls + "
+                              "D2H of n_acc/out_tok/path + host sync, every step"}
+
+    line = {"metric": "verify steps/s", "value": value, "unit": "steps/s", "n_gpus": ws, "steps": K,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16 (fp32 accumulate; fp32 acceptance)",
+            "data": "synthetic (seeded, Qwen2.5-shaped, random weights)",
+            "config": config_dict(w, mode, ws, chunk),
+            "draft_tokens_per_s": value * w.B * (w.R - 1),
+            "mean_accepted": float(np.mean(n_acc)),
+            "roofline": roofline, "kernels": kern, "e2e": e2e, "clocks": clk,
+            "gpu_launches": rnd.launches_per_step() * K}
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, mode)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -669,9 +669,14 @@ cudaError_t launch_accept_sample(const float* logits, const float* q, int Vq, co
     const int nblk = blocks_for(V);
     const int nlocal = (nblk + kCluster - 1) / kCluster;
     const size_t smem = static_cast<size_t>(nlocal) * kBlk * sizeof(float);
-    cudaError_t e = cudaFuncSetAttribute(sample_stats_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
+    cudaError_t e = cudaSuccess;
+    static bool attr_set = false;   // once per process: the largest row (2^18 entries) fits
+    if (!attr_set) {
+        e = cudaFuncSetAttribute(sample_stats_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kMaxLocalBlocks * kBlk * static_cast<int>(sizeof(float)));
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
     float2* stats = static_cast<float2*>(ws);
     sample_stats_kernel<<<B * R * kCluster, kThreads, smem, st>>>(logits, V, temperature, nblk, nlocal, stats, err);
     if (debug_sync()) {
