@@ -204,6 +204,26 @@ SV_API sv_status sv_accept_sample(const float* logits, const float* q, int32_t V
                            uint64_t seed, uint64_t step, const float* uniforms, int32_t* n_acc,
                            int32_t* out_tok, int32_t* path, void* ws, size_t ws_bytes, void* stream);
 
+/* sv_accept_sample without a workspace argument, for callers that cannot
+ * allocate device memory (for example a plugin that is handed only its input
+ * and output buffers by a host framework owning all device memory, or a loop
+ * that must not call an allocating routine while it runs).  The pages have no
+ * counterpart for this entry point; it exists for those callers only.
+ * Behaviour and outputs are those of sv_accept_sample.  Its scratch is a
+ * fixed 64 KiB device array (8192 rows of statistics) inside the library:
+ *   - B*R above 8192 returns SV_ERR_SHAPE before anything is enqueued;
+ *   - every GPU that loads the library holds the array until the process exits;
+ *   - all calls share the array and it keeps the last call's contents (no
+ *     entry needs to start at zero); calls that overlap on the GPU race on it,
+ *     so order them on one stream or with events;
+ *   - the first call on a device looks up the array's device address and
+ *     caches it; make that first call before any stream capture.
+ * No cudaMalloc, cudaFree or other allocating call is made. */
+SV_API sv_status sv_accept_sample_noalloc(const float* logits, const float* q, int32_t Vq, const int32_t* tok,
+                                          const int32_t* parent, int32_t B, int32_t R, int32_t V,
+                                          float temperature, uint64_t seed, uint64_t step, const float* uniforms,
+                                          int32_t* n_acc, int32_t* out_tok, int32_t* path, void* stream);
+
 /* ------------------------------------------------------------------------ */
 /* KV commit ([SCS] sec. 3.2; [TUT] sec. 3.2; [MINI] hidden KV position bug, */
 /* "v2"; [SUB] sec. 4.1).                                                    */

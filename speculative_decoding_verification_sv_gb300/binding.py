@@ -53,11 +53,14 @@ def _load():
     L.sv_accept_sample_workspace.restype = _SZ
     L.sv_accept_sample.argtypes = [_P, _P, _I32, _P, _P, _I32, _I32, _I32, _F32, _U64, _U64, _P, _P, _P, _P, _P,
                                    _SZ, _P]
+    L.sv_accept_sample_noalloc.argtypes = [_P, _P, _I32, _P, _P, _I32, _I32, _I32, _F32, _U64, _U64, _P, _P, _P,
+                                           _P, _P]
     L.sv_kv_commit.argtypes = [_P, _P, _P, _P, _I32, _I32, _I32, _I32, _I32, _I32, _P, _P, _P, _P]
     L.sv_diag_exp.argtypes = [_P, _P, _I64, _P]
     L.sv_diag_philox.argtypes = [_P, _P, _P, _I64, _P]
     L.sv_diag_canon.argtypes = [_P, _I32, _I32, _P, _P, _P, _P]
-    for fn in ("sv_verify_attn", "sv_lm_head", "sv_accept_greedy", "sv_accept_sample", "sv_kv_commit",
+    for fn in ("sv_verify_attn", "sv_lm_head", "sv_accept_greedy", "sv_accept_sample", "sv_accept_sample_noalloc",
+               "sv_kv_commit",
                "sv_diag_exp", "sv_diag_philox", "sv_diag_canon", "sv_get_device_error"):
         getattr(L, fn).restype = ctypes.c_int
     return L
@@ -180,6 +183,22 @@ def accept_sample(logits, q, tok, parent=None, temperature=1.0, seed=0, step=0, 
         B, R, V, float(temperature), int(seed) & (2 ** 64 - 1), int(step) & (2 ** 64 - 1),
         _ptr(uniforms, f32, "uniforms"), _ptr(n_acc, i32), _ptr(out_tok, i32), _ptr(path, i32), _ptr(ws), nbytes,
         _stream(stream)))
+    return n_acc, out_tok, path
+
+
+def accept_sample_noalloc(logits, q, tok, parent=None, temperature=1.0, seed=0, step=0, uniforms=None, n_acc=None,
+                          out_tok=None, path=None, stream=None):
+    """accept_sample for callers that cannot allocate device memory: the
+    library's fixed scratch array replaces the workspace (B*R <= 8192; calls
+    overlapping on the GPU race on it)."""
+    B, R, V = logits.shape
+    Vq = q.shape[-1]
+    n_acc, out_tok, path = _accept_outputs(B, R, logits.device, n_acc, out_tok, path)
+    i32, f32 = torch.int32, torch.float32
+    _check("sv_accept_sample_noalloc", lib.sv_accept_sample_noalloc(
+        _ptr(logits, f32, "logits"), _ptr(q, f32, "q"), Vq, _ptr(tok, i32, "tok"), _ptr(parent, i32, "parent"),
+        B, R, V, float(temperature), int(seed) & (2 ** 64 - 1), int(step) & (2 ** 64 - 1),
+        _ptr(uniforms, f32, "uniforms"), _ptr(n_acc, i32), _ptr(out_tok, i32), _ptr(path, i32), _stream(stream)))
     return n_acc, out_tok, path
 
 
