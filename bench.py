@@ -157,7 +157,7 @@ class Round:
     def launches_per_step(self) -> int:
         n = 0
         if self.has_model:
-            n += 2 * self.w.L                        # split kernel + combine per layer
+            n += self.w.L                            # one cluster kernel per layer
             n += (self.w.B * self.w.R + 63) // 64    # LM head passes of <= 64 rows
             n += 1                                   # commit
         n += 2                                       # accept: two kernels
@@ -448,6 +448,7 @@ def main():
     ap.add_argument("--workload", default="1")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=500)
+    ap.add_argument("--layers", type=int, default=None, help="override the layer count (small profiling cases)")
     args = ap.parse_args()
     ws, rank, local = dist_setup()
     if args.impl == "reference":
@@ -460,6 +461,9 @@ def main():
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     w, mode = workload_from_name(args.workload)
+    if args.layers is not None:
+        from dataclasses import replace
+        w = replace(w, L=args.layers, name=w.name.replace("28-layer", f"{args.layers}-layer"))
     rnd = Round(w, mode, dev)
 
     K = args.steps

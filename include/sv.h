@@ -110,7 +110,9 @@ typedef struct sv_attn_shape {
     int32_t T_cap;  /* cache capacity per (sequence, KV head) */
 } sv_attn_shape;
 
-/* Workspace bytes sv_verify_attn needs for this shape (split-KV partials). */
+/* Workspace bytes sv_verify_attn needs for this shape.  The split-KV partials
+ * are merged on chip, so this is currently 0 and ws may be NULL; the argument
+ * is kept so a future plan may use global scratch without an ABI change. */
 SV_API size_t sv_verify_attn_workspace(const sv_attn_shape* shape);
 
 /* For sequence b, query head h (KV head g = h / (Hq/Hkv), heads grouped

@@ -145,10 +145,11 @@ sv_status sv_verify_attn(const sv_attn_shape* shape, const uint16_t* q, const ui
                          void* stream) {
     const sv_status st = check_attn_shape(shape);
     if (st != SV_OK) return st;
-    if (!q || !k_cache || !v_cache || !len || !k_blk || !v_blk || !out || !ws) return SV_ERR_ARG;
+    if (!q || !k_cache || !v_cache || !len || !k_blk || !v_blk || !out) return SV_ERR_ARG;
     if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(k_blk) || !aligned16(v_blk) ||
-        !aligned16(out) || !aligned16(ws))
+        !aligned16(out) || (ws && !aligned16(ws)))
         return SV_ERR_ARG;
+    if (!ws && sv::attn_workspace(*shape) > 0) return SV_ERR_ARG;
     if (!(scale > 0.0f)) return SV_ERR_ARG;
     if (ws_bytes < sv::attn_workspace(*shape)) return SV_ERR_WORKSPACE;
     return launch_status(sv::launch_verify_attn(*shape, q, k_cache, v_cache, len, k_blk, v_blk, parent, scale, out,

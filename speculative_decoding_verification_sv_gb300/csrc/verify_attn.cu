@@ -7,23 +7,34 @@
 // positions at once; [SubSpec summary, sec. 4.2]: for a draft tree row j sees
 // its ancestors instead.
 //
-// Decomposition: for every (sequence b, KV head g) the R*G query rows of the
+// Decomposition.  For every (sequence b, KV head g) the R*G query rows of the
 // G query heads that share g are packed together (row r = j*G + local head),
-// so each K/V tile streamed from HBM serves all of them (GQA).  The context
-// is split into `splits` equal chunks (flash-decoding style split-KV, sized
-// so the grid covers the SMs); one extra split handles the R block rows with
-// the chain or tree mask.  Each CTA:
+// so each K/V tile streamed from HBM serves all of them (GQA); rows are cut
+// into tiles of 64.  One thread-block cluster of C CTAs (C up to 16) handles
+// one (b, g, row tile): the key tiles -- ceil(t/64) context tiles followed by
+// ceil(R/64) block tiles -- are split evenly over the C CTAs (split-KV over the
+// context, sized so the grid fills the SMs).  Each CTA:
 //   * streams 64-key K and V tiles through a TMA (cp.async.bulk.tensor, 128B
 //     swizzle) ring of mbarrier-tracked stages;
 //   * computes S = Q K^T and O += P V on the tensor cores (mma.sync bf16,
-//     fp32 accumulate; Q fragments stay in registers for the whole split);
+//     fp32 accumulate; Q fragments stay in registers);
 //   * keeps an online softmax per row in registers (quad shuffles);
-//   * writes its unnormalised partial (max, sum, o) to the workspace.
-// attn_combine_kernel merges the splits of every row and rounds to bf16.
+//   * leaves its unnormalised partial (max, sum, o[128]) in shared memory.
+// The cluster then merges the C partials of every row through distributed
+// shared memory (each CTA merges every C-th row) and writes bf16 rows.  No
+// partial goes through global memory and there is no second kernel.
+//
+// Launch: programmatic dependent launch -- the CTA prologue (barrier set-up,
+// descriptor prefetch) overlaps the previous kernel; everything the previous
+// kernels may have written (lengths, cache rows, Q, block K/V, tree) is read
+// only after griddepcontrol.wait.
+#include <cooperative_groups.h>
 #include <math.h>
 
 #include "sv_device.cuh"
 #include "sv_internal.h"
+
+namespace cg = cooperative_groups;
 
 namespace sv {
 namespace {
@@ -35,67 +46,66 @@ constexpr int kTileBytes = kKT * kD * 2; // 16 KB: two 64x64 swizzled boxes
 constexpr int kStageBytes = 2 * kTileBytes;
 constexpr int kRec = kD + 4;             // partial record: m, l, 2 pad, o[128] (16-byte aligned)
 constexpr int kMaxR = 128;
+constexpr int kMaxCluster = 16;
 constexpr int kSmemBytes = kStages * kStageBytes + kStages * 8 + kMaxR * 16 + 1024;
+static_assert(64 * kRec * 4 <= kStages * kStageBytes, "partials reuse the stage ring");
 
 struct AttnArgs {
     const uint16_t* q;
     const int32_t* len;
     const int32_t* parent;
-    float* part;
+    uint16_t* out;
     unsigned int* err;
-    int B, R, Hq, Hkv, G, T_cap, rows, row_tiles, splits;
+    int B, R, Hq, Hkv, G, T_cap, rows, row_tiles;
     float scale_log2;
 };
 
-__global__ void __launch_bounds__(128) attn_split_kernel(const __grid_constant__ CUtensorMap tmK,
-                                                        const __grid_constant__ CUtensorMap tmV,
-                                                        const __grid_constant__ CUtensorMap tmKb,
-                                                        const __grid_constant__ CUtensorMap tmVb, AttnArgs a) {
+__global__ void __launch_bounds__(128) attn_cluster_kernel(const __grid_constant__ CUtensorMap tmK,
+                                                          const __grid_constant__ CUtensorMap tmV,
+                                                          const __grid_constant__ CUtensorMap tmKb,
+                                                          const __grid_constant__ CUtensorMap tmVb, AttnArgs a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
     uint64_t* anc = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes + kStages * 8);   // [kMaxR][2]
+    float* part = reinterpret_cast<float*>(smem);                                              // [64][kRec] after the loop
 
+    cg::cluster_group cluster = cg::this_cluster();
+    const int C = static_cast<int>(cluster.num_blocks());
+    const int rank = static_cast<int>(cluster.block_rank());
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int split = blockIdx.x, hg = blockIdx.y, rt = blockIdx.z;
+    const int nwarps = blockDim.x >> 5;
+    const int hg = blockIdx.y, rt = blockIdx.z;
     const int b = hg / a.Hkv, g = hg % a.Hkv;
-    const bool is_block = split == a.splits;
-
-    int t = a.len[b];
-    if (t < 0 || t > a.T_cap) {
-        if (tid == 0 && split == 0 && rt == 0 && g == 0) raise_error(a.err, SV_DEVERR_LENGTH);
-        t = t < 0 ? 0 : a.T_cap;
-    }
-    int k_begin, nkeys;
-    const void* tk;
-    const void* tv;
-    int row0;
-    if (!is_block) {
-        int chunk = (t + a.splits - 1) / a.splits;
-        chunk = ((chunk + kKT - 1) / kKT) * kKT;
-        if (chunk < kKT) chunk = kKT;
-        k_begin = split * chunk;
-        const int k_end = min(t, k_begin + chunk);
-        nkeys = k_end > k_begin ? k_end - k_begin : 0;
-        tk = &tmK;
-        tv = &tmV;
-        row0 = hg * a.T_cap + k_begin;
-    } else {
-        k_begin = 0;
-        nkeys = a.R;
-        tk = &tmKb;
-        tv = &tmVb;
-        row0 = hg * a.R;
-    }
-    const int ntiles = (nkeys + kKT - 1) / kKT;
 
     if (tid == 0) {
+        prefetch_tmap(&tmK);
+        prefetch_tmap(&tmV);
+        prefetch_tmap(&tmKb);
+        prefetch_tmap(&tmVb);
         for (int s = 0; s < kStages; ++s) mbar_init(&full[s], 1);
         fence_mbar_init();
     }
-    // tree ancestor masks (block split only): bit i of anc[j] set iff block
-    // row i is j itself or one of its ancestors
-    if (is_block && a.parent) {
+    // Inputs may come from the kernels before this one.
+    pdl_wait();
+    pdl_launch_dependents();
+
+    int t = a.len[b];
+    if (t < 0 || t > a.T_cap) {
+        if (tid == 0 && rank == 0 && rt == 0) raise_error(a.err, SV_DEVERR_LENGTH);
+        t = t < 0 ? 0 : a.T_cap;
+    }
+    const int n_ctx = (t + kKT - 1) / kKT;
+    const int n_blk = (a.R + kKT - 1) / kKT;
+    const int n_all = n_ctx + n_blk;
+    const int first = static_cast<int>((static_cast<int64_t>(n_all) * rank) / C);
+    const int last = static_cast<int>((static_cast<int64_t>(n_all) * (rank + 1)) / C);
+    const int ntiles = last - first;
+
+    // tree ancestor masks: bit i of anc[j] set iff block row i is j or one of
+    // its ancestors (only CTAs that own a block tile need them)
+    const bool has_block = last > n_ctx;
+    if (has_block && a.parent) {
         const int32_t* par = a.parent + static_cast<size_t>(b) * a.R;
         for (int j = tid; j < a.R; j += blockDim.x) {
             uint64_t m0 = 0, m1 = 0;
@@ -118,10 +128,13 @@ __global__ void __launch_bounds__(128) attn_split_kernel(const __grid_constant__
     }
     __syncthreads();
 
-    auto issue = [&](int it) {
-        const int s = it % kStages;
+    auto issue = [&](int i) {
+        const int s = i % kStages;
+        const int gt = first + i;
         uint8_t* st = smem + s * kStageBytes;
-        const int y = row0 + it * kKT;
+        const void* tk = gt < n_ctx ? static_cast<const void*>(&tmK) : static_cast<const void*>(&tmKb);
+        const void* tv = gt < n_ctx ? static_cast<const void*>(&tmV) : static_cast<const void*>(&tmVb);
+        const int y = gt < n_ctx ? hg * a.T_cap + gt * kKT : hg * a.R + (gt - n_ctx) * kKT;
         mbar_arrive_expect_tx(&full[s], kStageBytes);
         tma_load_2d(st, tk, 0, y, &full[s]);
         tma_load_2d(st + kKT * 128, tk, 64, y, &full[s]);
@@ -129,9 +142,9 @@ __global__ void __launch_bounds__(128) attn_split_kernel(const __grid_constant__
         tma_load_2d(st + kTileBytes + kKT * 128, tv, 64, y, &full[s]);
     };
     if (tid == 0)
-        for (int it = 0; it < ntiles && it < kStages; ++it) issue(it);
+        for (int i = 0; i < ntiles && i < kStages; ++i) issue(i);
 
-    // rows owned by this warp: ra = rb + lane/4 and rb_ = ra + 8
+    // rows owned by this warp: ra = rbase + lane/4 and rb = ra + 8
     const int rbase = rt * 64 + warp * 16;
     const bool active = rbase < a.rows;
     const int ra = rbase + (lane >> 2), rb = ra + 8;
@@ -158,14 +171,18 @@ __global__ void __launch_bounds__(128) attn_split_kernel(const __grid_constant__
 #pragma unroll
         for (int e = 0; e < 4; ++e) o[i][e] = 0.f;
 
-    const uint64_t anc_a0 = (is_block && a.parent && ra < a.rows) ? anc[2 * ja] : 0;
-    const uint64_t anc_a1 = (is_block && a.parent && ra < a.rows) ? anc[2 * ja + 1] : 0;
-    const uint64_t anc_b0 = (is_block && a.parent && rb < a.rows) ? anc[2 * jb] : 0;
-    const uint64_t anc_b1 = (is_block && a.parent && rb < a.rows) ? anc[2 * jb + 1] : 0;
+    const bool tree = a.parent != nullptr && has_block;
+    const uint64_t anc_a0 = (tree && ra < a.rows) ? anc[2 * ja] : 0;
+    const uint64_t anc_a1 = (tree && ra < a.rows) ? anc[2 * ja + 1] : 0;
+    const uint64_t anc_b0 = (tree && rb < a.rows) ? anc[2 * jb] : 0;
+    const uint64_t anc_b1 = (tree && rb < a.rows) ? anc[2 * jb + 1] : 0;
 
     for (int it = 0; it < ntiles; ++it) {
         const int s = it % kStages;
         mbar_wait(&full[s], (it / kStages) & 1, a.err);
+        const int gt = first + it;
+        const bool is_block = gt >= n_ctx;
+        const int k0 = is_block ? (gt - n_ctx) * kKT : gt * kKT;   // first key of the tile
         if (active) {
             const uint32_t kbase = smem_u32(smem + s * kStageBytes);
             const uint32_t vbase = kbase + kTileBytes;
@@ -193,14 +210,14 @@ __global__ void __launch_bounds__(128) attn_split_kernel(const __grid_constant__
             for (int nt = 0; nt < 8; ++nt)
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    const int kl = it * kKT + nt * 8 + 2 * (lane & 3) + (e & 1);
+                    const int kl = k0 + nt * 8 + 2 * (lane & 3) + (e & 1);
                     const bool row_a = e < 2;
                     bool vis;
                     if (!is_block) {
-                        vis = kl < nkeys;
+                        vis = kl < t;
                     } else if (kl >= a.R) {
                         vis = false;
-                    } else if (a.parent) {
+                    } else if (tree) {
                         const uint64_t w = kl < 64 ? (row_a ? anc_a0 : anc_b0) : (row_a ? anc_a1 : anc_b1);
                         vis = (w >> (kl & 63)) & 1ull;
                     } else {
@@ -262,67 +279,63 @@ __global__ void __launch_bounds__(128) attn_split_kernel(const __grid_constant__
         if (tid == 0 && it + kStages < ntiles) issue(it + kStages);
     }
 
-    if (!active) return;
-    l_a += __shfl_xor_sync(0xffffffffu, l_a, 1);
-    l_a += __shfl_xor_sync(0xffffffffu, l_a, 2);
-    l_b += __shfl_xor_sync(0xffffffffu, l_b, 1);
-    l_b += __shfl_xor_sync(0xffffffffu, l_b, 2);
-    const int nsplit = a.splits + 1;
-    const size_t rows_pad = static_cast<size_t>(a.row_tiles) * 64;
-    if (ra < a.rows) {
-        float* rec = a.part + ((static_cast<size_t>(hg) * rows_pad + ra) * nsplit + split) * kRec;
+    // this CTA's partial -> shared memory (the stage ring is free now)
+    if (active) {
+        l_a += __shfl_xor_sync(0xffffffffu, l_a, 1);
+        l_a += __shfl_xor_sync(0xffffffffu, l_a, 2);
+        l_b += __shfl_xor_sync(0xffffffffu, l_b, 1);
+        l_b += __shfl_xor_sync(0xffffffffu, l_b, 2);
+        float* rec_a = part + (ra - rt * 64) * kRec;
+        float* rec_b = part + (rb - rt * 64) * kRec;
         if ((lane & 3) == 0) {
-            rec[0] = m_a;
-            rec[1] = l_a;
+            rec_a[0] = m_a;
+            rec_a[1] = l_a;
+            rec_b[0] = m_b;
+            rec_b[1] = l_b;
         }
 #pragma unroll
-        for (int dt = 0; dt < 16; ++dt)
-            *reinterpret_cast<float2*>(rec + 4 + dt * 8 + 2 * (lane & 3)) = make_float2(o[dt][0], o[dt][1]);
-    }
-    if (rb < a.rows) {
-        float* rec = a.part + ((static_cast<size_t>(hg) * rows_pad + rb) * nsplit + split) * kRec;
-        if ((lane & 3) == 0) {
-            rec[0] = m_b;
-            rec[1] = l_b;
+        for (int dt = 0; dt < 16; ++dt) {
+            *reinterpret_cast<float2*>(rec_a + 4 + dt * 8 + 2 * (lane & 3)) = make_float2(o[dt][0], o[dt][1]);
+            *reinterpret_cast<float2*>(rec_b + 4 + dt * 8 + 2 * (lane & 3)) = make_float2(o[dt][2], o[dt][3]);
         }
-#pragma unroll
-        for (int dt = 0; dt < 16; ++dt)
-            *reinterpret_cast<float2*>(rec + 4 + dt * 8 + 2 * (lane & 3)) = make_float2(o[dt][2], o[dt][3]);
     }
-}
+    cluster.sync();   // all partials written (and every CTA of the cluster has started)
 
-// One warp per (sequence, KV head, row): merge the splits, normalise, round.
-__global__ void __launch_bounds__(128) attn_combine_kernel(const float* __restrict__ part, uint16_t* __restrict__ out,
-                                                          int B, int R, int Hq, int Hkv, int G, int rows,
-                                                          int row_tiles, int nsplit) {
-    const int wid = blockIdx.x * 4 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
-    if (wid >= B * Hkv * rows) return;
-    const int hg = wid / rows, r = wid % rows;
-    const int b = hg / Hkv, g = hg % Hkv;
-    const float* rec0 = part + (static_cast<size_t>(hg) * row_tiles * 64 + r) * nsplit * kRec;
-    float M = -INFINITY;
-    for (int s = 0; s < nsplit; ++s) M = fmaxf(M, rec0[s * kRec]);
-    float L = 0.f;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (M != -INFINITY) {
-        for (int s = 0; s < nsplit; ++s) {
-            const float* rec = rec0 + s * kRec;
-            const float l = rec[1];
-            if (l == 0.f) continue;
-            const float w = exp2f(rec[0] - M);
-            L += l * w;
-            const float4 x = *reinterpret_cast<const float4*>(rec + 4 + 4 * lane);
-            acc.x += w * x.x;
-            acc.y += w * x.y;
-            acc.z += w * x.z;
-            acc.w += w * x.w;
+    // merge: this CTA finalises rows rank, rank + C, ... of the row tile
+    const int nrows = min(64, a.rows - rt * 64);
+    for (int lr = rank + C * warp; lr < nrows; lr += C * nwarps) {
+        float ms = -INFINITY, ls = 0.f;
+        const float* rec_s = nullptr;
+        if (lane < C) {
+            rec_s = cluster.map_shared_rank(part + lr * kRec, lane);
+            ms = rec_s[0];
+            ls = rec_s[1];
         }
+        float M = ms;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+        const float wgt = (lane < C && ls > 0.f && M != -INFINITY) ? exp2f(ms - M) : 0.f;
+        float L = wgt * ls;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int s = 0; s < C; ++s) {
+            const float ws = __shfl_sync(0xffffffffu, wgt, s);
+            if (ws == 0.f) continue;
+            const float4 x = *reinterpret_cast<const float4*>(cluster.map_shared_rank(part + lr * kRec + 4, s) + 4 * lane);
+            acc.x += ws * x.x;
+            acc.y += ws * x.y;
+            acc.z += ws * x.z;
+            acc.w += ws * x.w;
+        }
+        const float inv = L > 0.f ? 1.0f / L : 0.f;
+        const int r = rt * 64 + lr;
+        const int j = r / a.G, h = g * a.G + r % a.G;
+        uint16_t* dst = a.out + ((static_cast<size_t>(b) * a.R + j) * a.Hq + h) * kD + 4 * lane;
+        *reinterpret_cast<uint2*>(dst) =
+            make_uint2(pack_bf16x2(acc.x * inv, acc.y * inv), pack_bf16x2(acc.z * inv, acc.w * inv));
     }
-    const float inv = L > 0.f ? 1.0f / L : 0.f;
-    const int j = r / G, h = g * G + r % G;
-    uint16_t* dst = out + ((static_cast<size_t>(b) * R + j) * Hq + h) * kD + 4 * lane;
-    const uint32_t lo = pack_bf16x2(acc.x * inv, acc.y * inv), hi = pack_bf16x2(acc.z * inv, acc.w * inv);
-    *reinterpret_cast<uint2*>(dst) = make_uint2(lo, hi);
+    cluster.sync();   // no CTA leaves while its partials may still be read
 }
 
 }  // namespace
@@ -333,25 +346,23 @@ AttnPlan attn_plan(const sv_attn_shape& s) {
     p.rows = s.R * p.G;
     p.row_tiles = (p.rows + 63) / 64;
     p.warps = p.row_tiles > 1 ? 4 : (p.rows + 15) / 16;
+    // cluster size: grow while the grid still fits in two CTAs per SM and
+    // every CTA keeps at least one key tile
     const int units = s.B * s.Hkv * p.row_tiles;
-    const int target = 2 * device_sm_count();
-    int splits = (target + units - 1) / units;
-    const int max_splits = (s.T_cap + kKT - 1) / kKT;
-    if (splits > max_splits) splits = max_splits;
-    if (splits < 1) splits = 1;
-    p.splits = splits;
+    const int slots = 2 * device_sm_count();
+    const int tiles = (s.T_cap + kKT - 1) / kKT + (s.R + kKT - 1) / kKT;
+    int C = 1;
+    while (C < kMaxCluster && units * C * 2 <= slots && C * 2 <= tiles) C *= 2;
+    p.splits = C;
     return p;
 }
 
-size_t attn_workspace(const sv_attn_shape& s) {
-    const AttnPlan p = attn_plan(s);
-    return static_cast<size_t>(s.B) * s.Hkv * p.row_tiles * 64 * (p.splits + 1) * kRec * sizeof(float);
-}
+size_t attn_workspace(const sv_attn_shape&) { return 0; }
 
 cudaError_t launch_verify_attn(const sv_attn_shape& s, const uint16_t* q, const uint16_t* k_cache,
                                const uint16_t* v_cache, const int32_t* len, const uint16_t* k_blk,
                                const uint16_t* v_blk, const int32_t* parent, float scale, uint16_t* out,
-                               void* ws, cudaStream_t st) {
+                               void* /*ws*/, cudaStream_t st) {
     const AttnPlan p = attn_plan(s);
     alignas(64) uint8_t tK[128], tV[128], tKb[128], tVb[128];
     const uint64_t ctx_rows = static_cast<uint64_t>(s.B) * s.Hkv * s.T_cap;
@@ -363,7 +374,10 @@ cudaError_t launch_verify_attn(const sv_attn_shape& s, const uint16_t* q, const 
         return cudaErrorInvalidValue;
     static bool attr_set = false;
     if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(attn_split_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+        cudaError_t e = cudaFuncSetAttribute(attn_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             kSmemBytes);
+        if (e != cudaSuccess) return e;
+        e = cudaFuncSetAttribute(attn_cluster_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
@@ -371,7 +385,7 @@ cudaError_t launch_verify_attn(const sv_attn_shape& s, const uint16_t* q, const 
     a.q = q;
     a.len = len;
     a.parent = parent;
-    a.part = static_cast<float*>(ws);
+    a.out = out;
     a.err = device_error_word();
     a.B = s.B;
     a.R = s.R;
@@ -381,18 +395,25 @@ cudaError_t launch_verify_attn(const sv_attn_shape& s, const uint16_t* q, const 
     a.T_cap = s.T_cap;
     a.rows = p.rows;
     a.row_tiles = p.row_tiles;
-    a.splits = p.splits;
     a.scale_log2 = scale * 1.4426950408889634f;
-    dim3 grid(p.splits + 1, s.B * s.Hkv, p.row_tiles);
-    attn_split_kernel<<<grid, 32 * p.warps, kSmemBytes, st>>>(
-        *reinterpret_cast<const CUtensorMap*>(tK), *reinterpret_cast<const CUtensorMap*>(tV),
-        *reinterpret_cast<const CUtensorMap*>(tKb), *reinterpret_cast<const CUtensorMap*>(tVb), a);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    const int nwarps = s.B * s.Hkv * p.rows;
-    attn_combine_kernel<<<(nwarps + 3) / 4, 128, 0, st>>>(static_cast<const float*>(ws), out, s.B, s.R, s.Hq, s.Hkv,
-                                                           p.G, p.rows, p.row_tiles, p.splits + 1);
-    return cudaGetLastError();
+
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(p.splits, s.B * s.Hkv, p.row_tiles);
+    cfg.blockDim = dim3(32 * p.warps, 1, 1);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = st;
+    cudaLaunchAttribute attrs[2];
+    attrs[0].id = cudaLaunchAttributeClusterDimension;
+    attrs[0].val.clusterDim.x = p.splits;
+    attrs[0].val.clusterDim.y = 1;
+    attrs[0].val.clusterDim.z = 1;
+    attrs[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attrs[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attrs;
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, attn_cluster_kernel, *reinterpret_cast<const CUtensorMap*>(tK),
+                              *reinterpret_cast<const CUtensorMap*>(tV), *reinterpret_cast<const CUtensorMap*>(tKb),
+                              *reinterpret_cast<const CUtensorMap*>(tVb), a);
 }
 
 }  // namespace sv

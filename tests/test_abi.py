@@ -60,11 +60,11 @@ def test_host_validation_rejects_before_launch(lib):
     s = b._AttnShape(1, 5, 12, 5, 128, 4096)   # Hq % Hkv != 0
     assert L.sv_verify_attn(ctypes.byref(s), fake, fake, fake, fake, fake, fake, None, ctypes.c_float(0.1), fake,
                             fake, 1 << 30, None) == 2
-    # short workspace
+    # the attention merges its splits on chip: no workspace
     s = b._AttnShape(1, 5, 12, 2, 128, 4096)
-    assert L.sv_verify_attn_workspace(ctypes.byref(s)) > 0
-    assert L.sv_verify_attn(ctypes.byref(s), fake, fake, fake, fake, fake, fake, None, ctypes.c_float(0.1), fake,
-                            fake, 16, None) == 4
+    assert L.sv_verify_attn_workspace(ctypes.byref(s)) == 0
+    # short workspace
+    assert L.sv_accept_greedy(fake, fake, None, 1, 5, 151936, fake, fake, fake, fake, 8, None) == 4
     # temperature must be positive; vocab must be a multiple of 4
     args = [fake, fake, 151936, fake, None, 64, 9, 151936, ctypes.c_float(0.0), 1, 0, None, fake, fake, fake, fake,
             1 << 20, None]
@@ -80,4 +80,4 @@ def test_workspace_queries(lib):
     from speculative_decoding_verification_sv_gb300 import binding as b
     assert b.lib.sv_accept_greedy_workspace(16, 9, 152064) == 16 * 9 * 19 * 8
     assert b.lib.sv_accept_sample_workspace(64, 9, 151936) == 64 * 9 * 8
-    assert b.verify_attn_workspace(16, 9, 28, 4, 128, 8320) > 0
+    assert b.verify_attn_workspace(16, 9, 28, 4, 128, 8320) == 0
