@@ -167,6 +167,16 @@ cudaError_t launch_nt(const uint16_t* hid, const uint16_t* W, float* logits, int
 
 cudaError_t launch_lm_head(const uint16_t* hid, const uint16_t* W, float* logits, int N, int H, int V,
                            cudaStream_t st) {
+    // Beyond 16 rows the product is a real dense contraction: tcgen05, up to
+    // 256 rows per pass over W.
+    if (N > 16) {
+        for (int n0 = 0; n0 < N; n0 += 256) {
+            const int rows = N - n0 < 256 ? N - n0 : 256;
+            const cudaError_t e = launch_lm_head_tc(hid, W, logits, N, H, V, n0, rows, st);
+            if (e != cudaSuccess) return e;
+        }
+        return cudaSuccess;
+    }
     for (int n0 = 0; n0 < N; n0 += 64) {
         const int rows = N - n0 < 64 ? N - n0 : 64;
         const int nt = (rows + 7) / 8;
