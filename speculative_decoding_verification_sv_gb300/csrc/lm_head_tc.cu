@@ -134,8 +134,7 @@ __global__ void __launch_bounds__(kThreads, 1) lm_head_tc_kernel(const __grid_co
 #pragma unroll 1
             for (int c0 = 0; c0 < NP; c0 += 16) {
                 uint32_t r[16];
-                tmem_ld16(taddr + c0, r);
-                tmem_ld_wait();
+                tmem_ld16_sync(taddr + c0, r);
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
                     const int n = c0 + i;
