@@ -126,7 +126,7 @@ class Round:
             self.length = ai.length.clone()
             self.attn_out = torch.empty_like(self.q)
             shape = (B, R, w.Hq, w.Hkv, w.D, w.T_cap)
-            self.attn_ws = torch.empty(sv.verify_attn_workspace(*shape), dtype=torch.uint8, device=device)
+            self.attn_ws = torch.zeros(max(sv.verify_attn_workspace(*shape), 16), dtype=torch.uint8, device=device)
             self.hid, self.W = synth.lm_inputs(w, device=device)
             self.logits = torch.empty(B * R, V, dtype=torch.float32, device=device)
             # planted drafts: argmax of every verify row of the synthetic logits

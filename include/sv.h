@@ -110,9 +110,16 @@ typedef struct sv_attn_shape {
     int32_t T_cap;  /* cache capacity per (sequence, KV head) */
 } sv_attn_shape;
 
-/* Workspace bytes sv_verify_attn needs for this shape.  The split-KV partials
- * are merged on chip, so this is currently 0 and ws may be NULL; the argument
- * is kept so a future plan may use global scratch without an ABI change. */
+/* Workspace bytes sv_verify_attn needs for this shape (device-dependent: the
+ * split-KV plan follows the SM count and how many thread-block clusters fit at
+ * once).  0 when every (sequence, KV head) is handled by one cluster, whose
+ * split partials merge on chip; ws may then be NULL.  Otherwise several
+ * clusters share a (sequence, KV head): the workspace holds one ticket word per
+ * (sequence, KV head, 128-row tile) followed by the clusters' fp32 partials.
+ * The ticket words must be zero before the first call on a workspace (e.g.
+ * cudaMemset to 0 once); every call that completes leaves them zero again, so
+ * one workspace serves any number of calls in stream order.  Calls running
+ * concurrently need separate workspaces. */
 SV_API size_t sv_verify_attn_workspace(const sv_attn_shape* shape);
 
 /* For sequence b, query head h (KV head g = h / (Hq/Hkv), heads grouped

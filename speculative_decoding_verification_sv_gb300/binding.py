@@ -124,6 +124,8 @@ def verify_attn(q, k_cache, v_cache, length, k_blk, v_blk, parent=None, scale=No
     if out is None:
         out = torch.empty_like(q)
     nbytes = int(lib.sv_verify_attn_workspace(ctypes.byref(s)))
+    if ws is None and nbytes > 0:
+        ws = torch.zeros(nbytes, dtype=torch.uint8, device=q.device)   # ticket words start at zero
     ws = _ws(nbytes, q.device, ws)
     bf = torch.bfloat16
     _check("sv_verify_attn", lib.sv_verify_attn(

@@ -48,9 +48,11 @@ cudaError_t launch_lm_head_tc(const uint16_t* hid, const uint16_t* W, float* log
 struct AttnPlan {
     int G;          // query heads per KV head
     int rows;       // R * G query rows per (sequence, KV head)
-    int row_tiles;  // ceil(rows / 64)
-    int warps;      // warps per CTA (16 rows each)
-    int splits;     // context splits (the block rows get one extra split)
+    int row_tiles;  // ceil(rows / 128)
+    bool half;      // rows <= 64: half-tile kernel (M = 64 MMAs, 4 row-owner warps)
+    int warps;      // warps per CTA
+    int splits;     // CTAs per thread-block cluster (split-KV merged through DSMEM)
+    int clusters;   // clusters per (sequence, KV head, row tile); > 1 merges in the workspace
 };
 AttnPlan attn_plan(const sv_attn_shape& s);
 size_t attn_workspace(const sv_attn_shape& s);

@@ -40,6 +40,8 @@
 #include <cooperative_groups.h>
 #include <math.h>
 
+#include <mutex>
+
 #include "sv_device.cuh"
 #include "sv_internal.h"
 
@@ -52,37 +54,65 @@ constexpr int kD = 128;
 constexpr int kNk = 64;                   // keys per TMA tile
 constexpr int kStepTiles = 1;             // TMA tiles per softmax step
 constexpr int kStepKeys = kStepTiles * kNk;   // keys per softmax step
-constexpr int kRows = 128;                // query rows per CTA (MMA M)
-constexpr int kStages = 4;                // TMA ring depth in tiles
-constexpr int kQBytes = kRows * kD * 2;   // 32 KB: two 64-column halves of 128 rows
-constexpr int kPBlock = kRows * kNk * 2;  // 16 KB: P for one 64-key tile
-constexpr int kPStep = kStepTiles * kPBlock;   // P for one step
-constexpr int kPBytes = 2 * kPStep;            // two P buffers: step st uses buffer st % 2
+constexpr int kRows = 128;                // query rows per full row tile
+constexpr int kPCols = kNk / 2;           // TMEM columns of one P buffer (two bf16 per column)
 constexpr int kHalfBytes = kNk * 128;     // one 64-key x 64-dim swizzled box: 8 KB
 constexpr int kStageBytes = 4 * kHalfBytes;   // K and V, two halves each: 32 KB
-constexpr int kRingBytes = kStages * kStageBytes;
 constexpr int kRec = kD + 4;              // partial record: m, l, 2 pad, o[128]
 constexpr int kMaxR = 128;
 constexpr int kMaxCluster = 16;
-constexpr int kSoftWarps = 16;            // row-owner warps
-constexpr int kGroups = 4;                // column groups of a step
-constexpr int kGCols = kStepKeys / kGroups;   // scores per thread per step
-constexpr int kTmaWarp = kSoftWarps, kMmaWarp = kSoftWarps + 1;
-constexpr int kThreads = 32 * (kSoftWarps + 2);
-constexpr uint32_t kTmemCols = 4 * kStepKeys;   // S buffers at 0 and kStepKeys, O (128 columns) after them
-constexpr float kRescale = 8.0f;          // log2 of the largest tolerated P
-static_assert(kRows * kRec * 4 <= kRingBytes, "partials reuse the K/V ring");
-// S of step st+1 is issued before the P V of step st: both tiles stay resident
-static_assert(kStages >= 2 * kStepTiles + 1, "ring too shallow for the S/PV overlap");
+#ifndef SV_ATTN_MERGE_COST
+#define SV_ATTN_MERGE_COST 6
+#endif
+constexpr int kMergeCost = SV_ATTN_MERGE_COST;   // workspace merge, in key-tile times
+constexpr int kGroups = 4;                // full tiles: column groups of a step
+constexpr int kGCols = kStepKeys / kGroups;   // full tiles: scores per thread per step
+constexpr int kHCols = kStepKeys / 2;     // half tiles: scores per thread per step
+#ifndef SV_ATTN_HALF_MAX_ROWS
+#define SV_ATTN_HALF_MAX_ROWS 64
+#endif
+// (b, g) groups of at most this many rows use the half-tile layout (<= 64)
+constexpr int kHalfMaxRows = SV_ATTN_HALF_MAX_ROWS;
+static_assert(kHalfMaxRows <= 64, "half tiles hold at most 64 rows");
 
-constexpr int kOffQ = 0;
-constexpr int kOffP = kOffQ + kQBytes;
-constexpr int kOffRing = kOffP + kPBytes;
-constexpr int kOffBar = kOffRing + kRingBytes;
-constexpr int kOffAnc = kOffBar + 256;
-constexpr int kOffRed = kOffAnc + kMaxR * 16;                 // [2][kGroups][kRows] partial row maxima
-constexpr int kOffLsum = kOffRed + 2 * kGroups * kRows * 4;    // [kGroups][kRows] partial row sums
-constexpr int kSmemBytes = kOffLsum + kGroups * kRows * 4 + 1024;
+// Full tiles (more than 64 rows): 16 row-owner warps, warp w on TMEM quadrant
+// w % 4 and column group w / 4.  Half tiles (at most 64 rows): 4 row-owner
+// warps, one per quadrant (= one per SM sub-partition), the rows spread over
+// the first 16 lanes of every quadrant, two threads per row.
+template <bool kHalf>
+struct Roles {
+    static constexpr int kSoft = kHalf ? 4 : 16;
+    static constexpr int kTma = kSoft, kMma = kSoft + 1;
+    static constexpr int kThreads = 32 * (kSoft + 2);
+};
+// TMEM columns: S buffers at 0 and 64, O at 128..255, P buffers at 256 and 288
+constexpr uint32_t kColS = 0, kColO = 2 * kStepKeys, kColP = kColO + kD;
+constexpr uint32_t kTmemCols = 512;
+static_assert(kColP + 2 * kPCols <= kTmemCols, "TMEM budget");
+constexpr float kRescale = 8.0f;          // log2 of the largest tolerated P
+// S of step st+1 is issued before the P V of step st: both tiles stay resident
+static_assert(kStepTiles == 1, "one key tile per softmax step");
+
+// Shared-memory layout.  Full tiles: M = 128 MMAs, 32 KB of Q, 5 ring stages.
+// Half tiles: M = 64 MMAs (row m of the tile in TMEM lane 32 * (m / 16) +
+// m % 16), 16 KB of Q, 6 ring stages -- more K/V bytes in flight per SM.
+template <bool kHalf>
+struct Lay {
+    static constexpr int kM = kHalf ? 64 : 128;            // MMA M (rows of the Q tile)
+    static constexpr int kStages = kHalf ? 6 : 5;           // TMA ring depth in tiles
+    static constexpr int kQBytes = kM * kD * 2;             // two 64-dim halves of kM rows
+    static constexpr int kRingBytes = kStages * kStageBytes;
+    static constexpr int kOffQ = 0;
+    static constexpr int kOffRing = kOffQ + kQBytes;
+    static constexpr int kOffBar = kOffRing + kRingBytes;
+    static constexpr int kOffAnc = kOffBar + 256;
+    static constexpr int kOffRed = kOffAnc + kMaxR * 16;               // [2][kGroups][kRows] partial row maxima
+    static constexpr int kOffLsum = kOffRed + 2 * kGroups * kRows * 4;  // [kGroups][kRows] partial row sums
+    static constexpr int kSmemBytes = kOffLsum + kGroups * kRows * 4 + 1024;
+    static_assert(kRows * kRec * 4 <= kRingBytes, "partials reuse the K/V ring");
+    static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
+    static_assert((2 * kStages + 9) * 8 + 4 <= 248, "barrier area (the word at +248 is the ticket flag)");
+};
 
 struct AttnArgs {
     const uint16_t* q;
@@ -90,17 +120,29 @@ struct AttnArgs {
     const int32_t* parent;
     uint16_t* out;
     unsigned int* err;
+    float* ws_part;          // [unit][cluster][part_rows][kRec] cluster partials (clusters > 1)
+    unsigned int* ws_cnt;    // [unit] tickets of clusters done; zero between launches
     int B, R, Hq, Hkv, G, T_cap, rows, row_tiles;
+    int clusters;            // clusters per (b, g, row tile); their partials meet in ws_part
+    int part_rows;           // rows of a partial record block: min(rows, kRows)
     float scale_log2;
 };
 
-__global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_constant__ CUtensorMap tmK,
-                                                             const __grid_constant__ CUtensorMap tmV,
-                                                             const __grid_constant__ CUtensorMap tmKb,
-                                                             const __grid_constant__ CUtensorMap tmVb, AttnArgs a) {
+// TMEM lane that holds row gr of (b, g): full tiles lane = gr - 128 * rt;
+// half tiles put row gr in lane 32 * (gr % 4) + gr / 4, so every quadrant
+// (SM sub-partition) carries a quarter of the rows.
+
+template <bool kHalf>
+__global__ void __launch_bounds__(Roles<kHalf>::kThreads, 1)
+    attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                   const __grid_constant__ CUtensorMap tmKb, const __grid_constant__ CUtensorMap tmVb, AttnArgs a) {
+    using Ro = Roles<kHalf>;
+    using Ly = Lay<kHalf>;
+    constexpr int kSoftWarps = Ro::kSoft, kTmaWarp = Ro::kTma, kMmaWarp = Ro::kMma, kThreads = Ro::kThreads;
+    constexpr int kStages = Ly::kStages, kM = Ly::kM;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Ly::kOffBar);
     uint64_t* kv_full = bars;                    // [kStages]
     uint64_t* kv_empty = bars + kStages;         // [kStages]
     uint64_t* s_full = bars + 2 * kStages;       // [2]
@@ -109,8 +151,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
     uint64_t* o_done = p_full + 2;               // [2], per P buffer
     uint64_t* q_ready = o_done + 2;
     uint32_t* tmem_s = reinterpret_cast<uint32_t*>(q_ready + 1);
-    uint64_t* anc = reinterpret_cast<uint64_t*>(smem + kOffAnc);   // [kMaxR][2]
-    float* part = reinterpret_cast<float*>(smem + kOffRing);        // [kRows][kRec] after the loop
+    uint64_t* anc = reinterpret_cast<uint64_t*>(smem + Ly::kOffAnc);   // [kMaxR][2]
+    float* part = reinterpret_cast<float*>(smem + Ly::kOffRing);        // [kRows][kRec] by row, after the loop
 
     cg::cluster_group cluster = cg::this_cluster();
     const int C = static_cast<int>(cluster.num_blocks());
@@ -144,8 +186,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_s;
-    const uint32_t tS[2] = {tmem, tmem + kStepKeys};
-    const uint32_t tO = tmem + 2 * kStepKeys;
+    const uint32_t tS[2] = {tmem + kColS, tmem + kColS + kStepKeys};
+    const uint32_t tO = tmem + kColO;
+    const uint32_t tP[2] = {tmem + kColP, tmem + kColP + kPCols};
 
     // inputs may come from the kernels before this one
     pdl_wait();
@@ -159,8 +202,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
     const int n_ctx = (t + kNk - 1) / kNk;
     const int n_blk = (a.R + kNk - 1) / kNk;
     const int n_all = n_ctx + n_blk;
-    const int first = static_cast<int>((static_cast<int64_t>(n_all) * rank) / C);
-    const int last = static_cast<int>((static_cast<int64_t>(n_all) * (rank + 1)) / C);
+    // this CTA's share of the key tiles: split blockIdx.x of the gridDim.x
+    // CTAs (a.clusters clusters of C) working on (b, g, row tile)
+    const int split = blockIdx.x, nsplit = gridDim.x;
+    const int first = static_cast<int>((static_cast<int64_t>(n_all) * split) / nsplit);
+    const int last = static_cast<int>((static_cast<int64_t>(n_all) * (split + 1)) / nsplit);
     const int ntiles = last - first;
     const int nsteps = (ntiles + kStepTiles - 1) / kStepTiles;
     const bool has_block = last > n_ctx;
@@ -176,7 +222,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
                 const void* tk = gt < n_ctx ? static_cast<const void*>(&tmK) : static_cast<const void*>(&tmKb);
                 const void* tv = gt < n_ctx ? static_cast<const void*>(&tmV) : static_cast<const void*>(&tmVb);
                 const int y = gt < n_ctx ? hg * a.T_cap + gt * kNk : hg * a.R + (gt - n_ctx) * kNk;
-                uint8_t* st = smem + kOffRing + s * kStageBytes;
+                uint8_t* st = smem + Ly::kOffRing + s * kStageBytes;
                 mbar_arrive_expect_tx(&kv_full[s], kStageBytes);
                 tma_load_2d(st, tk, 0, y, &kv_full[s]);
                 tma_load_2d(st + kHalfBytes, tk, 64, y, &kv_full[s]);
@@ -187,10 +233,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
     } else if (warp == kMmaWarp) {
         // ---------------- MMA issuer ----------------
         if (lane == 0 && ntiles > 0) {
-            constexpr uint32_t idesc_s = idesc_bf16_f32(kRows, kNk, false, false);   // S tile = Q K^T
-            constexpr uint32_t idesc_o = idesc_bf16_f32(kRows, kD, false, true);     // O += P V
-            const uint32_t sq = smem_u32(smem + kOffQ);
-            const uint32_t sp = smem_u32(smem + kOffP);
+            constexpr uint32_t idesc_s = idesc_bf16_f32(kM, kNk, false, false);   // S tile = Q K^T
+            constexpr uint32_t idesc_o = idesc_bf16_f32(kM, kD, false, true);     // O += P V
+            const uint32_t sq = smem_u32(smem + Ly::kOffQ);
             // both S operands K-major; the two 64-dim halves are separate boxes
             const uint64_t qd0 = smem_desc_sw128(sq, 16, 1024);
             mbar_wait(q_ready, 0, a.err);
@@ -201,16 +246,16 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
                 const int t0 = kStepTiles * st, nt = min(kStepTiles, ntiles - t0);
                 for (int h = 0; h < nt; ++h) {
                     const int s = (t0 + h) % kStages;
-                    const uint32_t sv = smem_u32(smem + kOffRing + s * kStageBytes + 2 * kHalfBytes);
-                    // A = P [128 rows][64 keys of tile h], K-major; B = V [64 keys][128
-                    // dims], MN-major: 8-key groups 1024 B apart, the two 64-dim halves
-                    // kHalfBytes apart, 16 keys = 2048 B (descriptor units of 16 B).
-                    const uint64_t ad0 = smem_desc_sw128(sp + pb * kPStep + h * kPBlock, 16, 1024);
+                    const uint32_t sv = smem_u32(smem + Ly::kOffRing + s * kStageBytes + 2 * kHalfBytes);
+                    // A = P [128 lanes][64 keys] in TMEM (8 columns per 16 keys); B = V
+                    // [64 keys][128 dims], MN-major: 8-key groups 1024 B apart, the two
+                    // 64-dim halves kHalfBytes apart, 16 keys = 2048 B (descriptor units
+                    // of 16 B).
                     const uint64_t bd0 = smem_desc_sw128(sv, kHalfBytes, 1024);
 #pragma unroll
                     for (int k16 = 0; k16 < kNk / 16; ++k16)
-                        tc_mma(tO, ad0 + k16 * (32 >> 4), bd0 + k16 * (2048 >> 4), idesc_o,
-                               (st > 0 || h > 0 || k16 > 0) ? 1u : 0u);
+                        tc_mma_ts(tO, tP[pb] + h * kPCols + k16 * 8, bd0 + k16 * (2048 >> 4), idesc_o,
+                                  (st > 0 || h > 0 || k16 > 0) ? 1u : 0u);
                 }
                 tc_commit(&o_done[pb]);
                 for (int h = 0; h < nt; ++h) tc_commit(&kv_empty[(t0 + h) % kStages]);
@@ -224,11 +269,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
                     const int s = i % kStages;
                     mbar_wait(&kv_full[s], (i / kStages) & 1, a.err);
                     tc_fence_after();
-                    const uint64_t kd0 = smem_desc_sw128(smem_u32(smem + kOffRing + s * kStageBytes), 16, 1024);
+                    const uint64_t kd0 = smem_desc_sw128(smem_u32(smem + Ly::kOffRing + s * kStageBytes), 16, 1024);
 #pragma unroll
                     for (int k16 = 0; k16 < kD / 16; ++k16) {
                         const uint32_t half = k16 >> 2, kin = (k16 & 3) * 32;
-                        tc_mma(tS[sb] + h * kNk, qd0 + ((half * (kRows * 128) + kin) >> 4),
+                        tc_mma(tS[sb] + h * kNk, qd0 + ((half * (kM * 128) + kin) >> 4),
                                kd0 + ((half * kHalfBytes + kin) >> 4), idesc_s, k16 > 0 ? 1u : 0u);
                     }
                 }
@@ -238,17 +283,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
             pv(nsteps - 1);
         }
     } else {
-        // ---------------- row-owner warps: row r, column group cgp ----------------
-        const int cgp = warp / 4;                         // 16-column group of each step
-        const int r = (warp & 3) * 32 + lane;             // row inside the tile (TMEM lane)
-        const int gr = rt * kRows + r;                    // row inside (b, g)
-        const bool valid = gr < a.rows;
-        const int j = valid ? gr / a.G : 0;
-        // rows of this warp's TMEM quarter that exist (the rest of a 128-row
-        // tile is padding whose P and O are never read)
-        const bool quarter_live = rt * kRows + (warp & 3) * 32 < a.rows;
-        float* red = reinterpret_cast<float*>(smem + kOffRed);
-        float* lsx = reinterpret_cast<float*>(smem + kOffLsum);
+        // ---------------- row-owner warps ----------------
         // tree ancestor masks: bit i of anc[jj] set iff block row i is jj or an ancestor
         if (tree) {
             const int32_t* par = a.parent + static_cast<size_t>(b) * a.R;
@@ -271,59 +306,80 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
                 anc[2 * jj + 1] = m1;
             }
         }
-        // gather the Q tile (zero rows beyond the group) into the K-major
+        // gather the Q tile (zero rows for padding lanes) into the K-major
         // 128-byte-swizzled layout the MMA reads
         {
-            uint8_t* q_s = smem + kOffQ;
-            for (int x = threadIdx.x; x < kRows * 16; x += 32 * kSoftWarps) {
-                const int row = x >> 4, c = x & 15;
+            uint8_t* q_s = smem + Ly::kOffQ;
+            for (int x = threadIdx.x; x < kM * 16; x += 32 * kSoftWarps) {
+                const int row = x >> 4, c = x & 15;   // row of the MMA's A operand
                 uint4 v = make_uint4(0u, 0u, 0u, 0u);
-                const int grow = rt * kRows + row;
+                // half tiles: A row m sits in TMEM lane 32 * (m / 16) + m % 16 and
+                // carries row 4 * (m % 16) + m / 16 of (b, g)
+                const int grow = kHalf ? 4 * (row & 15) + (row >> 4) : rt * kRows + row;
+                const int half = c >> 3, cc = c & 7;
+                uint8_t* dst = q_s + half * (kM * 128) + row * 128 + ((cc ^ (row & 7)) << 4);
                 if (grow < a.rows) {
+                    // all of a thread's copies in flight at once
                     const int jr = grow / a.G, hl = grow % a.G;
                     const uint16_t* src = a.q + ((static_cast<size_t>(b) * a.R + jr) * a.Hq + g * a.G + hl) * kD;
-                    v = __ldg(reinterpret_cast<const uint4*>(src) + c);
+                    cp_async16(dst, reinterpret_cast<const uint4*>(src) + c);
+                } else {
+                    *reinterpret_cast<uint4*>(dst) = v;
                 }
-                const int half = c >> 3, cc = c & 7;
-                *reinterpret_cast<uint4*>(q_s + half * (kRows * 128) + row * 128 + ((cc ^ (row & 7)) << 4)) = v;
             }
+            cp_async_wait_all();
         }
         fence_proxy_async_smem();
         named_barrier(1, 32 * kSoftWarps);   // anc and Q written by every row-owner warp
         if (lane == 0) mbar_arrive(q_ready);
+
+        // this thread's row: TMEM lane r (also its P row), row gr of (b, g)
+        const int r = kHalf ? (warp * 32 + (lane & 15)) : ((warp & 3) * 32 + lane);
+        const int gr = kHalf ? (4 * (lane & 15) + warp) : (rt * kRows + r);
+        const bool valid = gr < a.rows;
+        const int j = valid ? gr / a.G : 0;
+        // the warp's quadrant holds at least one real row (padding lanes' P and
+        // O are never read, so a warp with none skips the arithmetic)
+        const bool quarter_live = kHalf ? (warp < a.rows) : (rt * kRows + (warp & 3) * 32 < a.rows);
         const uint64_t anc0 = (tree && valid) ? anc[2 * j] : 0, anc1 = (tree && valid) ? anc[2 * j + 1] : 0;
+        const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+        // full tiles: 16 consecutive columns of the step (group cgp); half
+        // tiles: 32 (thread half `sub` of the row's pair)
+        constexpr int kCols = kHalf ? kHCols : kGCols;
+        const int cgp = kHalf ? 0 : warp / 4;
+        const int sub = kHalf ? (lane >> 4) : 0;
+        const int col0 = kHalf ? sub * kHCols : cgp * kGCols;
+        float* red = reinterpret_cast<float*>(smem + Ly::kOffRed);
+        float* lsx = reinterpret_cast<float*>(smem + Ly::kOffLsum);
 
         float m_ref = -INFINITY, lsum = 0.f;
-        const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
         for (int st = 0; st < nsteps; ++st) {
             const int sb = st & 1;
             mbar_wait(&s_full[sb], (st >> 1) & 1, a.err);
             tc_fence_after();
-            // this thread's scores: columns kGCols*cgp.. of the step, all in tile ti
-            const int ti = kStepTiles * st + (cgp * kGCols) / kNk;
-            const int col_in_tile = (cgp * kGCols) % kNk;
-            const bool work = quarter_live && ti < ntiles;
-            uint32_t ra[16], rb[16];
+            const bool work = quarter_live;
+            uint32_t rs[kCols];
             if (work) {
-                tmem_ld16_sync(tS[sb] + lane_off + cgp * kGCols, ra);
-                if (kGCols > 16) tmem_ld16_sync(tS[sb] + lane_off + cgp * kGCols + 16, rb);
+                if constexpr (kHalf) {
+                    tmem_ld32_h_sync<kHCols>(tS[sb] + lane_off, rs);
+                } else {
+                    tmem_ld16_sync(tS[sb] + lane_off + col0, rs);
+                }
             }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&s_empty[sb]);
-            const int gt = first + ti;
+            const int gt = first + st;
             const bool is_block = gt >= n_ctx;
-            const int kb = (is_block ? (gt - n_ctx) * kNk : gt * kNk) + col_in_tile;
-            float sc[kGCols];
+            const int kb = (is_block ? (gt - n_ctx) * kNk : gt * kNk) + col0;
+            float sc[kCols];
             float mpart = -INFINITY;
             if (work) {
 #pragma unroll
-                for (int e = 0; e < 16; ++e) sc[e] = __uint_as_float(ra[e]) * a.scale_log2;
+                for (int e = 0; e < kCols; ++e) sc[e] = __uint_as_float(rs[e]) * a.scale_log2;
+                if (is_block || kb + kCols > t) {
 #pragma unroll
-                for (int e = 16; e < kGCols; ++e) sc[e] = __uint_as_float(rb[e - 16]) * a.scale_log2;
-                if (is_block || kb + kGCols > t) {
-#pragma unroll
-                    for (int e = 0; e < kGCols; ++e) {
+                    for (int e = 0; e < kCols; ++e) {
                         const int kl = kb + e;
                         bool vis;
                         if (!is_block) {
@@ -338,31 +394,37 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
                         if (!vis) sc[e] = -INFINITY;
                     }
                 }
-                float mx[kGCols / 2];
+                float mx[kCols / 2];
 #pragma unroll
-                for (int e = 0; e < kGCols / 2; ++e) mx[e] = fmaxf(sc[e], sc[e + kGCols / 2]);
+                for (int e = 0; e < kCols / 2; ++e) mx[e] = fmaxf(sc[e], sc[e + kCols / 2]);
 #pragma unroll
-                for (int w2 = kGCols / 4; w2 >= 1; w2 >>= 1)
+                for (int w2 = kCols / 4; w2 >= 1; w2 >>= 1)
 #pragma unroll
                     for (int e = 0; e < w2; ++e) mx[e] = fmaxf(mx[e], mx[e + w2]);
                 mpart = mx[0];
             }
-            red[(sb * kGroups + cgp) * kRows + r] = mpart;
-            named_barrier(2, 32 * kSoftWarps);
-            float mt = red[(sb * kGroups + 0) * kRows + r];
+            float mt;
+            if constexpr (kHalf) {
+                // the row's other half sits 16 lanes away in the same warp
+                mt = fmaxf(mpart, __shfl_xor_sync(0xffffffffu, mpart, 16));
+            } else {
+                red[(sb * kGroups + cgp) * kRows + r] = mpart;
+                named_barrier(2, 32 * kSoftWarps);
+                mt = red[(sb * kGroups + 0) * kRows + r];
 #pragma unroll
-            for (int c2 = 1; c2 < kGroups; ++c2) mt = fmaxf(mt, red[(sb * kGroups + c2) * kRows + r]);
+                for (int c2 = 1; c2 < kGroups; ++c2) mt = fmaxf(mt, red[(sb * kGroups + c2) * kRows + r]);
+            }
             float m_new = m_ref, corr = 1.f;
             if (mt > -INFINITY && (m_ref == -INFINITY || mt > m_ref + kRescale)) {
                 m_new = mt;
                 corr = m_ref == -INFINITY ? 0.f : fast_exp2(m_ref - m_new);
             }
             // P (bf16) and this thread's share of its sum
-            uint32_t pk[kGCols / 2];
+            uint32_t pk[kCols / 2];
             float ps0 = 0.f, ps1 = 0.f;
             if (work) {
 #pragma unroll
-                for (int e = 0; e < kGCols; e += 2) {
+                for (int e = 0; e < kCols; e += 2) {
                     const float p0 = (m_new == -INFINITY) ? 0.f : fast_exp2(sc[e] - m_new);
                     const float p1 = (m_new == -INFINITY) ? 0.f : fast_exp2(sc[e + 1] - m_new);
                     const __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
@@ -382,7 +444,18 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
                 // rescale O: wait for the P V of step st-1 to settle it
                 mbar_wait(&o_done[sb ^ 1], ((st - 1) >> 1) & 1, a.err);
                 tc_fence_after();
-                {
+                if constexpr (kHalf) {
+                    // columns 64*sub .. of the row
+#pragma unroll
+                    for (int c0 = 0; c0 < kD / 2; c0 += 16) {
+                        const uint32_t ta = tO + lane_off + c0;
+                        uint32_t o16[16];
+                        tmem_ld16_h_sync<kD / 2>(ta, o16);
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) o16[e] = __float_as_uint(__uint_as_float(o16[e]) * corr);
+                        tmem_st16_h<kD / 2>(ta, o16);
+                    }
+                } else {
 #pragma unroll
                     for (int c0 = 0; c0 < kD / kGroups; c0 += 16) {
                         const uint32_t ta = tO + lane_off + cgp * (kD / kGroups) + c0;
@@ -392,19 +465,15 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
                         for (int e = 0; e < 16; ++e) o16[e] = __float_as_uint(__uint_as_float(o16[e]) * corr);
                         tmem_st16(ta, o16);
                     }
-                    tmem_st_wait();
                 }
+                tmem_st_wait();
             }
             if (work) {
-                uint8_t* p_row = smem + kOffP + sb * kPStep + ((cgp * kGCols) / kNk) * kPBlock + r * 128;
-#pragma unroll
-                for (int h = 0; h < kGCols / 8; ++h) {
-                    const int cc = col_in_tile / 8 + h;
-                    *reinterpret_cast<uint4*>(p_row + ((cc ^ (r & 7)) << 4)) =
-                        make_uint4(pk[4 * h], pk[4 * h + 1], pk[4 * h + 2], pk[4 * h + 3]);
-                }
+                // P of this thread's columns into TMEM buffer sb, two keys per column
+                if constexpr (kHalf) tmem_st16_h<kHCols / 2>(tP[sb] + lane_off, pk);
+                else tmem_st8(tP[sb] + lane_off + col0 / 2, pk);
+                tmem_st_wait();
             }
-            fence_proxy_async_smem();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&p_full[sb]);
@@ -413,35 +482,60 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
             mbar_wait(&o_done[(nsteps - 1) & 1], ((nsteps - 1) >> 1) & 1, a.err);
             tc_fence_after();
         }
-        // row sum across the four column groups -> this CTA's partial
-        lsx[cgp * kRows + r] = lsum;
-        named_barrier(2, 32 * kSoftWarps);
-        float lt = 0.f;
+        // row sum across the row's threads -> this CTA's partial record, kept
+        // by row of (b, g) relative to the tile
+        float lt;
+        if constexpr (kHalf) {
+            lt = lsum + __shfl_xor_sync(0xffffffffu, lsum, 16);
+        } else {
+            lsx[cgp * kRows + r] = lsum;
+            named_barrier(2, 32 * kSoftWarps);
+            lt = 0.f;
 #pragma unroll
-        for (int c2 = 0; c2 < kGroups; ++c2) lt += lsx[c2 * kRows + r];
+            for (int c2 = 0; c2 < kGroups; ++c2) lt += lsx[c2 * kRows + r];
+        }
         const bool use = nsteps >= 1 && lt > 0.f;
-        float* rec = part + r * kRec;
-        if (cgp == 0) {
+        const int prow = gr - rt * kRows;              // < kRows for every real row
+        float* rec = part + (valid ? prow : 0) * kRec;
+        if (valid && cgp == 0 && sub == 0) {
             rec[0] = use ? m_ref : -INFINITY;
             rec[1] = use ? lt : 0.f;
         }
+        constexpr int kOCols = kHalf ? kD / 2 : kD / kGroups;   // O columns per thread
+        const int ocol0 = kHalf ? sub * (kD / 2) : cgp * (kD / kGroups);
 #pragma unroll
-        for (int c0 = 0; c0 < kD / kGroups; c0 += 16) {
-            const uint32_t col = cgp * (kD / kGroups) + c0;
+        for (int c0 = 0; c0 < kOCols; c0 += 16) {
             uint32_t o16[16] = {};
-            if (nsteps >= 1) tmem_ld16_sync(tO + lane_off + col, o16);
+            if (nsteps >= 1) {
+                if constexpr (kHalf) tmem_ld16_h_sync<kD / 2>(tO + lane_off + c0, o16);
+                else tmem_ld16_sync(tO + lane_off + ocol0 + c0, o16);
+            }
+            if (valid) {
 #pragma unroll
-            for (int e = 0; e < 16; e += 4)
-                *reinterpret_cast<uint4*>(rec + 4 + col + e) =
-                    use ? make_uint4(o16[e], o16[e + 1], o16[e + 2], o16[e + 3]) : make_uint4(0u, 0u, 0u, 0u);
+                for (int e = 0; e < 16; e += 4)
+                    *reinterpret_cast<uint4*>(rec + 4 + ocol0 + c0 + e) =
+                        use ? make_uint4(o16[e], o16[e + 1], o16[e + 2], o16[e + 3]) : make_uint4(0u, 0u, 0u, 0u);
+            }
         }
     }
     tc_fence_before();
     __syncthreads();
     cluster.sync();   // all partials written (and every CTA of the cluster has started)
 
-    // merge: this CTA finalises rows rank, rank + C, ... of the row tile (all warps)
+    // merge: this CTA finalises rows rank, rank + C, ... of the row tile (all
+    // warps); with one cluster per (b, g, row tile) it writes the bf16 rows,
+    // otherwise the cluster's merged partial (max, sum, unnormalised O)
     const int nrows = min(kRows, a.rows - rt * kRows);
+    const int unit = hg * a.row_tiles + rt;
+    const int ci = blockIdx.x / C;
+    auto store_row = [&](int lr, float4 acc, float L) {
+        const float inv = L > 0.f ? 1.0f / L : 0.f;
+        const int row = rt * kRows + lr;
+        const int jr = row / a.G, h = g * a.G + row % a.G;
+        uint16_t* dst = a.out + ((static_cast<size_t>(b) * a.R + jr) * a.Hq + h) * kD + 4 * lane;
+        *reinterpret_cast<uint2*>(dst) =
+            make_uint2(pack_bf16x2(acc.x * inv, acc.y * inv), pack_bf16x2(acc.z * inv, acc.w * inv));
+    };
     for (int lr = rank + C * warp; lr < nrows; lr += C * (kThreads / 32)) {
         float ms = -INFINITY, ls = 0.f;
         if (lane < C) {
@@ -456,23 +550,97 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
         float L = wgt * ls;
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
+        // O: branch-free, eight remote loads in flight at a time (an empty
+        // partial has weight 0 and an all-zero record)
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int s = 0; s < C; ++s) {
-            const float ws = __shfl_sync(0xffffffffu, wgt, s);
-            if (ws == 0.f) continue;
-            const float4 x =
-                *reinterpret_cast<const float4*>(cluster.map_shared_rank(part + lr * kRec + 4, s) + 4 * lane);
-            acc.x += ws * x.x;
-            acc.y += ws * x.y;
-            acc.z += ws * x.z;
-            acc.w += ws * x.w;
+        for (int s0 = 0; s0 < C; s0 += 8) {
+            float4 x[8];
+            float wv[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int sr = s0 + u < C ? s0 + u : 0;
+                wv[u] = __shfl_sync(0xffffffffu, wgt, sr);
+                x[u] = *reinterpret_cast<const float4*>(cluster.map_shared_rank(part + lr * kRec + 4, sr) + 4 * lane);
+                if (s0 + u >= C) wv[u] = 0.f;
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                acc.x += wv[u] * x[u].x;
+                acc.y += wv[u] * x[u].y;
+                acc.z += wv[u] * x[u].z;
+                acc.w += wv[u] * x[u].w;
+            }
         }
-        const float inv = L > 0.f ? 1.0f / L : 0.f;
-        const int row = rt * kRows + lr;
-        const int jr = row / a.G, h = g * a.G + row % a.G;
-        uint16_t* dst = a.out + ((static_cast<size_t>(b) * a.R + jr) * a.Hq + h) * kD + 4 * lane;
-        *reinterpret_cast<uint2*>(dst) =
-            make_uint2(pack_bf16x2(acc.x * inv, acc.y * inv), pack_bf16x2(acc.z * inv, acc.w * inv));
+        if (a.clusters == 1) {
+            store_row(lr, acc, L);
+        } else {
+            float* rec_g = a.ws_part + ((static_cast<size_t>(unit) * a.clusters + ci) * a.part_rows + lr) * kRec;
+            if (lane == 0) {
+                rec_g[0] = L > 0.f ? M : -INFINITY;
+                rec_g[1] = L;
+            }
+            *reinterpret_cast<float4*>(rec_g + 4 + 4 * lane) = acc;
+        }
+    }
+    if (a.clusters > 1) {
+        // ticket: the last cluster of (b, g, row tile) to finish merges all the
+        // cluster partials (written above, made visible by the fence) and
+        // resets the ticket for the next launch
+        uint32_t* last_flag = reinterpret_cast<uint32_t*>(smem + Ly::kOffBar + 248);
+        __threadfence();
+        cluster.sync();
+        if (rank == 0 && threadIdx.x == 0) {
+            const unsigned int done = atomicAdd(a.ws_cnt + unit, 1u);
+            const bool is_last = done == static_cast<unsigned int>(a.clusters - 1);
+            if (is_last) a.ws_cnt[unit] = 0u;
+            *last_flag = is_last ? 1u : 0u;
+        }
+        cluster.sync();
+        if (*cluster.map_shared_rank(last_flag, 0) != 0u) {
+            __threadfence();
+            const float* base = a.ws_part + static_cast<size_t>(unit) * a.clusters * a.part_rows * kRec;
+            const int nc = a.clusters;
+            for (int lr = rank + C * warp; lr < nrows; lr += C * (kThreads / 32)) {
+                // lane c holds partial c's (max, sum) (nc <= 32), then the O
+                // records are read eight at a time, branch-free
+                float mc = -INFINITY, lc = 0.f;
+                if (lane < nc) {
+                    const float2 ml = __ldcg(reinterpret_cast<const float2*>(
+                        base + (static_cast<size_t>(lane) * a.part_rows + lr) * kRec));
+                    mc = ml.x;
+                    lc = ml.y;
+                }
+                float M = lc > 0.f ? mc : -INFINITY;
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+                const float wc = (lc > 0.f && M != -INFINITY) ? exp2f(mc - M) : 0.f;
+                float L = wc * lc;
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
+                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int c0 = 0; c0 < nc; c0 += 8) {
+                    float4 x[8];
+                    float wv[8];
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        const int c = c0 + u < nc ? c0 + u : 0;
+                        wv[u] = __shfl_sync(0xffffffffu, wc, c);
+                        x[u] = __ldcg(reinterpret_cast<const float4*>(
+                                          base + (static_cast<size_t>(c) * a.part_rows + lr) * kRec + 4) +
+                                      lane);
+                        if (c0 + u >= nc) wv[u] = 0.f;
+                    }
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        acc.x += wv[u] * x[u].x;
+                        acc.y += wv[u] * x[u].y;
+                        acc.z += wv[u] * x[u].z;
+                        acc.w += wv[u] * x[u].w;
+                    }
+                }
+                store_row(lr, acc, L);
+            }
+        }
     }
     cluster.sync();   // no CTA leaves while its partials may still be read
     if (warp == kMmaWarp) {
@@ -481,68 +649,66 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
     }
 }
 
-}  // namespace
-
-AttnPlan attn_plan(const sv_attn_shape& s) {
-    AttnPlan p;
-    p.G = s.Hq / s.Hkv;
-    p.rows = s.R * p.G;
-    p.row_tiles = (p.rows + kRows - 1) / kRows;
-    p.warps = kThreads / 32;
-    // cluster size: grow while the grid still fits in one CTA per SM and every
-    // CTA keeps at least one step of key tiles
-    const int units = s.B * s.Hkv * p.row_tiles;
-    const int slots = device_sm_count();
-    const int tiles = (s.T_cap + kNk - 1) / kNk + (s.R + kNk - 1) / kNk;
-    int C = 1;
-    while (C < kMaxCluster && units * C * 2 <= slots && C * 4 <= tiles) C *= 2;
-    p.splits = C;
-    return p;
+template <bool kHalf>
+cudaError_t prepare_kernel() {
+    static bool done[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (done[dev]) return cudaSuccess;
+    cudaError_t e =
+        cudaFuncSetAttribute(attn_tc_kernel<kHalf>, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay<kHalf>::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(attn_tc_kernel<kHalf>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return e;
+    done[dev] = true;
+    return cudaSuccess;
 }
 
-size_t attn_workspace(const sv_attn_shape&) { return 0; }
-
-cudaError_t launch_verify_attn(const sv_attn_shape& s, const uint16_t* q, const uint16_t* k_cache,
-                               const uint16_t* v_cache, const int32_t* len, const uint16_t* k_blk,
-                               const uint16_t* v_blk, const int32_t* parent, float scale, uint16_t* out,
-                               void* /*ws*/, cudaStream_t st) {
-    const AttnPlan p = attn_plan(s);
-    alignas(64) uint8_t tK[128], tV[128], tKb[128], tVb[128];
-    const uint64_t ctx_rows = static_cast<uint64_t>(s.B) * s.Hkv * s.T_cap;
-    const uint64_t blk_rows = static_cast<uint64_t>(s.B) * s.Hkv * s.R;
-    if (!encode_tmap_2d_bf16(tK, k_cache, kD, ctx_rows, kD * 2, 64, kNk) ||
-        !encode_tmap_2d_bf16(tV, v_cache, kD, ctx_rows, kD * 2, 64, kNk) ||
-        !encode_tmap_2d_bf16(tKb, k_blk, kD, blk_rows, kD * 2, 64, kNk) ||
-        !encode_tmap_2d_bf16(tVb, v_blk, kD, blk_rows, kD * 2, 64, kNk))
-        return cudaErrorInvalidValue;
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-        if (e != cudaSuccess) return e;
-        e = cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-        if (e != cudaSuccess) return e;
-        attr_set = true;
+// Clusters of C CTAs that can be resident at once (a cluster must fit in one
+// GPC, so large clusters leave SMs idle); SMs / C when the query fails.
+template <bool kHalf>
+int active_clusters(int C) {
+    static std::mutex mu;
+    static int cache[64][17] = {};
+    int dev = 0;
+    const int fallback = device_sm_count() / C > 0 ? device_sm_count() / C : 1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+        cudaGetLastError();
+        return fallback;
     }
-    AttnArgs a;
-    a.q = q;
-    a.len = len;
-    a.parent = parent;
-    a.out = out;
-    a.err = device_error_word();
-    a.B = s.B;
-    a.R = s.R;
-    a.Hq = s.Hq;
-    a.Hkv = s.Hkv;
-    a.G = p.G;
-    a.T_cap = s.T_cap;
-    a.rows = p.rows;
-    a.row_tiles = p.row_tiles;
-    a.scale_log2 = scale * 1.4426950408889634f;
+    std::lock_guard<std::mutex> lk(mu);
+    if (cache[dev][C]) return cache[dev][C];
+    int n = 0;
+    if (prepare_kernel<kHalf>() == cudaSuccess) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(C, 1, 1);
+        cfg.blockDim = dim3(Roles<kHalf>::kThreads, 1, 1);
+        cfg.dynamicSmemBytes = Lay<kHalf>::kSmemBytes;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = C;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (cudaOccupancyMaxActiveClusters(&n, attn_tc_kernel<kHalf>, &cfg) != cudaSuccess) n = 0;
+    }
+    cudaGetLastError();
+    if (n <= 0) n = fallback;
+    cache[dev][C] = n;
+    return n;
+}
 
+template <bool kHalf>
+cudaError_t launch_mode(const AttnPlan& p, const sv_attn_shape& s, const uint8_t* tK, const uint8_t* tV,
+                        const uint8_t* tKb, const uint8_t* tVb, const AttnArgs& a, cudaStream_t st) {
+    constexpr int kThreads = Roles<kHalf>::kThreads;
+    cudaError_t e = prepare_kernel<kHalf>();
+    if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(p.splits, s.B * s.Hkv, p.row_tiles);
+    cfg.gridDim = dim3(p.splits * p.clusters, s.B * s.Hkv, p.row_tiles);
     cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.dynamicSmemBytes = Lay<kHalf>::kSmemBytes;
     cfg.stream = st;
     cudaLaunchAttribute attrs[2];
     attrs[0].id = cudaLaunchAttributeClusterDimension;
@@ -553,9 +719,102 @@ cudaError_t launch_verify_attn(const sv_attn_shape& s, const uint16_t* q, const 
     attrs[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attrs;
     cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, attn_tc_kernel, *reinterpret_cast<const CUtensorMap*>(tK),
+    return cudaLaunchKernelEx(&cfg, attn_tc_kernel<kHalf>, *reinterpret_cast<const CUtensorMap*>(tK),
                               *reinterpret_cast<const CUtensorMap*>(tV), *reinterpret_cast<const CUtensorMap*>(tKb),
                               *reinterpret_cast<const CUtensorMap*>(tVb), a);
+}
+
+}  // namespace
+
+// Split-KV plan.  Every (sequence, KV head, row tile) -- a unit -- gets
+// `clusters` clusters of `splits` CTAs; its key tiles are divided evenly over
+// those CTAs.  Candidates C = 16, 8, 4, 2, 1 take as many clusters per unit as
+// fit in one wave of resident clusters (at most 32, at least one key tile per
+// CTA); the cost counts the key tiles of the busiest CTA plus a fixed start-up
+// of three tiles per wave, and a merge through the workspace as six tiles (its
+// partials cross the L2 in a few dependent round trips, measured at several
+// microseconds).  Ties keep the larger cluster.
+AttnPlan attn_plan(const sv_attn_shape& s) {
+    AttnPlan p;
+    p.G = s.Hq / s.Hkv;
+    p.rows = s.R * p.G;
+    p.row_tiles = (p.rows + kRows - 1) / kRows;
+    p.half = p.rows <= kHalfMaxRows;
+    p.warps = p.half ? Roles<true>::kThreads / 32 : Roles<false>::kThreads / 32;
+    const int64_t units = static_cast<int64_t>(s.B) * s.Hkv * p.row_tiles;
+    const int64_t tiles = (s.T_cap + kNk - 1) / kNk + (s.R + kNk - 1) / kNk;
+    int64_t best = -1;
+    p.splits = 1;
+    p.clusters = 1;
+    for (int C = kMaxCluster; C >= 1; C >>= 1) {
+        if (C > tiles && C > 1) continue;
+        const int64_t cap = p.half ? active_clusters<true>(C) : active_clusters<false>(C);
+        int64_t nc = cap / units;
+        if (nc > 32) nc = 32;
+        if (nc > tiles / C) nc = tiles / C;
+        if (nc < 1) nc = 1;
+        const int64_t waves = (units * nc + cap - 1) / cap;
+        const int64_t per_cta = (tiles + C * nc - 1) / (C * nc);
+        const int64_t cost = waves * (3 + per_cta) + (nc > 1 ? kMergeCost : 0);
+        if (best < 0 || cost < best) {
+            best = cost;
+            p.splits = C;
+            p.clusters = static_cast<int>(nc);
+        }
+    }
+    return p;
+}
+
+// Ticket words (one per unit, 256-byte aligned block) then the partial records.
+static size_t attn_ticket_bytes(const AttnPlan& p, const sv_attn_shape& s) {
+    const size_t units = static_cast<size_t>(s.B) * s.Hkv * p.row_tiles;
+    return (units * 4 + 255) / 256 * 256;
+}
+
+size_t attn_workspace(const sv_attn_shape& s) {
+    const AttnPlan p = attn_plan(s);
+    if (p.clusters <= 1) return 0;
+    const size_t units = static_cast<size_t>(s.B) * s.Hkv * p.row_tiles;
+    const size_t part_rows = p.rows < kRows ? p.rows : kRows;
+    return attn_ticket_bytes(p, s) + units * p.clusters * part_rows * kRec * sizeof(float);
+}
+
+cudaError_t launch_verify_attn(const sv_attn_shape& s, const uint16_t* q, const uint16_t* k_cache,
+                               const uint16_t* v_cache, const int32_t* len, const uint16_t* k_blk,
+                               const uint16_t* v_blk, const int32_t* parent, float scale, uint16_t* out,
+                               void* ws, cudaStream_t st) {
+    const AttnPlan p = attn_plan(s);
+    if (p.clusters > 1 && ws == nullptr) return cudaErrorInvalidValue;
+    alignas(64) uint8_t tK[128], tV[128], tKb[128], tVb[128];
+    const uint64_t ctx_rows = static_cast<uint64_t>(s.B) * s.Hkv * s.T_cap;
+    const uint64_t blk_rows = static_cast<uint64_t>(s.B) * s.Hkv * s.R;
+    if (!encode_tmap_2d_bf16(tK, k_cache, kD, ctx_rows, kD * 2, 64, kNk) ||
+        !encode_tmap_2d_bf16(tV, v_cache, kD, ctx_rows, kD * 2, 64, kNk) ||
+        !encode_tmap_2d_bf16(tKb, k_blk, kD, blk_rows, kD * 2, 64, kNk) ||
+        !encode_tmap_2d_bf16(tVb, v_blk, kD, blk_rows, kD * 2, 64, kNk))
+        return cudaErrorInvalidValue;
+    AttnArgs a;
+    a.q = q;
+    a.len = len;
+    a.parent = parent;
+    a.out = out;
+    a.err = device_error_word();
+    a.ws_cnt = p.clusters > 1 ? static_cast<unsigned int*>(ws) : nullptr;
+    a.ws_part = p.clusters > 1 ? reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + attn_ticket_bytes(p, s))
+                               : nullptr;
+    a.B = s.B;
+    a.R = s.R;
+    a.Hq = s.Hq;
+    a.Hkv = s.Hkv;
+    a.G = p.G;
+    a.T_cap = s.T_cap;
+    a.rows = p.rows;
+    a.row_tiles = p.row_tiles;
+    a.clusters = p.clusters;
+    a.part_rows = p.rows < kRows ? p.rows : kRows;
+    a.scale_log2 = scale * 1.4426950408889634f;
+    return p.half ? launch_mode<true>(p, s, tK, tV, tKb, tVb, a, st)
+                  : launch_mode<false>(p, s, tK, tV, tKb, tVb, a, st);
 }
 
 }  // namespace sv

@@ -60,9 +60,15 @@ def test_host_validation_rejects_before_launch(lib):
     s = b._AttnShape(1, 5, 12, 5, 128, 4096)   # Hq % Hkv != 0
     assert L.sv_verify_attn(ctypes.byref(s), fake, fake, fake, fake, fake, fake, None, ctypes.c_float(0.1), fake,
                             fake, 1 << 30, None) == 2
-    # the attention merges its splits on chip: no workspace
-    s = b._AttnShape(1, 5, 12, 2, 128, 4096)
-    assert L.sv_verify_attn_workspace(ctypes.byref(s)) == 0
+    # batch 1: several clusters per KV head meet in the workspace, which is
+    # then required (NULL -> argument error, short -> workspace error)
+    s = b._AttnShape(1, 5, 12, 2, 128, 4224)
+    need = L.sv_verify_attn_workspace(ctypes.byref(s))
+    assert need > 0 and need % 16 == 0
+    assert L.sv_verify_attn(ctypes.byref(s), fake, fake, fake, fake, fake, fake, None, ctypes.c_float(0.1), fake,
+                            None, need, None) == 1
+    assert L.sv_verify_attn(ctypes.byref(s), fake, fake, fake, fake, fake, fake, None, ctypes.c_float(0.1), fake,
+                            fake, need - 16, None) == 4
     # short workspace
     assert L.sv_accept_greedy(fake, fake, None, 1, 5, 151936, fake, fake, fake, fake, 8, None) == 4
     # temperature must be positive; vocab must be a multiple of 4
