@@ -9,7 +9,7 @@ than the 129 MB L2 (the KV cache of all layers plus the LM-head weights), so
 no L2 flush is needed between steps.
 
 Default workload: the 28-layer Qwen2.5-1.5B-shaped round (t = 4096, k = 4,
-batch 1, greedy).  `--workload` selects another (0, 1, 2, 3, 3b16, 3s, 3b16s).
+batch 1, greedy).  `--workload` selects another (0, 1, 2, 3, 3b16, 3s, 3b16s, 4 = draft tree).
 
 Timing: the step is captured into a CUDA graph through the library's C ABI;
 the timed region replays a graph of `chunk` steps (K steps in total) between
@@ -61,9 +61,16 @@ def workload_from_name(name: str):
         "0": (0, {}, "greedy"), "1": (1, {}, "greedy"), "2": (2, {}, "sampled"),
         "3": (3, {}, "greedy"), "3s": (3, {}, "sampled"),
         "3b16": (3, {"B": 16}, "greedy"), "3b16s": (3, {"B": 16}, "sampled"),
+        "4": (4, {}, "greedy"),
     }
     wid, over, mode = table[name]
     return synth.workload(wid, **over), mode
+
+
+def tree_parents(w) -> np.ndarray:
+    """[B, R] parent arrays of the workload's draft trees (one per sequence)."""
+    return np.stack([synth.random_tree(w.R - 1, w.tree_depth, 3, synth.seed_for(w.wid, 12 + b))
+                     for b in range(w.B)]).astype(np.int32)
 
 
 def attn_bytes(w) -> int:
@@ -129,10 +136,15 @@ class Round:
             self.attn_ws = torch.zeros(max(sv.verify_attn_workspace(*shape), 16), dtype=torch.uint8, device=device)
             self.hid, self.W = synth.lm_inputs(w, device=device)
             self.logits = torch.empty(B * R, V, dtype=torch.float32, device=device)
+            par = tree_parents(w) if w.tree else None
+            self.parent = None if par is None else torch.from_numpy(par).to(device)
             # planted drafts: argmax of every verify row of the synthetic logits
             g = torch.argmax(self.hid.float() @ self.W.float(), dim=-1).reshape(B, R).cpu().numpy()
             if mode == "greedy":
-                tok = synth.plant_chain_drafts(g, w.accept_rate, V, synth.seed_for(w.wid, 11))
+                if w.tree:
+                    tok = synth.plant_tree_drafts(g, par, w.accept_rate, V, synth.seed_for(w.wid, 11))
+                else:
+                    tok = synth.plant_chain_drafts(g, w.accept_rate, V, synth.seed_for(w.wid, 11))
                 self.tok = torch.from_numpy(tok).to(device)
             else:
                 # draft distributions around the round's actual target logits
@@ -141,6 +153,7 @@ class Round:
                                          logits=self.logits.reshape(B, R, V).clone())
                 self.q_draft, self.tok = si.q, si.tok
         else:
+            self.parent = None
             si = synth.sample_inputs(B, R - 1, V, wid=w.wid, device=device)
             self.logits = si.logits.reshape(B * R, V)
             self.q_draft, self.tok = si.q, si.tok
@@ -158,9 +171,10 @@ class Round:
         n = 0
         if self.has_model:
             n += self.w.L                            # one cluster kernel per layer
-            n += (self.w.B * self.w.R + 63) // 64    # LM head passes of <= 64 rows
+            N = self.w.B * self.w.R                  # LM head: <= 16 rows per 64-row pass, else 256
+            n += (N + 63) // 64 if N <= 16 else (N + 255) // 256
             n += 1                                   # commit
-        n += 2                                       # accept: two kernels
+        n += 2 if self.mode == "greedy" else 4      # accept: greedy two kernels; sampled chain: stats + three
         return n
 
     def step(self, ev=None):
@@ -173,7 +187,7 @@ class Round:
             rec("attn0")
             for l in range(w.L):
                 sv.verify_attn(self.q[l], self.kc[l], self.vc[l], self.length, self.kb[l], self.vb[l],
-                               out=self.attn_out[l], ws=self.attn_ws)
+                               parent=self.parent, out=self.attn_out[l], ws=self.attn_ws)
             rec("attn1")
             sv.lm_head(self.hid, self.W, logits=self.logits)
             rec("lm1")
@@ -181,7 +195,8 @@ class Round:
             rec("attn0"); rec("attn1"); rec("lm1")
         lg = self.logits.reshape(w.B, w.R, w.V)
         if self.mode == "greedy":
-            sv.accept_greedy(lg, self.tok, n_acc=self.n_acc, out_tok=self.out_tok, path=self.path, ws=self.acc_ws)
+            sv.accept_greedy(lg, self.tok, parent=self.parent, n_acc=self.n_acc, out_tok=self.out_tok,
+                             path=self.path, ws=self.acc_ws)
         else:
             sv.accept_sample(lg, self.q_draft, self.tok, temperature=w.temperature, seed=0x5EED, step=0,
                              n_acc=self.n_acc, out_tok=self.out_tok, path=self.path, ws=self.acc_ws)
@@ -293,7 +308,7 @@ class OracleRound:
             edges = np.linspace(0, V, n + 1).astype(int)
             self.lm_units = [(int(edges[i]), int(edges[i + 1])) for i in range(n)]
             self.G = G
-            self.kc_sl = {}
+            self.parent = tree_parents(w) if w.tree else None
             self.logits = np.random.default_rng(1).standard_normal((B, R, V)).astype(np.float32)
         else:
             si = synth.sample_inputs(B, R - 1, V, wid=w.wid)
@@ -318,7 +333,8 @@ class OracleRound:
             q = np.ascontiguousarray(self.q[:, :, g * G:(g + 1) * G])
             kc = np.ascontiguousarray(self.kc[:, g:g + 1, k0:k1])
             vc = np.ascontiguousarray(self.vc[:, g:g + 1, k0:k1])
-            o.verify_attn(q, kc, vc, np.full(w.B, k1 - k0, np.int32), self.kb[:, g:g + 1], self.vb[:, g:g + 1])
+            o.verify_attn(q, kc, vc, np.full(w.B, k1 - k0, np.int32), self.kb[:, g:g + 1], self.vb[:, g:g + 1],
+                          self.parent)
             v0, v1 = self.lm_units[i]
             o.lm_head(self.hid, np.ascontiguousarray(self.W[:, v0:v1]))
             if i == self.units - 1:
@@ -334,7 +350,7 @@ class OracleRound:
     def _accept_commit(self):
         o, w = self.oracle, self.w
         if self.mode == "greedy":
-            n_acc, _, path = o.accept_greedy(self.logits, self.tok)
+            n_acc, _, path = o.accept_greedy(self.logits, self.tok, getattr(self, "parent", None))
         else:
             n_acc, _, path = o.accept_sample(self.logits, self.qd, self.tok, seed=0x5EED)
         # commit of every layer: the same per-layer copy, done L times
@@ -354,13 +370,13 @@ def time_oracle(w, mode, units_total: int):
     return steps / dt, orc, dt
 
 
-def cpu_baseline(w, mode, seconds=12.0):
+def cpu_baseline(w, mode, seconds=15.0):
     orc = OracleRound(w, mode)
     t0 = time.perf_counter()
     orc.run_unit(0)
     per_unit = max(time.perf_counter() - t0, 1e-4)
     units = max(orc.units, int(seconds / per_unit))
-    units = min(units, 3 * orc.units)
+    units = min(units, 200 * orc.units)
     value, orc, dt = time_oracle(w, mode, units)
     return {"value": value, "unit": "steps/s", "cores": orc.oracle.num_threads(), "kind": "oracle",
             "sample": f"{units} of the {orc.units} equal work units of one round "
@@ -414,7 +430,7 @@ def run_reference(args, ws, rank):
     t0 = time.perf_counter()
     orc.run_unit(0)
     per_unit = max(time.perf_counter() - t0, 1e-4)
-    budget = 150.0
+    budget = args.ref_seconds
     per_step_units = max(1, min(orc.units, int(budget / max(1, args.steps + args.warmup) / per_unit)))
     for i in range(args.warmup):
         for j in range(per_step_units):
@@ -449,6 +465,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=500)
     ap.add_argument("--layers", type=int, default=None, help="override the layer count (small profiling cases)")
+    ap.add_argument("--ref-seconds", type=float, default=150.0,
+                    help="host-time budget of the reference (oracle) arm's timed steps")
     args = ap.parse_args()
     ws, rank, local = dist_setup()
     if args.impl == "reference":

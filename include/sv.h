@@ -207,6 +207,13 @@ SV_API sv_status sv_accept_greedy(const float* logits, const int32_t* tok, const
  *            alignment: the draft vocab is zero-padded to the target's).
  *   tok, parent as for sv_accept_greedy;  temperature > 0
  *   outputs as for sv_accept_greedy. */
+/* Workspace: the (M, Z) statistics of every row (B*R float2, padded to 256
+ * bytes), then for chain drafts one record per sequence and the summation-tree
+ * sums of the one full-vocab pass it needs (B * 16 bytes padded to 256, then
+ * B * 2 * (64*32 + 64) floats).  Chains then run three short launches (all
+ * ratio tests at once, the residual or bonus pass spread over the GPU, one
+ * warp per sequence for the draw); trees walk each sequence with one cluster.
+ * Both give the same result bit for bit. */
 SV_API size_t sv_accept_sample_workspace(int32_t B, int32_t R, int32_t V);
 SV_API sv_status sv_accept_sample(const float* logits, const float* q, int32_t Vq, const int32_t* tok,
                            const int32_t* parent, int32_t B, int32_t R, int32_t V, float temperature,

@@ -43,6 +43,10 @@ constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kMaxLocalBlocks = kMaxBlocks / kCluster;
 constexpr int kMaxR = 128;
+#ifndef SV_ROW_STATS_MIN_ROWS
+#define SV_ROW_STATS_MIN_ROWS 128
+#endif
+constexpr int kRowStatsMinRows = SV_ROW_STATS_MIN_ROWS;   // B*R from which statistics use one CTA per row
 
 // With SV_SYNC_EACH_KERNEL=1 in the environment the launchers synchronise
 // after every kernel so a failing kernel is reported by name.
@@ -237,7 +241,7 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads)
 
     // local max of z = l / T (z stored back when T != 1)
     float m = -INFINITY;
-    bool bad = false;
+    float nf = 0.0f;   // stays 0 unless some z is NaN or infinite (z * 0 is then NaN)
     for (int lb = 0; lb < nlocal; ++lb) {
         const int gb = rank + lb * kCluster;
         const int n = min(kBlk, V - gb * kBlk);
@@ -248,11 +252,11 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads)
                 x = make_float4(__fdiv_rn(x.x, T), __fdiv_rn(x.y, T), __fdiv_rn(x.z, T), __fdiv_rn(x.w, T));
                 *reinterpret_cast<float4*>(s + i) = x;
             }
-            bad |= !(isfinite(x.x) && isfinite(x.y) && isfinite(x.z) && isfinite(x.w));
+            nf = __fmaf_rn(x.x, 0.0f, __fmaf_rn(x.y, 0.0f, __fmaf_rn(x.z, 0.0f, __fmaf_rn(x.w, 0.0f, nf))));
             m = fmaxf(fmaxf(m, fmaxf(x.x, x.y)), fmaxf(x.z, x.w));
         }
     }
-    if (bad) raise_error(err, SV_DEVERR_NONFINITE);
+    if (nf != 0.0f) raise_error(err, SV_DEVERR_NONFINITE);
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
     if (lane == 0) wred[warp] = m;
@@ -276,8 +280,8 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads)
         float4 e = make_float4(0.f, 0.f, 0.f, 0.f);
         if (v < V) {
             const float4 z = *reinterpret_cast<const float4*>(srow + lb * kBlk + c * kChunk + 4 * lane);
-            e = make_float4(sv_exp(__fsub_rn(z.x, M)), sv_exp(__fsub_rn(z.y, M)), sv_exp(__fsub_rn(z.z, M)),
-                            sv_exp(__fsub_rn(z.w, M)));
+            e = make_float4(sv_exp_nb(__fsub_rn(z.x, M)), sv_exp_nb(__fsub_rn(z.y, M)), sv_exp_nb(__fsub_rn(z.z, M)),
+                            sv_exp_nb(__fsub_rn(z.w, M)));
         }
         const float cs = warp_tree_sum(quad_sum(e));
         if (lane == 0) csum[cid] = cs;
@@ -297,6 +301,100 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads)
             stats[row] = make_float2(M, Z);
         }
     }
+}
+
+// Many rows (B*R large): persistent CTAs, one per SM, each taking whole rows
+// (row blockIdx.x, + gridDim.x, ...), no cluster and no staging.  Pass 1
+// takes the exact maximum of z = l / T from HBM; pass 2 re-reads the row and
+// builds the same canonical tree: chunk sums of exp(z - M) over 128 leaves (4
+// per lane), block sums over 32 chunks, then the 64 zero-padded block sums.
+// One row in flight per SM keeps the re-read in L2 (152 x 600 KB < 126 MB).
+constexpr int kRowThreads = 512;
+constexpr int kRowWarps = kRowThreads / 32;
+
+__global__ void __launch_bounds__(kRowThreads, 1) sample_stats_row_kernel(const float* __restrict__ logits, int V,
+                                                                         float T, int nblk, int nrows,
+                                                                         float2* __restrict__ stats,
+                                                                         unsigned int* err) {
+    __shared__ float csum[kMaxBlocks * kChunksPerBlk];
+    __shared__ float bsum[kMaxBlocks];
+    __shared__ float wred[kRowWarps];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int nvec = V / 4;
+  for (int row = blockIdx.x; row < nrows; row += gridDim.x) {
+    const float* L = logits + static_cast<size_t>(row) * V;
+
+    // pass 1: max, eight loads in flight per thread
+    float m = -INFINITY;
+    float nf = 0.0f;   // stays 0 unless some z is NaN or infinite (z * 0 is then NaN)
+    for (int i0 = tid; i0 < nvec; i0 += 8 * kRowThreads) {
+        float4 x[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int i = i0 + u * kRowThreads;
+            x[u] = i < nvec ? __ldg(reinterpret_cast<const float4*>(L) + i) : make_float4(-INFINITY, -INFINITY,
+                                                                                           -INFINITY, -INFINITY);
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            if (i0 + u * kRowThreads >= nvec) continue;
+            float4 z = x[u];
+            if (T != 1.0f) z = make_float4(__fdiv_rn(z.x, T), __fdiv_rn(z.y, T), __fdiv_rn(z.z, T), __fdiv_rn(z.w, T));
+            nf = __fmaf_rn(z.x, 0.0f, __fmaf_rn(z.y, 0.0f, __fmaf_rn(z.z, 0.0f, __fmaf_rn(z.w, 0.0f, nf))));
+            m = fmaxf(fmaxf(m, fmaxf(z.x, z.y)), fmaxf(z.z, z.w));
+        }
+    }
+    if (nf != 0.0f) raise_error(err, SV_DEVERR_NONFINITE);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+    if (lane == 0) wred[warp] = m;
+    __syncthreads();
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kRowWarps; ++w) M = fmaxf(M, wred[w]);
+
+    // pass 2: chunk sums (level 7), four chunks' loads in flight per warp
+    const int nch = nblk * kChunksPerBlk;
+    for (int c0 = warp; c0 < nch; c0 += 4 * kRowWarps) {
+        float4 x[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int v = (c0 + u * kRowWarps) * kChunk + 4 * lane;
+            x[u] = (c0 + u * kRowWarps < nch && v < V) ? __ldg(reinterpret_cast<const float4*>(L + v))
+                                                       : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int c = c0 + u * kRowWarps;
+            const int v = c * kChunk + 4 * lane;
+            float4 e = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (c < nch && v < V) {
+                float4 z = x[u];
+                if (T != 1.0f)
+                    z = make_float4(__fdiv_rn(z.x, T), __fdiv_rn(z.y, T), __fdiv_rn(z.z, T), __fdiv_rn(z.w, T));
+                e = make_float4(sv_exp_nb(__fsub_rn(z.x, M)), sv_exp_nb(__fsub_rn(z.y, M)), sv_exp_nb(__fsub_rn(z.z, M)),
+                                sv_exp_nb(__fsub_rn(z.w, M)));
+            }
+            const float cs = warp_tree_sum(quad_sum(e));
+            if (lane == 0 && c < nch) csum[c] = cs;
+        }
+    }
+    __syncthreads();
+    // block sums (level 12); blocks beyond the vocab are zero
+    for (int bk = warp; bk < kMaxBlocks; bk += kRowWarps) {
+        const float bs = bk < nblk ? warp_tree_sum(csum[bk * kChunksPerBlk + lane]) : 0.0f;
+        if (lane == 0) bsum[bk] = bs;
+    }
+    __syncthreads();
+    if (warp == 0) {
+        const float Z = warp_tree_sum(__fadd_rn(bsum[2 * lane], bsum[2 * lane + 1]));   // level 13 -> 18
+        if (lane == 0) {
+            if (!(Z > 0.0f) || !isfinite(Z)) raise_error(err, SV_DEVERR_NONFINITE);
+            stats[row] = make_float2(M, Z);
+        }
+    }
+    __syncthreads();   // wred, csum and bsum are reused by the next row
+  }
 }
 
 // ==========================================================================
@@ -334,7 +432,7 @@ struct RowValues {
 
     __device__ __forceinline__ float one(float l, float qv) const {
         const float z = (T == 1.0f) ? l : __fdiv_rn(l, T);
-        float w = __fdiv_rn(sv_exp(__fsub_rn(z, M)), Z);
+        float w = __fdiv_rn(sv_exp_nb(__fsub_rn(z, M)), Z);
         for (int s = 0; s < nsteps; ++s) {
             const float d = __fsub_rn(w, qv);
             const float rho = d > 0.0f ? d : 0.0f;
@@ -351,20 +449,31 @@ struct RowValues {
         const float qv = (Q != nullptr && v < Vq) ? __ldg(Q + v) : 0.0f;
         return one(__ldg(L + v), qv);
     }
-    // 4 consecutive entries starting at v (v % 4 == 0, v < V, V % 4 == 0)
-    __device__ __forceinline__ float4 at4(int v) const {
-        if (!SV_CHECK(v >= 0 && v + 3 < V && (v & 3) == 0, err, 6)) return make_float4(0.f, 0.f, 0.f, 0.f);
-        const float4 l = __ldg(reinterpret_cast<const float4*>(L + v));
-        float4 qv = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (Q != nullptr && v < Vq) qv = __ldg(reinterpret_cast<const float4*>(Q + v));
-        return make_float4(one(l.x, qv.x), one(l.y, qv.y), one(l.z, qv.z), one(l.w, qv.w));
+    // 4 consecutive entries starting at v (v % 4 == 0, v < V, V % 4 == 0),
+    // as a load (raw) and an evaluation, so callers can batch the loads
+    struct Raw {
+        float4 l, q;
+    };
+    __device__ __forceinline__ Raw load4(int v) const {
+        Raw r{make_float4(0.f, 0.f, 0.f, 0.f), make_float4(0.f, 0.f, 0.f, 0.f)};
+        if (!SV_CHECK(v >= 0 && v + 3 < V && (v & 3) == 0, err, 6)) return r;
+        r.l = __ldg(reinterpret_cast<const float4*>(L + v));
+        if (Q != nullptr && v < Vq) r.q = __ldg(reinterpret_cast<const float4*>(Q + v));
+        return r;
     }
+    __device__ __forceinline__ float4 eval4(const Raw& r) const {
+        return make_float4(one(r.l.x, r.q.x), one(r.l.y, r.q.y), one(r.l.z, r.q.z), one(r.l.w, r.q.w));
+    }
+    __device__ __forceinline__ float4 at4(int v) const { return eval4(load4(v)); }
 };
 
 // Raw values of a float array (diagnostic path).
 struct ArrayValues {
     const float* x;
-    __device__ __forceinline__ float4 at4(int v) const { return __ldg(reinterpret_cast<const float4*>(x + v)); }
+    using Raw = float4;
+    __device__ __forceinline__ Raw load4(int v) const { return __ldg(reinterpret_cast<const float4*>(x + v)); }
+    __device__ __forceinline__ float4 eval4(const Raw& r) const { return r; }
+    __device__ __forceinline__ float4 at4(int v) const { return load4(v); }
 };
 
 // Shared state of one cluster's full-vocab pass.
@@ -375,6 +484,7 @@ struct PassSmem {
     int token;
     int node;
     float acc;
+    float total;   // canonical sum of the last full pass
 };
 
 // Builds the levels above `n` leaves (n a power of two <= 64) in sm.tree by
@@ -421,12 +531,26 @@ __device__ float full_pass(const Vals& vals, int V, int nblk, PassSmem& sm, cg::
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nlocal = rank < nblk ? (nblk - rank + kCluster - 1) / kCluster : 0;
     cluster.sync();   // all CTAs started (first pass) / previous pass fully consumed everywhere
-    for (int cid = warp; cid < nlocal * kChunksPerBlk; cid += kWarps) {
-        const int lb = cid / kChunksPerBlk, c = cid % kChunksPerBlk;
-        const int v = (rank + lb * kCluster) * kBlk + c * kChunk + 4 * lane;
-        const float4 x = v < V ? vals.at4(v) : make_float4(0.f, 0.f, 0.f, 0.f);
-        const float cs = warp_tree_sum(quad_sum(x));
-        if (lane == 0) sm.csum[cid] = cs;
+    const int nch = nlocal * kChunksPerBlk;
+    constexpr int kBatch = 2;   // chunks whose loads a warp keeps in flight
+    for (int cid0 = warp; cid0 < nch; cid0 += kBatch * kWarps) {
+        typename Vals::Raw raw[kBatch];
+        bool live[kBatch];
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+            const int cid = cid0 + u * kWarps;
+            const int lb = cid / kChunksPerBlk, c = cid % kChunksPerBlk;
+            const int v = (rank + lb * kCluster) * kBlk + c * kChunk + 4 * lane;
+            live[u] = cid < nch && v < V;
+            if (live[u]) raw[u] = vals.load4(v);
+        }
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+            const int cid = cid0 + u * kWarps;
+            const float4 x = live[u] ? vals.eval4(raw[u]) : make_float4(0.f, 0.f, 0.f, 0.f);
+            const float cs = warp_tree_sum(quad_sum(x));
+            if (lane == 0 && cid < nch) sm.csum[cid] = cs;
+        }
     }
     __syncthreads();
     if (warp < nlocal) {
@@ -434,19 +558,56 @@ __device__ float full_pass(const Vals& vals, int V, int nblk, PassSmem& sm, cg::
         if (lane < kCluster) *cluster.map_shared_rank(&sm.bsum[rank + warp * kCluster], lane) = bs;
     }
     cluster.sync();
-    float lvl[kMaxBlocks / 2];
-#pragma unroll
-    for (int i = 0; i < kMaxBlocks / 2; ++i) lvl[i] = __fadd_rn(sm.bsum[2 * i], sm.bsum[2 * i + 1]);
-#pragma unroll
-    for (int n = kMaxBlocks / 4; n >= 1; n >>= 1)
-#pragma unroll
-        for (int i = 0; i < n; ++i) lvl[i] = __fadd_rn(lvl[2 * i], lvl[2 * i + 1]);
-    return lvl[0];
+    // levels 13 -> 18 over the 64 block sums (lane i: blocks 2i, 2i+1)
+    if (warp == 0) {
+        const float tot = warp_tree_sum(__fadd_rn(sm.bsum[2 * lane], sm.bsum[2 * lane + 1]));
+        if (lane == 0) sm.total = tot;
+    }
+    __syncthreads();
+    return sm.total;
 }
 
 // One descent step: children sums sl, sr of the current node.
 __device__ __forceinline__ bool go_left(float tau, float acc, float sl, float sr) {
     return tau < __fadd_rn(acc, sl) || sr == 0.0f;
+}
+
+// Levels 7 -> 0 of the summation tree inside one 128-leaf chunk starting at
+// v0, by one full warp that recomputes the chunk's leaves; acc is the prefix
+// sum before the chunk and tau the target.  Returns the token (every lane).
+template <class Vals>
+__device__ __forceinline__ int descend_chunk(const Vals& vals, int v0, int V, float tau, float acc) {
+    const int lane = threadIdx.x & 31;
+    const int v = v0 + 4 * lane;
+    const float4 x = v < V ? vals.at4(v) : make_float4(0.f, 0.f, 0.f, 0.f);
+    const float n1a = __fadd_rn(x.x, x.y), n1b = __fadd_rn(x.z, x.w);
+    float lvl[6];                      // lvl[k]: node at level k+2 containing this lane
+    lvl[0] = __fadd_rn(n1a, n1b);
+#pragma unroll
+    for (int k = 1; k < 6; ++k) lvl[k] = __fadd_rn(lvl[k - 1], __shfl_xor_sync(0xffffffffu, lvl[k - 1], 1 << (k - 1)));
+    int base = 0;                       // first lane of the current node
+#pragma unroll
+    for (int k = 5; k >= 1; --k) {      // node at level k+2 -> children at level k+1
+        const int half = 1 << (k - 1);
+        const float sl = __shfl_sync(0xffffffffu, lvl[k - 1], base);
+        const float sr = __shfl_sync(0xffffffffu, lvl[k - 1], base + half);
+        if (!go_left(tau, acc, sl, sr)) {
+            acc = __fadd_rn(acc, sl);
+            base += half;
+        }
+    }
+    // level 2 -> 1 -> 0 inside lane `base`
+    const float a = __shfl_sync(0xffffffffu, x.x, base), bb = __shfl_sync(0xffffffffu, x.y, base);
+    const float c = __shfl_sync(0xffffffffu, x.z, base), d = __shfl_sync(0xffffffffu, x.w, base);
+    const float s01 = __fadd_rn(a, bb), s23 = __fadd_rn(c, d);
+    int leaf;
+    if (go_left(tau, acc, s01, s23)) {
+        leaf = go_left(tau, acc, a, bb) ? 0 : 1;
+    } else {
+        acc = __fadd_rn(acc, s01);
+        leaf = go_left(tau, acc, c, d) ? 2 : 3;
+    }
+    return min(v0 + 4 * base + leaf, V - 1);
 }
 
 // Inverse-CDF draw after full_pass(vals): returns the token in the CTA that
@@ -484,38 +645,8 @@ __device__ int tree_descent(const Vals& vals, int V, float total, float u, PassS
     if (!SV_CHECK(chunk >= 0 && chunk < kChunksPerBlk, err, 2)) return -1;
     // levels 7 -> 0 inside the chunk: warp 0 recomputes its 128 leaves
     if ((threadIdx.x >> 5) == 0) {
-        const int lane = threadIdx.x & 31;
-        const int v0 = blk * kBlk + chunk * kChunk;
-        const int v = v0 + 4 * lane;
-        const float4 x = v < V ? vals.at4(v) : make_float4(0.f, 0.f, 0.f, 0.f);
-        const float n1a = __fadd_rn(x.x, x.y), n1b = __fadd_rn(x.z, x.w);
-        float lvl[6];                      // lvl[k]: node at level k+2 containing this lane
-        lvl[0] = __fadd_rn(n1a, n1b);
-#pragma unroll
-        for (int k = 1; k < 6; ++k) lvl[k] = __fadd_rn(lvl[k - 1], __shfl_xor_sync(0xffffffffu, lvl[k - 1], 1 << (k - 1)));
-        int base = 0;                       // first lane of the current node
-#pragma unroll
-        for (int k = 5; k >= 1; --k) {      // node at level k+2 -> children at level k+1
-            const int half = 1 << (k - 1);
-            const float sl = __shfl_sync(0xffffffffu, lvl[k - 1], base);
-            const float sr = __shfl_sync(0xffffffffu, lvl[k - 1], base + half);
-            if (!go_left(tau, acc, sl, sr)) {
-                acc = __fadd_rn(acc, sl);
-                base += half;
-            }
-        }
-        // level 2 -> 1 -> 0 inside lane `base`
-        const float a = __shfl_sync(0xffffffffu, x.x, base), bb = __shfl_sync(0xffffffffu, x.y, base);
-        const float c = __shfl_sync(0xffffffffu, x.z, base), d = __shfl_sync(0xffffffffu, x.w, base);
-        const float s01 = __fadd_rn(a, bb), s23 = __fadd_rn(c, d);
-        int leaf;
-        if (go_left(tau, acc, s01, s23)) {
-            leaf = go_left(tau, acc, a, bb) ? 0 : 1;
-        } else {
-            acc = __fadd_rn(acc, s01);
-            leaf = go_left(tau, acc, c, d) ? 2 : 3;
-        }
-        if (lane == 0) sm.token = min(v0 + 4 * base + leaf, V - 1);
+        const int tokn = descend_chunk(vals, blk * kBlk + chunk * kChunk, V, tau, acc);
+        if ((threadIdx.x & 31) == 0) sm.token = tokn;
     }
     __syncthreads();
     return sm.token;
@@ -604,13 +735,174 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads)
 }
 
 // ==========================================================================
+// sampled, chain drafts: three launches instead of one walk per cluster
+// ==========================================================================
+//
+// In a chain every ratio test depends only on its own row's statistics, so
+// all k tests run at once (one thread per draft) and the first rejection is
+// found by a reduction; the one full-vocab pass the round then needs (the
+// residual max(0, p - q) of the rejection row, or p of the last row for the
+// bonus) is spread over one CTA per (sequence, 4096-block); one warp per
+// sequence finally descends the summation tree.  Values, sums, uniforms and
+// the descent are those of the cluster walk, term for term.
+
+constexpr int kChainResidual = 0, kChainBonus = 1;
+constexpr int kSumFloats = kMaxBlocks * kChunksPerBlk + kMaxBlocks;   // chunk sums then block sums
+
+struct ChainWs {
+    int4* rec;       // [B]: row u, mode, -, -
+    float* sums;     // [B][2][kSumFloats]: set 0 = residual, set 1 = p
+};
+
+__host__ __device__ constexpr size_t chain_ws_bytes(int B) {
+    return ((static_cast<size_t>(B) * sizeof(int4) + 255) / 256) * 256 +
+           static_cast<size_t>(B) * 2 * kSumFloats * sizeof(float);
+}
+
+__global__ void __launch_bounds__(kMaxR) chain_walk_kernel(SampleArgs a, ChainWs w) {
+    __shared__ int first_rej;
+    const int b = blockIdx.x, t = threadIdx.x;
+    const int R = a.R, V = a.V, Vq = a.Vq;
+    if (t == 0) first_rej = R - 1;
+    __syncthreads();
+    bool accept = true, tok_bad = false, q_bad = false;
+    if (t < R - 1) {   // draft j = t + 1 against row u = t
+        const int u = t, d = a.tok[static_cast<size_t>(b) * R + t + 1];
+        const float2 ms = a.stats[static_cast<size_t>(b) * R + u];
+        RowValues rv{a.logits + (static_cast<size_t>(b) * R + u) * V, a.q + (static_cast<size_t>(b) * (R - 1) + u) * Vq,
+                     Vq, a.T, ms.x, ms.y, nullptr, 0, false, V, a.err};
+        tok_bad = !(d >= 0 && d < V);
+        accept = false;
+        if (!tok_bad) {
+            const float qd = d < Vq ? __ldg(rv.Q + d) : 0.0f;
+            q_bad = !(qd >= 0.0f);
+            const float wd = rv.at(d);
+            const float ua = node_uniforms(a.seed, a.step, b, t + 1, a.uniforms, R).x;
+            accept = (qd == 0.0f) || (ua < __fdiv_rn(wd, qd));
+        }
+        if (!accept) atomicMin(&first_rej, t);
+    }
+    __syncthreads();
+    const int depth = first_rej;   // drafts 1..depth accepted
+    // flags only for the drafts the sequential walk reaches
+    if (t < R - 1 && t <= depth) {
+        if (tok_bad) raise_error(a.err, SV_DEVERR_TOKEN);
+        if (q_bad) raise_error(a.err, SV_DEVERR_QPROB);
+    }
+    int32_t* pth = a.path + static_cast<size_t>(b) * R;
+    for (int j = t; j < R; j += blockDim.x) pth[j] = j <= depth ? j : -1;
+    if (t == 0) {
+        const bool rejected = depth < R - 1;
+        a.n_acc[b] = depth;
+        w.rec[b] = make_int4(depth, rejected ? kChainResidual : kChainBonus, 0, 0);
+    }
+}
+
+// One CTA per (4096-block, sequence): chunk and block sums of the residual and
+// of p over the row the walk stopped at.
+__global__ void __launch_bounds__(kThreads) chain_sums_kernel(SampleArgs a, ChainWs w) {
+    const int blk = blockIdx.x, b = blockIdx.y;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int V = a.V, Vq = a.Vq, R = a.R;
+    const int4 rc = w.rec[b];
+    const int u = rc.x;
+    const float2 ms = a.stats[static_cast<size_t>(b) * R + u];
+    const float* Qrow = rc.y == kChainResidual ? a.q + (static_cast<size_t>(b) * (R - 1) + u) * Vq : nullptr;
+    RowValues rv{a.logits + (static_cast<size_t>(b) * R + u) * V, Qrow, Vq, a.T, ms.x, ms.y, nullptr, 0, false, V,
+                 a.err};
+    float* sr = w.sums + static_cast<size_t>(b) * 2 * kSumFloats;
+    float* sp = sr + kSumFloats;
+    __shared__ float cr[kChunksPerBlk], cp[kChunksPerBlk];
+    constexpr int kPer = kChunksPerBlk / kWarps;   // chunks per warp
+    typename RowValues::Raw raw[kPer];
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+        const int v = blk * kBlk + (warp * kPer + i) * kChunk + 4 * lane;
+        if (v < V) raw[i] = rv.load4(v);
+    }
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+        const int c = warp * kPer + i;
+        const int v = blk * kBlk + c * kChunk + 4 * lane;
+        float4 p = make_float4(0.f, 0.f, 0.f, 0.f), r = p;
+        if (v < V) {
+            rv.residual = false;
+            p = rv.eval4(raw[i]);
+            auto res = [](float w, float qv) {   // RowValues::one with residual: max(0, w - q)
+                const float d = __fsub_rn(w, qv);
+                return d > 0.0f ? d : 0.0f;
+            };
+            r = make_float4(res(p.x, raw[i].q.x), res(p.y, raw[i].q.y), res(p.z, raw[i].q.z), res(p.w, raw[i].q.w));
+        }
+        const float csr = warp_tree_sum(quad_sum(r)), csp = warp_tree_sum(quad_sum(p));
+        if (lane == 0) {
+            cr[c] = csr;
+            cp[c] = csp;
+        }
+    }
+    __syncthreads();
+    if (warp == 0) {
+        const float br = warp_tree_sum(cr[lane]), bp = warp_tree_sum(cp[lane]);
+        sr[blk * kChunksPerBlk + lane] = cr[lane];
+        sp[blk * kChunksPerBlk + lane] = cp[lane];
+        if (lane == 0) {
+            sr[kMaxBlocks * kChunksPerBlk + blk] = br;
+            sp[kMaxBlocks * kChunksPerBlk + blk] = bp;
+        }
+    }
+}
+
+// One warp per sequence: totals (levels 13 -> 18), the choice between the
+// residual and p, and the descent.
+__global__ void __launch_bounds__(32) chain_draw_kernel(SampleArgs a, ChainWs w) {
+    __shared__ float bs[kMaxBlocks];
+    __shared__ float tree[2 * kMaxBlocks];
+    const int b = blockIdx.x, lane = threadIdx.x;
+    const int V = a.V, Vq = a.Vq, R = a.R;
+    const int4 rc = w.rec[b];
+    const int u = rc.x;
+    const float* base = w.sums + static_cast<size_t>(b) * 2 * kSumFloats;
+    auto block_sum = [&](const float* set, int i) { return i < a.nblk ? set[kMaxBlocks * kChunksPerBlk + i] : 0.0f; };
+    const float Sr = warp_tree_sum(__fadd_rn(block_sum(base, 2 * lane), block_sum(base, 2 * lane + 1)));
+    const float Sp = warp_tree_sum(__fadd_rn(block_sum(base + kSumFloats, 2 * lane),
+                                             block_sum(base + kSumFloats, 2 * lane + 1)));
+    // residual when it has mass, else p (also for the bonus)
+    const bool use_r = rc.y == kChainResidual && Sr > 0.0f;
+    const float* set = use_r ? base : base + kSumFloats;
+    const float total = use_r ? Sr : Sp;
+    const float2 ms = a.stats[static_cast<size_t>(b) * R + u];
+    RowValues rv{a.logits + (static_cast<size_t>(b) * R + u) * V,
+                 use_r ? a.q + (static_cast<size_t>(b) * (R - 1) + u) * Vq : nullptr, Vq, a.T, ms.x, ms.y, nullptr, 0,
+                 use_r, V, a.err};
+    const float tau = __fmul_rn(node_uniforms(a.seed, a.step, b, u, a.uniforms, R).y, total);
+    bs[lane] = block_sum(set, lane);
+    bs[lane + 32] = block_sum(set, lane + 32);
+    __syncwarp();
+    build_levels(bs, kMaxBlocks, tree);
+    float acc = 0.0f;
+    const int blk = descend_levels(tree, kMaxBlocks, tau, acc);
+    __syncwarp();
+    if (!SV_CHECK(blk >= 0 && blk < a.nblk, a.err, 10)) return;
+    build_levels(set + blk * kChunksPerBlk, kChunksPerBlk, tree);
+    const int chunk = descend_levels(tree, kChunksPerBlk, tau, acc);
+    const int tokn = descend_chunk(rv, blk * kBlk + chunk * kChunk, V, tau, acc);
+    if (lane == 0) a.out_tok[b] = tokn;
+}
+
+// ==========================================================================
 // diagnostics
 // ==========================================================================
 
 __global__ void diag_exp_kernel(const float* x, float* y, int64_t n) {
     for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
          i += static_cast<int64_t>(gridDim.x) * blockDim.x)
-        y[i] = sv_exp(x[i]);
+    {
+        // the branch-free form used by the softmax passes must agree bit for
+        // bit wherever it is defined; a disagreement shows up as 12345
+        const float e = sv_exp(x[i]);
+        const bool defined = !(x[i] != x[i]) && x[i] <= 88.0f;
+        y[i] = (defined && __float_as_uint(sv_exp_nb(x[i])) != __float_as_uint(e)) ? 12345.0f : e;
+    }
 }
 
 __global__ void diag_philox_kernel(const uint32_t* ctr, const uint32_t* key, uint32_t* out, int64_t n) {
@@ -659,12 +951,15 @@ cudaError_t launch_accept_greedy(const float* logits, const int32_t* tok, const 
     return cudaGetLastError();
 }
 
-size_t sample_workspace(int B, int R, int /*V*/) { return static_cast<size_t>(B) * R * sizeof(float2); }
+// Row statistics (B*R float2); then, for the chain path, the per-sequence
+// records and summation-tree sums.
+static size_t stats_bytes(int B, int R) { return ((static_cast<size_t>(B) * R * sizeof(float2) + 255) / 256) * 256; }
+size_t sample_workspace(int B, int R, int /*V*/) { return stats_bytes(B, R) + chain_ws_bytes(B); }
 
 cudaError_t launch_accept_sample(const float* logits, const float* q, int Vq, const int32_t* tok,
                                  const int32_t* parent, int B, int R, int V, float temperature, uint64_t seed,
                                  uint64_t step, const float* uniforms, int32_t* n_acc, int32_t* out_tok,
-                                 int32_t* path, void* ws, cudaStream_t st) {
+                                 int32_t* path, void* ws, size_t ws_bytes, cudaStream_t st) {
     unsigned int* err = device_error_word();
     const int nblk = blocks_for(V);
     const int nlocal = (nblk + kCluster - 1) / kCluster;
@@ -678,7 +973,15 @@ cudaError_t launch_accept_sample(const float* logits, const float* q, int Vq, co
         attr_set = true;
     }
     float2* stats = static_cast<float2*>(ws);
-    sample_stats_kernel<<<B * R * kCluster, kThreads, smem, st>>>(logits, V, temperature, nblk, nlocal, stats, err);
+    // Few rows: an 8-CTA cluster per row keeps each row's latency short.  Many
+    // rows: one CTA per row keeps every SM busy without cluster waves.
+    if (static_cast<int64_t>(B) * R >= kRowStatsMinRows)
+    {
+        const int nrows = B * R, grid = nrows < device_sm_count() ? nrows : device_sm_count();
+        sample_stats_row_kernel<<<grid, kRowThreads, 0, st>>>(logits, V, temperature, nblk, nrows, stats, err);
+    }
+    else
+        sample_stats_kernel<<<B * R * kCluster, kThreads, smem, st>>>(logits, V, temperature, nblk, nlocal, stats, err);
     if (debug_sync()) {
         e = cudaStreamSynchronize(st);
         if (e != cudaSuccess) return e;
@@ -702,7 +1005,20 @@ cudaError_t launch_accept_sample(const float* logits, const float* q, int Vq, co
     a.Vq = Vq;
     a.nblk = nblk;
     a.T = temperature;
-    sample_finish_kernel<<<B * kCluster, kThreads, 0, st>>>(a);
+    if (parent == nullptr && ws_bytes >= sample_workspace(B, R, V)) {
+        // chain: parallel ratio tests, one full-vocab pass over the whole GPU
+        ChainWs w;
+        w.rec = reinterpret_cast<int4*>(static_cast<uint8_t*>(ws) + stats_bytes(B, R));
+        w.sums = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + stats_bytes(B, R) +
+                                          ((static_cast<size_t>(B) * sizeof(int4) + 255) / 256) * 256);
+        chain_walk_kernel<<<B, kMaxR, 0, st>>>(a, w);
+        chain_sums_kernel<<<dim3(nblk, B), kThreads, 0, st>>>(a, w);
+        chain_draw_kernel<<<B, 32, 0, st>>>(a, w);
+    } else {
+        // trees (sibling residuals depend on each other), or a workspace that
+        // only holds the row statistics: one cluster walks each sequence
+        sample_finish_kernel<<<B * kCluster, kThreads, 0, st>>>(a);
+    }
     if (debug_sync()) {
         e = cudaStreamSynchronize(st);
         if (e != cudaSuccess) return e;

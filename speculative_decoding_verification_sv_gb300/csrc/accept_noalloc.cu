@@ -73,6 +73,7 @@ extern "C" sv_status sv_accept_sample_noalloc(const float* logits, const float* 
     if (!scratch) return SV_ERR_CUDA;
     const cudaError_t e = sv::launch_accept_sample(logits, q, Vq, tok, parent, B, R, V, temperature, seed, step,
                                                    uniforms, n_acc, out_tok, path, scratch,
+                                                   static_cast<size_t>(kNoAllocMaxRows) * sizeof(float2),
                                                    static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? SV_OK : SV_ERR_CUDA;
 }

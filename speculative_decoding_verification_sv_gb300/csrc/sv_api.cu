@@ -201,7 +201,7 @@ sv_status sv_accept_sample(const float* logits, const float* q, int32_t Vq, cons
     if (static_cast<int64_t>(B) * R * 8 > (int64_t(1) << 31) - 1) return SV_ERR_SHAPE;
     if (ws_bytes < sv::sample_workspace(B, R, V)) return SV_ERR_WORKSPACE;
     return launch_status(sv::launch_accept_sample(logits, q, Vq, tok, parent, B, R, V, temperature, seed, step,
-                                                  uniforms, n_acc, out_tok, path, ws, as_stream(stream)));
+                                                  uniforms, n_acc, out_tok, path, ws, ws_bytes, as_stream(stream)));
 }
 
 sv_status sv_kv_commit(uint16_t* k_cache, uint16_t* v_cache, const uint16_t* k_blk, const uint16_t* v_blk, int32_t L,

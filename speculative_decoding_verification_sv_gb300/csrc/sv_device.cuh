@@ -411,7 +411,11 @@ __device__ __forceinline__ float sv_exp(float x) {
     const float kInvLn2 = 1.44269504088896340736f;
     const float kLn2Head = 0.693145751953125f;    // 12 significant bits: n * head exact
     const float kLn2Tail = 1.428606820309417232e-06f;
-    const float n = rintf(__fmul_rn(x, kInvLn2));
+    // n = rint(x / ln 2): adding 1.5 * 2^23 rounds to an integer (ties to even)
+    // and leaves it in the low mantissa bits, which gives k without a convert
+    const float kRound = 12582912.0f;
+    const float t = __fadd_rn(__fmul_rn(x, kInvLn2), kRound);
+    const float n = __fsub_rn(t, kRound);
     float r = __fmaf_rn(-n, kLn2Head, x);
     r = __fmaf_rn(-n, kLn2Tail, r);
     float s = 1.0f / 5040.0f;                      // Taylor coefficients 1/k!
@@ -422,10 +426,40 @@ __device__ __forceinline__ float sv_exp(float x) {
     s = __fmaf_rn(s, r, 0.5f);
     s = __fmaf_rn(s, r, 1.0f);
     s = __fmaf_rn(s, r, 1.0f);
-    const int k = static_cast<int>(n);
+    const int k = __float_as_int(t) - __float_as_int(kRound);
     if (k >= -126) return __fmul_rn(s, __int_as_float((k + 127) << 23));
     // 2^k subnormal: an exact scaling by 2^(k+64), then one rounding by 2^-64
     return __fmul_rn(__fmul_rn(s, __int_as_float((k + 64 + 127) << 23)), __int_as_float((127 - 64) << 23));
+}
+
+// sv_exp without branches, for the softmax terms exp(z - M) (argument <= 0):
+// the same operations on max(x, -104), with the underflow and subnormal cases
+// selected afterwards, so several evaluations can interleave.  Bit-identical
+// to sv_exp for every x that is not NaN and not above 88 (the NaN and
+// overflow returns are the only cases it leaves out).
+__device__ __forceinline__ float sv_exp_nb(float x) {
+    const float kInvLn2 = 1.44269504088896340736f;
+    const float kLn2Head = 0.693145751953125f;
+    const float kLn2Tail = 1.428606820309417232e-06f;
+    const float kRound = 12582912.0f;   // as in sv_exp
+    const float xc = fmaxf(x, -104.0f);
+    const float t = __fadd_rn(__fmul_rn(xc, kInvLn2), kRound);
+    const float n = __fsub_rn(t, kRound);
+    float r = __fmaf_rn(-n, kLn2Head, xc);
+    r = __fmaf_rn(-n, kLn2Tail, r);
+    float s = 1.0f / 5040.0f;
+    s = __fmaf_rn(s, r, 1.0f / 720.0f);
+    s = __fmaf_rn(s, r, 1.0f / 120.0f);
+    s = __fmaf_rn(s, r, 1.0f / 24.0f);
+    s = __fmaf_rn(s, r, 1.0f / 6.0f);
+    s = __fmaf_rn(s, r, 0.5f);
+    s = __fmaf_rn(s, r, 1.0f);
+    s = __fmaf_rn(s, r, 1.0f);
+    const int k = __float_as_int(t) - __float_as_int(kRound);
+    const bool normal = k >= -126;
+    float y = __fmul_rn(s, __int_as_float((normal ? k + 127 : k + 64 + 127) << 23));
+    y = normal ? y : __fmul_rn(y, __int_as_float((127 - 64) << 23));
+    return x < -104.0f ? 0.0f : y;
 }
 
 // --------------------------------------------------------------------------

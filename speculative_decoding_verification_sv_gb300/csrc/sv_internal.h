@@ -24,7 +24,7 @@ size_t sample_workspace(int B, int R, int V);
 cudaError_t launch_accept_sample(const float* logits, const float* q, int Vq, const int32_t* tok,
                                  const int32_t* parent, int B, int R, int V, float temperature, uint64_t seed,
                                  uint64_t step, const float* uniforms, int32_t* n_acc, int32_t* out_tok,
-                                 int32_t* path, void* ws, cudaStream_t st);
+                                 int32_t* path, void* ws, size_t ws_bytes, cudaStream_t st);
 cudaError_t launch_diag_exp(const float* x, float* y, int64_t n, cudaStream_t st);
 cudaError_t launch_diag_philox(const uint32_t* ctr, const uint32_t* key, uint32_t* out, int64_t n,
                                cudaStream_t st);

@@ -749,17 +749,19 @@ AttnPlan attn_plan(const sv_attn_shape& s) {
     for (int C = kMaxCluster; C >= 1; C >>= 1) {
         if (C > tiles && C > 1) continue;
         const int64_t cap = p.half ? active_clusters<true>(C) : active_clusters<false>(C);
-        int64_t nc = cap / units;
-        if (nc > 32) nc = 32;
-        if (nc > tiles / C) nc = tiles / C;
-        if (nc < 1) nc = 1;
-        const int64_t waves = (units * nc + cap - 1) / cap;
-        const int64_t per_cta = (tiles + C * nc - 1) / (C * nc);
-        const int64_t cost = waves * (3 + per_cta) + (nc > 1 ? kMergeCost : 0);
-        if (best < 0 || cost < best) {
-            best = cost;
-            p.splits = C;
-            p.clusters = static_cast<int>(nc);
+        int64_t nc_max = cap / units;
+        if (nc_max > 32) nc_max = 32;
+        if (nc_max > tiles / C) nc_max = tiles / C;
+        if (nc_max < 1) nc_max = 1;
+        for (int64_t nc = 1; nc <= nc_max; nc = nc < nc_max ? nc_max : nc_max + 1) {   // one cluster, or the most
+            const int64_t waves = (units * nc + cap - 1) / cap;
+            const int64_t per_cta = (tiles + C * nc - 1) / (C * nc);
+            const int64_t cost = waves * (3 + per_cta) + (nc > 1 ? kMergeCost : 0);
+            if (best < 0 || cost < best) {
+                best = cost;
+                p.splits = C;
+                p.clusters = static_cast<int>(nc);
+            }
         }
     }
     return p;

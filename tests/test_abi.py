@@ -60,9 +60,11 @@ def test_host_validation_rejects_before_launch(lib):
     s = b._AttnShape(1, 5, 12, 5, 128, 4096)   # Hq % Hkv != 0
     assert L.sv_verify_attn(ctypes.byref(s), fake, fake, fake, fake, fake, fake, None, ctypes.c_float(0.1), fake,
                             fake, 1 << 30, None) == 2
-    # batch 1: several clusters per KV head meet in the workspace, which is
-    # then required (NULL -> argument error, short -> workspace error)
-    s = b._AttnShape(1, 5, 12, 2, 128, 4224)
+    # batch 1, 32K context: several clusters per KV head meet in the
+    # workspace, which is then required (NULL -> argument error, short ->
+    # workspace error); at 4K context one cluster per KV head needs none
+    assert L.sv_verify_attn_workspace(ctypes.byref(b._AttnShape(1, 5, 12, 2, 128, 4224))) == 0
+    s = b._AttnShape(1, 5, 12, 2, 128, 32832)
     need = L.sv_verify_attn_workspace(ctypes.byref(s))
     assert need > 0 and need % 16 == 0
     assert L.sv_verify_attn(ctypes.byref(s), fake, fake, fake, fake, fake, fake, None, ctypes.c_float(0.1), fake,
@@ -85,5 +87,6 @@ def test_host_validation_rejects_before_launch(lib):
 def test_workspace_queries(lib):
     from speculative_decoding_verification_sv_gb300 import binding as b
     assert b.lib.sv_accept_greedy_workspace(16, 9, 152064) == 16 * 9 * 19 * 8
-    assert b.lib.sv_accept_sample_workspace(64, 9, 151936) == 64 * 9 * 8
+    # row statistics, then the chain path's per-sequence records and sums
+    assert b.lib.sv_accept_sample_workspace(64, 9, 151936) == 64 * 9 * 8 + 64 * 16 + 64 * 2 * (64 * 32 + 64) * 4
     assert b.verify_attn_workspace(16, 9, 28, 4, 128, 8320) == 0

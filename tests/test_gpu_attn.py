@@ -103,17 +103,18 @@ def test_attn_full_layer(sv, wid, B, layer):
 
 
 def test_attn_workspace_tickets_reset(sv):
-    """Batch-1 shapes split each KV head over several clusters that meet in the
-    workspace through a ticket word; every call must leave the tickets at zero
-    so one workspace serves consecutive calls (same result as a fresh one)."""
-    B, R, Hq, Hkv, T_cap = 1, 5, 12, 2, 4224
+    """A batch-1, 32K-context layer splits each KV head over several clusters
+    that meet in the workspace through a ticket word; every call must leave
+    the tickets at zero so one workspace serves consecutive calls (same result
+    as a fresh one), and the merged rows match the oracle."""
+    B, R, Hq, Hkv, T_cap = 1, 5, 12, 2, 32832
     nbytes = sv.verify_attn_workspace(B, R, Hq, Hkv, 128, T_cap)
     assert nbytes > 0
     ws = torch.zeros(nbytes, dtype=torch.uint8, device="cuda")
     g = torch.Generator().manual_seed(11)
     mk = lambda *s: torch.randn(*s, generator=g).to(torch.bfloat16).cuda()
     kc, vc, kb, vb = mk(B, Hkv, T_cap, 128), mk(B, Hkv, T_cap, 128), mk(B, Hkv, R, 128), mk(B, Hkv, R, 128)
-    ln = torch.tensor([4096], dtype=torch.int32, device="cuda")
+    ln = torch.tensor([32768], dtype=torch.int32, device="cuda")
     for it in range(3):
         q = mk(B, R, Hq, 128)
         shared = sv.verify_attn(q, kc, vc, ln, kb, vb, ws=ws)
