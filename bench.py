@@ -44,11 +44,20 @@ PEAKS_PATH = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK_HBM_GBS = 6800.0
 
 # DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) from an
-# ncu capture, keyed by kernel, with the hash of the source file it was taken
-# on; a different hash (the kernel changed) reports null.
+# ncu capture, keyed by (workload, kernel), with the hash of the source file it
+# was taken on; a different hash (the kernel changed) reports null.
 TRAFFIC = {
     # ncu --set full, 28-layer 1.5B round, LM head N=5 H=1536 V=151936
-    "lm_head": {"bytes": 466805504 + 5640192, "src_hash": "014d4cc2603280a9"},
+    ("1", "lm_head"): {"bytes": 466805504 + 5640192, "src": "lm_head.cu", "src_hash": "28b4a698ab2e95cb"},
+    # ncu --set full, 7B batch-16 layer (2-layer case, same per-layer launch)
+    ("3b16", "verify_attn"): {"bytes": 269845760 + 3999488, "src": "verify_attn.cu",
+                              "src_hash": "65f5f031fa957a68"},
+    ("3b16s", "verify_attn"): {"bytes": 269845760 + 3999488, "src": "verify_attn.cu",
+                               "src_hash": "65f5f031fa957a68"},
+    # ncu --set full, sampled B64 k8: statistics pass + chain residual pass (the
+    # walk and draw launches move < 0.1 MB and were not captured)
+    ("2", "accept_sampled"): {"bytes": 395190272 + 3251968 + 77821440 + 1253888, "src": "accept.cu",
+                              "src_hash": "06c930a1cdbe09e0"},
 }
 
 
@@ -572,10 +581,8 @@ def main():
         v["frac_of_peak"] = v["gbs"] / hbm
     dom = max(kern, key=lambda k: kern[k]["bytes_per_launch"] * kern[k]["launches_per_step"])
     dk = kern[dom]
-    src = {"lm_head": "lm_head.cu", "verify_attn": "verify_attn.cu", "accept_greedy": "accept.cu",
-           "accept_sampled": "accept.cu", "kv_commit": "kv_commit.cu"}[dom]
-    tr = TRAFFIC.get(dom)
-    traffic = tr["bytes"] if tr and tr["src_hash"] == src_hash(src) else None
+    tr = TRAFFIC.get((args.workload, dom))
+    traffic = tr["bytes"] if tr and tr["src_hash"] == src_hash(tr["src"]) else None
     roofline = {"kernel": dom, "bound": "hbm", "achieved": dk["gbs"], "peak": hbm, "unit": "GB/s",
                 "frac": dk["gbs"] / hbm, "traffic": traffic, "peak_source": f"hbm_gbs of {peak_kind}",
                 "bytes_per_launch": dk["bytes_per_launch"], "us_per_launch": dk["us_per_launch"],

@@ -81,7 +81,13 @@ WORKLOADS = {
 
 def workload(wid: int, **overrides) -> Workload:
     w = WORKLOADS[wid]
-    return replace(w, **overrides) if overrides else w
+    if not overrides:
+        return w
+    w = replace(w, **overrides)
+    if "B" in overrides:   # keep the name true to the batch
+        import re
+        w = replace(w, name=re.sub(r"\bb=\d+", f"b={w.B}", w.name))
+    return w
 
 
 def seed_for(wid: int, tensor_id: int) -> int:
