@@ -95,9 +95,19 @@ __global__ void __launch_bounds__(kGreedyThreads) greedy_partial_kernel(const fl
     ArgMax best{-INFINITY, INT_MAX};
     bool bad = false;
     if ((V & 3) == 0) {
-        for (int i = c0 + 4 * threadIdx.x; i < c1; i += 4 * kGreedyThreads) {
-            const float4 x = __ldg(reinterpret_cast<const float4*>(L + i));
-            const float xs[4] = {x.x, x.y, x.z, x.w};
+        // all of a thread's loads of the chunk in flight at once (8 float4)
+        constexpr int kPer = kGreedyChunk / (4 * kGreedyThreads);
+        float4 xv[kPer];
+#pragma unroll
+        for (int u = 0; u < kPer; ++u) {
+            const int i = c0 + 4 * (threadIdx.x + u * kGreedyThreads);
+            xv[u] = i < c1 ? __ldg(reinterpret_cast<const float4*>(L + i)) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int u = 0; u < kPer; ++u) {
+            const int i = c0 + 4 * (threadIdx.x + u * kGreedyThreads);
+            if (i >= c1) continue;
+            const float xs[4] = {xv[u].x, xv[u].y, xv[u].z, xv[u].w};
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 if (xs[e] != xs[e]) { bad = true; continue; }
