@@ -62,7 +62,10 @@ bool debug_sync() {
 // greedy
 // ==========================================================================
 
-constexpr int kGreedyChunk = 8192;
+#ifndef SV_GREEDY_CHUNK
+#define SV_GREEDY_CHUNK 8192
+#endif
+constexpr int kGreedyChunk = SV_GREEDY_CHUNK;   // vocab columns per argmax CTA
 constexpr int kGreedyThreads = 256;
 
 struct ArgMax {
@@ -319,10 +322,14 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads)
 // builds the same canonical tree: chunk sums of exp(z - M) over 128 leaves (4
 // per lane), block sums over 32 chunks, then the 64 zero-padded block sums.
 // One row in flight per SM keeps the re-read in L2 (152 x 600 KB < 126 MB).
-constexpr int kRowThreads = 512;
+#ifndef SV_ROW_THREADS
+#define SV_ROW_THREADS 512
+#endif
+constexpr int kRowThreads = SV_ROW_THREADS;       // 512: one CTA per SM; 256: two
+constexpr int kRowCtasPerSm = 512 / kRowThreads;
 constexpr int kRowWarps = kRowThreads / 32;
 
-__global__ void __launch_bounds__(kRowThreads, 1) sample_stats_row_kernel(const float* __restrict__ logits, int V,
+__global__ void __launch_bounds__(kRowThreads, kRowCtasPerSm) sample_stats_row_kernel(const float* __restrict__ logits, int V,
                                                                          float T, int nblk, int nrows,
                                                                          float2* __restrict__ stats,
                                                                          unsigned int* err) {
@@ -987,7 +994,8 @@ cudaError_t launch_accept_sample(const float* logits, const float* q, int Vq, co
     // rows: one CTA per row keeps every SM busy without cluster waves.
     if (static_cast<int64_t>(B) * R >= kRowStatsMinRows)
     {
-        const int nrows = B * R, grid = nrows < device_sm_count() ? nrows : device_sm_count();
+        const int slots = device_sm_count() * kRowCtasPerSm;
+        const int nrows = B * R, grid = nrows < slots ? nrows : slots;
         sample_stats_row_kernel<<<grid, kRowThreads, 0, st>>>(logits, V, temperature, nblk, nrows, stats, err);
     }
     else

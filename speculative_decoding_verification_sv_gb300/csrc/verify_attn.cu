@@ -378,20 +378,17 @@ __global__ void __launch_bounds__(Roles<kHalf>::kThreads, 1)
 #pragma unroll
                 for (int e = 0; e < kCols; ++e) sc[e] = __uint_as_float(rs[e]) * a.scale_log2;
                 if (is_block || kb + kCols > t) {
+                    // branch-free mask: key kb + e is visible iff e < lim (context:
+                    // kl < t; chain block: kl <= j and kl < R) or, for a tree block,
+                    // iff bit e of the ancestor window starting at key kb is set
+                    const bool tree_blk = is_block && tree;
+                    const int lim = !is_block ? t - kb : (j + 1 < a.R ? j + 1 : a.R) - kb;
+                    const uint32_t win =
+                        tree_blk ? static_cast<uint32_t>((kb < 64 ? anc0 : anc1) >> (kb & 63)) : 0u;
 #pragma unroll
                     for (int e = 0; e < kCols; ++e) {
-                        const int kl = kb + e;
-                        bool vis;
-                        if (!is_block) {
-                            vis = kl < t;
-                        } else if (kl >= a.R) {
-                            vis = false;
-                        } else if (tree) {
-                            vis = ((kl < 64 ? anc0 : anc1) >> (kl & 63)) & 1ull;
-                        } else {
-                            vis = kl <= j;
-                        }
-                        if (!vis) sc[e] = -INFINITY;
+                        const bool vis = tree_blk ? ((win >> e) & 1u) != 0u : e < lim;
+                        sc[e] = vis ? sc[e] : -INFINITY;
                     }
                 }
                 float mx[kCols / 2];
