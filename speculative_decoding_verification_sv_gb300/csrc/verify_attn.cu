@@ -132,7 +132,10 @@ struct AttnArgs {
 // half tiles put row gr in lane 32 * (gr % 4) + gr / 4, so every quadrant
 // (SM sub-partition) carries a quarter of the rows.
 
-template <bool kHalf>
+// kTree: the launch carries a draft tree (parent != NULL).  Chains compile
+// without any ancestor-mask code: the speculatively evaluated 64-bit window
+// of the tree mask stalled the chain's block-tile step by ~2500 cycles.
+template <bool kHalf, bool kTree>
 __global__ void __launch_bounds__(Roles<kHalf>::kThreads, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                    const __grid_constant__ CUtensorMap tmKb, const __grid_constant__ CUtensorMap tmVb, AttnArgs a) {
@@ -186,9 +189,11 @@ __global__ void __launch_bounds__(Roles<kHalf>::kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_s;
-    const uint32_t tS[2] = {tmem + kColS, tmem + kColS + kStepKeys};
+    // TMEM addresses of score buffer / P buffer `i` (arithmetic, not arrays: a
+    // runtime-indexed array would live in local memory)
+    auto tS = [tmem](int i) { return tmem + kColS + static_cast<uint32_t>(i) * kStepKeys; };
     const uint32_t tO = tmem + kColO;
-    const uint32_t tP[2] = {tmem + kColP, tmem + kColP + kPCols};
+    auto tP = [tmem](int i) { return tmem + kColP + static_cast<uint32_t>(i) * kPCols; };
 
     // inputs may come from the kernels before this one
     pdl_wait();
@@ -210,7 +215,7 @@ __global__ void __launch_bounds__(Roles<kHalf>::kThreads, 1)
     const int ntiles = last - first;
     const int nsteps = (ntiles + kStepTiles - 1) / kStepTiles;
     const bool has_block = last > n_ctx;
-    const bool tree = a.parent != nullptr && has_block;
+    const bool tree = kTree && has_block;
 
     if (warp == kTmaWarp) {
         // ---------------- TMA producer ----------------
@@ -254,7 +259,7 @@ __global__ void __launch_bounds__(Roles<kHalf>::kThreads, 1)
                     const uint64_t bd0 = smem_desc_sw128(sv, kHalfBytes, 1024);
 #pragma unroll
                     for (int k16 = 0; k16 < kNk / 16; ++k16)
-                        tc_mma_ts(tO, tP[pb] + h * kPCols + k16 * 8, bd0 + k16 * (2048 >> 4), idesc_o,
+                        tc_mma_ts(tO, tP(pb) + h * kPCols + k16 * 8, bd0 + k16 * (2048 >> 4), idesc_o,
                                   (st > 0 || h > 0 || k16 > 0) ? 1u : 0u);
                 }
                 tc_commit(&o_done[pb]);
@@ -273,7 +278,7 @@ __global__ void __launch_bounds__(Roles<kHalf>::kThreads, 1)
 #pragma unroll
                     for (int k16 = 0; k16 < kD / 16; ++k16) {
                         const uint32_t half = k16 >> 2, kin = (k16 & 3) * 32;
-                        tc_mma(tS[sb] + h * kNk, qd0 + ((half * (kM * 128) + kin) >> 4),
+                        tc_mma(tS(sb) + h * kNk, qd0 + ((half * (kM * 128) + kin) >> 4),
                                kd0 + ((half * kHalfBytes + kin) >> 4), idesc_s, k16 > 0 ? 1u : 0u);
                     }
                 }
@@ -341,7 +346,6 @@ __global__ void __launch_bounds__(Roles<kHalf>::kThreads, 1)
         // the warp's quadrant holds at least one real row (padding lanes' P and
         // O are never read, so a warp with none skips the arithmetic)
         const bool quarter_live = kHalf ? (warp < a.rows) : (rt * kRows + (warp & 3) * 32 < a.rows);
-        const uint64_t anc0 = (tree && valid) ? anc[2 * j] : 0, anc1 = (tree && valid) ? anc[2 * j + 1] : 0;
         const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
         // full tiles: 16 consecutive columns of the step (group cgp); half
         // tiles: 32 (thread half `sub` of the row's pair)
@@ -349,6 +353,13 @@ __global__ void __launch_bounds__(Roles<kHalf>::kThreads, 1)
         const int cgp = kHalf ? 0 : warp / 4;
         const int sub = kHalf ? (lane >> 4) : 0;
         const int col0 = kHalf ? sub * kHCols : cgp * kGCols;
+        // tree: this thread's 32-bit windows of the row's ancestor mask, one per
+        // block tile (block keys col0.. of tile 0 and of tile 1)
+        uint32_t win_t0 = 0u, win_t1 = 0u;
+        if (tree && valid) {
+            win_t0 = static_cast<uint32_t>(anc[2 * j] >> col0);
+            win_t1 = static_cast<uint32_t>(anc[2 * j + 1] >> col0);
+        }
         float* red = reinterpret_cast<float*>(smem + Ly::kOffRed);
         float* lsx = reinterpret_cast<float*>(smem + Ly::kOffLsum);
 
@@ -361,9 +372,9 @@ __global__ void __launch_bounds__(Roles<kHalf>::kThreads, 1)
             uint32_t rs[kCols];
             if (work) {
                 if constexpr (kHalf) {
-                    tmem_ld32_h_sync<kHCols>(tS[sb] + lane_off, rs);
+                    tmem_ld32_h_sync<kHCols>(tS(sb) + lane_off, rs);
                 } else {
-                    tmem_ld16_sync(tS[sb] + lane_off + col0, rs);
+                    tmem_ld16_sync(tS(sb) + lane_off + col0, rs);
                 }
             }
             tc_fence_before();
@@ -381,10 +392,9 @@ __global__ void __launch_bounds__(Roles<kHalf>::kThreads, 1)
                     // branch-free mask: key kb + e is visible iff e < lim (context:
                     // kl < t; chain block: kl <= j and kl < R) or, for a tree block,
                     // iff bit e of the ancestor window starting at key kb is set
-                    const bool tree_blk = is_block && tree;
+                    const bool tree_blk = kTree && is_block;
                     const int lim = !is_block ? t - kb : (j + 1 < a.R ? j + 1 : a.R) - kb;
-                    const uint32_t win =
-                        tree_blk ? static_cast<uint32_t>((kb < 64 ? anc0 : anc1) >> (kb & 63)) : 0u;
+                    const uint32_t win = tree_blk ? (gt - n_ctx == 0 ? win_t0 : win_t1) : 0u;
 #pragma unroll
                     for (int e = 0; e < kCols; ++e) {
                         const bool vis = tree_blk ? ((win >> e) & 1u) != 0u : e < lim;
@@ -467,8 +477,8 @@ __global__ void __launch_bounds__(Roles<kHalf>::kThreads, 1)
             }
             if (work) {
                 // P of this thread's columns into TMEM buffer sb, two keys per column
-                if constexpr (kHalf) tmem_st16_h<kHCols / 2>(tP[sb] + lane_off, pk);
-                else tmem_st8(tP[sb] + lane_off + col0 / 2, pk);
+                if constexpr (kHalf) tmem_st16_h<kHCols / 2>(tP(sb) + lane_off, pk);
+                else tmem_st8(tP(sb) + lane_off + col0 / 2, pk);
                 tmem_st_wait();
             }
             tc_fence_before();
@@ -646,16 +656,16 @@ __global__ void __launch_bounds__(Roles<kHalf>::kThreads, 1)
     }
 }
 
-template <bool kHalf>
+template <bool kHalf, bool kTree>
 cudaError_t prepare_kernel() {
     static bool done[64] = {};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (done[dev]) return cudaSuccess;
-    cudaError_t e =
-        cudaFuncSetAttribute(attn_tc_kernel<kHalf>, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay<kHalf>::kSmemBytes);
+    cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<kHalf, kTree>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         Lay<kHalf>::kSmemBytes);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(attn_tc_kernel<kHalf>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    e = cudaFuncSetAttribute(attn_tc_kernel<kHalf, kTree>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e != cudaSuccess) return e;
     done[dev] = true;
     return cudaSuccess;
@@ -676,7 +686,7 @@ int active_clusters(int C) {
     std::lock_guard<std::mutex> lk(mu);
     if (cache[dev][C]) return cache[dev][C];
     int n = 0;
-    if (prepare_kernel<kHalf>() == cudaSuccess) {
+    if (prepare_kernel<kHalf, false>() == cudaSuccess) {   // both tree variants use the same resources
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(C, 1, 1);
         cfg.blockDim = dim3(Roles<kHalf>::kThreads, 1, 1);
@@ -688,7 +698,7 @@ int active_clusters(int C) {
         attr[0].val.clusterDim.z = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        if (cudaOccupancyMaxActiveClusters(&n, attn_tc_kernel<kHalf>, &cfg) != cudaSuccess) n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, attn_tc_kernel<kHalf, false>, &cfg) != cudaSuccess) n = 0;
     }
     cudaGetLastError();
     if (n <= 0) n = fallback;
@@ -696,11 +706,11 @@ int active_clusters(int C) {
     return n;
 }
 
-template <bool kHalf>
+template <bool kHalf, bool kTree>
 cudaError_t launch_mode(const AttnPlan& p, const sv_attn_shape& s, const uint8_t* tK, const uint8_t* tV,
                         const uint8_t* tKb, const uint8_t* tVb, const AttnArgs& a, cudaStream_t st) {
     constexpr int kThreads = Roles<kHalf>::kThreads;
-    cudaError_t e = prepare_kernel<kHalf>();
+    cudaError_t e = prepare_kernel<kHalf, kTree>();
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(p.splits * p.clusters, s.B * s.Hkv, p.row_tiles);
@@ -716,7 +726,7 @@ cudaError_t launch_mode(const AttnPlan& p, const sv_attn_shape& s, const uint8_t
     attrs[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attrs;
     cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, attn_tc_kernel<kHalf>, *reinterpret_cast<const CUtensorMap*>(tK),
+    return cudaLaunchKernelEx(&cfg, attn_tc_kernel<kHalf, kTree>, *reinterpret_cast<const CUtensorMap*>(tK),
                               *reinterpret_cast<const CUtensorMap*>(tV), *reinterpret_cast<const CUtensorMap*>(tKb),
                               *reinterpret_cast<const CUtensorMap*>(tVb), a);
 }
@@ -812,8 +822,11 @@ cudaError_t launch_verify_attn(const sv_attn_shape& s, const uint16_t* q, const 
     a.clusters = p.clusters;
     a.part_rows = p.rows < kRows ? p.rows : kRows;
     a.scale_log2 = scale * 1.4426950408889634f;
-    return p.half ? launch_mode<true>(p, s, tK, tV, tKb, tVb, a, st)
-                  : launch_mode<false>(p, s, tK, tV, tKb, tVb, a, st);
+    if (parent != nullptr)
+        return p.half ? launch_mode<true, true>(p, s, tK, tV, tKb, tVb, a, st)
+                      : launch_mode<false, true>(p, s, tK, tV, tKb, tVb, a, st);
+    return p.half ? launch_mode<true, false>(p, s, tK, tV, tKb, tVb, a, st)
+                  : launch_mode<false, false>(p, s, tK, tV, tKb, tVb, a, st);
 }
 
 }  // namespace sv
