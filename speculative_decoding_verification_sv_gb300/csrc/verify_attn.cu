@@ -41,6 +41,7 @@
 #include <math.h>
 
 #include <mutex>
+#include <type_traits>
 
 #include "sv_device.cuh"
 #include "sv_internal.h"
@@ -52,12 +53,9 @@ namespace {
 
 constexpr int kD = 128;
 constexpr int kNk = 64;                   // keys per TMA tile
-constexpr int kStepTiles = 1;             // TMA tiles per softmax step
-constexpr int kStepKeys = kStepTiles * kNk;   // keys per softmax step
 constexpr int kRows = 128;                // query rows per full row tile
-constexpr int kPCols = kNk / 2;           // TMEM columns of one P buffer (two bf16 per column)
 constexpr int kHalfBytes = kNk * 128;     // one 64-key x 64-dim swizzled box: 8 KB
-constexpr int kStageBytes = 4 * kHalfBytes;   // K and V, two halves each: 32 KB
+constexpr int kTileBytes = 4 * kHalfBytes;   // K and V of one tile, two halves each: 32 KB
 constexpr int kRec = kD + 4;              // partial record: m, l, 2 pad, o[128]
 constexpr int kMaxR = 128;
 constexpr int kMaxCluster = 16;
@@ -66,8 +64,6 @@ constexpr int kMaxCluster = 16;
 #endif
 constexpr int kMergeCost = SV_ATTN_MERGE_COST;   // workspace merge, in key-tile times
 constexpr int kGroups = 4;                // full tiles: column groups of a step
-constexpr int kGCols = kStepKeys / kGroups;   // full tiles: scores per thread per step
-constexpr int kHCols = kStepKeys / 2;     // half tiles: scores per thread per step
 #ifndef SV_ATTN_HALF_MAX_ROWS
 #define SV_ATTN_HALF_MAX_ROWS 64
 #endif
@@ -85,23 +81,30 @@ struct Roles {
     static constexpr int kTma = kSoft, kMma = kSoft + 1;
     static constexpr int kThreads = 32 * (kSoft + 2);
 };
-// TMEM columns: S buffers at 0 and 64, O at 128..255, P buffers at 256 and 288
-constexpr uint32_t kColS = 0, kColO = 2 * kStepKeys, kColP = kColO + kD;
 constexpr uint32_t kTmemCols = 512;
-static_assert(kColP + 2 * kPCols <= kTmemCols, "TMEM budget");
 constexpr float kRescale = 8.0f;          // log2 of the largest tolerated P
-// S of step st+1 is issued before the P V of step st: both tiles stay resident
-static_assert(kStepTiles == 1, "one key tile per softmax step");
 
-// Shared-memory layout.  Full tiles: M = 128 MMAs, 32 KB of Q, 5 ring stages.
-// Half tiles: M = 64 MMAs (row m of the tile in TMEM lane 32 * (m / 16) +
-// m % 16), 16 KB of Q, 6 ring stages -- more K/V bytes in flight per SM.
+// Shared-memory and TMEM layout.  Full tiles: M = 128 MMAs, 32 KB of Q, one
+// key tile per softmax step, 5 ring stages.  Half tiles: M = 64 MMAs (row m of
+// the tile in TMEM lane 32 * (m / 16) + m % 16), 16 KB of Q, two key tiles per
+// step (S = Q K^T as one N = 128 MMA chain over both: the single MMA-issuing
+// thread bounds a step, so fewer, larger MMAs per key), 3 stages of two tiles.
+// A stage holds its tiles' boxes region by region: K dims 0-63 of every tile,
+// K dims 64-127, V dims 0-63, V dims 64-127, so keys are contiguous per region.
 template <bool kHalf>
 struct Lay {
     static constexpr int kM = kHalf ? 64 : 128;            // MMA M (rows of the Q tile)
-    static constexpr int kStages = kHalf ? 6 : 5;           // TMA ring depth in tiles
+    static constexpr int kT = kHalf ? 2 : 1;                // key tiles per softmax step
+    static constexpr int kStepKeys = kT * kNk;
+    static constexpr int kStageBytes = kT * kTileBytes;
+    static constexpr int kRegion = kT * kHalfBytes;        // one region of a stage
+    static constexpr int kStages = kHalf ? 3 : 5;           // ring depth in steps
     static constexpr int kQBytes = kM * kD * 2;             // two 64-dim halves of kM rows
     static constexpr int kRingBytes = kStages * kStageBytes;
+    // TMEM columns: two S buffers, O (128 columns), two P buffers (two bf16 per column)
+    static constexpr uint32_t kColS = 0, kColO = 2 * kStepKeys, kColP = kColO + kD;
+    static constexpr int kPCols = kStepKeys / 2;
+    static_assert(kColP + 2 * kPCols <= kTmemCols, "TMEM budget");
     static constexpr int kOffQ = 0;
     static constexpr int kOffRing = kOffQ + kQBytes;
     static constexpr int kOffBar = kOffRing + kRingBytes;
@@ -142,7 +145,8 @@ __global__ void __launch_bounds__(Roles<kHalf>::kThreads, 1)
     using Ro = Roles<kHalf>;
     using Ly = Lay<kHalf>;
     constexpr int kSoftWarps = Ro::kSoft, kTmaWarp = Ro::kTma, kMmaWarp = Ro::kMma, kThreads = Ro::kThreads;
-    constexpr int kStages = Ly::kStages, kM = Ly::kM;
+    constexpr int kStages = Ly::kStages, kM = Ly::kM, kT = Ly::kT, kStepKeys = Ly::kStepKeys;
+    constexpr int kStageBytes = Ly::kStageBytes, kRegion = Ly::kRegion;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Ly::kOffBar);
@@ -191,9 +195,9 @@ __global__ void __launch_bounds__(Roles<kHalf>::kThreads, 1)
     const uint32_t tmem = *tmem_s;
     // TMEM addresses of score buffer / P buffer `i` (arithmetic, not arrays: a
     // runtime-indexed array would live in local memory)
-    auto tS = [tmem](int i) { return tmem + kColS + static_cast<uint32_t>(i) * kStepKeys; };
-    const uint32_t tO = tmem + kColO;
-    auto tP = [tmem](int i) { return tmem + kColP + static_cast<uint32_t>(i) * kPCols; };
+    auto tS = [tmem](int i) { return tmem + Ly::kColS + static_cast<uint32_t>(i) * Ly::kStepKeys; };
+    const uint32_t tO = tmem + Ly::kColO;
+    auto tP = [tmem](int i) { return tmem + Ly::kColP + static_cast<uint32_t>(i) * Ly::kPCols; };
 
     // inputs may come from the kernels before this one
     pdl_wait();
@@ -213,74 +217,71 @@ __global__ void __launch_bounds__(Roles<kHalf>::kThreads, 1)
     const int first = static_cast<int>((static_cast<int64_t>(n_all) * split) / nsplit);
     const int last = static_cast<int>((static_cast<int64_t>(n_all) * (split + 1)) / nsplit);
     const int ntiles = last - first;
-    const int nsteps = (ntiles + kStepTiles - 1) / kStepTiles;
+    const int nsteps = (ntiles + kT - 1) / kT;
     const bool has_block = last > n_ctx;
     const bool tree = kTree && has_block;
 
     if (warp == kTmaWarp) {
         // ---------------- TMA producer ----------------
         if (lane == 0) {
-            for (int i = 0; i < ntiles; ++i) {
+            for (int i = 0; i < nsteps; ++i) {
                 const int s = i % kStages;
                 mbar_wait(&kv_empty[s], ((i / kStages) & 1) ^ 1, a.err);
-                const int gt = first + i;
-                const void* tk = gt < n_ctx ? static_cast<const void*>(&tmK) : static_cast<const void*>(&tmKb);
-                const void* tv = gt < n_ctx ? static_cast<const void*>(&tmV) : static_cast<const void*>(&tmVb);
-                const int y = gt < n_ctx ? hg * a.T_cap + gt * kNk : hg * a.R + (gt - n_ctx) * kNk;
+                const int t0 = first + i * kT, nt = min(kT, last - t0);
                 uint8_t* st = smem + Ly::kOffRing + s * kStageBytes;
-                mbar_arrive_expect_tx(&kv_full[s], kStageBytes);
-                tma_load_2d(st, tk, 0, y, &kv_full[s]);
-                tma_load_2d(st + kHalfBytes, tk, 64, y, &kv_full[s]);
-                tma_load_2d(st + 2 * kHalfBytes, tv, 0, y, &kv_full[s]);
-                tma_load_2d(st + 3 * kHalfBytes, tv, 64, y, &kv_full[s]);
+                mbar_arrive_expect_tx(&kv_full[s], static_cast<uint32_t>(nt * kTileBytes));
+                for (int h = 0; h < nt; ++h) {
+                    const int gt = t0 + h;
+                    const void* tk = gt < n_ctx ? static_cast<const void*>(&tmK) : static_cast<const void*>(&tmKb);
+                    const void* tv = gt < n_ctx ? static_cast<const void*>(&tmV) : static_cast<const void*>(&tmVb);
+                    const int y = gt < n_ctx ? hg * a.T_cap + gt * kNk : hg * a.R + (gt - n_ctx) * kNk;
+                    tma_load_2d(st + h * kHalfBytes, tk, 0, y, &kv_full[s]);
+                    tma_load_2d(st + kRegion + h * kHalfBytes, tk, 64, y, &kv_full[s]);
+                    tma_load_2d(st + 2 * kRegion + h * kHalfBytes, tv, 0, y, &kv_full[s]);
+                    tma_load_2d(st + 3 * kRegion + h * kHalfBytes, tv, 64, y, &kv_full[s]);
+                }
             }
         }
     } else if (warp == kMmaWarp) {
         // ---------------- MMA issuer ----------------
         if (lane == 0 && ntiles > 0) {
-            constexpr uint32_t idesc_s = idesc_bf16_f32(kM, kNk, false, false);   // S tile = Q K^T
-            constexpr uint32_t idesc_o = idesc_bf16_f32(kM, kD, false, true);     // O += P V
+            // S = Q K^T over the step's tiles (N = 64 per tile), O += P V
+            constexpr uint32_t idesc_s = idesc_bf16_f32(kM, kStepKeys, false, false);
+            constexpr uint32_t idesc_s1 = idesc_bf16_f32(kM, kNk, false, false);      // a last, single tile
+            constexpr uint32_t idesc_o = idesc_bf16_f32(kM, kD, false, true);
             const uint32_t sq = smem_u32(smem + Ly::kOffQ);
             // both S operands K-major; the two 64-dim halves are separate boxes
             const uint64_t qd0 = smem_desc_sw128(sq, 16, 1024);
             mbar_wait(q_ready, 0, a.err);
             auto pv = [&](int st) {
-                const int pb = st & 1;
+                const int pb = st & 1, s = st % kStages;
+                const int nt = min(kT, ntiles - st * kT);
                 mbar_wait(&p_full[pb], (st >> 1) & 1, a.err);
                 tc_fence_after();
-                const int t0 = kStepTiles * st, nt = min(kStepTiles, ntiles - t0);
-                for (int h = 0; h < nt; ++h) {
-                    const int s = (t0 + h) % kStages;
-                    const uint32_t sv = smem_u32(smem + Ly::kOffRing + s * kStageBytes + 2 * kHalfBytes);
-                    // A = P [128 lanes][64 keys] in TMEM (8 columns per 16 keys); B = V
-                    // [64 keys][128 dims], MN-major: 8-key groups 1024 B apart, the two
-                    // 64-dim halves kHalfBytes apart, 16 keys = 2048 B (descriptor units
-                    // of 16 B).
-                    const uint64_t bd0 = smem_desc_sw128(sv, kHalfBytes, 1024);
-#pragma unroll
-                    for (int k16 = 0; k16 < kNk / 16; ++k16)
-                        tc_mma_ts(tO, tP(pb) + h * kPCols + k16 * 8, bd0 + k16 * (2048 >> 4), idesc_o,
-                                  (st > 0 || h > 0 || k16 > 0) ? 1u : 0u);
-                }
+                // A = P [M lanes][keys] in TMEM (8 columns per 16 keys); B = V
+                // [keys][128 dims], MN-major: 8-key groups 1024 B apart (keys run
+                // on across the step's tiles), the two 64-dim halves one region
+                // apart, 16 keys = 2048 B (descriptor units of 16 B)
+                const uint32_t sv = smem_u32(smem + Ly::kOffRing + s * kStageBytes + 2 * kRegion);
+                const uint64_t bd0 = smem_desc_sw128(sv, kRegion, 1024);
+                for (int kc = 0; kc < nt * (kNk / 16); ++kc)
+                    tc_mma_ts(tO, tP(pb) + kc * 8, bd0 + kc * (2048 >> 4), idesc_o, (st > 0 || kc > 0) ? 1u : 0u);
                 tc_commit(&o_done[pb]);
-                for (int h = 0; h < nt; ++h) tc_commit(&kv_empty[(t0 + h) % kStages]);
+                tc_commit(&kv_empty[s]);
             };
             for (int st = 0; st < nsteps; ++st) {
-                const int sb = st & 1;
+                const int sb = st & 1, s = st % kStages;
+                const int nt = min(kT, ntiles - st * kT);
                 mbar_wait(&s_empty[sb], ((st >> 1) & 1) ^ 1, a.err);
-                const int t0 = kStepTiles * st, nt = min(kStepTiles, ntiles - t0);
-                for (int h = 0; h < nt; ++h) {
-                    const int i = t0 + h;
-                    const int s = i % kStages;
-                    mbar_wait(&kv_full[s], (i / kStages) & 1, a.err);
-                    tc_fence_after();
-                    const uint64_t kd0 = smem_desc_sw128(smem_u32(smem + Ly::kOffRing + s * kStageBytes), 16, 1024);
+                mbar_wait(&kv_full[s], (st / kStages) & 1, a.err);
+                tc_fence_after();
+                const uint64_t kd0 = smem_desc_sw128(smem_u32(smem + Ly::kOffRing + s * kStageBytes), 16, 1024);
+                const uint32_t id = nt == kT ? idesc_s : idesc_s1;
 #pragma unroll
-                    for (int k16 = 0; k16 < kD / 16; ++k16) {
-                        const uint32_t half = k16 >> 2, kin = (k16 & 3) * 32;
-                        tc_mma(tS(sb) + h * kNk, qd0 + ((half * (kM * 128) + kin) >> 4),
-                               kd0 + ((half * kHalfBytes + kin) >> 4), idesc_s, k16 > 0 ? 1u : 0u);
-                    }
+                for (int k16 = 0; k16 < kD / 16; ++k16) {
+                    const uint32_t half = k16 >> 2, kin = (k16 & 3) * 32;
+                    tc_mma(tS(sb), qd0 + ((half * (kM * 128) + kin) >> 4), kd0 + ((half * kRegion + kin) >> 4), id,
+                           k16 > 0 ? 1u : 0u);
                 }
                 tc_commit(&s_full[sb]);
                 if (st > 0) pv(st - 1);
@@ -347,18 +348,21 @@ __global__ void __launch_bounds__(Roles<kHalf>::kThreads, 1)
         // O are never read, so a warp with none skips the arithmetic)
         const bool quarter_live = kHalf ? (warp < a.rows) : (rt * kRows + (warp & 3) * 32 < a.rows);
         const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
-        // full tiles: 16 consecutive columns of the step (group cgp); half
-        // tiles: 32 (thread half `sub` of the row's pair)
-        constexpr int kCols = kHalf ? kHCols : kGCols;
+        // full tiles: 16 consecutive columns of the one-tile step (group cgp);
+        // half tiles: half of the step's columns (thread half `sub` of the
+        // row's pair) -- with two tiles per step, one whole tile per thread
+        constexpr int kCols = kHalf ? kStepKeys / 2 : kStepKeys / kGroups;
         const int cgp = kHalf ? 0 : warp / 4;
         const int sub = kHalf ? (lane >> 4) : 0;
-        const int col0 = kHalf ? sub * kHCols : cgp * kGCols;
-        // tree: this thread's 32-bit windows of the row's ancestor mask, one per
-        // block tile (block keys col0.. of tile 0 and of tile 1)
-        uint32_t win_t0 = 0u, win_t1 = 0u;
+        const int col0 = kHalf ? sub * kCols : cgp * kCols;   // S columns of the step
+        const int tsub = col0 / kNk, ctile = col0 % kNk;     // tile within the step, first key in it
+        // tree: this thread's windows of the row's ancestor mask, one per block
+        // tile (block keys ctile.. of tile 0 and of tile 1)
+        using Win = typename std::conditional<(kCols > 32), uint64_t, uint32_t>::type;
+        Win win_t0 = 0, win_t1 = 0;
         if (tree && valid) {
-            win_t0 = static_cast<uint32_t>(anc[2 * j] >> col0);
-            win_t1 = static_cast<uint32_t>(anc[2 * j + 1] >> col0);
+            win_t0 = static_cast<Win>(anc[2 * j] >> ctile);
+            win_t1 = static_cast<Win>(anc[2 * j + 1] >> ctile);
         }
         float* red = reinterpret_cast<float*>(smem + Ly::kOffRed);
         float* lsx = reinterpret_cast<float*>(smem + Ly::kOffLsum);
@@ -371,8 +375,12 @@ __global__ void __launch_bounds__(Roles<kHalf>::kThreads, 1)
             const bool work = quarter_live;
             uint32_t rs[kCols];
             if (work) {
-                if constexpr (kHalf) {
-                    tmem_ld32_h_sync<kHCols>(tS(sb) + lane_off, rs);
+                if constexpr (kHalf && kCols == 64) {
+                    // columns col0 .. col0+31 and col0+32 .. col0+63
+                    tmem_ld32_h_sync<64>(tS(sb) + lane_off, *reinterpret_cast<uint32_t(*)[32]>(rs));
+                    tmem_ld32_h_sync<64>(tS(sb) + lane_off + 32, *reinterpret_cast<uint32_t(*)[32]>(rs + 32));
+                } else if constexpr (kHalf) {
+                    tmem_ld32_h_sync<32>(tS(sb) + lane_off, rs);
                 } else {
                     tmem_ld16_sync(tS(sb) + lane_off + col0, rs);
                 }
@@ -380,24 +388,26 @@ __global__ void __launch_bounds__(Roles<kHalf>::kThreads, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&s_empty[sb]);
-            const int gt = first + st;
+            const int ti = st * kT + tsub;            // this thread's tile of the CTA's range
+            const bool tile_live = ti < ntiles;       // a last, odd step has one tile
+            const int gt = first + ti;
             const bool is_block = gt >= n_ctx;
-            const int kb = (is_block ? (gt - n_ctx) * kNk : gt * kNk) + col0;
+            const int kb = (is_block ? (gt - n_ctx) * kNk : gt * kNk) + ctile;
             float sc[kCols];
             float mpart = -INFINITY;
             if (work) {
 #pragma unroll
                 for (int e = 0; e < kCols; ++e) sc[e] = __uint_as_float(rs[e]) * a.scale_log2;
-                if (is_block || kb + kCols > t) {
+                if (is_block || kb + kCols > t || !tile_live) {
                     // branch-free mask: key kb + e is visible iff e < lim (context:
-                    // kl < t; chain block: kl <= j and kl < R) or, for a tree block,
-                    // iff bit e of the ancestor window starting at key kb is set
-                    const bool tree_blk = kTree && is_block;
-                    const int lim = !is_block ? t - kb : (j + 1 < a.R ? j + 1 : a.R) - kb;
-                    const uint32_t win = tree_blk ? (gt - n_ctx == 0 ? win_t0 : win_t1) : 0u;
+                    // kl < t; chain block: kl <= j and kl < R; no tile: none) or,
+                    // for a tree block, iff bit e of the ancestor window is set
+                    const bool tree_blk = kTree && is_block && tile_live;
+                    const int lim = !tile_live ? 0 : !is_block ? t - kb : (j + 1 < a.R ? j + 1 : a.R) - kb;
+                    const Win win = tree_blk ? (gt - n_ctx == 0 ? win_t0 : win_t1) : Win(0);
 #pragma unroll
                     for (int e = 0; e < kCols; ++e) {
-                        const bool vis = tree_blk ? ((win >> e) & 1u) != 0u : e < lim;
+                        const bool vis = tree_blk ? ((win >> e) & Win(1)) != Win(0) : e < lim;
                         sc[e] = vis ? sc[e] : -INFINITY;
                     }
                 }
@@ -477,8 +487,15 @@ __global__ void __launch_bounds__(Roles<kHalf>::kThreads, 1)
             }
             if (work) {
                 // P of this thread's columns into TMEM buffer sb, two keys per column
-                if constexpr (kHalf) tmem_st16_h<kHCols / 2>(tP(sb) + lane_off, pk);
-                else tmem_st8(tP(sb) + lane_off + col0 / 2, pk);
+                if constexpr (kHalf && kCols == 64) {
+                    // P columns col0/2 .. col0/2+31 (two keys per column)
+                    tmem_st16_h<32>(tP(sb) + lane_off, *reinterpret_cast<const uint32_t(*)[16]>(pk));
+                    tmem_st16_h<32>(tP(sb) + lane_off + 16, *reinterpret_cast<const uint32_t(*)[16]>(pk + 16));
+                } else if constexpr (kHalf) {
+                    tmem_st16_h<16>(tP(sb) + lane_off, pk);
+                } else {
+                    tmem_st8(tP(sb) + lane_off + col0 / 2, pk);
+                }
                 tmem_st_wait();
             }
             tc_fence_before();
