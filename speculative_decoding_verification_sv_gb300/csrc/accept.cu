@@ -91,6 +91,8 @@ __device__ __forceinline__ ArgMax warp_pick(ArgMax a) {
 __global__ void __launch_bounds__(kGreedyThreads) greedy_partial_kernel(const float* __restrict__ logits, int V,
                                                                          int nchunk, int2* __restrict__ part,
                                                                          unsigned int* err) {
+    pdl_wait();   // inputs come from the kernels before this one
+    pdl_launch_dependents();
     const int row = blockIdx.y;
     const int c0 = blockIdx.x * kGreedyChunk;
     const int c1 = min(c0 + kGreedyChunk, V);
@@ -168,6 +170,8 @@ __global__ void __launch_bounds__(128) greedy_finish_kernel(const int2* __restri
                                                              const int32_t* __restrict__ parent, int R, int V,
                                                              int32_t* n_acc, int32_t* out_tok, int32_t* path,
                                                              unsigned int* err) {
+    pdl_wait();   // inputs come from the kernels before this one
+    pdl_launch_dependents();
     __shared__ int g[kMaxR];
     __shared__ int par_s[kMaxR];
     const int b = blockIdx.x;
@@ -215,6 +219,8 @@ __global__ void __launch_bounds__(128) greedy_finish_kernel(const int2* __restri
 __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads)
     sample_stats_kernel(const float* __restrict__ logits, int V, float T, int nblk, int smem_blocks,
                         float2* __restrict__ stats, unsigned int* err) {
+    pdl_wait();   // inputs come from the kernels before this one
+    pdl_launch_dependents();
     extern __shared__ __align__(128) float srow[];   // [local blocks][4096]
     __shared__ float cmax[kCluster];
     __shared__ float bsum[kMaxBlocks];
@@ -333,6 +339,8 @@ __global__ void __launch_bounds__(kRowThreads, kRowCtasPerSm) sample_stats_row_k
                                                                          float T, int nblk, int nrows,
                                                                          float2* __restrict__ stats,
                                                                          unsigned int* err) {
+    pdl_wait();   // inputs come from the kernels before this one
+    pdl_launch_dependents();
     __shared__ float csum[kMaxBlocks * kChunksPerBlk];
     __shared__ float bsum[kMaxBlocks];
     __shared__ float wred[kRowWarps];
@@ -671,6 +679,8 @@ __device__ int tree_descent(const Vals& vals, int V, float total, float u, PassS
 
 __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads)
     sample_finish_kernel(SampleArgs a) {
+    pdl_wait();   // inputs come from the kernels before this one
+    pdl_launch_dependents();
     __shared__ PassSmem sm;
     __shared__ int par_s[kMaxR];
     __shared__ float Schain[kMaxR];
@@ -777,6 +787,8 @@ __host__ __device__ constexpr size_t chain_ws_bytes(int B) {
 }
 
 __global__ void __launch_bounds__(kMaxR) chain_walk_kernel(SampleArgs a, ChainWs w) {
+    pdl_wait();   // inputs come from the kernels before this one
+    pdl_launch_dependents();
     __shared__ int first_rej;
     const int b = blockIdx.x, t = threadIdx.x;
     const int R = a.R, V = a.V, Vq = a.Vq;
@@ -818,6 +830,8 @@ __global__ void __launch_bounds__(kMaxR) chain_walk_kernel(SampleArgs a, ChainWs
 // One CTA per (4096-block, sequence): chunk and block sums of the residual and
 // of p over the row the walk stopped at.
 __global__ void __launch_bounds__(kThreads) chain_sums_kernel(SampleArgs a, ChainWs w) {
+    pdl_wait();   // inputs come from the kernels before this one
+    pdl_launch_dependents();
     const int blk = blockIdx.x, b = blockIdx.y;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int V = a.V, Vq = a.Vq, R = a.R;
@@ -872,6 +886,8 @@ __global__ void __launch_bounds__(kThreads) chain_sums_kernel(SampleArgs a, Chai
 // One warp per sequence: totals (levels 13 -> 18), the choice between the
 // residual and p, and the descent.
 __global__ void __launch_bounds__(32) chain_draw_kernel(SampleArgs a, ChainWs w) {
+    pdl_wait();   // inputs come from the kernels before this one
+    pdl_launch_dependents();
     __shared__ float bs[kMaxBlocks];
     __shared__ float tree[2 * kMaxBlocks];
     const int b = blockIdx.x, lane = threadIdx.x;
@@ -963,8 +979,12 @@ cudaError_t launch_accept_greedy(const float* logits, const int32_t* tok, const 
     const int nchunk = (V + kGreedyChunk - 1) / kGreedyChunk;
     int2* part = static_cast<int2*>(ws);
     unsigned int* err = device_error_word();
-    greedy_partial_kernel<<<dim3(nchunk, B * R), kGreedyThreads, 0, st>>>(logits, V, nchunk, part, err);
-    greedy_finish_kernel<<<B, 128, 0, st>>>(part, nchunk, tok, parent, R, V, n_acc, out_tok, path, err);
+    cudaError_t e = launch_pdl(greedy_partial_kernel, dim3(nchunk, B * R), dim3(kGreedyThreads), 0, st, logits, V,
+                               nchunk, part, err);
+    if (e != cudaSuccess) return e;
+    e = launch_pdl(greedy_finish_kernel, dim3(B), dim3(128), 0, st, static_cast<const int2*>(part), nchunk, tok, parent,
+                   R, V, n_acc, out_tok, path, err);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
@@ -996,10 +1016,16 @@ cudaError_t launch_accept_sample(const float* logits, const float* q, int Vq, co
     {
         const int slots = device_sm_count() * kRowCtasPerSm;
         const int nrows = B * R, grid = nrows < slots ? nrows : slots;
-        sample_stats_row_kernel<<<grid, kRowThreads, 0, st>>>(logits, V, temperature, nblk, nrows, stats, err);
+        e = launch_pdl(sample_stats_row_kernel, dim3(grid), dim3(kRowThreads), 0, st, logits, V, temperature, nblk, nrows,
+                       stats, err);
+        if (e != cudaSuccess) return e;
     }
     else
-        sample_stats_kernel<<<B * R * kCluster, kThreads, smem, st>>>(logits, V, temperature, nblk, nlocal, stats, err);
+    {
+        e = launch_pdl(sample_stats_kernel, dim3(B * R * kCluster), dim3(kThreads), smem, st, logits, V, temperature, nblk,
+                       nlocal, stats, err);
+        if (e != cudaSuccess) return e;
+    }
     if (debug_sync()) {
         e = cudaStreamSynchronize(st);
         if (e != cudaSuccess) return e;
@@ -1029,13 +1055,17 @@ cudaError_t launch_accept_sample(const float* logits, const float* q, int Vq, co
         w.rec = reinterpret_cast<int4*>(static_cast<uint8_t*>(ws) + stats_bytes(B, R));
         w.sums = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + stats_bytes(B, R) +
                                           ((static_cast<size_t>(B) * sizeof(int4) + 255) / 256) * 256);
-        chain_walk_kernel<<<B, kMaxR, 0, st>>>(a, w);
-        chain_sums_kernel<<<dim3(nblk, B), kThreads, 0, st>>>(a, w);
-        chain_draw_kernel<<<B, 32, 0, st>>>(a, w);
+        e = launch_pdl(chain_walk_kernel, dim3(B), dim3(kMaxR), 0, st, a, w);
+        if (e != cudaSuccess) return e;
+        e = launch_pdl(chain_sums_kernel, dim3(nblk, B), dim3(kThreads), 0, st, a, w);
+        if (e != cudaSuccess) return e;
+        e = launch_pdl(chain_draw_kernel, dim3(B), dim3(32), 0, st, a, w);
+        if (e != cudaSuccess) return e;
     } else {
         // trees (sibling residuals depend on each other), or a workspace that
         // only holds the row statistics: one cluster walks each sequence
-        sample_finish_kernel<<<B * kCluster, kThreads, 0, st>>>(a);
+        e = launch_pdl(sample_finish_kernel, dim3(B * kCluster), dim3(kThreads), 0, st, a);
+        if (e != cudaSuccess) return e;
     }
     if (debug_sync()) {
         e = cudaStreamSynchronize(st);

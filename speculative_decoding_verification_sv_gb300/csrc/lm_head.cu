@@ -42,6 +42,8 @@ __global__ void __launch_bounds__(kThreads) lm_head_kernel(const __grid_constant
                                                           float* __restrict__ logits, int N, int H, int V, int n0,
                                                           int nslab, unsigned int* err) {
     using S = LmSmem<NT>;
+    pdl_wait();   // the hidden rows come from the kernels before this one
+    pdl_launch_dependents();
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     float* out_s = reinterpret_cast<float*>(smem + kStages * S::kStageBytes);
@@ -157,10 +159,9 @@ cudaError_t launch_nt(const uint16_t* hid, const uint16_t* W, float* logits, int
     const int per_sm = S::kTotal <= 110 * 1024 ? 2 : 1;
     int grid = device_sm_count() * per_sm;
     if (grid > nslab) grid = nslab;
-    lm_head_kernel<NT><<<grid, kThreads, S::kTotal, st>>>(*reinterpret_cast<const CUtensorMap*>(tmW),
-                                                           *reinterpret_cast<const CUtensorMap*>(tmH), logits, N, H, V,
-                                                           n0, nslab, device_error_word());
-    return cudaGetLastError();
+    return launch_pdl(lm_head_kernel<NT>, dim3(grid), dim3(kThreads), S::kTotal, st,
+                      *reinterpret_cast<const CUtensorMap*>(tmW), *reinterpret_cast<const CUtensorMap*>(tmH), logits, N,
+                      H, V, n0, nslab, device_error_word());
 }
 
 }  // namespace

@@ -10,6 +10,25 @@
 
 namespace sv {
 
+// Launch with programmatic dependent launch allowed: the kernel may start
+// while the previous kernel on the stream drains, and waits
+// (griddepcontrol.wait) before it touches anything that kernel produced.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                              Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
+}
+
 constexpr int kSmCount = 152;   // GB300; launch heuristics query the device when it differs
 
 unsigned int* device_error_word();          // per-device __device__ word (sv_api.cu)
