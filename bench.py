@@ -617,6 +617,16 @@ def main():
            "steps": E, "how": "pinned H2D of the round's inputs + CUDA-graph replay of the C-ABI calls + "
                               "D2H of n_acc/out_tok/path + host sync, every step"}
 
+    # greedy decisions too close to call within the logits tolerance: rows whose
+    # top-1 / top-2 margin is below 1e-2 max|logit| (counted, not failed)
+    near_ties = None
+    if mode == "greedy":
+        lg = rnd.logits.float()
+        top2 = torch.topk(lg, 2, dim=-1).values
+        bound = 1e-2 * float(lg.abs().max())
+        near_ties = {"rows": int(lg.shape[0]), "below_bound": int(((top2[:, 0] - top2[:, 1]) < bound).sum()),
+                     "bound": bound}
+
     line = {"metric": "verify steps/s", "value": value, "unit": "steps/s", "n_gpus": ws, "steps": K,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16 (fp32 accumulate; fp32 acceptance)",
@@ -624,7 +634,7 @@ def main():
             "config": config_dict(w, mode, ws, chunk),
             "draft_tokens_per_s": value * w.B * (w.R - 1),
             "mean_accepted": float(np.mean(n_acc)),
-            "roofline": roofline, "kernels": kern, "e2e": e2e, "clocks": clk,
+            "roofline": roofline, "kernels": kern, "e2e": e2e, "clocks": clk, "greedy_near_ties": near_ties,
             "gpu_launches": rnd.launches_per_step() * K}
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, mode)
