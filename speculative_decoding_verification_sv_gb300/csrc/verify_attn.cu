@@ -63,6 +63,7 @@ constexpr int kMaxCluster = 16;
 #define SV_ATTN_MERGE_COST 6
 #endif
 constexpr int kMergeCost = SV_ATTN_MERGE_COST;   // workspace merge, in key-tile times
+constexpr int kWsMergeBatch = 12;         // workspace partials per unit merged in one round of loads
 constexpr int kGroups = 4;                // full tiles: column groups of a step
 #ifndef SV_ATTN_HALF_MAX_ROWS
 #define SV_ATTN_HALF_MAX_ROWS 64
@@ -624,6 +625,51 @@ __global__ void __launch_bounds__(Roles<kHalf>::kThreads, 1)
             __threadfence();
             const float* base = a.ws_part + static_cast<size_t>(unit) * a.clusters * a.part_rows * kRec;
             const int nc = a.clusters;
+            const size_t pstride = static_cast<size_t>(a.part_rows) * kRec;
+            if (nc <= kWsMergeBatch) {
+                // one work item per (row, 4 output dims) over every thread of the
+                // cluster; each item's partials are all loaded in one round
+                const int nitems = nrows * 32;
+                for (int it = rank * kThreads + threadIdx.x; it < nitems; it += C * kThreads) {
+                    const int lr = it >> 5, l4 = it & 31;
+                    float2 ml[kWsMergeBatch];
+                    float4 ox[kWsMergeBatch];
+#pragma unroll
+                    for (int c = 0; c < kWsMergeBatch; ++c) {
+                        if (c < nc) {
+                            const float* rc = base + c * pstride + static_cast<size_t>(lr) * kRec;
+                            ml[c] = __ldcg(reinterpret_cast<const float2*>(rc));
+                            ox[c] = __ldcg(reinterpret_cast<const float4*>(rc + 4) + l4);
+                        } else {
+                            ml[c] = make_float2(-INFINITY, 0.f);
+                            ox[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+                        }
+                    }
+                    float M = -INFINITY;
+#pragma unroll
+                    for (int c = 0; c < kWsMergeBatch; ++c)
+                        if (ml[c].y > 0.f) M = fmaxf(M, ml[c].x);
+                    float L = 0.f;
+                    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                    if (M != -INFINITY) {
+#pragma unroll
+                        for (int c = 0; c < kWsMergeBatch; ++c) {
+                            const float w = ml[c].y > 0.f ? exp2f(ml[c].x - M) : 0.f;
+                            L += w * ml[c].y;
+                            acc.x += w * ox[c].x;
+                            acc.y += w * ox[c].y;
+                            acc.z += w * ox[c].z;
+                            acc.w += w * ox[c].w;
+                        }
+                    }
+                    const float inv = L > 0.f ? 1.0f / L : 0.f;
+                    const int row = rt * kRows + lr;
+                    const int jr = row / a.G, h = g * a.G + row % a.G;
+                    uint16_t* dst = a.out + ((static_cast<size_t>(b) * a.R + jr) * a.Hq + h) * kD + 4 * l4;
+                    *reinterpret_cast<uint2*>(dst) =
+                        make_uint2(pack_bf16x2(acc.x * inv, acc.y * inv), pack_bf16x2(acc.z * inv, acc.w * inv));
+                }
+            } else
             for (int lr = rank + C * warp; lr < nrows; lr += C * (kThreads / 32)) {
                 // lane c holds partial c's (max, sum) (nc <= 32), then the O
                 // records are read eight at a time, branch-free
@@ -757,7 +803,8 @@ cudaError_t launch_mode(const AttnPlan& p, const sv_attn_shape& s, const uint8_t
 // CTA); the cost counts the key tiles of the busiest CTA plus a fixed start-up
 // of three tiles per wave, and a merge through the workspace as six tiles (its
 // partials cross the L2 in a few dependent round trips, measured at several
-// microseconds).  Ties keep the larger cluster.
+// microseconds) plus the partial bytes each merging SM reads (one SM pulls
+// about 40 KB per tile time).  Ties keep the larger cluster.
 AttnPlan attn_plan(const sv_attn_shape& s) {
     AttnPlan p;
     p.G = s.Hq / s.Hkv;
@@ -780,7 +827,9 @@ AttnPlan attn_plan(const sv_attn_shape& s) {
         for (int64_t nc = 1; nc <= nc_max; nc = nc < nc_max ? nc_max : nc_max + 1) {   // one cluster, or the most
             const int64_t waves = (units * nc + cap - 1) / cap;
             const int64_t per_cta = (tiles + C * nc - 1) / (C * nc);
-            const int64_t cost = waves * (3 + per_cta) + (nc > 1 ? kMergeCost : 0);
+            const int64_t part_rows = p.rows < kRows ? p.rows : kRows;
+            const int64_t merge_bytes = nc * part_rows * kRec * 4 / C;   // per SM of the merging cluster
+            const int64_t cost = waves * (3 + per_cta) + (nc > 1 ? kMergeCost + merge_bytes / (40 * 1024) : 0);
             if (best < 0 || cost < best) {
                 best = cost;
                 p.splits = C;
