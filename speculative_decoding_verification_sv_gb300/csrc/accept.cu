@@ -329,10 +329,10 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads)
 // per lane), block sums over 32 chunks, then the 64 zero-padded block sums.
 // One row in flight per SM keeps the re-read in L2 (152 x 600 KB < 126 MB).
 #ifndef SV_ROW_THREADS
-#define SV_ROW_THREADS 512
+#define SV_ROW_THREADS 1024
 #endif
-constexpr int kRowThreads = SV_ROW_THREADS;       // 512: one CTA per SM; 256: two
-constexpr int kRowCtasPerSm = 512 / kRowThreads;
+constexpr int kRowThreads = SV_ROW_THREADS;       // one CTA of 32 warps per SM (latency hiding)
+constexpr int kRowCtasPerSm = kRowThreads >= 512 ? 1 : 512 / kRowThreads;
 constexpr int kRowWarps = kRowThreads / 32;
 
 __global__ void __launch_bounds__(kRowThreads, kRowCtasPerSm) sample_stats_row_kernel(const float* __restrict__ logits, int V,
