@@ -161,6 +161,13 @@ __device__ __forceinline__ void cluster_arrive_relaxed() {
     asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
 }
 __device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.aligned;" ::: "memory"); }
+// Full cluster barrier with release / acquire ordering of shared-memory
+// writes (local and remote).  Warp-collective (.aligned): call it from
+// converged warps only -- a warp whose other lanes are still busy (a lone
+// producer lane) must __syncwarp() first.
+__device__ __forceinline__ void cluster_sync_warp() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
 
 // Programmatic dependent launch: wait for the preceding kernel's results /
 // let the next kernel start its prologue.

@@ -113,7 +113,7 @@ struct Lay {
     static constexpr int kOffRed = kOffAnc + kMaxR * 16;               // [2][kGroups][kRows] partial row maxima
     static constexpr int kOffLsum = kOffRed + 2 * kGroups * kRows * 4;  // [kGroups][kRows] partial row sums
     static constexpr int kSmemBytes = kOffLsum + kGroups * kRows * 4 + 1024;
-    static_assert(kRows * kRec * 4 <= kRingBytes, "partials reuse the K/V ring");
+    static_assert((kRows + kMaxCluster - 1) * kRec * 4 <= kRingBytes, "pushed partials reuse the K/V ring");
     static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
     static_assert((2 * kStages + 9) * 8 + 4 <= 248, "barrier area (the word at +248 is the ticket flag)");
 };
@@ -160,7 +160,8 @@ __global__ void __launch_bounds__(Roles<kHalf>::kThreads, 1)
     uint64_t* q_ready = o_done + 2;
     uint32_t* tmem_s = reinterpret_cast<uint32_t*>(q_ready + 1);
     uint64_t* anc = reinterpret_cast<uint64_t*>(smem + Ly::kOffAnc);   // [kMaxR][2]
-    float* part = reinterpret_cast<float*>(smem + Ly::kOffRing);        // [kRows][kRec] by row, after the loop
+    // after the loop: partial records pushed to this CTA, [row / C][source rank][kRec]
+    float* part = reinterpret_cast<float*>(smem + Ly::kOffRing);
 
     cg::cluster_group cluster = cg::this_cluster();
     const int C = static_cast<int>(cluster.num_blocks());
@@ -520,36 +521,48 @@ __global__ void __launch_bounds__(Roles<kHalf>::kThreads, 1)
             for (int c2 = 0; c2 < kGroups; ++c2) lt += lsx[c2 * kRows + r];
         }
         const bool use = nsteps >= 1 && lt > 0.f;
-        const int prow = gr - rt * kRows;              // < kRows for every real row
-        float* rec = part + (valid ? prow : 0) * kRec;
-        if (valid && cgp == 0 && sub == 0) {
-            rec[0] = use ? m_ref : -INFINITY;
-            rec[1] = use ? lt : 0.f;
-        }
+        // O of this thread's columns, held in registers across the barrier
         constexpr int kOCols = kHalf ? kD / 2 : kD / kGroups;   // O columns per thread
         const int ocol0 = kHalf ? sub * (kD / 2) : cgp * (kD / kGroups);
+        uint32_t ov[kOCols];
 #pragma unroll
         for (int c0 = 0; c0 < kOCols; c0 += 16) {
-            uint32_t o16[16] = {};
+            uint32_t(&o16)[16] = *reinterpret_cast<uint32_t(*)[16]>(ov + c0);
+            // the condition of a warp-collective TMEM load must be warp-uniform
+            // (nsteps is; `use` is per row)
             if (nsteps >= 1) {
                 if constexpr (kHalf) tmem_ld16_h_sync<kD / 2>(tO + lane_off + c0, o16);
                 else tmem_ld16_sync(tO + lane_off + ocol0 + c0, o16);
             }
-            if (valid) {
 #pragma unroll
-                for (int e = 0; e < 16; e += 4)
-                    *reinterpret_cast<uint4*>(rec + 4 + ocol0 + c0 + e) =
-                        use ? make_uint4(o16[e], o16[e + 1], o16[e + 2], o16[e + 3]) : make_uint4(0u, 0u, 0u, 0u);
-            }
+            for (int e = 0; e < 16; ++e) o16[e] = (nsteps >= 1 && use) ? o16[e] : 0u;
+        }
+        tc_fence_before();
+        __syncwarp();
+        cluster_sync_warp();   // (1) every CTA of the cluster has drained its ring
+        // push the partial record of row prow into slot `rank` of the row's
+        // owner, CTA prow % C: slots [(prow / C) * C + src] in its ring area
+        if (valid) {
+            const int prow = gr - rt * kRows;          // < kRows for every real row
+            float* rec = cluster.map_shared_rank(part + ((prow / C) * C + rank) * kRec, prow % C);
+            if (cgp == 0 && sub == 0)
+                *reinterpret_cast<float2*>(rec) = make_float2(use ? m_ref : -INFINITY, use ? lt : 0.f);
+#pragma unroll
+            for (int e = 0; e < kOCols; e += 4)
+                *reinterpret_cast<uint4*>(rec + 4 + ocol0 + e) = make_uint4(ov[e], ov[e + 1], ov[e + 2], ov[e + 3]);
         }
     }
-    tc_fence_before();
-    __syncthreads();
-    cluster.sync();   // all partials written (and every CTA of the cluster has started)
+    if (warp >= kSoftWarps) {   // (1), producer and MMA warps, once their lane 0 is done
+        __syncwarp();
+        cluster_sync_warp();
+    }
+    __syncwarp();
+    cluster_sync_warp();   // (2) every record pushed and visible to its owner
 
     // merge: this CTA finalises rows rank, rank + C, ... of the row tile (all
-    // warps); with one cluster per (b, g, row tile) it writes the bf16 rows,
-    // otherwise the cluster's merged partial (max, sum, unnormalised O)
+    // warps) from the records pushed to it; with one cluster per (b, g, row
+    // tile) it writes the bf16 rows, otherwise the cluster's merged partial
+    // (max, sum, unnormalised O)
     const int nrows = min(kRows, a.rows - rt * kRows);
     const int unit = hg * a.row_tiles + rt;
     const int ci = blockIdx.x / C;
@@ -561,12 +574,14 @@ __global__ void __launch_bounds__(Roles<kHalf>::kThreads, 1)
         *reinterpret_cast<uint2*>(dst) =
             make_uint2(pack_bf16x2(acc.x * inv, acc.y * inv), pack_bf16x2(acc.z * inv, acc.w * inv));
     };
-    for (int lr = rank + C * warp; lr < nrows; lr += C * (kThreads / 32)) {
+    for (int li = warp; rank + C * li < nrows; li += kThreads / 32) {
+        const int lr = rank + C * li;
+        const float* slots = part + li * C * kRec;
         float ms = -INFINITY, ls = 0.f;
         if (lane < C) {
-            const float* rec_s = cluster.map_shared_rank(part + lr * kRec, lane);
-            ms = rec_s[0];
-            ls = rec_s[1];
+            const float2 ml = *reinterpret_cast<const float2*>(slots + lane * kRec);
+            ms = ml.x;
+            ls = ml.y;
         }
         float M = ms;
 #pragma unroll
@@ -575,8 +590,8 @@ __global__ void __launch_bounds__(Roles<kHalf>::kThreads, 1)
         float L = wgt * ls;
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
-        // O: branch-free, eight remote loads in flight at a time (an empty
-        // partial has weight 0 and an all-zero record)
+        // O: branch-free, eight slots at a time (an empty partial has weight 0
+        // and an all-zero record)
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
         for (int s0 = 0; s0 < C; s0 += 8) {
             float4 x[8];
@@ -585,7 +600,7 @@ __global__ void __launch_bounds__(Roles<kHalf>::kThreads, 1)
             for (int u = 0; u < 8; ++u) {
                 const int sr = s0 + u < C ? s0 + u : 0;
                 wv[u] = __shfl_sync(0xffffffffu, wgt, sr);
-                x[u] = *reinterpret_cast<const float4*>(cluster.map_shared_rank(part + lr * kRec + 4, sr) + 4 * lane);
+                x[u] = *reinterpret_cast<const float4*>(slots + sr * kRec + 4 + 4 * lane);
                 if (s0 + u >= C) wv[u] = 0.f;
             }
 #pragma unroll
@@ -618,10 +633,13 @@ __global__ void __launch_bounds__(Roles<kHalf>::kThreads, 1)
             const unsigned int done = atomicAdd(a.ws_cnt + unit, 1u);
             const bool is_last = done == static_cast<unsigned int>(a.clusters - 1);
             if (is_last) a.ws_cnt[unit] = 0u;
-            *last_flag = is_last ? 1u : 0u;
+            // the verdict goes to every CTA's own flag, so that no CTA reads
+            // another's shared memory after the barrier below (and none waits
+            // for the others before it exits)
+            for (int r = 0; r < C; ++r) *cluster.map_shared_rank(last_flag, r) = is_last ? 1u : 0u;
         }
         cluster.sync();
-        if (*cluster.map_shared_rank(last_flag, 0) != 0u) {
+        if (*last_flag != 0u) {
             __threadfence();
             const float* base = a.ws_part + static_cast<size_t>(unit) * a.clusters * a.part_rows * kRec;
             const int nc = a.clusters;
@@ -712,7 +730,6 @@ __global__ void __launch_bounds__(Roles<kHalf>::kThreads, 1)
             }
         }
     }
-    cluster.sync();   // no CTA leaves while its partials may still be read
     if (warp == kMmaWarp) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
