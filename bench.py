@@ -195,8 +195,10 @@ class Round:
             self.length.copy_(self.len0, non_blocking=True)
             rec("attn0")
             for l in range(w.L):
+                # layers after the first follow a kernel that writes neither the
+                # length nor the cache
                 sv.verify_attn(self.q[l], self.kc[l], self.vc[l], self.length, self.kb[l], self.vb[l],
-                               parent=self.parent, out=self.attn_out[l], ws=self.attn_ws)
+                               parent=self.parent, out=self.attn_out[l], ws=self.attn_ws, cache_ready=l > 0)
             rec("attn1")
             sv.lm_head(self.hid, self.W, logits=self.logits)
             rec("lm1")

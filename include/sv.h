@@ -144,6 +144,21 @@ SV_API sv_status sv_verify_attn(const sv_attn_shape* shape, const uint16_t* q, c
                          const uint16_t* v_blk, const int32_t* parent, float scale, uint16_t* out,
                          void* ws, size_t ws_bytes, void* stream);
 
+/* sv_verify_attn with launch flags (sv_verify_attn is flags = 0).
+ *   SV_ATTN_CACHE_READY  the caller promises that the kernel enqueued on
+ *       `stream` just before this call writes neither len nor k_cache /
+ *       v_cache (e.g. the previous layer's attention within one verify round;
+ *       NOT the first layer after sv_kv_commit).  The kernel then reads len
+ *       and starts loading the committed cache rows while that kernel is
+ *       still finishing (programmatic dependent launch); q, the block K/V,
+ *       parent and every output are still touched only after it completes.
+ * Unknown flag bits return SV_ERR_ARG. */
+#define SV_ATTN_CACHE_READY 1u
+SV_API sv_status sv_verify_attn_ex(const sv_attn_shape* shape, const uint16_t* q, const uint16_t* k_cache,
+                                   const uint16_t* v_cache, const int32_t* len, const uint16_t* k_blk,
+                                   const uint16_t* v_blk, const int32_t* parent, float scale, uint16_t* out,
+                                   void* ws, size_t ws_bytes, uint32_t flags, void* stream);
+
 /* ------------------------------------------------------------------------ */
 /* LM head ([SCS] sec. 3: the target's block forward yields one logits row   */
 /* per block row; [TUT] sec. 1.1: the weights are read once per forward).    */

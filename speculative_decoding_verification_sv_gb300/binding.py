@@ -45,6 +45,8 @@ def _load():
     L.sv_verify_attn_workspace.argtypes = [ctypes.POINTER(_AttnShape)]
     L.sv_verify_attn_workspace.restype = _SZ
     L.sv_verify_attn.argtypes = [ctypes.POINTER(_AttnShape), _P, _P, _P, _P, _P, _P, _P, _F32, _P, _P, _SZ, _P]
+    L.sv_verify_attn_ex.argtypes = [ctypes.POINTER(_AttnShape), _P, _P, _P, _P, _P, _P, _P, _F32, _P, _P, _SZ,
+                                    ctypes.c_uint32, _P]
     L.sv_lm_head.argtypes = [_P, _P, _P, _I32, _I32, _I32, _P]
     L.sv_accept_greedy_workspace.argtypes = [_I32, _I32, _I32]
     L.sv_accept_greedy_workspace.restype = _SZ
@@ -59,8 +61,8 @@ def _load():
     L.sv_diag_exp.argtypes = [_P, _P, _I64, _P]
     L.sv_diag_philox.argtypes = [_P, _P, _P, _I64, _P]
     L.sv_diag_canon.argtypes = [_P, _I32, _I32, _P, _P, _P, _P]
-    for fn in ("sv_verify_attn", "sv_lm_head", "sv_accept_greedy", "sv_accept_sample", "sv_accept_sample_noalloc",
-               "sv_kv_commit",
+    for fn in ("sv_verify_attn", "sv_verify_attn_ex", "sv_lm_head", "sv_accept_greedy", "sv_accept_sample",
+               "sv_accept_sample_noalloc", "sv_kv_commit",
                "sv_diag_exp", "sv_diag_philox", "sv_diag_canon", "sv_get_device_error"):
         getattr(L, fn).restype = ctypes.c_int
     return L
@@ -114,10 +116,15 @@ def verify_attn_workspace(B, R, Hq, Hkv, D, T_cap) -> int:
     return int(lib.sv_verify_attn_workspace(ctypes.byref(s)))
 
 
+ATTN_CACHE_READY = 1
+
+
 def verify_attn(q, k_cache, v_cache, length, k_blk, v_blk, parent=None, scale=None, out=None, ws=None,
-                stream=None):
+                stream=None, cache_ready=False):
     """q [B,R,Hq,D]; caches [B,Hkv,T_cap,D]; blocks [B,Hkv,R,D] (bf16); length [B] int32;
-    parent None or [B,R] int32.  Returns out [B,R,Hq,D] bf16."""
+    parent None or [B,R] int32.  Returns out [B,R,Hq,D] bf16.  cache_ready: the
+    kernel enqueued just before this call writes neither `length` nor the caches
+    (sv_verify_attn_ex, SV_ATTN_CACHE_READY)."""
     s = attn_shape(q, k_cache)
     if scale is None:
         scale = q.shape[-1] ** -0.5
@@ -128,11 +135,11 @@ def verify_attn(q, k_cache, v_cache, length, k_blk, v_blk, parent=None, scale=No
         ws = torch.zeros(nbytes, dtype=torch.uint8, device=q.device)   # ticket words start at zero
     ws = _ws(nbytes, q.device, ws)
     bf = torch.bfloat16
-    _check("sv_verify_attn", lib.sv_verify_attn(
+    _check("sv_verify_attn_ex", lib.sv_verify_attn_ex(
         ctypes.byref(s), _ptr(q, bf, "q"), _ptr(k_cache, bf, "k_cache"), _ptr(v_cache, bf, "v_cache"),
         _ptr(length, torch.int32, "len"), _ptr(k_blk, bf, "k_blk"), _ptr(v_blk, bf, "v_blk"),
         _ptr(parent, torch.int32, "parent"), float(scale), _ptr(out, bf, "out"), _ptr(ws), nbytes,
-        _stream(stream)))
+        ATTN_CACHE_READY if cache_ready else 0, _stream(stream)))
     return out
 
 

@@ -143,6 +143,15 @@ sv_status sv_verify_attn(const sv_attn_shape* shape, const uint16_t* q, const ui
                          const uint16_t* v_cache, const int32_t* len, const uint16_t* k_blk, const uint16_t* v_blk,
                          const int32_t* parent, float scale, uint16_t* out, void* ws, size_t ws_bytes,
                          void* stream) {
+    return sv_verify_attn_ex(shape, q, k_cache, v_cache, len, k_blk, v_blk, parent, scale, out, ws, ws_bytes, 0u,
+                             stream);
+}
+
+sv_status sv_verify_attn_ex(const sv_attn_shape* shape, const uint16_t* q, const uint16_t* k_cache,
+                            const uint16_t* v_cache, const int32_t* len, const uint16_t* k_blk,
+                            const uint16_t* v_blk, const int32_t* parent, float scale, uint16_t* out, void* ws,
+                            size_t ws_bytes, uint32_t flags, void* stream) {
+    if (flags & ~SV_ATTN_CACHE_READY) return SV_ERR_ARG;
     const sv_status st = check_attn_shape(shape);
     if (st != SV_OK) return st;
     if (!q || !k_cache || !v_cache || !len || !k_blk || !v_blk || !out) return SV_ERR_ARG;
@@ -153,7 +162,7 @@ sv_status sv_verify_attn(const sv_attn_shape* shape, const uint16_t* q, const ui
     if (!(scale > 0.0f)) return SV_ERR_ARG;
     if (ws_bytes < sv::attn_workspace(*shape)) return SV_ERR_WORKSPACE;
     return launch_status(sv::launch_verify_attn(*shape, q, k_cache, v_cache, len, k_blk, v_blk, parent, scale, out,
-                                                ws, as_stream(stream)));
+                                                ws, (flags & SV_ATTN_CACHE_READY) != 0, as_stream(stream)));
 }
 
 sv_status sv_lm_head(const uint16_t* hid, const uint16_t* W, float* logits, int32_t N, int32_t H, int32_t V,

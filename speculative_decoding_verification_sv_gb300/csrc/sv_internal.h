@@ -78,7 +78,7 @@ size_t attn_workspace(const sv_attn_shape& s);
 cudaError_t launch_verify_attn(const sv_attn_shape& s, const uint16_t* q, const uint16_t* k_cache,
                                const uint16_t* v_cache, const int32_t* len, const uint16_t* k_blk,
                                const uint16_t* v_blk, const int32_t* parent, float scale, uint16_t* out,
-                               void* ws, cudaStream_t st);
+                               void* ws, bool cache_ready, cudaStream_t st);
 
 // TMA descriptor encoding (driver entry point fetched through the runtime).
 bool encode_tmap_2d_bf16(void* tmap, const void* base, uint64_t inner, uint64_t outer, uint64_t row_stride_bytes,

@@ -130,6 +130,7 @@ struct AttnArgs {
     int clusters;            // clusters per (b, g, row tile); their partials meet in ws_part
     int part_rows;           // rows of a partial record block: min(rows, kRows)
     float scale_log2;
+    int cache_ready;         // len and the cache are final before the preceding kernel runs
 };
 
 // TMEM lane that holds row gr of (b, g): full tiles lane = gr - 128 * rt;
@@ -201,11 +202,18 @@ __global__ void __launch_bounds__(Roles<kHalf>::kThreads, 1)
     const uint32_t tO = tmem + Ly::kColO;
     auto tP = [tmem](int i) { return tmem + Ly::kColP + static_cast<uint32_t>(i) * Ly::kPCols; };
 
-    // inputs may come from the kernels before this one
-    pdl_wait();
-    pdl_launch_dependents();
-
-    int t = a.len[b];
+    // Inputs may come from the kernel before this one: every thread waits for
+    // it before touching them (and before letting the next kernel start).  With
+    // cache_ready the length and the committed cache rows were final before that
+    // kernel started, so they are read first, and the producer issues its
+    // context loads before waiting.
+    const bool early = a.cache_ready != 0;
+    int t = early ? a.len[b] : 0;
+    if (!early || warp != kTmaWarp) {
+        pdl_wait();
+        pdl_launch_dependents();
+    }
+    if (!early) t = a.len[b];
     if (t < 0 || t > a.T_cap) {
         if (threadIdx.x == 0 && rank == 0 && rt == 0) raise_error(a.err, SV_DEVERR_LENGTH);
         t = t < 0 ? 0 : a.T_cap;
@@ -225,24 +233,38 @@ __global__ void __launch_bounds__(Roles<kHalf>::kThreads, 1)
 
     if (warp == kTmaWarp) {
         // ---------------- TMA producer ----------------
-        if (lane == 0) {
-            for (int i = 0; i < nsteps; ++i) {
-                const int s = i % kStages;
-                mbar_wait(&kv_empty[s], ((i / kStages) & 1) ^ 1, a.err);
-                const int t0 = first + i * kT, nt = min(kT, last - t0);
-                uint8_t* st = smem + Ly::kOffRing + s * kStageBytes;
-                mbar_arrive_expect_tx(&kv_full[s], static_cast<uint32_t>(nt * kTileBytes));
-                for (int h = 0; h < nt; ++h) {
-                    const int gt = t0 + h;
-                    const void* tk = gt < n_ctx ? static_cast<const void*>(&tmK) : static_cast<const void*>(&tmKb);
-                    const void* tv = gt < n_ctx ? static_cast<const void*>(&tmV) : static_cast<const void*>(&tmVb);
-                    const int y = gt < n_ctx ? hg * a.T_cap + gt * kNk : hg * a.R + (gt - n_ctx) * kNk;
-                    tma_load_2d(st + h * kHalfBytes, tk, 0, y, &kv_full[s]);
-                    tma_load_2d(st + kRegion + h * kHalfBytes, tk, 64, y, &kv_full[s]);
-                    tma_load_2d(st + 2 * kRegion + h * kHalfBytes, tv, 0, y, &kv_full[s]);
-                    tma_load_2d(st + 3 * kRegion + h * kHalfBytes, tv, 64, y, &kv_full[s]);
-                }
+        auto load_step = [&](int i) {
+            const int s = i % kStages;
+            mbar_wait(&kv_empty[s], ((i / kStages) & 1) ^ 1, a.err);
+            const int t0 = first + i * kT, nt = min(kT, last - t0);
+            uint8_t* st = smem + Ly::kOffRing + s * kStageBytes;
+            mbar_arrive_expect_tx(&kv_full[s], static_cast<uint32_t>(nt * kTileBytes));
+            for (int h = 0; h < nt; ++h) {
+                const int gt = t0 + h;
+                const void* tk = gt < n_ctx ? static_cast<const void*>(&tmK) : static_cast<const void*>(&tmKb);
+                const void* tv = gt < n_ctx ? static_cast<const void*>(&tmV) : static_cast<const void*>(&tmVb);
+                const int y = gt < n_ctx ? hg * a.T_cap + gt * kNk : hg * a.R + (gt - n_ctx) * kNk;
+                tma_load_2d(st + h * kHalfBytes, tk, 0, y, &kv_full[s]);
+                tma_load_2d(st + kRegion + h * kHalfBytes, tk, 64, y, &kv_full[s]);
+                tma_load_2d(st + 2 * kRegion + h * kHalfBytes, tv, 0, y, &kv_full[s]);
+                tma_load_2d(st + 3 * kRegion + h * kHalfBytes, tv, 64, y, &kv_full[s]);
             }
+        };
+        if (lane == 0) {
+            int i = 0;
+            if (early) {
+                // the first ring pass of context-only steps, while the preceding
+                // kernel drains (committed rows: no kernel writes them now)
+                for (; i < nsteps && i < kStages && min(first + (i + 1) * kT, last) <= n_ctx; ++i) load_step(i);
+            }
+            if (early) {
+                pdl_wait();
+                pdl_launch_dependents();
+            }
+            for (; i < nsteps; ++i) load_step(i);
+        } else if (early) {
+            pdl_wait();
+            pdl_launch_dependents();
         }
     } else if (warp == kMmaWarp) {
         // ---------------- MMA issuer ----------------
@@ -399,7 +421,7 @@ __global__ void __launch_bounds__(Roles<kHalf>::kThreads, 1)
             float mpart = -INFINITY;
             if (work) {
 #pragma unroll
-                for (int e = 0; e < kCols; ++e) sc[e] = __uint_as_float(rs[e]) * a.scale_log2;
+                for (int e = 0; e < kCols; ++e) sc[e] = __uint_as_float(rs[e]);   // raw q.k; scaled in the exponent
                 if (is_block || kb + kCols > t || !tile_live) {
                     // branch-free mask: key kb + e is visible iff e < lim (context:
                     // kl < t; chain block: kl <= j and kl < R; no tile: none) or,
@@ -420,7 +442,7 @@ __global__ void __launch_bounds__(Roles<kHalf>::kThreads, 1)
                 for (int w2 = kCols / 4; w2 >= 1; w2 >>= 1)
 #pragma unroll
                     for (int e = 0; e < w2; ++e) mx[e] = fmaxf(mx[e], mx[e + w2]);
-                mpart = mx[0];
+                mpart = mx[0] * a.scale_log2;   // the scale is positive: max commutes with it
             }
             float mt;
             if constexpr (kHalf) {
@@ -438,17 +460,21 @@ __global__ void __launch_bounds__(Roles<kHalf>::kThreads, 1)
                 m_new = mt;
                 corr = m_ref == -INFINITY ? 0.f : fast_exp2(m_ref - m_new);
             }
-            // P (bf16) and this thread's share of its sum
+            // P (bf16, rounded to nearest even) and this thread's share of the
+            // row sum (of the fp32 values).  exp2(scale * s - m) is one FMA and
+            // one ex2; a row with no visible key yet (m = -inf) has every score
+            // -inf, and exp2(-inf - 0) = 0.
             uint32_t pk[kCols / 2];
             float ps0 = 0.f, ps1 = 0.f;
             if (work) {
+                const float nm = m_new == -INFINITY ? 0.f : -m_new;
 #pragma unroll
                 for (int e = 0; e < kCols; e += 2) {
-                    const float p0 = (m_new == -INFINITY) ? 0.f : fast_exp2(sc[e] - m_new);
-                    const float p1 = (m_new == -INFINITY) ? 0.f : fast_exp2(sc[e + 1] - m_new);
+                    const float p0 = fast_exp2(fmaf(sc[e], a.scale_log2, nm));
+                    const float p1 = fast_exp2(fmaf(sc[e + 1], a.scale_log2, nm));
+                    ps0 += p0;
+                    ps1 += p1;
                     const __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
-                    ps0 += __bfloat162float(pb.x);
-                    ps1 += __bfloat162float(pb.y);
                     pk[e / 2] = *reinterpret_cast<const uint32_t*>(&pb);
                 }
             }
@@ -499,6 +525,22 @@ __global__ void __launch_bounds__(Roles<kHalf>::kThreads, 1)
                     tmem_st8(tP(sb) + lane_off + col0 / 2, pk);
                 }
                 tmem_st_wait();
+            }
+            {
+                // V rows of cache positions >= t in the last, partial context
+                // tile: P is 0 there, but 0 * a non-finite cache entry is NaN in
+                // P V, so they are zeroed before the P V of this step
+                const int tl = n_ctx - 1 - first - st * kT;   // that tile within this step
+                if ((t & (kNk - 1)) != 0 && tl >= 0 && tl < kT && tl < ntiles - st * kT) {
+                    uint8_t* vt = smem + Ly::kOffRing + (st % kStages) * kStageBytes + 2 * kRegion + tl * kHalfBytes;
+                    const int r0 = t & (kNk - 1);
+                    for (int x = threadIdx.x; x < (kNk - r0) * 16; x += 32 * kSoftWarps) {
+                        const int row = r0 + (x >> 4), c = x & 15;   // a whole 128-byte row of each half
+                        *reinterpret_cast<uint4*>(vt + (c >> 3) * kRegion + row * 128 + (c & 7) * 16) =
+                            make_uint4(0u, 0u, 0u, 0u);
+                    }
+                    fence_proxy_async_smem();
+                }
             }
             tc_fence_before();
             __syncwarp();
@@ -874,7 +916,7 @@ size_t attn_workspace(const sv_attn_shape& s) {
 cudaError_t launch_verify_attn(const sv_attn_shape& s, const uint16_t* q, const uint16_t* k_cache,
                                const uint16_t* v_cache, const int32_t* len, const uint16_t* k_blk,
                                const uint16_t* v_blk, const int32_t* parent, float scale, uint16_t* out,
-                               void* ws, cudaStream_t st) {
+                               void* ws, bool cache_ready, cudaStream_t st) {
     const AttnPlan p = attn_plan(s);
     if (p.clusters > 1 && ws == nullptr) return cudaErrorInvalidValue;
     alignas(64) uint8_t tK[128], tV[128], tKb[128], tVb[128];
@@ -905,6 +947,7 @@ cudaError_t launch_verify_attn(const sv_attn_shape& s, const uint16_t* q, const 
     a.clusters = p.clusters;
     a.part_rows = p.rows < kRows ? p.rows : kRows;
     a.scale_log2 = scale * 1.4426950408889634f;
+    a.cache_ready = cache_ready ? 1 : 0;
     if (parent != nullptr)
         return p.half ? launch_mode<true, true>(p, s, tK, tV, tKb, tVb, a, st)
                       : launch_mode<false, true>(p, s, tK, tV, tKb, tVb, a, st);

@@ -71,6 +71,12 @@ def test_host_validation_rejects_before_launch(lib):
                             None, need, None) == 1
     assert L.sv_verify_attn(ctypes.byref(s), fake, fake, fake, fake, fake, fake, None, ctypes.c_float(0.1), fake,
                             fake, need - 16, None) == 4
+    # launch flags: only SV_ATTN_CACHE_READY (1) is defined
+    s = b._AttnShape(1, 5, 12, 2, 128, 4224)
+    assert L.sv_verify_attn_ex(ctypes.byref(s), fake, fake, fake, fake, fake, fake, None, ctypes.c_float(0.1), fake,
+                               None, 0, 2, None) == 1
+    assert L.sv_verify_attn_ex(ctypes.byref(s), None, fake, fake, fake, fake, fake, None, ctypes.c_float(0.1), fake,
+                               None, 0, 1, None) == 1
     # short workspace
     assert L.sv_accept_greedy(fake, fake, None, 1, 5, 151936, fake, fake, fake, fake, 8, None) == 4
     # temperature must be positive; vocab must be a multiple of 4

@@ -50,6 +50,64 @@ def test_attn_chain(sv, B, R, Hq, Hkv, T_cap, lengths):
     assert sv.get_device_error() == 0
 
 
+@pytest.mark.parametrize("R,Hq,Hkv,lengths,tree", [
+    (5, 12, 2, [2048 + 37, 100, 1], False),     # half tiles, partial last tiles
+    (17, 16, 2, [600, 65], False),              # full tiles
+    (65, 28, 4, [513, 300], True),              # tree, full tiles, two block tiles
+])
+def test_attn_cache_rows_past_len_ignored(sv, R, Hq, Hkv, lengths, tree):
+    """Cache positions >= len hold NaN (K) and +inf (V) bit patterns: the
+    output must not see them (P is 0 there, and 0 * inf must not reach O)."""
+    B, D, T_cap = len(lengths), 128, 2304
+    g = torch.Generator().manual_seed(404 + R)
+    mk = lambda *s: torch.randn(*s, generator=g).to(torch.bfloat16)
+    q, kc, vc, kb, vb = mk(B, R, Hq, D), mk(B, Hkv, T_cap, D), mk(B, Hkv, T_cap, D), mk(B, Hkv, R, D), mk(B, Hkv, R, D)
+    kcb, vcb = kc.view(torch.int16), vc.view(torch.int16)
+    for bi, t in enumerate(lengths):
+        kcb[bi, :, t:] = 0x7FC0        # NaN
+        vcb[bi, :, t:] = 0x7F80        # +inf
+    ln = torch.tensor(lengths, dtype=torch.int32)
+    par = None
+    if tree:
+        par = np.tile(synth.random_tree(R - 1, 8, 3, 5), (B, 1)).astype(np.int32)
+    out = sv.verify_attn(q.cuda(), kc.cuda(), vc.cuda(), ln.cuda(), kb.cuda(), vb.cuda(),
+                         None if par is None else torch.from_numpy(par).cuda())
+    got = out.float().cpu().numpy()
+    ref = oracle.verify_attn(bits(q), bits(kc), bits(vc), ln.numpy(), bits(kb), bits(vb), par)
+    assert np.isfinite(got).all()
+    ok, err, bound = within_tol(got, ref)
+    assert ok, (err, bound)
+    assert sv.get_device_error() == 0
+
+
+@pytest.mark.parametrize("B,R,Hq,Hkv,T_cap,t", [(1, 5, 12, 2, 4160, 4096), (16, 9, 28, 4, 1152, 1000),
+                                                 (2, 65, 28, 4, 704, 600)])
+def test_attn_cache_ready_same_result(sv, B, R, Hq, Hkv, T_cap, t):
+    """Layers of one round back to back on a stream, the later ones launched
+    with SV_ATTN_CACHE_READY (length and cache read before the preceding
+    kernel completes): every layer's output equals the flag-free launch,
+    bit for bit."""
+    D, L = 128, 4
+    g = torch.Generator().manual_seed(B * 7 + R)
+    mk = lambda *s: torch.randn(*s, generator=g).to(torch.bfloat16).cuda()
+    q, kc, vc = mk(L, B, R, Hq, D), mk(L, B, Hkv, T_cap, D), mk(L, B, Hkv, T_cap, D)
+    kb, vb = mk(L, B, Hkv, R, D), mk(L, B, Hkv, R, D)
+    ln = torch.full((B,), t, dtype=torch.int32).cuda()
+    par = None
+    if R > 9:
+        par = torch.from_numpy(np.tile(synth.random_tree(R - 1, 8, 3, 1), (B, 1)).astype(np.int32)).cuda()
+    ws = torch.zeros(max(sv.verify_attn_workspace(B, R, Hq, Hkv, D, T_cap), 16), dtype=torch.uint8, device="cuda")
+    ref = [sv.verify_attn(q[l], kc[l], vc[l], ln, kb[l], vb[l], par, ws=ws) for l in range(L)]
+    torch.cuda.synchronize()
+    out = torch.empty(L, B, R, Hq, D, dtype=torch.bfloat16, device="cuda")
+    for l in range(L):
+        sv.verify_attn(q[l], kc[l], vc[l], ln, kb[l], vb[l], par, out=out[l], ws=ws, cache_ready=l > 0)
+    torch.cuda.synchronize()
+    for l in range(L):
+        assert torch.equal(out[l], ref[l]), l
+    assert sv.get_device_error() == 0
+
+
 def test_attn_custom_scale(sv):
     got, ref = _run(sv, 2, 5, 12, 2, 400, [300, 211], seed=3, scale=0.21)
     ok, err, bound = within_tol(got, ref)
