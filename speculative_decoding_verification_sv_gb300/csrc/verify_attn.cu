@@ -195,6 +195,9 @@ __global__ void __launch_bounds__(Roles<kHalf>::kThreads, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    // this CTA has started (and initialised its barriers): waited for by every
+    // thread before the first store into another CTA's shared memory
+    cluster_arrive_relaxed();
     const uint32_t tmem = *tmem_s;
     // TMEM addresses of score buffer / P buffer `i` (arithmetic, not arrays: a
     // runtime-indexed array would live in local memory)
@@ -230,6 +233,37 @@ __global__ void __launch_bounds__(Roles<kHalf>::kThreads, 1)
     const int nsteps = (ntiles + kT - 1) / kT;
     const bool has_block = last > n_ctx;
     const bool tree = kTree && has_block;
+    const int nrows = min(kRows, a.rows - rt * kRows);
+
+    // Receive plan of the cluster merge (computed by each warp, lane r for CTA
+    // r of the cluster).  A CTA whose steps never reach the last `need` ring
+    // stages is "light": those stages can take pushed partial records from the
+    // start.  When the light CTAs can hold every row, they own the rows and each
+    // CTA pushes as soon as its own loop ends; otherwise (need = 0) every CTA
+    // owns rows prow % C, received at the front of the ring once all CTAs of
+    // the cluster have drained theirs.
+    auto merge_plan = [&](int& need_o, uint32_t& light_o) {
+        int st_r = 1 << 30;
+        if (lane < C) {
+            const int64_t sr = split - rank + lane;
+            const int f = static_cast<int>((static_cast<int64_t>(n_all) * sr) / nsplit);
+            const int l = static_cast<int>((static_cast<int64_t>(n_all) * (sr + 1)) / nsplit);
+            st_r = (l - f + kT - 1) / kT;
+        }
+        need_o = 0;
+        light_o = 0u;
+        for (int nd = 1; nd < kStages; ++nd) {
+            const uint32_t m = __ballot_sync(0xffffffffu, st_r <= kStages - nd);
+            const int nl = __popc(m);
+            if (nl > 0 && ((nrows + nl - 1) / nl) * C * kRec * 4 <= nd * kStageBytes) {
+                need_o = nd;
+                light_o = m;
+                break;
+            }
+        }
+    };
+    int need = 0;
+    uint32_t light = 0u;
 
     if (warp == kTmaWarp) {
         // ---------------- TMA producer ----------------
@@ -266,8 +300,11 @@ __global__ void __launch_bounds__(Roles<kHalf>::kThreads, 1)
             pdl_wait();
             pdl_launch_dependents();
         }
+        __syncwarp();
+        merge_plan(need, light);
     } else if (warp == kMmaWarp) {
         // ---------------- MMA issuer ----------------
+        merge_plan(need, light);   // while the Q tile is still on its way
         if (lane == 0 && ntiles > 0) {
             // S = Q K^T over the step's tiles (N = 64 per tile), O += P V
             constexpr uint32_t idesc_s = idesc_bf16_f32(kM, kStepKeys, false, false);
@@ -357,6 +394,7 @@ __global__ void __launch_bounds__(Roles<kHalf>::kThreads, 1)
                     *reinterpret_cast<uint4*>(dst) = v;
                 }
             }
+            merge_plan(need, light);   // while the Q copies are in flight
             cp_async_wait_all();
         }
         fence_proxy_async_smem();
@@ -581,12 +619,26 @@ __global__ void __launch_bounds__(Roles<kHalf>::kThreads, 1)
         }
         tc_fence_before();
         __syncwarp();
-        cluster_sync_warp();   // (1) every CTA of the cluster has drained its ring
+        cluster_wait();                      // every CTA of the cluster has started
+        if (need == 0) cluster_sync_warp();  // (1) and has drained its ring
         // push the partial record of row prow into slot `rank` of the row's
-        // owner, CTA prow % C: slots [(prow / C) * C + src] in its ring area
+        // owner: slots [(prow / n_owners) * C + src] of its receive area
         if (valid) {
             const int prow = gr - rt * kRows;          // < kRows for every real row
-            float* rec = cluster.map_shared_rank(part + ((prow / C) * C + rank) * kRec, prow % C);
+            int owner, li;
+            if (need > 0) {
+                const int nl = __popc(light);
+                uint32_t m = light;
+                for (int k = prow % nl; k > 0; --k) m &= m - 1u;   // the (prow % nl)-th light CTA
+                owner = __ffs(m) - 1;
+                li = prow / nl;
+            } else {
+                owner = prow % C;
+                li = prow / C;
+            }
+            float* recv = need > 0 ? reinterpret_cast<float*>(smem + Ly::kOffRing + (kStages - need) * kStageBytes)
+                                   : part;
+            float* rec = cluster.map_shared_rank(recv + (li * C + rank) * kRec, owner);
             if (cgp == 0 && sub == 0)
                 *reinterpret_cast<float2*>(rec) = make_float2(use ? m_ref : -INFINITY, use ? lt : 0.f);
 #pragma unroll
@@ -594,9 +646,10 @@ __global__ void __launch_bounds__(Roles<kHalf>::kThreads, 1)
                 *reinterpret_cast<uint4*>(rec + 4 + ocol0 + e) = make_uint4(ov[e], ov[e + 1], ov[e + 2], ov[e + 3]);
         }
     }
-    if (warp >= kSoftWarps) {   // (1), producer and MMA warps, once their lane 0 is done
+    if (warp >= kSoftWarps) {   // producer and MMA warps, once their lane 0 is done
         __syncwarp();
-        cluster_sync_warp();
+        cluster_wait();
+        if (need == 0) cluster_sync_warp();   // (1)
     }
     __syncwarp();
     cluster_sync_warp();   // (2) every record pushed and visible to its owner
@@ -605,7 +658,6 @@ __global__ void __launch_bounds__(Roles<kHalf>::kThreads, 1)
     // warps) from the records pushed to it; with one cluster per (b, g, row
     // tile) it writes the bf16 rows, otherwise the cluster's merged partial
     // (max, sum, unnormalised O)
-    const int nrows = min(kRows, a.rows - rt * kRows);
     const int unit = hg * a.row_tiles + rt;
     const int ci = blockIdx.x / C;
     auto store_row = [&](int lr, float4 acc, float L) {
@@ -616,9 +668,15 @@ __global__ void __launch_bounds__(Roles<kHalf>::kThreads, 1)
         *reinterpret_cast<uint2*>(dst) =
             make_uint2(pack_bf16x2(acc.x * inv, acc.y * inv), pack_bf16x2(acc.z * inv, acc.w * inv));
     };
-    for (int li = warp; rank + C * li < nrows; li += kThreads / 32) {
-        const int lr = rank + C * li;
-        const float* slots = part + li * C * kRec;
+    // the rows this CTA owns: k0, k0 + n_owners, ...
+    const bool owns = need == 0 || ((light >> rank) & 1u) != 0u;
+    const int k0 = need > 0 ? __popc(light & ((1u << rank) - 1u)) : rank;
+    const int n_owners = need > 0 ? __popc(light) : C;
+    const float* recv = need > 0 ? reinterpret_cast<const float*>(smem + Ly::kOffRing + (kStages - need) * kStageBytes)
+                                 : part;
+    for (int li = warp; owns && k0 + n_owners * li < nrows; li += kThreads / 32) {
+        const int lr = k0 + n_owners * li;
+        const float* slots = recv + li * C * kRec;
         float ms = -INFINITY, ls = 0.f;
         if (lane < C) {
             const float2 ml = *reinterpret_cast<const float2*>(slots + lane * kRec);
