@@ -48,16 +48,16 @@ FALLBACK_HBM_GBS = 6800.0
 # was taken on; a different hash (the kernel changed) reports null.
 TRAFFIC = {
     # ncu --set full, 28-layer 1.5B round, LM head N=5 H=1536 V=151936
-    ("1", "lm_head"): {"bytes": 466805504 + 5640192, "src": "lm_head.cu", "src_hash": "28b4a698ab2e95cb"},
+    ("1", "lm_head"): {"bytes": 466803200 + 5557504, "src": "lm_head.cu", "src_hash": "43daf2fa01b4f0d6"},
     # ncu --set full, 7B batch-16 layer (2-layer case, same per-layer launch)
-    ("3b16", "verify_attn"): {"bytes": 269838848 + 3434752, "src": "verify_attn.cu",
-                              "src_hash": "7870179c0d3ca0ad"},
-    ("3b16s", "verify_attn"): {"bytes": 269838848 + 3434752, "src": "verify_attn.cu",
-                               "src_hash": "7870179c0d3ca0ad"},
+    ("3b16", "verify_attn"): {"bytes": 269846272 + 3296768, "src": "verify_attn.cu",
+                              "src_hash": "0aedacb62922d9fc"},
+    ("3b16s", "verify_attn"): {"bytes": 269846272 + 3296768, "src": "verify_attn.cu",
+                               "src_hash": "0aedacb62922d9fc"},
     # ncu --set full, sampled B64 k8: statistics pass + chain residual pass (the
     # walk and draw launches move < 0.1 MB and were not captured)
-    ("2", "accept_sampled"): {"bytes": 395190272 + 3251968 + 77821440 + 1253888, "src": "accept.cu",
-                              "src_hash": "16ddb18f999764cd"},
+    ("2", "accept_sampled"): {"bytes": 389491200 + 3341568 + 77821696 + 1400320, "src": "accept.cu",
+                              "src_hash": "3e022b7bfe29e81f"},
 }
 
 
