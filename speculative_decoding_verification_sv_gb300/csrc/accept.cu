@@ -933,7 +933,7 @@ __global__ void diag_exp_kernel(const float* x, float* y, int64_t n) {
         // the branch-free form used by the softmax passes must agree bit for
         // bit wherever it is defined; a disagreement shows up as 12345
         const float e = sv_exp(x[i]);
-        const bool defined = !(x[i] != x[i]) && x[i] <= 88.0f;
+        const bool defined = !(x[i] != x[i]) && x[i] <= 0.0f;
         y[i] = (defined && __float_as_uint(sv_exp_nb(x[i])) != __float_as_uint(e)) ? 12345.0f : e;
     }
 }

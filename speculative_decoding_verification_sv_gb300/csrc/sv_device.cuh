@@ -440,10 +440,12 @@ __device__ __forceinline__ float sv_exp(float x) {
 }
 
 // sv_exp without branches, for the softmax terms exp(z - M) (argument <= 0):
-// the same operations on max(x, -104), with the underflow and subnormal cases
-// selected afterwards, so several evaluations can interleave.  Bit-identical
-// to sv_exp for every x that is not NaN and not above 88 (the NaN and
-// overflow returns are the only cases it leaves out).
+// the same operations on max(x, -104), the underflow case selected afterwards,
+// so several evaluations can interleave.  The scaling by 2^k is always done as
+// 2^(k+64) (exact: the product is normal) and then 2^-64, whose single rounding
+// is the one sv_exp's subnormal branch performs, and which is exact whenever
+// the result is normal.  Bit-identical to sv_exp for every x <= 0 that is not
+// NaN (for x above ~44, 2^(k+64) would overflow).
 __device__ __forceinline__ float sv_exp_nb(float x) {
     const float kInvLn2 = 1.44269504088896340736f;
     const float kLn2Head = 0.693145751953125f;
@@ -463,9 +465,7 @@ __device__ __forceinline__ float sv_exp_nb(float x) {
     s = __fmaf_rn(s, r, 1.0f);
     s = __fmaf_rn(s, r, 1.0f);
     const int k = __float_as_int(t) - __float_as_int(kRound);
-    const bool normal = k >= -126;
-    float y = __fmul_rn(s, __int_as_float((normal ? k + 127 : k + 64 + 127) << 23));
-    y = normal ? y : __fmul_rn(y, __int_as_float((127 - 64) << 23));
+    const float y = __fmul_rn(__fmul_rn(s, __int_as_float((k + 64 + 127) << 23)), __int_as_float((127 - 64) << 23));
     return x < -104.0f ? 0.0f : y;
 }
 
