@@ -351,7 +351,9 @@ __global__ void __launch_bounds__(kRowThreads, kRowCtasPerSm) sample_stats_row_k
 
     // pass 1: max, eight loads in flight per thread
     float m = -INFINITY;
-    float nf = 0.0f;   // stays 0 unless some z is NaN or infinite (z * 0 is then NaN)
+    // stay 0 unless some z is NaN or infinite (z * 0 is then NaN); one
+    // accumulator per component keeps the dependency chains short
+    float4 nf = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int i0 = tid; i0 < nvec; i0 += 8 * kRowThreads) {
         float4 x[8];
 #pragma unroll
@@ -365,11 +367,14 @@ __global__ void __launch_bounds__(kRowThreads, kRowCtasPerSm) sample_stats_row_k
             if (i0 + u * kRowThreads >= nvec) continue;
             float4 z = x[u];
             if (T != 1.0f) z = make_float4(__fdiv_rn(z.x, T), __fdiv_rn(z.y, T), __fdiv_rn(z.z, T), __fdiv_rn(z.w, T));
-            nf = __fmaf_rn(z.x, 0.0f, __fmaf_rn(z.y, 0.0f, __fmaf_rn(z.z, 0.0f, __fmaf_rn(z.w, 0.0f, nf))));
-            m = fmaxf(fmaxf(m, fmaxf(z.x, z.y)), fmaxf(z.z, z.w));
+            nf.x = __fmaf_rn(z.x, 0.0f, nf.x);
+            nf.y = __fmaf_rn(z.y, 0.0f, nf.y);
+            nf.z = __fmaf_rn(z.z, 0.0f, nf.z);
+            nf.w = __fmaf_rn(z.w, 0.0f, nf.w);
+            m = fmax3(m, fmax3(z.x, z.y, z.z), z.w);
         }
     }
-    if (nf != 0.0f) raise_error(err, SV_DEVERR_NONFINITE);
+    if (__fadd_rn(__fadd_rn(nf.x, nf.y), __fadd_rn(nf.z, nf.w)) != 0.0f) raise_error(err, SV_DEVERR_NONFINITE);
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
     if (lane == 0) wred[warp] = m;

@@ -150,6 +150,13 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const void* tmap, int32_t
         : "memory");
 }
 
+// max(a, b, c) in one instruction (a NaN operand is ignored, as by fmaxf)
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
 __device__ __forceinline__ void prefetch_tmap(const void* tmap) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
 }
@@ -440,8 +447,9 @@ __device__ __forceinline__ float sv_exp(float x) {
 }
 
 // sv_exp without branches, for the softmax terms exp(z - M) (argument <= 0):
-// the same operations on max(x, -104), the underflow case selected afterwards,
-// so several evaluations can interleave.  The scaling by 2^k is always done as
+// the same operations on max(x, -104), so several evaluations can interleave;
+// below -104 the clamped evaluation is exp(-104) ~ 6.8e-46, which rounds to 0
+// like sv_exp's underflow return.  The scaling by 2^k is always done as
 // 2^(k+64) (exact: the product is normal) and then 2^-64, whose single rounding
 // is the one sv_exp's subnormal branch performs, and which is exact whenever
 // the result is normal.  Bit-identical to sv_exp for every x <= 0 that is not
@@ -465,8 +473,7 @@ __device__ __forceinline__ float sv_exp_nb(float x) {
     s = __fmaf_rn(s, r, 1.0f);
     s = __fmaf_rn(s, r, 1.0f);
     const int k = __float_as_int(t) - __float_as_int(kRound);
-    const float y = __fmul_rn(__fmul_rn(s, __int_as_float((k + 64 + 127) << 23)), __int_as_float((127 - 64) << 23));
-    return x < -104.0f ? 0.0f : y;
+    return __fmul_rn(__fmul_rn(s, __int_as_float((k + 64 + 127) << 23)), __int_as_float((127 - 64) << 23));
 }
 
 // --------------------------------------------------------------------------
