@@ -166,9 +166,11 @@ class Round:
             si = synth.sample_inputs(B, R - 1, V, wid=w.wid, device=device)
             self.logits = si.logits.reshape(B * R, V)
             self.q_draft, self.tok = si.q, si.tok
-        self.n_acc = torch.zeros(B, dtype=torch.int32, device=device)
-        self.out_tok = torch.zeros(B, dtype=torch.int32, device=device)
-        self.path = torch.zeros(B, R, dtype=torch.int32, device=device)
+        # the round's outputs in one buffer (one device-to-host copy per step)
+        self.out_buf = torch.zeros(B * (R + 2), dtype=torch.int32, device=device)
+        self.n_acc = self.out_buf[:B]
+        self.out_tok = self.out_buf[B:2 * B]
+        self.path = self.out_buf[2 * B:].view(B, R)
         if mode == "greedy":
             self.acc_ws = torch.empty(sv.lib.sv_accept_greedy_workspace(B, R, V), dtype=torch.uint8, device=device)
         else:
@@ -216,14 +218,32 @@ class Round:
             sv.kv_commit(self.kc, self.vc, self.kb, self.vb, self.path, self.n_acc, self.length)
         rec("commit1")
 
+    def pack_inputs(self):
+        """Moves the per-round inputs into one device buffer (16-byte aligned
+        views), so a caller sends them with one host-to-device copy."""
+        names = ["q", "kb", "vb", "hid", "tok"] if self.has_model else ["logits", "q_draft", "tok"]
+        ts = [getattr(self, n) for n in names]
+        offs, off = [], 0
+        for t in ts:
+            offs.append(off)
+            off += (t.numel() * t.element_size() + 255) // 256 * 256
+        self.in_buf = torch.empty(off, dtype=torch.uint8, device=self.dev)
+        for n, t, o in zip(names, ts, offs):
+            nb = t.numel() * t.element_size()
+            v = self.in_buf[o:o + nb].view(t.dtype).view(t.shape)
+            v.copy_(t)
+            setattr(self, n, v)
+        torch.cuda.synchronize()
+
     def step_inputs(self):
-        """The per-round inputs a caller would send from the host."""
-        if self.has_model:
-            return [self.q, self.kb, self.vb, self.hid, self.tok]
-        return [self.logits, self.q_draft, self.tok]
+        """The per-round inputs a caller sends from the host (one buffer after
+        pack_inputs: Q, block K/V, hidden rows and draft tokens, or for the
+        acceptance-only workload the logits, q and draft tokens)."""
+        return [self.in_buf]
 
     def step_outputs(self):
-        return [self.n_acc, self.out_tok, self.path]
+        """n_acc, out_tok and path, in one buffer."""
+        return [self.out_buf]
 
 
 # ----------------------------------------------------------------------------
@@ -494,6 +514,7 @@ def main():
         from dataclasses import replace
         w = replace(w, L=args.layers, name=w.name.replace("28-layer", f"{args.layers}-layer"))
     rnd = Round(w, mode, dev)
+    rnd.pack_inputs()
 
     K = args.steps
     chunk = max(d for d in range(1, min(100, K) + 1) if K % d == 0)
@@ -600,24 +621,46 @@ def main():
     d2h = sum(t.numel() * t.element_size() for t in outs)
     E = args.e2e_steps
     done = torch.cuda.Event()
+    # the copy in, the round and the copy out as one CUDA graph (how a serving
+    # loop would issue them); if this torch cannot capture host copies, the
+    # three are issued one by one
+    gX = None
+    try:
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for d, h in zip(ins, h_in):
+                d.copy_(h, non_blocking=True)
+            rnd.step()
+            for h, d in zip(h_out, outs):
+                h.copy_(d, non_blocking=True)
+        gX = g
+    except Exception:
+        torch.cuda.synchronize()
     for phase in ("warm", "timed"):
         n = 5 if phase == "warm" else E
         barrier(ws)
         t0 = time.perf_counter()
         for _ in range(n):
             with torch.cuda.stream(stream):
-                for d, h in zip(ins, h_in):
-                    d.copy_(h, non_blocking=True)
-                g1.replay()
-                for h, d in zip(h_out, outs):
-                    h.copy_(d, non_blocking=True)
+                if gX is not None:
+                    gX.replay()
+                else:
+                    for d, h in zip(ins, h_in):
+                        d.copy_(h, non_blocking=True)
+                    g1.replay()
+                    for h, d in zip(h_out, outs):
+                        h.copy_(d, non_blocking=True)
                 done.record()
             done.synchronize()
         e2e_s = time.perf_counter() - t0
     e2e_s = max_over_ranks(e2e_s, ws, dev)
     e2e = {"value": ws * E / e2e_s, "unit": "steps/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-           "steps": E, "how": "pinned H2D of the round's inputs + CUDA-graph replay of the C-ABI calls + "
-                              "D2H of n_acc/out_tok/path + host sync, every step"}
+           "steps": E, "how": ("one CUDA graph per step: pinned H2D of the round's inputs (one buffer), the "
+                               "C-ABI calls, D2H of n_acc/out_tok/path (one buffer); host sync every step"
+                               if gX is not None else
+                               "pinned H2D of the round's inputs + CUDA-graph replay of the C-ABI calls + "
+                               "D2H of n_acc/out_tok/path + host sync, every step")}
 
     # greedy decisions too close to call within the logits tolerance: rows whose
     # top-1 / top-2 margin is below 1e-2 max|logit| (counted, not failed)
