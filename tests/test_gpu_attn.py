@@ -124,6 +124,20 @@ def test_attn_tree_65_nodes(sv, seed):
     assert ok, (err, bound)
 
 
+@pytest.mark.parametrize("seed", [3, 4])
+def test_attn_tree_small_unit(sv, seed):
+    """A 9-node tree with 3 query heads per KV head: 27 query rows per
+    (sequence, KV head), the half-tile layout under a tree mask, with an
+    empty-ish context (t = 1) in the batch."""
+    par = synth.random_tree(8, 4, 3, seed)
+    B = 3
+    parent = np.tile(par, (B, 1))
+    got, ref = _run(sv, B, 9, 12, 4, 600, [513, 1, 300], parent=parent, seed=seed + 70)
+    ok, err, bound = within_tol(got, ref)
+    assert ok, (err, bound)
+    assert sv.get_device_error() == 0
+
+
 def test_attn_chain_equals_path_tree(sv):
     B, R = 2, 9
     parent = np.tile(np.arange(-1, R - 1, dtype=np.int32), (B, 1))
