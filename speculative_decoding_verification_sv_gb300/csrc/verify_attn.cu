@@ -68,9 +68,16 @@ constexpr int kGroups = 4;                // full tiles: column groups of a step
 #ifndef SV_ATTN_HALF_MAX_ROWS
 #define SV_ATTN_HALF_MAX_ROWS 64
 #endif
-// (b, g) groups of at most this many rows use the half-tile layout (<= 64)
+#ifndef SV_ATTN_HALF_MAX_UNITS
+#define SV_ATTN_HALF_MAX_UNITS 16
+#endif
+// Row tiles: (b, g) groups of at most kHalfMaxRows rows use one half tile (64
+// rows, two key tiles per step); larger groups use half tiles too when there
+// are at most kHalfMaxUnits (b, g) groups (few units: the shorter step per key
+// wins), else full tiles (128 rows, one key tile per step: each K/V tile read
+// once for twice the rows)
 constexpr int kHalfMaxRows = SV_ATTN_HALF_MAX_ROWS;
-static_assert(kHalfMaxRows <= 64, "half tiles hold at most 64 rows");
+constexpr int kHalfMaxUnits = SV_ATTN_HALF_MAX_UNITS;
 
 // Full tiles (more than 64 rows): 16 row-owner warps, warp w on TMEM quadrant
 // w % 4 and column group w / 4.  Half tiles (at most 64 rows): 4 row-owner
@@ -128,7 +135,7 @@ struct AttnArgs {
     unsigned int* ws_cnt;    // [unit] tickets of clusters done; zero between launches
     int B, R, Hq, Hkv, G, T_cap, rows, row_tiles;
     int clusters;            // clusters per (b, g, row tile); their partials meet in ws_part
-    int part_rows;           // rows of a partial record block: min(rows, kRows)
+    int part_rows;           // rows of a partial record block: min(rows, rows per row tile)
     float scale_log2;
     int cache_ready;         // len and the cache are final before the preceding kernel runs
 };
@@ -168,7 +175,10 @@ __global__ void __launch_bounds__(Roles<kHalf>::kThreads, 1)
     const int C = static_cast<int>(cluster.num_blocks());
     const int rank = static_cast<int>(cluster.block_rank());
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int hg = blockIdx.y, rt = blockIdx.z;
+    // (sequence, KV head) and row tile: the row tiles of one KV head are
+    // adjacent in launch order, so their CTAs share its K/V tiles through L2
+    const int hg = blockIdx.y / a.row_tiles, rt = blockIdx.y % a.row_tiles;
+    constexpr int kTileRows = Lay<kHalf>::kM;   // query rows per row tile
     const int b = hg / a.Hkv, g = hg % a.Hkv;
 
     if (threadIdx.x == 0) {
@@ -233,7 +243,7 @@ __global__ void __launch_bounds__(Roles<kHalf>::kThreads, 1)
     const int nsteps = (ntiles + kT - 1) / kT;
     const bool has_block = last > n_ctx;
     const bool tree = kTree && has_block;
-    const int nrows = min(kRows, a.rows - rt * kRows);
+    const int nrows = min(kTileRows, a.rows - rt * kTileRows);
 
     // Receive plan of the cluster merge (computed by each warp, lane r for CTA
     // r of the cluster).  A CTA whose steps never reach the last `need` ring
@@ -382,7 +392,7 @@ __global__ void __launch_bounds__(Roles<kHalf>::kThreads, 1)
                 uint4 v = make_uint4(0u, 0u, 0u, 0u);
                 // half tiles: A row m sits in TMEM lane 32 * (m / 16) + m % 16 and
                 // carries row 4 * (m % 16) + m / 16 of (b, g)
-                const int grow = kHalf ? 4 * (row & 15) + (row >> 4) : rt * kRows + row;
+                const int grow = rt * kTileRows + (kHalf ? 4 * (row & 15) + (row >> 4) : row);
                 const int half = c >> 3, cc = c & 7;
                 uint8_t* dst = q_s + half * (kM * 128) + row * 128 + ((cc ^ (row & 7)) << 4);
                 if (grow < a.rows) {
@@ -403,12 +413,12 @@ __global__ void __launch_bounds__(Roles<kHalf>::kThreads, 1)
 
         // this thread's row: TMEM lane r (also its P row), row gr of (b, g)
         const int r = kHalf ? (warp * 32 + (lane & 15)) : ((warp & 3) * 32 + lane);
-        const int gr = kHalf ? (4 * (lane & 15) + warp) : (rt * kRows + r);
+        const int gr = rt * kTileRows + (kHalf ? 4 * (lane & 15) + warp : r);
         const bool valid = gr < a.rows;
         const int j = valid ? gr / a.G : 0;
         // the warp's quadrant holds at least one real row (padding lanes' P and
         // O are never read, so a warp with none skips the arithmetic)
-        const bool quarter_live = kHalf ? (warp < a.rows) : (rt * kRows + (warp & 3) * 32 < a.rows);
+        const bool quarter_live = rt * kTileRows + (kHalf ? warp : (warp & 3) * 32) < a.rows;
         const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
         // full tiles: 16 consecutive columns of the one-tile step (group cgp);
         // half tiles: half of the step's columns (thread half `sub` of the
@@ -624,7 +634,7 @@ __global__ void __launch_bounds__(Roles<kHalf>::kThreads, 1)
         // push the partial record of row prow into slot `rank` of the row's
         // owner: slots [(prow / n_owners) * C + src] of its receive area
         if (valid) {
-            const int prow = gr - rt * kRows;          // < kRows for every real row
+            const int prow = gr - rt * kTileRows;      // < kTileRows for every real row
             int owner, li;
             if (need > 0) {
                 const int nl = __popc(light);
@@ -662,7 +672,7 @@ __global__ void __launch_bounds__(Roles<kHalf>::kThreads, 1)
     const int ci = blockIdx.x / C;
     auto store_row = [&](int lr, float4 acc, float L) {
         const float inv = L > 0.f ? 1.0f / L : 0.f;
-        const int row = rt * kRows + lr;
+        const int row = rt * kTileRows + lr;
         const int jr = row / a.G, h = g * a.G + row % a.G;
         uint16_t* dst = a.out + ((static_cast<size_t>(b) * a.R + jr) * a.Hq + h) * kD + 4 * lane;
         *reinterpret_cast<uint2*>(dst) =
@@ -781,7 +791,7 @@ __global__ void __launch_bounds__(Roles<kHalf>::kThreads, 1)
                         }
                     }
                     const float inv = L > 0.f ? 1.0f / L : 0.f;
-                    const int row = rt * kRows + lr;
+                    const int row = rt * kTileRows + lr;
                     const int jr = row / a.G, h = g * a.G + row % a.G;
                     uint16_t* dst = a.out + ((static_cast<size_t>(b) * a.R + jr) * a.Hq + h) * kD + 4 * l4;
                     *reinterpret_cast<uint2*>(dst) =
@@ -893,7 +903,7 @@ cudaError_t launch_mode(const AttnPlan& p, const sv_attn_shape& s, const uint8_t
     cudaError_t e = prepare_kernel<kHalf, kTree>();
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(p.splits * p.clusters, s.B * s.Hkv, p.row_tiles);
+    cfg.gridDim = dim3(p.splits * p.clusters, s.B * s.Hkv * p.row_tiles, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = Lay<kHalf>::kSmemBytes;
     cfg.stream = st;
@@ -926,8 +936,9 @@ AttnPlan attn_plan(const sv_attn_shape& s) {
     AttnPlan p;
     p.G = s.Hq / s.Hkv;
     p.rows = s.R * p.G;
-    p.row_tiles = (p.rows + kRows - 1) / kRows;
-    p.half = p.rows <= kHalfMaxRows;
+    p.half = p.rows <= kHalfMaxRows || static_cast<int64_t>(s.B) * s.Hkv <= kHalfMaxUnits;
+    const int tile_rows = p.half ? Lay<true>::kM : Lay<false>::kM;
+    p.row_tiles = (p.rows + tile_rows - 1) / tile_rows;
     p.warps = p.half ? Roles<true>::kThreads / 32 : Roles<false>::kThreads / 32;
     const int64_t units = static_cast<int64_t>(s.B) * s.Hkv * p.row_tiles;
     const int64_t tiles = (s.T_cap + kNk - 1) / kNk + (s.R + kNk - 1) / kNk;
@@ -944,7 +955,7 @@ AttnPlan attn_plan(const sv_attn_shape& s) {
         for (int64_t nc = 1; nc <= nc_max; nc = nc < nc_max ? nc_max : nc_max + 1) {   // one cluster, or the most
             const int64_t waves = (units * nc + cap - 1) / cap;
             const int64_t per_cta = (tiles + C * nc - 1) / (C * nc);
-            const int64_t part_rows = p.rows < kRows ? p.rows : kRows;
+            const int64_t part_rows = p.rows < tile_rows ? p.rows : tile_rows;
             const int64_t merge_bytes = nc * part_rows * kRec * 4 / C;   // per SM of the merging cluster
             const int64_t cost = waves * (3 + per_cta) + (nc > 1 ? kMergeCost + merge_bytes / (40 * 1024) : 0);
             if (best < 0 || cost < best) {
@@ -967,7 +978,8 @@ size_t attn_workspace(const sv_attn_shape& s) {
     const AttnPlan p = attn_plan(s);
     if (p.clusters <= 1) return 0;
     const size_t units = static_cast<size_t>(s.B) * s.Hkv * p.row_tiles;
-    const size_t part_rows = p.rows < kRows ? p.rows : kRows;
+    const int tile_rows = p.half ? Lay<true>::kM : Lay<false>::kM;
+    const size_t part_rows = p.rows < tile_rows ? p.rows : tile_rows;
     return attn_ticket_bytes(p, s) + units * p.clusters * part_rows * kRec * sizeof(float);
 }
 
@@ -1003,7 +1015,8 @@ cudaError_t launch_verify_attn(const sv_attn_shape& s, const uint16_t* q, const 
     a.rows = p.rows;
     a.row_tiles = p.row_tiles;
     a.clusters = p.clusters;
-    a.part_rows = p.rows < kRows ? p.rows : kRows;
+    const int tile_rows = p.half ? Lay<true>::kM : Lay<false>::kM;
+    a.part_rows = p.rows < tile_rows ? p.rows : tile_rows;
     a.scale_log2 = scale * 1.4426950408889634f;
     a.cache_ready = cache_ready ? 1 : 0;
     if (parent != nullptr)

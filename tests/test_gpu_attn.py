@@ -42,6 +42,7 @@ def _run(sv, B, R, Hq, Hkv, T_cap, lengths, parent=None, seed=0, scale=None):
     (4, 9, 28, 4, 1100, [1000, 513, 1024, 77]),  # ragged batch, multiple tiles and splits
     (1, 17, 16, 2, 700, [600]),                  # 136 rows: 3 row tiles
     (2, 3, 4, 1, 130, [130, 129]),               # full cache
+    (8, 17, 16, 4, 700, [600, 1, 64, 65, 300, 0, 511, 700]),   # 68 rows x 32 units: 128-row tiles
 ])
 def test_attn_chain(sv, B, R, Hq, Hkv, T_cap, lengths):
     got, ref = _run(sv, B, R, Hq, Hkv, T_cap, lengths, seed=B * 31 + R)
