@@ -79,13 +79,14 @@ constexpr int kGroups = 4;                // full tiles: column groups of a step
 constexpr int kHalfMaxRows = SV_ATTN_HALF_MAX_ROWS;
 constexpr int kHalfMaxUnits = SV_ATTN_HALF_MAX_UNITS;
 
-// Full tiles (more than 64 rows): 16 row-owner warps, warp w on TMEM quadrant
-// w % 4 and column group w / 4.  Half tiles (at most 64 rows): 4 row-owner
-// warps, one per quadrant (= one per SM sub-partition), the rows spread over
-// the first 16 lanes of every quadrant, two threads per row.
+// Full tiles (128 rows): 16 row-owner warps, warp w on TMEM quadrant w % 4
+// and column group w / 4.  Half tiles (64 rows): 8 row-owner warps, two per
+// quadrant (= per SM sub-partition, so one hides the other's latency), the
+// rows spread over the first 16 lanes of every quadrant, four threads per row
+// (two per warp via the 16x32bx2 access, one warp per column half).
 template <bool kHalf>
 struct Roles {
-    static constexpr int kSoft = kHalf ? 4 : 16;
+    static constexpr int kSoft = kHalf ? 8 : 16;
     static constexpr int kTma = kSoft, kMma = kSoft + 1;
     static constexpr int kThreads = 32 * (kSoft + 2);
 };
@@ -412,21 +413,22 @@ __global__ void __launch_bounds__(Roles<kHalf>::kThreads, 1)
         if (lane == 0) mbar_arrive(q_ready);
 
         // this thread's row: TMEM lane r (also its P row), row gr of (b, g)
-        const int r = kHalf ? (warp * 32 + (lane & 15)) : ((warp & 3) * 32 + lane);
-        const int gr = rt * kTileRows + (kHalf ? 4 * (lane & 15) + warp : r);
+        const int q4 = warp & 3;   // TMEM quadrant = SM sub-partition
+        const int r = kHalf ? (q4 * 32 + (lane & 15)) : (q4 * 32 + lane);
+        const int gr = rt * kTileRows + (kHalf ? 4 * (lane & 15) + q4 : r);
         const bool valid = gr < a.rows;
         const int j = valid ? gr / a.G : 0;
         // the warp's quadrant holds at least one real row (padding lanes' P and
         // O are never read, so a warp with none skips the arithmetic)
-        const bool quarter_live = rt * kTileRows + (kHalf ? warp : (warp & 3) * 32) < a.rows;
-        const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+        const bool quarter_live = rt * kTileRows + (kHalf ? q4 : q4 * 32) < a.rows;
+        const uint32_t lane_off = static_cast<uint32_t>(q4 * 32) << 16;
         // full tiles: 16 consecutive columns of the one-tile step (group cgp);
-        // half tiles: half of the step's columns (thread half `sub` of the
-        // row's pair) -- with two tiles per step, one whole tile per thread
-        constexpr int kCols = kHalf ? kStepKeys / 2 : kStepKeys / kGroups;
-        const int cgp = kHalf ? 0 : warp / 4;
+        // half tiles: 32 columns -- key tile `sub` of the step (thread half of
+        // the warp), its column half `cgp` (the quadrant's warp)
+        constexpr int kCols = kHalf ? kStepKeys / 4 : kStepKeys / kGroups;
+        const int cgp = warp / 4;
         const int sub = kHalf ? (lane >> 4) : 0;
-        const int col0 = kHalf ? sub * kCols : cgp * kCols;   // S columns of the step
+        const int col0 = kHalf ? sub * (kStepKeys / 2) + cgp * kCols : cgp * kCols;   // S columns of the step
         const int tsub = col0 / kNk, ctile = col0 % kNk;     // tile within the step, first key in it
         // tree: this thread's windows of the row's ancestor mask, one per block
         // tile (block keys ctile.. of tile 0 and of tile 1)
@@ -447,12 +449,10 @@ __global__ void __launch_bounds__(Roles<kHalf>::kThreads, 1)
             const bool work = quarter_live;
             uint32_t rs[kCols];
             if (work) {
-                if constexpr (kHalf && kCols == 64) {
-                    // columns col0 .. col0+31 and col0+32 .. col0+63
-                    tmem_ld32_h_sync<64>(tS(sb) + lane_off, *reinterpret_cast<uint32_t(*)[32]>(rs));
-                    tmem_ld32_h_sync<64>(tS(sb) + lane_off + 32, *reinterpret_cast<uint32_t(*)[32]>(rs + 32));
-                } else if constexpr (kHalf) {
-                    tmem_ld32_h_sync<32>(tS(sb) + lane_off, rs);
+                if constexpr (kHalf) {
+                    // columns 32 cgp .. of the step's first tile (threads 0-15)
+                    // and of its second tile (threads 16-31)
+                    tmem_ld32_h_sync<kStepKeys / 2>(tS(sb) + lane_off + cgp * kCols, rs);
                 } else {
                     tmem_ld16_sync(tS(sb) + lane_off + col0, rs);
                 }
@@ -494,8 +494,12 @@ __global__ void __launch_bounds__(Roles<kHalf>::kThreads, 1)
             }
             float mt;
             if constexpr (kHalf) {
-                // the row's other half sits 16 lanes away in the same warp
+                // the row's other tile sits 16 lanes away in the same warp, its
+                // other column half in the quadrant's other warp
                 mt = fmaxf(mpart, __shfl_xor_sync(0xffffffffu, mpart, 16));
+                red[(sb * kGroups + cgp) * kRows + r] = mt;
+                named_barrier(3 + q4, 64);
+                mt = fmaxf(mt, red[(sb * kGroups + (cgp ^ 1)) * kRows + r]);
             } else {
                 red[(sb * kGroups + cgp) * kRows + r] = mpart;
                 named_barrier(2, 32 * kSoftWarps);
@@ -538,10 +542,10 @@ __global__ void __launch_bounds__(Roles<kHalf>::kThreads, 1)
                 mbar_wait(&o_done[sb ^ 1], ((st - 1) >> 1) & 1, a.err);
                 tc_fence_after();
                 if constexpr (kHalf) {
-                    // columns 64*sub .. of the row
+                    // O columns 64 sub + 32 cgp .. of the row
 #pragma unroll
-                    for (int c0 = 0; c0 < kD / 2; c0 += 16) {
-                        const uint32_t ta = tO + lane_off + c0;
+                    for (int c0 = 0; c0 < kD / 4; c0 += 16) {
+                        const uint32_t ta = tO + lane_off + cgp * (kD / 4) + c0;
                         uint32_t o16[16];
                         tmem_ld16_h_sync<kD / 2>(ta, o16);
 #pragma unroll
@@ -563,12 +567,9 @@ __global__ void __launch_bounds__(Roles<kHalf>::kThreads, 1)
             }
             if (work) {
                 // P of this thread's columns into TMEM buffer sb, two keys per column
-                if constexpr (kHalf && kCols == 64) {
-                    // P columns col0/2 .. col0/2+31 (two keys per column)
-                    tmem_st16_h<32>(tP(sb) + lane_off, *reinterpret_cast<const uint32_t(*)[16]>(pk));
-                    tmem_st16_h<32>(tP(sb) + lane_off + 16, *reinterpret_cast<const uint32_t(*)[16]>(pk + 16));
-                } else if constexpr (kHalf) {
-                    tmem_st16_h<16>(tP(sb) + lane_off, pk);
+                if constexpr (kHalf) {
+                    // P columns col0/2 .. col0/2 + 15 (two keys per column)
+                    tmem_st16_h<kStepKeys / 4>(tP(sb) + lane_off + cgp * (kCols / 2), pk);
                 } else {
                     tmem_st8(tP(sb) + lane_off + col0 / 2, pk);
                 }
@@ -603,6 +604,9 @@ __global__ void __launch_bounds__(Roles<kHalf>::kThreads, 1)
         float lt;
         if constexpr (kHalf) {
             lt = lsum + __shfl_xor_sync(0xffffffffu, lsum, 16);
+            lsx[cgp * kRows + r] = lt;
+            named_barrier(3 + q4, 64);
+            lt += lsx[(cgp ^ 1) * kRows + r];
         } else {
             lsx[cgp * kRows + r] = lsum;
             named_barrier(2, 32 * kSoftWarps);
@@ -612,8 +616,8 @@ __global__ void __launch_bounds__(Roles<kHalf>::kThreads, 1)
         }
         const bool use = nsteps >= 1 && lt > 0.f;
         // O of this thread's columns, held in registers across the barrier
-        constexpr int kOCols = kHalf ? kD / 2 : kD / kGroups;   // O columns per thread
-        const int ocol0 = kHalf ? sub * (kD / 2) : cgp * (kD / kGroups);
+        constexpr int kOCols = kHalf ? kD / 4 : kD / kGroups;   // O columns per thread
+        const int ocol0 = kHalf ? sub * (kD / 2) + cgp * (kD / 4) : cgp * (kD / kGroups);
         uint32_t ov[kOCols];
 #pragma unroll
         for (int c0 = 0; c0 < kOCols; c0 += 16) {
@@ -621,7 +625,7 @@ __global__ void __launch_bounds__(Roles<kHalf>::kThreads, 1)
             // the condition of a warp-collective TMEM load must be warp-uniform
             // (nsteps is; `use` is per row)
             if (nsteps >= 1) {
-                if constexpr (kHalf) tmem_ld16_h_sync<kD / 2>(tO + lane_off + c0, o16);
+                if constexpr (kHalf) tmem_ld16_h_sync<kD / 2>(tO + lane_off + cgp * (kD / 4) + c0, o16);
                 else tmem_ld16_sync(tO + lane_off + ocol0 + c0, o16);
             }
 #pragma unroll
