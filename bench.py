@@ -50,14 +50,14 @@ TRAFFIC = {
     # ncu --set full, 28-layer 1.5B round, LM head N=5 H=1536 V=151936
     ("1", "lm_head"): {"bytes": 466803200 + 5557504, "src": "lm_head.cu", "src_hash": "43daf2fa01b4f0d6"},
     # ncu --set full, 7B batch-16 layer (2-layer case, same per-layer launch)
-    ("3b16", "verify_attn"): {"bytes": 269846272 + 3296768, "src": "verify_attn.cu",
-                              "src_hash": "0aedacb62922d9fc"},
-    ("3b16s", "verify_attn"): {"bytes": 269846272 + 3296768, "src": "verify_attn.cu",
-                               "src_hash": "0aedacb62922d9fc"},
+    ("3b16", "verify_attn"): {"bytes": 269846528 + 3409664, "src": "verify_attn.cu",
+                              "src_hash": "d1dd8fbe95a18c2a"},
+    ("3b16s", "verify_attn"): {"bytes": 269846528 + 3409664, "src": "verify_attn.cu",
+                               "src_hash": "d1dd8fbe95a18c2a"},
     # ncu --set full, sampled B64 k8: statistics pass + chain residual pass (the
     # walk and draw launches move < 0.1 MB and were not captured)
-    ("2", "accept_sampled"): {"bytes": 389491200 + 3341568 + 77821696 + 1400320, "src": "accept.cu",
-                              "src_hash": "3e022b7bfe29e81f"},
+    ("2", "accept_sampled"): {"bytes": 381219840 + 3627520 + 77820672 + 1609984, "src": "accept.cu",
+                              "src_hash": "a1b4dfc0598b8c78"},
 }
 
 
