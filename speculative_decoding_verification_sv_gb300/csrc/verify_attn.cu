@@ -465,11 +465,9 @@ __global__ void __launch_bounds__(Roles<kHalf>::kThreads, 1)
             const int gt = first + ti;
             const bool is_block = gt >= n_ctx;
             const int kb = (is_block ? (gt - n_ctx) * kNk : gt * kNk) + ctile;
-            float sc[kCols];
+            // rs holds the raw q.k bits (scaled in the exponent), masked in place
             float mpart = -INFINITY;
             if (work) {
-#pragma unroll
-                for (int e = 0; e < kCols; ++e) sc[e] = __uint_as_float(rs[e]);   // raw q.k; scaled in the exponent
                 if (is_block || kb + kCols > t || !tile_live) {
                     // branch-free mask: key kb + e is visible iff e < lim (context:
                     // kl < t; chain block: kl <= j and kl < R; no tile: none) or,
@@ -480,17 +478,17 @@ __global__ void __launch_bounds__(Roles<kHalf>::kThreads, 1)
 #pragma unroll
                     for (int e = 0; e < kCols; ++e) {
                         const bool vis = tree_blk ? ((win >> e) & Win(1)) != Win(0) : e < lim;
-                        sc[e] = vis ? sc[e] : -INFINITY;
+                        rs[e] = vis ? rs[e] : __float_as_uint(-INFINITY);
                     }
                 }
-                float mx[kCols / 2];
+                // four running maxima of three-input max.f32 (short chains)
+                float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-                for (int e = 0; e < kCols / 2; ++e) mx[e] = fmaxf(sc[e], sc[e + kCols / 2]);
+                for (int e = 0; e < kCols; e += 8)
 #pragma unroll
-                for (int w2 = kCols / 4; w2 >= 1; w2 >>= 1)
-#pragma unroll
-                    for (int e = 0; e < w2; ++e) mx[e] = fmaxf(mx[e], mx[e + w2]);
-                mpart = mx[0] * a.scale_log2;   // the scale is positive: max commutes with it
+                    for (int u = 0; u < 4; ++u)
+                        mq[u] = fmax3(mq[u], __uint_as_float(rs[e + 2 * u]), __uint_as_float(rs[e + 2 * u + 1]));
+                mpart = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3])) * a.scale_log2;   // the scale is positive
             }
             float mt;
             if constexpr (kHalf) {
@@ -522,8 +520,8 @@ __global__ void __launch_bounds__(Roles<kHalf>::kThreads, 1)
                 const float nm = m_new == -INFINITY ? 0.f : -m_new;
 #pragma unroll
                 for (int e = 0; e < kCols; e += 2) {
-                    const float p0 = fast_exp2(fmaf(sc[e], a.scale_log2, nm));
-                    const float p1 = fast_exp2(fmaf(sc[e + 1], a.scale_log2, nm));
+                    const float p0 = fast_exp2(fmaf(__uint_as_float(rs[e]), a.scale_log2, nm));
+                    const float p1 = fast_exp2(fmaf(__uint_as_float(rs[e + 1]), a.scale_log2, nm));
                     ps0 += p0;
                     ps1 += p1;
                     const __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
