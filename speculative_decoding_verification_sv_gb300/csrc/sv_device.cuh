@@ -405,6 +405,13 @@ __device__ __forceinline__ void tmem_st16_h(uint32_t taddr, const uint32_t (&r)[
         : "memory");
 }
 
+template <int OFF>
+__device__ __forceinline__ void tmem_st8_h(uint32_t taddr, const uint32_t (&r)[8]) {
+    asm volatile("tcgen05.st.sync.aligned.16x32bx2.x8.b32 [%0], %9, {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr),
+                 "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "n"(OFF)
+                 : "memory");
+}
+
 // Barrier over a subset of the CTA's warps (ids 1..15; 0 is __syncthreads).
 __device__ __forceinline__ void named_barrier(uint32_t id, uint32_t nthreads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");

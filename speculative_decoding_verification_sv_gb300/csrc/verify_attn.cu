@@ -84,9 +84,14 @@ constexpr int kHalfMaxUnits = SV_ATTN_HALF_MAX_UNITS;
 // quadrant (= per SM sub-partition, so one hides the other's latency), the
 // rows spread over the first 16 lanes of every quadrant, four threads per row
 // (two per warp via the 16x32bx2 access, one warp per column half).
+#ifndef SV_ATTN_HALF_WARPS
+#define SV_ATTN_HALF_WARPS 2
+#endif
+constexpr int kHalfWarps = SV_ATTN_HALF_WARPS;   // half tiles: row-owner warps per TMEM quadrant
+static_assert(kHalfWarps == 2 || kHalfWarps == 4, "two or four warps per quadrant");
 template <bool kHalf>
 struct Roles {
-    static constexpr int kSoft = kHalf ? 8 : 16;
+    static constexpr int kSoft = kHalf ? 4 * kHalfWarps : 16;
     static constexpr int kTma = kSoft, kMma = kSoft + 1;
     static constexpr int kThreads = 32 * (kSoft + 2);
 };
@@ -425,7 +430,7 @@ __global__ void __launch_bounds__(Roles<kHalf>::kThreads, 1)
         // full tiles: 16 consecutive columns of the one-tile step (group cgp);
         // half tiles: 32 columns -- key tile `sub` of the step (thread half of
         // the warp), its column half `cgp` (the quadrant's warp)
-        constexpr int kCols = kHalf ? kStepKeys / 4 : kStepKeys / kGroups;
+        constexpr int kCols = kHalf ? kStepKeys / (2 * kHalfWarps) : kStepKeys / kGroups;
         const int cgp = warp / 4;
         const int sub = kHalf ? (lane >> 4) : 0;
         const int col0 = kHalf ? sub * (kStepKeys / 2) + cgp * kCols : cgp * kCols;   // S columns of the step
@@ -452,7 +457,8 @@ __global__ void __launch_bounds__(Roles<kHalf>::kThreads, 1)
                 if constexpr (kHalf) {
                     // columns 32 cgp .. of the step's first tile (threads 0-15)
                     // and of its second tile (threads 16-31)
-                    tmem_ld32_h_sync<kStepKeys / 2>(tS(sb) + lane_off + cgp * kCols, rs);
+                    if constexpr (kCols == 32) tmem_ld32_h_sync<kStepKeys / 2>(tS(sb) + lane_off + cgp * kCols, rs);
+                    else tmem_ld16_h_sync<kStepKeys / 2>(tS(sb) + lane_off + cgp * kCols, rs);
                 } else {
                     tmem_ld16_sync(tS(sb) + lane_off + col0, rs);
                 }
@@ -496,8 +502,9 @@ __global__ void __launch_bounds__(Roles<kHalf>::kThreads, 1)
                 // other column half in the quadrant's other warp
                 mt = fmaxf(mpart, __shfl_xor_sync(0xffffffffu, mpart, 16));
                 red[(sb * kGroups + cgp) * kRows + r] = mt;
-                named_barrier(3 + q4, 64);
-                mt = fmaxf(mt, red[(sb * kGroups + (cgp ^ 1)) * kRows + r]);
+                named_barrier(3 + q4, 32 * kHalfWarps);
+#pragma unroll
+                for (int c2 = 0; c2 < kHalfWarps; ++c2) mt = fmaxf(mt, red[(sb * kGroups + c2) * kRows + r]);
             } else {
                 red[(sb * kGroups + cgp) * kRows + r] = mpart;
                 named_barrier(2, 32 * kSoftWarps);
@@ -540,10 +547,10 @@ __global__ void __launch_bounds__(Roles<kHalf>::kThreads, 1)
                 mbar_wait(&o_done[sb ^ 1], ((st - 1) >> 1) & 1, a.err);
                 tc_fence_after();
                 if constexpr (kHalf) {
-                    // O columns 64 sub + 32 cgp .. of the row
+                    // O columns 64 sub + (64 / kHalfWarps) cgp .. of the row
 #pragma unroll
-                    for (int c0 = 0; c0 < kD / 4; c0 += 16) {
-                        const uint32_t ta = tO + lane_off + cgp * (kD / 4) + c0;
+                    for (int c0 = 0; c0 < kD / (2 * kHalfWarps); c0 += 16) {
+                        const uint32_t ta = tO + lane_off + cgp * (kD / (2 * kHalfWarps)) + c0;
                         uint32_t o16[16];
                         tmem_ld16_h_sync<kD / 2>(ta, o16);
 #pragma unroll
@@ -566,8 +573,9 @@ __global__ void __launch_bounds__(Roles<kHalf>::kThreads, 1)
             if (work) {
                 // P of this thread's columns into TMEM buffer sb, two keys per column
                 if constexpr (kHalf) {
-                    // P columns col0/2 .. col0/2 + 15 (two keys per column)
-                    tmem_st16_h<kStepKeys / 4>(tP(sb) + lane_off + cgp * (kCols / 2), pk);
+                    // P columns col0/2 .. (two keys per column)
+                    if constexpr (kCols == 32) tmem_st16_h<kStepKeys / 4>(tP(sb) + lane_off + cgp * (kCols / 2), pk);
+                    else tmem_st8_h<kStepKeys / 4>(tP(sb) + lane_off + cgp * (kCols / 2), pk);
                 } else {
                     tmem_st8(tP(sb) + lane_off + col0 / 2, pk);
                 }
@@ -603,8 +611,10 @@ __global__ void __launch_bounds__(Roles<kHalf>::kThreads, 1)
         if constexpr (kHalf) {
             lt = lsum + __shfl_xor_sync(0xffffffffu, lsum, 16);
             lsx[cgp * kRows + r] = lt;
-            named_barrier(3 + q4, 64);
-            lt += lsx[(cgp ^ 1) * kRows + r];
+            named_barrier(3 + q4, 32 * kHalfWarps);
+            lt = 0.f;
+#pragma unroll
+            for (int c2 = 0; c2 < kHalfWarps; ++c2) lt += lsx[c2 * kRows + r];
         } else {
             lsx[cgp * kRows + r] = lsum;
             named_barrier(2, 32 * kSoftWarps);
@@ -614,8 +624,8 @@ __global__ void __launch_bounds__(Roles<kHalf>::kThreads, 1)
         }
         const bool use = nsteps >= 1 && lt > 0.f;
         // O of this thread's columns, held in registers across the barrier
-        constexpr int kOCols = kHalf ? kD / 4 : kD / kGroups;   // O columns per thread
-        const int ocol0 = kHalf ? sub * (kD / 2) + cgp * (kD / 4) : cgp * (kD / kGroups);
+        constexpr int kOCols = kHalf ? kD / (2 * kHalfWarps) : kD / kGroups;   // O columns per thread
+        const int ocol0 = kHalf ? sub * (kD / 2) + cgp * kOCols : cgp * (kD / kGroups);
         uint32_t ov[kOCols];
 #pragma unroll
         for (int c0 = 0; c0 < kOCols; c0 += 16) {
@@ -623,7 +633,7 @@ __global__ void __launch_bounds__(Roles<kHalf>::kThreads, 1)
             // the condition of a warp-collective TMEM load must be warp-uniform
             // (nsteps is; `use` is per row)
             if (nsteps >= 1) {
-                if constexpr (kHalf) tmem_ld16_h_sync<kD / 2>(tO + lane_off + cgp * (kD / 4) + c0, o16);
+                if constexpr (kHalf) tmem_ld16_h_sync<kD / 2>(tO + lane_off + cgp * kOCols + c0, o16);
                 else tmem_ld16_sync(tO + lane_off + ocol0 + c0, o16);
             }
 #pragma unroll
