@@ -67,8 +67,9 @@ cudaError_t launch_lm_head_tc(const uint16_t* hid, const uint16_t* W, float* log
 struct AttnPlan {
     int G;          // query heads per KV head
     int rows;       // R * G query rows per (sequence, KV head)
-    int row_tiles;  // ceil(rows / 128)
-    bool half;      // rows <= 64: half-tile kernel (M = 64 MMAs, 4 row-owner warps)
+    int row_tiles;  // ceil(rows / rows per tile)
+    bool half;      // 64-row tiles (M = 64 MMAs, two key tiles per step), else 128-row tiles
+    bool hw4;       // half tiles with four row-owner warps per TMEM quadrant (long loops), else two
     int warps;      // warps per CTA
     int splits;     // CTAs per thread-block cluster (split-KV merged through DSMEM)
     int clusters;   // clusters per (sequence, KV head, row tile); > 1 merges in the workspace

@@ -84,14 +84,18 @@ constexpr int kHalfMaxUnits = SV_ATTN_HALF_MAX_UNITS;
 // quadrant (= per SM sub-partition, so one hides the other's latency), the
 // rows spread over the first 16 lanes of every quadrant, four threads per row
 // (two per warp via the 16x32bx2 access, one warp per column half).
-#ifndef SV_ATTN_HALF_WARPS
-#define SV_ATTN_HALF_WARPS 2
+#ifndef SV_ATTN_HW4_MIN_TILES
+#define SV_ATTN_HW4_MIN_TILES 16
 #endif
-constexpr int kHalfWarps = SV_ATTN_HALF_WARPS;   // half tiles: row-owner warps per TMEM quadrant
-static_assert(kHalfWarps == 2 || kHalfWarps == 4, "two or four warps per quadrant");
-template <bool kHalf>
+// half tiles: four row-owner warps per quadrant when every CTA streams at least
+// this many key tiles (long loops: more latency hiding pays), else two (a few
+// steps: the smaller cross-warp exchange wins)
+constexpr int kHw4MinTiles = SV_ATTN_HW4_MIN_TILES;
+// kHW: row-owner warps per TMEM quadrant with half tiles (2 or 4)
+template <bool kHalf, int kHW = 2>
 struct Roles {
-    static constexpr int kSoft = kHalf ? 4 * kHalfWarps : 16;
+    static_assert(kHW == 2 || kHW == 4, "two or four warps per quadrant");
+    static constexpr int kSoft = kHalf ? 4 * kHW : 16;
     static constexpr int kTma = kSoft, kMma = kSoft + 1;
     static constexpr int kThreads = 32 * (kSoft + 2);
 };
@@ -153,11 +157,12 @@ struct AttnArgs {
 // kTree: the launch carries a draft tree (parent != NULL).  Chains compile
 // without any ancestor-mask code: the speculatively evaluated 64-bit window
 // of the tree mask stalled the chain's block-tile step by ~2500 cycles.
-template <bool kHalf, bool kTree>
-__global__ void __launch_bounds__(Roles<kHalf>::kThreads, 1)
+template <bool kHalf, bool kTree, int kHW>
+__global__ void __launch_bounds__(Roles<kHalf, kHW>::kThreads, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                    const __grid_constant__ CUtensorMap tmKb, const __grid_constant__ CUtensorMap tmVb, AttnArgs a) {
-    using Ro = Roles<kHalf>;
+    using Ro = Roles<kHalf, kHW>;
+    constexpr int kHalfWarps = kHW;
     using Ly = Lay<kHalf>;
     constexpr int kSoftWarps = Ro::kSoft, kTmaWarp = Ro::kTma, kMmaWarp = Ro::kMma, kThreads = Ro::kThreads;
     constexpr int kStages = Ly::kStages, kM = Ly::kM, kT = Ly::kT, kStepKeys = Ly::kStepKeys;
@@ -858,16 +863,16 @@ __global__ void __launch_bounds__(Roles<kHalf>::kThreads, 1)
     }
 }
 
-template <bool kHalf, bool kTree>
+template <bool kHalf, bool kTree, int kHW>
 cudaError_t prepare_kernel() {
     static bool done[64] = {};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (done[dev]) return cudaSuccess;
-    cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<kHalf, kTree>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<kHalf, kTree, kHW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          Lay<kHalf>::kSmemBytes);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(attn_tc_kernel<kHalf, kTree>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    e = cudaFuncSetAttribute(attn_tc_kernel<kHalf, kTree, kHW>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e != cudaSuccess) return e;
     done[dev] = true;
     return cudaSuccess;
@@ -888,10 +893,10 @@ int active_clusters(int C) {
     std::lock_guard<std::mutex> lk(mu);
     if (cache[dev][C]) return cache[dev][C];
     int n = 0;
-    if (prepare_kernel<kHalf, false>() == cudaSuccess) {   // both tree variants use the same resources
+    if (prepare_kernel<kHalf, false, 2>() == cudaSuccess) {   // both tree variants use the same resources
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(C, 1, 1);
-        cfg.blockDim = dim3(Roles<kHalf>::kThreads, 1, 1);
+        cfg.blockDim = dim3(Roles<kHalf, 2>::kThreads, 1, 1);
         cfg.dynamicSmemBytes = Lay<kHalf>::kSmemBytes;
         cudaLaunchAttribute attr[1];
         attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -900,7 +905,7 @@ int active_clusters(int C) {
         attr[0].val.clusterDim.z = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        if (cudaOccupancyMaxActiveClusters(&n, attn_tc_kernel<kHalf, false>, &cfg) != cudaSuccess) n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, attn_tc_kernel<kHalf, false, 2>, &cfg) != cudaSuccess) n = 0;
     }
     cudaGetLastError();
     if (n <= 0) n = fallback;
@@ -908,11 +913,11 @@ int active_clusters(int C) {
     return n;
 }
 
-template <bool kHalf, bool kTree>
+template <bool kHalf, bool kTree, int kHW>
 cudaError_t launch_mode(const AttnPlan& p, const sv_attn_shape& s, const uint8_t* tK, const uint8_t* tV,
                         const uint8_t* tKb, const uint8_t* tVb, const AttnArgs& a, cudaStream_t st) {
-    constexpr int kThreads = Roles<kHalf>::kThreads;
-    cudaError_t e = prepare_kernel<kHalf, kTree>();
+    constexpr int kThreads = Roles<kHalf, kHW>::kThreads;
+    cudaError_t e = prepare_kernel<kHalf, kTree, kHW>();
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(p.splits * p.clusters, s.B * s.Hkv * p.row_tiles, 1);
@@ -928,7 +933,7 @@ cudaError_t launch_mode(const AttnPlan& p, const sv_attn_shape& s, const uint8_t
     attrs[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attrs;
     cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, attn_tc_kernel<kHalf, kTree>, *reinterpret_cast<const CUtensorMap*>(tK),
+    return cudaLaunchKernelEx(&cfg, attn_tc_kernel<kHalf, kTree, kHW>, *reinterpret_cast<const CUtensorMap*>(tK),
                               *reinterpret_cast<const CUtensorMap*>(tV), *reinterpret_cast<const CUtensorMap*>(tKb),
                               *reinterpret_cast<const CUtensorMap*>(tVb), a);
 }
@@ -951,7 +956,7 @@ AttnPlan attn_plan(const sv_attn_shape& s) {
     p.half = p.rows <= kHalfMaxRows || static_cast<int64_t>(s.B) * s.Hkv <= kHalfMaxUnits;
     const int tile_rows = p.half ? Lay<true>::kM : Lay<false>::kM;
     p.row_tiles = (p.rows + tile_rows - 1) / tile_rows;
-    p.warps = p.half ? Roles<true>::kThreads / 32 : Roles<false>::kThreads / 32;
+    p.hw4 = false;
     const int64_t units = static_cast<int64_t>(s.B) * s.Hkv * p.row_tiles;
     const int64_t tiles = (s.T_cap + kNk - 1) / kNk + (s.R + kNk - 1) / kNk;
     int64_t best = -1;
@@ -977,6 +982,8 @@ AttnPlan attn_plan(const sv_attn_shape& s) {
             }
         }
     }
+    p.hw4 = p.half && (tiles + p.splits * p.clusters - 1) / (p.splits * p.clusters) >= kHw4MinTiles;
+    p.warps = !p.half ? Roles<false>::kThreads / 32 : p.hw4 ? Roles<true, 4>::kThreads / 32 : Roles<true, 2>::kThreads / 32;
     return p;
 }
 
@@ -1032,10 +1039,12 @@ cudaError_t launch_verify_attn(const sv_attn_shape& s, const uint16_t* q, const 
     a.scale_log2 = scale * 1.4426950408889634f;
     a.cache_ready = cache_ready ? 1 : 0;
     if (parent != nullptr)
-        return p.half ? launch_mode<true, true>(p, s, tK, tV, tKb, tVb, a, st)
-                      : launch_mode<false, true>(p, s, tK, tV, tKb, tVb, a, st);
-    return p.half ? launch_mode<true, false>(p, s, tK, tV, tKb, tVb, a, st)
-                  : launch_mode<false, false>(p, s, tK, tV, tKb, tVb, a, st);
+        return !p.half ? launch_mode<false, true, 2>(p, s, tK, tV, tKb, tVb, a, st)
+               : p.hw4 ? launch_mode<true, true, 4>(p, s, tK, tV, tKb, tVb, a, st)
+                       : launch_mode<true, true, 2>(p, s, tK, tV, tKb, tVb, a, st);
+    return !p.half ? launch_mode<false, false, 2>(p, s, tK, tV, tKb, tVb, a, st)
+           : p.hw4 ? launch_mode<true, false, 4>(p, s, tK, tV, tKb, tVb, a, st)
+                   : launch_mode<true, false, 2>(p, s, tK, tV, tKb, tVb, a, st);
 }
 
 }  // namespace sv
