@@ -202,7 +202,8 @@ class Round:
                 sv.verify_attn(self.q[l], self.kc[l], self.vc[l], self.length, self.kb[l], self.vb[l],
                                parent=self.parent, out=self.attn_out[l], ws=self.attn_ws, cache_ready=l > 0)
             rec("attn1")
-            sv.lm_head(self.hid, self.W, logits=self.logits)
+            # the weights are never written by the kernel before
+            sv.lm_head(self.hid, self.W, logits=self.logits, weights_ready=True)
             rec("lm1")
         else:
             rec("attn0"); rec("attn1"); rec("lm1")

@@ -172,6 +172,18 @@ SV_API sv_status sv_verify_attn_ex(const sv_attn_shape* shape, const uint16_t* q
 SV_API sv_status sv_lm_head(const uint16_t* hid, const uint16_t* W, float* logits, int32_t N, int32_t H,
                      int32_t V, void* stream);
 
+/* sv_lm_head with launch flags (sv_lm_head is flags = 0).
+ *   SV_LM_WEIGHTS_READY  the caller promises that the kernel enqueued on
+ *       `stream` just before this call does not write W (model weights: true
+ *       unless, e.g., a dequantisation kernel produces W right before).  The
+ *       kernel then starts loading W while that kernel is still finishing
+ *       (programmatic dependent launch); hid and logits are touched only after
+ *       it completes.
+ * Unknown flag bits return SV_ERR_ARG. */
+#define SV_LM_WEIGHTS_READY 1u
+SV_API sv_status sv_lm_head_ex(const uint16_t* hid, const uint16_t* W, float* logits, int32_t N, int32_t H,
+                               int32_t V, uint32_t flags, void* stream);
+
 /* ------------------------------------------------------------------------ */
 /* Greedy acceptance ([SCS] sec. 3 and 3.1).                                 */
 /* ------------------------------------------------------------------------ */

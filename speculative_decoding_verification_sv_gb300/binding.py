@@ -45,6 +45,7 @@ def _load():
     L.sv_verify_attn_workspace.argtypes = [ctypes.POINTER(_AttnShape)]
     L.sv_verify_attn_workspace.restype = _SZ
     L.sv_verify_attn.argtypes = [ctypes.POINTER(_AttnShape), _P, _P, _P, _P, _P, _P, _P, _F32, _P, _P, _SZ, _P]
+    L.sv_lm_head_ex.argtypes = [_P, _P, _P, _I32, _I32, _I32, ctypes.c_uint32, _P]
     L.sv_verify_attn_ex.argtypes = [ctypes.POINTER(_AttnShape), _P, _P, _P, _P, _P, _P, _P, _F32, _P, _P, _SZ,
                                     ctypes.c_uint32, _P]
     L.sv_lm_head.argtypes = [_P, _P, _P, _I32, _I32, _I32, _P]
@@ -61,7 +62,7 @@ def _load():
     L.sv_diag_exp.argtypes = [_P, _P, _I64, _P]
     L.sv_diag_philox.argtypes = [_P, _P, _P, _I64, _P]
     L.sv_diag_canon.argtypes = [_P, _I32, _I32, _P, _P, _P, _P]
-    for fn in ("sv_verify_attn", "sv_verify_attn_ex", "sv_lm_head", "sv_accept_greedy", "sv_accept_sample",
+    for fn in ("sv_verify_attn", "sv_verify_attn_ex", "sv_lm_head", "sv_lm_head_ex", "sv_accept_greedy", "sv_accept_sample",
                "sv_accept_sample_noalloc", "sv_kv_commit",
                "sv_diag_exp", "sv_diag_philox", "sv_diag_canon", "sv_get_device_error"):
         getattr(L, fn).restype = ctypes.c_int
@@ -143,14 +144,20 @@ def verify_attn(q, k_cache, v_cache, length, k_blk, v_blk, parent=None, scale=No
     return out
 
 
-def lm_head(hid, W, logits=None, stream=None):
-    """hid [N,H] bf16; W [H,V] bf16 -> logits [N,V] fp32."""
+LM_WEIGHTS_READY = 1
+
+
+def lm_head(hid, W, logits=None, stream=None, weights_ready=False):
+    """hid [N,H] bf16; W [H,V] bf16 -> logits [N,V] fp32.  weights_ready: the
+    kernel enqueued just before this call does not write W (sv_lm_head_ex,
+    SV_LM_WEIGHTS_READY)."""
     N, H = hid.shape
     V = W.shape[1]
     if logits is None:
         logits = torch.empty(N, V, dtype=torch.float32, device=hid.device)
-    _check("sv_lm_head", lib.sv_lm_head(_ptr(hid, torch.bfloat16, "hid"), _ptr(W, torch.bfloat16, "W"),
-                                        _ptr(logits, torch.float32, "logits"), N, H, V, _stream(stream)))
+    _check("sv_lm_head_ex", lib.sv_lm_head_ex(_ptr(hid, torch.bfloat16, "hid"), _ptr(W, torch.bfloat16, "W"),
+                                              _ptr(logits, torch.float32, "logits"), N, H, V,
+                                              LM_WEIGHTS_READY if weights_ready else 0, _stream(stream)))
     return logits
 
 

@@ -40,10 +40,8 @@ template <int NT>
 __global__ void __launch_bounds__(kThreads) lm_head_kernel(const __grid_constant__ CUtensorMap tmW,
                                                           const __grid_constant__ CUtensorMap tmH,
                                                           float* __restrict__ logits, int N, int H, int V, int n0,
-                                                          int nslab, unsigned int* err) {
+                                                          int nslab, int w_ready, unsigned int* err) {
     using S = LmSmem<NT>;
-    pdl_wait();   // the hidden rows come from the kernels before this one
-    pdl_launch_dependents();
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     float* out_s = reinterpret_cast<float*>(smem + kStages * S::kStageBytes);
@@ -62,7 +60,7 @@ __global__ void __launch_bounds__(kThreads) lm_head_kernel(const __grid_constant
     }
     __syncthreads();
 
-    auto issue = [&](int it) {
+    auto issue_w = [&](int it) {   // W of step it (and the stage's whole byte count)
         const int slab = blockIdx.x + (it / nk) * gridDim.x;
         const int kc = it % nk;
         const int s = it % kStages;
@@ -70,10 +68,29 @@ __global__ void __launch_bounds__(kThreads) lm_head_kernel(const __grid_constant
         mbar_arrive_expect_tx(&full[s], S::kStageBytes);
         tma_load_2d(st, &tmW, slab * kVT, kc * kHK, &full[s]);
         tma_load_2d(st + kHK * 128, &tmW, slab * kVT + 64, kc * kHK, &full[s]);
-        tma_load_2d(st + S::kWBytes, &tmH, kc * kHK, n0, &full[s]);
     };
+    auto issue_h = [&](int it) {   // the hidden rows' slice of step it
+        const int kc = it % nk;
+        const int s = it % kStages;
+        tma_load_2d(smem + s * S::kStageBytes + S::kWBytes, &tmH, kc * kHK, n0, &full[s]);
+    };
+    auto issue = [&](int it) {
+        issue_w(it);
+        issue_h(it);
+    };
+    // The hidden rows come from the kernels before this one.  With w_ready the
+    // weights are final before the preceding kernel runs, so the first ring
+    // pass of W is on its way before waiting for it.
+    const int npre = total_it < kStages ? total_it : kStages;
+    if (w_ready && tid == 0)
+        for (int it = 0; it < npre; ++it) issue_w(it);
+    pdl_wait();
+    pdl_launch_dependents();
     if (tid == 0)
-        for (int it = 0; it < total_it && it < kStages; ++it) issue(it);
+        for (int it = 0; it < npre; ++it) {
+            if (!w_ready) issue_w(it);
+            issue_h(it);
+        }
 
     float acc[2][NT][4];
     int it = 0;
@@ -144,7 +161,7 @@ __global__ void __launch_bounds__(kThreads) lm_head_kernel(const __grid_constant
 
 template <int NT>
 cudaError_t launch_nt(const uint16_t* hid, const uint16_t* W, float* logits, int N, int H, int V, int n0,
-                      cudaStream_t st) {
+                      bool w_ready, cudaStream_t st) {
     using S = LmSmem<NT>;
     alignas(64) uint8_t tmW[128], tmH[128];
     if (!encode_tmap_2d_bf16(tmW, W, V, H, static_cast<uint64_t>(V) * 2, 64, kHK)) return cudaErrorInvalidValue;
@@ -161,19 +178,19 @@ cudaError_t launch_nt(const uint16_t* hid, const uint16_t* W, float* logits, int
     if (grid > nslab) grid = nslab;
     return launch_pdl(lm_head_kernel<NT>, dim3(grid), dim3(kThreads), S::kTotal, st,
                       *reinterpret_cast<const CUtensorMap*>(tmW), *reinterpret_cast<const CUtensorMap*>(tmH), logits, N,
-                      H, V, n0, nslab, device_error_word());
+                      H, V, n0, nslab, w_ready ? 1 : 0, device_error_word());
 }
 
 }  // namespace
 
 cudaError_t launch_lm_head(const uint16_t* hid, const uint16_t* W, float* logits, int N, int H, int V,
-                           cudaStream_t st) {
+                           bool w_ready, cudaStream_t st) {
     // Beyond 16 rows the product is a real dense contraction: tcgen05, up to
     // 256 rows per pass over W.
     if (N > 16) {
         for (int n0 = 0; n0 < N; n0 += 256) {
             const int rows = N - n0 < 256 ? N - n0 : 256;
-            const cudaError_t e = launch_lm_head_tc(hid, W, logits, N, H, V, n0, rows, st);
+            const cudaError_t e = launch_lm_head_tc(hid, W, logits, N, H, V, n0, rows, w_ready, st);
             if (e != cudaSuccess) return e;
         }
         return cudaSuccess;
@@ -183,14 +200,14 @@ cudaError_t launch_lm_head(const uint16_t* hid, const uint16_t* W, float* logits
         const int nt = (rows + 7) / 8;
         cudaError_t e;
         switch (nt) {
-            case 1: e = launch_nt<1>(hid, W, logits, N, H, V, n0, st); break;
-            case 2: e = launch_nt<2>(hid, W, logits, N, H, V, n0, st); break;
-            case 3: e = launch_nt<3>(hid, W, logits, N, H, V, n0, st); break;
-            case 4: e = launch_nt<4>(hid, W, logits, N, H, V, n0, st); break;
-            case 5: e = launch_nt<5>(hid, W, logits, N, H, V, n0, st); break;
-            case 6: e = launch_nt<6>(hid, W, logits, N, H, V, n0, st); break;
-            case 7: e = launch_nt<7>(hid, W, logits, N, H, V, n0, st); break;
-            default: e = launch_nt<8>(hid, W, logits, N, H, V, n0, st); break;
+            case 1: e = launch_nt<1>(hid, W, logits, N, H, V, n0, w_ready, st); break;
+            case 2: e = launch_nt<2>(hid, W, logits, N, H, V, n0, w_ready, st); break;
+            case 3: e = launch_nt<3>(hid, W, logits, N, H, V, n0, w_ready, st); break;
+            case 4: e = launch_nt<4>(hid, W, logits, N, H, V, n0, w_ready, st); break;
+            case 5: e = launch_nt<5>(hid, W, logits, N, H, V, n0, w_ready, st); break;
+            case 6: e = launch_nt<6>(hid, W, logits, N, H, V, n0, w_ready, st); break;
+            case 7: e = launch_nt<7>(hid, W, logits, N, H, V, n0, w_ready, st); break;
+            default: e = launch_nt<8>(hid, W, logits, N, H, V, n0, w_ready, st); break;
         }
         if (e != cudaSuccess) return e;
     }

@@ -39,7 +39,7 @@ template <int NP>
 __global__ void __launch_bounds__(kThreads, 1) lm_head_tc_kernel(const __grid_constant__ CUtensorMap tmW,
                                                                 const __grid_constant__ CUtensorMap tmH,
                                                                 float* __restrict__ logits, int N, int H, int V,
-                                                                int n0, int nslab, unsigned int* err) {
+                                                                int n0, int nslab, int w_ready, unsigned int* err) {
     using C = TcCfg<NP>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -71,25 +71,45 @@ __global__ void __launch_bounds__(kThreads, 1) lm_head_tc_kernel(const __grid_co
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_base_s;
-    pdl_wait();
-    pdl_launch_dependents();
+    // The hidden rows come from the kernels before this one.  With w_ready the
+    // weights are final before the preceding kernel runs: the producer issues
+    // the first ring pass of W before waiting for it.
+    const bool early = w_ready != 0;
+    if (!early || warp != 4) {
+        pdl_wait();
+        pdl_launch_dependents();
+    }
 
     if (warp == 4) {
         // ---------------- TMA producer ----------------
         if (lane == 0) {
-            int it = 0;
-            for (int si = 0; si < my_slabs; ++si) {
-                const int slab = blockIdx.x + si * gridDim.x;
-                for (int kc = 0; kc < nk; ++kc, ++it) {
-                    const int s = it % C::kStages;
-                    mbar_wait(&empty[s], ((it / C::kStages) & 1) ^ 1, err);
-                    uint8_t* st = smem + s * C::kStageBytes;
-                    mbar_arrive_expect_tx(&full[s], C::kStageBytes);
-                    tma_load_2d(st, &tmW, slab * kM, kc * kHK, &full[s]);
-                    tma_load_2d(st + kHK * 128, &tmW, slab * kM + 64, kc * kHK, &full[s]);
-                    tma_load_2d(st + kWBytes, &tmH, kc * kHK, n0, &full[s]);
-                }
+            const int total_it = my_slabs * nk;
+            auto load_w = [&](int it) {   // W of step it (and the stage's whole byte count)
+                const int slab = blockIdx.x + (it / nk) * gridDim.x, kc = it % nk, s = it % C::kStages;
+                mbar_wait(&empty[s], ((it / C::kStages) & 1) ^ 1, err);
+                uint8_t* st = smem + s * C::kStageBytes;
+                mbar_arrive_expect_tx(&full[s], C::kStageBytes);
+                tma_load_2d(st, &tmW, slab * kM, kc * kHK, &full[s]);
+                tma_load_2d(st + kHK * 128, &tmW, slab * kM + 64, kc * kHK, &full[s]);
+            };
+            auto load_h = [&](int it) {   // the hidden rows' slice of step it
+                const int kc = it % nk, s = it % C::kStages;
+                tma_load_2d(smem + s * C::kStageBytes + kWBytes, &tmH, kc * kHK, n0, &full[s]);
+            };
+            const int npre = early ? (total_it < C::kStages ? total_it : C::kStages) : 0;
+            for (int it = 0; it < npre; ++it) load_w(it);
+            if (early) {
+                pdl_wait();
+                pdl_launch_dependents();
             }
+            for (int it = 0; it < npre; ++it) load_h(it);
+            for (int it = npre; it < total_it; ++it) {
+                load_w(it);
+                load_h(it);
+            }
+        } else if (early) {
+            pdl_wait();
+            pdl_launch_dependents();
         }
     } else if (warp == 5) {
         // ---------------- MMA issuer ----------------
@@ -157,7 +177,7 @@ __global__ void __launch_bounds__(kThreads, 1) lm_head_tc_kernel(const __grid_co
 
 template <int NP>
 cudaError_t launch_tc(const uint16_t* hid, const uint16_t* W, float* logits, int N, int H, int V, int n0,
-                      cudaStream_t st) {
+                      bool w_ready, cudaStream_t st) {
     using C = TcCfg<NP>;
     alignas(64) uint8_t tmW[128], tmH[128];
     if (!encode_tmap_2d_bf16(tmW, W, V, H, static_cast<uint64_t>(V) * 2, 64, kHK)) return cudaErrorInvalidValue;
@@ -184,32 +204,32 @@ cudaError_t launch_tc(const uint16_t* hid, const uint16_t* W, float* logits, int
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, lm_head_tc_kernel<NP>, *reinterpret_cast<const CUtensorMap*>(tmW),
                               *reinterpret_cast<const CUtensorMap*>(tmH), logits, N, H, V, n0, nslab,
-                              device_error_word());
+                              w_ready ? 1 : 0, device_error_word());
 }
 
 }  // namespace
 
 // Rows n0 .. n0+rows-1 of the pass (17 <= rows <= 256 after padding to 16).
 cudaError_t launch_lm_head_tc(const uint16_t* hid, const uint16_t* W, float* logits, int N, int H, int V, int n0,
-                              int rows, cudaStream_t st) {
+                              int rows, bool w_ready, cudaStream_t st) {
     const int np = (rows + 15) / 16 * 16;
     switch (np) {
-        case 16: return launch_tc<16>(hid, W, logits, N, H, V, n0, st);
-        case 32: return launch_tc<32>(hid, W, logits, N, H, V, n0, st);
-        case 48: return launch_tc<48>(hid, W, logits, N, H, V, n0, st);
-        case 64: return launch_tc<64>(hid, W, logits, N, H, V, n0, st);
-        case 80: return launch_tc<80>(hid, W, logits, N, H, V, n0, st);
-        case 96: return launch_tc<96>(hid, W, logits, N, H, V, n0, st);
-        case 112: return launch_tc<112>(hid, W, logits, N, H, V, n0, st);
-        case 128: return launch_tc<128>(hid, W, logits, N, H, V, n0, st);
-        case 144: return launch_tc<144>(hid, W, logits, N, H, V, n0, st);
-        case 160: return launch_tc<160>(hid, W, logits, N, H, V, n0, st);
-        case 176: return launch_tc<176>(hid, W, logits, N, H, V, n0, st);
-        case 192: return launch_tc<192>(hid, W, logits, N, H, V, n0, st);
-        case 208: return launch_tc<208>(hid, W, logits, N, H, V, n0, st);
-        case 224: return launch_tc<224>(hid, W, logits, N, H, V, n0, st);
-        case 240: return launch_tc<240>(hid, W, logits, N, H, V, n0, st);
-        default: return launch_tc<256>(hid, W, logits, N, H, V, n0, st);
+        case 16: return launch_tc<16>(hid, W, logits, N, H, V, n0, w_ready, st);
+        case 32: return launch_tc<32>(hid, W, logits, N, H, V, n0, w_ready, st);
+        case 48: return launch_tc<48>(hid, W, logits, N, H, V, n0, w_ready, st);
+        case 64: return launch_tc<64>(hid, W, logits, N, H, V, n0, w_ready, st);
+        case 80: return launch_tc<80>(hid, W, logits, N, H, V, n0, w_ready, st);
+        case 96: return launch_tc<96>(hid, W, logits, N, H, V, n0, w_ready, st);
+        case 112: return launch_tc<112>(hid, W, logits, N, H, V, n0, w_ready, st);
+        case 128: return launch_tc<128>(hid, W, logits, N, H, V, n0, w_ready, st);
+        case 144: return launch_tc<144>(hid, W, logits, N, H, V, n0, w_ready, st);
+        case 160: return launch_tc<160>(hid, W, logits, N, H, V, n0, w_ready, st);
+        case 176: return launch_tc<176>(hid, W, logits, N, H, V, n0, w_ready, st);
+        case 192: return launch_tc<192>(hid, W, logits, N, H, V, n0, w_ready, st);
+        case 208: return launch_tc<208>(hid, W, logits, N, H, V, n0, w_ready, st);
+        case 224: return launch_tc<224>(hid, W, logits, N, H, V, n0, w_ready, st);
+        case 240: return launch_tc<240>(hid, W, logits, N, H, V, n0, w_ready, st);
+        default: return launch_tc<256>(hid, W, logits, N, H, V, n0, w_ready, st);
     }
 }
 

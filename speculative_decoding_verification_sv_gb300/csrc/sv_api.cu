@@ -167,10 +167,17 @@ sv_status sv_verify_attn_ex(const sv_attn_shape* shape, const uint16_t* q, const
 
 sv_status sv_lm_head(const uint16_t* hid, const uint16_t* W, float* logits, int32_t N, int32_t H, int32_t V,
                      void* stream) {
+    return sv_lm_head_ex(hid, W, logits, N, H, V, 0u, stream);
+}
+
+sv_status sv_lm_head_ex(const uint16_t* hid, const uint16_t* W, float* logits, int32_t N, int32_t H, int32_t V,
+                        uint32_t flags, void* stream) {
+    if (flags & ~SV_LM_WEIGHTS_READY) return SV_ERR_ARG;
     if (!hid || !W || !logits) return SV_ERR_ARG;
     if (!aligned16(hid) || !aligned16(W) || !aligned16(logits)) return SV_ERR_ARG;
     if (N < 1 || N > 4096 || H < 8 || V < 8 || H % 8 || V % 8) return SV_ERR_SHAPE;
-    return launch_status(sv::launch_lm_head(hid, W, logits, N, H, V, as_stream(stream)));
+    return launch_status(
+        sv::launch_lm_head(hid, W, logits, N, H, V, (flags & SV_LM_WEIGHTS_READY) != 0, as_stream(stream)));
 }
 
 size_t sv_accept_greedy_workspace(int32_t B, int32_t R, int32_t V) {

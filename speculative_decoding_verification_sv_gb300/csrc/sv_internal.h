@@ -57,11 +57,11 @@ cudaError_t launch_kv_commit(uint16_t* k_cache, uint16_t* v_cache, const uint16_
 
 // lm_head.cu
 cudaError_t launch_lm_head(const uint16_t* hid, const uint16_t* W, float* logits, int N, int H, int V,
-                           cudaStream_t st);
+                           bool w_ready, cudaStream_t st);
 
 // lm_head_tc.cu (rows n0 .. n0+rows-1, 1 <= rows <= 256)
 cudaError_t launch_lm_head_tc(const uint16_t* hid, const uint16_t* W, float* logits, int N, int H, int V, int n0,
-                              int rows, cudaStream_t st);
+                              int rows, bool w_ready, cudaStream_t st);
 
 // verify_attn.cu
 struct AttnPlan {

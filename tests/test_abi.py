@@ -77,6 +77,8 @@ def test_host_validation_rejects_before_launch(lib):
                                None, 0, 2, None) == 1
     assert L.sv_verify_attn_ex(ctypes.byref(s), None, fake, fake, fake, fake, fake, None, ctypes.c_float(0.1), fake,
                                None, 0, 1, None) == 1
+    assert L.sv_lm_head_ex(fake, fake, fake, 5, 1536, 151936, 2, None) == 1
+    assert L.sv_lm_head_ex(None, fake, fake, 5, 1536, 151936, 1, None) == 1
     # short workspace
     assert L.sv_accept_greedy(fake, fake, None, 1, 5, 151936, fake, fake, fake, fake, 8, None) == 4
     # temperature must be positive; vocab must be a multiple of 4

@@ -127,3 +127,21 @@ def test_lm_head_full_shape_sampled_columns(sv, wid, B):
         ref = oracle.lm_head(hid_b, W_c)
         ok, err, bound = within_tol(got[:, v0:v1].cpu().numpy(), ref)
         assert ok, (v0, err, bound)
+
+
+@pytest.mark.parametrize("N,H,V", [(5, 1536, 151936), (9, 3584, 8200), (65, 3584, 4096), (144, 3584, 2048)])
+def test_lm_head_weights_ready_same_result(sv, N, H, V):
+    """SV_LM_WEIGHTS_READY (W loaded before the preceding kernel completes):
+    launched right after another LM head on the stream, the logits equal a
+    flag-free launch bit for bit, for both kernels (<= 16 rows, tcgen05)."""
+    g = torch.Generator().manual_seed(N + H)
+    hid = [torch.randn(N, H, generator=g).to(torch.bfloat16).cuda() for _ in range(2)]
+    W = (torch.randn(H, V, generator=g) * 0.02).to(torch.bfloat16).cuda()
+    ref = [sv.lm_head(h, W) for h in hid]
+    torch.cuda.synchronize()
+    out = [torch.empty(N, V, dtype=torch.float32, device="cuda") for _ in range(2)]
+    sv.lm_head(hid[0], W, logits=out[0])
+    sv.lm_head(hid[1], W, logits=out[1], weights_ready=True)
+    torch.cuda.synchronize()
+    for a, b in zip(out, ref):
+        assert torch.equal(a, b)
