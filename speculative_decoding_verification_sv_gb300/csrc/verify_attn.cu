@@ -80,10 +80,10 @@ constexpr int kHalfMaxRows = SV_ATTN_HALF_MAX_ROWS;
 constexpr int kHalfMaxUnits = SV_ATTN_HALF_MAX_UNITS;
 
 // Full tiles (128 rows): 16 row-owner warps, warp w on TMEM quadrant w % 4
-// and column group w / 4.  Half tiles (64 rows): 8 row-owner warps, two per
-// quadrant (= per SM sub-partition, so one hides the other's latency), the
-// rows spread over the first 16 lanes of every quadrant, four threads per row
-// (two per warp via the 16x32bx2 access, one warp per column half).
+// and column group w / 4.  Half tiles (64 rows): kHW = 2 or 4 row-owner warps
+// per quadrant (= per SM sub-partition, so one hides another's latency), the
+// rows spread over the first 16 lanes of every quadrant, 2 kHW threads per row
+// (two per warp via the 16x32bx2 access, one warp per column slice).
 #ifndef SV_ATTN_HW4_MIN_TILES
 #define SV_ATTN_HW4_MIN_TILES 16
 #endif
@@ -105,8 +105,8 @@ constexpr float kRescale = 8.0f;          // log2 of the largest tolerated P
 // Shared-memory and TMEM layout.  Full tiles: M = 128 MMAs, 32 KB of Q, one
 // key tile per softmax step, 5 ring stages.  Half tiles: M = 64 MMAs (row m of
 // the tile in TMEM lane 32 * (m / 16) + m % 16), 16 KB of Q, two key tiles per
-// step (S = Q K^T as one N = 128 MMA chain over both: the single MMA-issuing
-// thread bounds a step, so fewer, larger MMAs per key), 3 stages of two tiles.
+// step (S = Q K^T as one N = 128 MMA chain over both: fewer, larger MMAs per
+// key; an M = 64 MMA takes as long as an M = 128 one), 3 stages of two tiles.
 // A stage holds its tiles' boxes region by region: K dims 0-63 of every tile,
 // K dims 64-127, V dims 0-63, V dims 64-127, so keys are contiguous per region.
 template <bool kHalf>
