@@ -48,12 +48,12 @@ FALLBACK_HBM_GBS = 6800.0
 # was taken on; a different hash (the kernel changed) reports null.
 TRAFFIC = {
     # ncu --set full, 28-layer 1.5B round, LM head N=5 H=1536 V=151936
-    ("1", "lm_head"): {"bytes": 466803200 + 5557504, "src": "lm_head.cu", "src_hash": "43daf2fa01b4f0d6"},
+    ("1", "lm_head"): {"bytes": 466809856 + 5381632, "src": "lm_head.cu", "src_hash": "f74183b9259d0f09"},
     # ncu --set full, 7B batch-16 layer (2-layer case, same per-layer launch)
-    ("3b16", "verify_attn"): {"bytes": 269846528 + 3409664, "src": "verify_attn.cu",
-                              "src_hash": "d1dd8fbe95a18c2a"},
-    ("3b16s", "verify_attn"): {"bytes": 269846528 + 3409664, "src": "verify_attn.cu",
-                               "src_hash": "d1dd8fbe95a18c2a"},
+    ("3b16", "verify_attn"): {"bytes": 269842432 + 3261696, "src": "verify_attn.cu",
+                              "src_hash": "b81f585a7d44226b"},
+    ("3b16s", "verify_attn"): {"bytes": 269842432 + 3261696, "src": "verify_attn.cu",
+                               "src_hash": "b81f585a7d44226b"},
     # ncu --set full, sampled B64 k8: statistics pass + chain residual pass (the
     # walk and draw launches move < 0.1 MB and were not captured)
     ("2", "accept_sampled"): {"bytes": 381219840 + 3627520 + 77820672 + 1609984, "src": "accept.cu",
