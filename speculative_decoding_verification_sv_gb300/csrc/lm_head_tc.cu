@@ -84,28 +84,36 @@ __global__ void __launch_bounds__(kThreads, 1) lm_head_tc_kernel(const __grid_co
         // ---------------- TMA producer ----------------
         if (lane == 0) {
             const int total_it = my_slabs * nk;
-            auto load_w = [&](int it) {   // W of step it (and the stage's whole byte count)
-                const int slab = blockIdx.x + (it / nk) * gridDim.x, kc = it % nk, s = it % C::kStages;
+            // step it = slab si, hidden-row block kc (counters, no division per step)
+            auto load_w = [&](int it, int si, int kc) {   // W of step it (and the stage's whole byte count)
+                const int slab = blockIdx.x + si * gridDim.x, s = it % C::kStages;
                 mbar_wait(&empty[s], ((it / C::kStages) & 1) ^ 1, err);
                 uint8_t* st = smem + s * C::kStageBytes;
                 mbar_arrive_expect_tx(&full[s], C::kStageBytes);
                 tma_load_2d(st, &tmW, slab * kM, kc * kHK, &full[s]);
                 tma_load_2d(st + kHK * 128, &tmW, slab * kM + 64, kc * kHK, &full[s]);
             };
-            auto load_h = [&](int it) {   // the hidden rows' slice of step it
-                const int kc = it % nk, s = it % C::kStages;
+            auto load_h = [&](int it, int kc) {   // the hidden rows' slice of step it
+                const int s = it % C::kStages;
                 tma_load_2d(smem + s * C::kStageBytes + kWBytes, &tmH, kc * kHK, n0, &full[s]);
             };
             const int npre = early ? (total_it < C::kStages ? total_it : C::kStages) : 0;
-            for (int it = 0; it < npre; ++it) load_w(it);
+            for (int it = 0, si = 0, kc = 0; it < npre; ++it) {
+                load_w(it, si, kc);
+                if (++kc == nk) { kc = 0; ++si; }
+            }
             if (early) {
                 pdl_wait();
                 pdl_launch_dependents();
             }
-            for (int it = 0; it < npre; ++it) load_h(it);
-            for (int it = npre; it < total_it; ++it) {
-                load_w(it);
-                load_h(it);
+            for (int it = 0, kc = 0; it < npre; ++it) {
+                load_h(it, kc);
+                if (++kc == nk) kc = 0;
+            }
+            for (int it = npre, si = npre / nk, kc = npre % nk; it < total_it; ++it) {
+                load_w(it, si, kc);
+                load_h(it, kc);
+                if (++kc == nk) { kc = 0; ++si; }
             }
         } else if (early) {
             pdl_wait();
