@@ -175,6 +175,46 @@ def test_attn_full_layer(sv, wid, B, layer):
         assert ok, (b, err, bound)
 
 
+def test_attn_full_tree_layer(sv):
+    """A full-size layer of the 7B tree workload (64 draft nodes, depth 8,
+    t = 8192): 455 query rows per KV head in eight half tiles, each CTA
+    streaming enough key tiles for four row-owner warps per quadrant; every
+    output row is checked against the oracle."""
+    w = synth.workload(4)
+    ai = synth.attn_inputs(w, device="cuda", layers=1)
+    par = np.stack([synth.random_tree(w.R - 1, w.tree_depth, 3, synth.seed_for(w.wid, 12 + b))
+                    for b in range(w.B)]).astype(np.int32)
+    out = sv.verify_attn(ai.q[0], ai.k_cache[0], ai.v_cache[0], ai.length, ai.k_blk[0], ai.v_blk[0],
+                         torch.from_numpy(par).cuda())
+    ref = oracle.verify_attn(bits(ai.q[0]), bits(ai.k_cache[0]), bits(ai.v_cache[0]), ai.length.cpu().numpy(),
+                             bits(ai.k_blk[0]), bits(ai.v_blk[0]), par)
+    ok, err, bound = within_tol(out.float().cpu().numpy(), ref)
+    assert ok, (err, bound)
+    assert sv.get_device_error() == 0
+
+
+def test_attn_workspace_multi_row_tiles(sv):
+    """72 query rows per KV head (two half tiles) over a 32K context: several
+    clusters per (KV head, row tile) meet in the workspace; the merged rows of
+    both row tiles match the oracle and the tickets end at zero."""
+    B, R, Hq, Hkv, T_cap = 1, 9, 8, 1, 32832
+    nbytes = sv.verify_attn_workspace(B, R, Hq, Hkv, 128, T_cap)
+    assert nbytes > 0
+    ws = torch.zeros(nbytes, dtype=torch.uint8, device="cuda")
+    g = torch.Generator().manual_seed(13)
+    mk = lambda *s: torch.randn(*s, generator=g).to(torch.bfloat16)
+    q, kc, vc = mk(B, R, Hq, 128), mk(B, Hkv, T_cap, 128), mk(B, Hkv, T_cap, 128)
+    kb, vb = mk(B, Hkv, R, 128), mk(B, Hkv, R, 128)
+    ln = torch.tensor([32700], dtype=torch.int32)
+    out = sv.verify_attn(q.cuda(), kc.cuda(), vc.cuda(), ln.cuda(), kb.cuda(), vb.cuda(), ws=ws)
+    torch.cuda.synchronize()
+    assert int(ws[:256].view(torch.int32).abs().sum()) == 0
+    ref = oracle.verify_attn(bits(q), bits(kc), bits(vc), ln.numpy(), bits(kb), bits(vb))
+    ok, err, bound = within_tol(out.float().cpu().numpy(), ref)
+    assert ok, (err, bound)
+    assert sv.get_device_error() == 0
+
+
 def test_attn_workspace_tickets_reset(sv):
     """A batch-1, 32K-context layer splits each KV head over several clusters
     that meet in the workspace through a ticket word; every call must leave
