@@ -251,7 +251,13 @@ __global__ void __launch_bounds__(Roles<kHalf, kHW>::kThreads, 1)
     const int first = static_cast<int>((static_cast<int64_t>(n_all) * split) / nsplit);
     const int last = static_cast<int>((static_cast<int64_t>(n_all) * (split + 1)) / nsplit);
     const int ntiles = last - first;
-    const int nsteps = (ntiles + kT - 1) / kT;
+    const int nsteps = (ntiles + kT - 1) / kT;   // ring steps (stages of up to kT tiles)
+    // Fold (half tiles, two warps per quadrant): an odd last tile joins the step
+    // before it as a third tile -- its scores in the first 64 columns of the
+    // other score buffer, its P in the other P buffer -- instead of a step of
+    // its own; softmax steps are then one fewer than ring steps
+    const bool fold = kHalf && kHW == 2 && (ntiles & 1) != 0 && ntiles >= 3;
+    const int nsoft = nsteps - (fold ? 1 : 0);
     const bool has_block = last > n_ctx;
     const bool tree = kTree && has_block;
     const int nrows = min(kTileRows, a.rows - rt * kTileRows);
@@ -348,10 +354,19 @@ __global__ void __launch_bounds__(Roles<kHalf, kHW>::kThreads, 1)
                 const uint64_t bd0 = smem_desc_sw128(sv, kRegion, 1024);
                 for (int kc = 0; kc < nt * (kNk / 16); ++kc)
                     tc_mma_ts(tO, tP(pb) + kc * 8, bd0 + kc * (2048 >> 4), idesc_o, (st > 0 || kc > 0) ? 1u : 0u);
+                if (fold && st == nsoft - 1) {
+                    // the folded tile: P in the other P buffer, V in ring step st + 1
+                    const int sx = (st + 1) % kStages;
+                    const uint64_t bdx =
+                        smem_desc_sw128(smem_u32(smem + Ly::kOffRing + sx * kStageBytes + 2 * kRegion), kRegion, 1024);
+                    for (int kc = 0; kc < kNk / 16; ++kc)
+                        tc_mma_ts(tO, tP(pb ^ 1) + kc * 8, bdx + kc * (2048 >> 4), idesc_o, 1u);
+                    tc_commit(&kv_empty[sx]);
+                }
                 tc_commit(&o_done[pb]);
                 tc_commit(&kv_empty[s]);
             };
-            for (int st = 0; st < nsteps; ++st) {
+            for (int st = 0; st < nsoft; ++st) {
                 const int sb = st & 1, s = st % kStages;
                 const int nt = min(kT, ntiles - st * kT);
                 mbar_wait(&s_empty[sb], ((st >> 1) & 1) ^ 1, a.err);
@@ -365,10 +380,25 @@ __global__ void __launch_bounds__(Roles<kHalf, kHW>::kThreads, 1)
                     tc_mma(tS(sb), qd0 + ((half * (kM * 128) + kin) >> 4), kd0 + ((half * kRegion + kin) >> 4), id,
                            k16 > 0 ? 1u : 0u);
                 }
+                if (fold && st == nsoft - 1) {
+                    // the folded tile (ring step st + 1): scores into the first 64
+                    // columns of the other buffer, once step st - 1 has read it
+                    const int sx = (st + 1) % kStages;
+                    if (st >= 1) mbar_wait(&s_empty[sb ^ 1], ((st - 1) >> 1) & 1, a.err);
+                    mbar_wait(&kv_full[sx], ((st + 1) / kStages) & 1, a.err);
+                    tc_fence_after();
+                    const uint64_t kdx = smem_desc_sw128(smem_u32(smem + Ly::kOffRing + sx * kStageBytes), 16, 1024);
+#pragma unroll
+                    for (int k16 = 0; k16 < kD / 16; ++k16) {
+                        const uint32_t half = k16 >> 2, kin = (k16 & 3) * 32;
+                        tc_mma(tS(sb ^ 1), qd0 + ((half * (kM * 128) + kin) >> 4),
+                               kdx + ((half * kRegion + kin) >> 4), idesc_s1, k16 > 0 ? 1u : 0u);
+                    }
+                }
                 tc_commit(&s_full[sb]);
                 if (st > 0) pv(st - 1);
             }
-            pv(nsteps - 1);
+            pv(nsoft - 1);
         }
     } else {
         // ---------------- row-owner warps ----------------
@@ -450,14 +480,26 @@ __global__ void __launch_bounds__(Roles<kHalf, kHW>::kThreads, 1)
         }
         float* red = reinterpret_cast<float*>(smem + Ly::kOffRed);
         float* lsx = reinterpret_cast<float*>(smem + Ly::kOffLsum);
+        // the folded tile (the CTA's last): this thread's 16 of its 64 columns,
+        // 32 sub + 16 cgp .., and for a tree block tile the ancestor window there
+        constexpr int kCX = kNk / 4;
+        const int cx0 = sub * (kNk / 2) + cgp * kCX;
+        uint32_t winx = 0;
+        if (kTree && fold && valid && last - 1 >= n_ctx)
+            winx = static_cast<uint32_t>(anc[2 * j + (last - 1 - n_ctx)] >> cx0) & 0xFFFFu;
 
         float m_ref = -INFINITY, lsum = 0.f;
-        for (int st = 0; st < nsteps; ++st) {
+        for (int st = 0; st < nsoft; ++st) {
             const int sb = st & 1;
+            const bool fx = fold && st == nsoft - 1;   // this step also takes the folded tile
             mbar_wait(&s_full[sb], (st >> 1) & 1, a.err);
             tc_fence_after();
             const bool work = quarter_live;
             uint32_t rs[kCols];
+            uint32_t rx[kCX];
+            if constexpr (kHalf && kHW == 2) {
+                if (work && fx) tmem_ld16_h_sync<kNk / 2>(tS(sb ^ 1) + lane_off + cgp * kCX, rx);
+            }
             if (work) {
                 if constexpr (kHalf) {
                     // columns 32 cgp .. of the step's first tile (threads 0-15)
@@ -500,6 +542,26 @@ __global__ void __launch_bounds__(Roles<kHalf, kHW>::kThreads, 1)
                     for (int u = 0; u < 4; ++u)
                         mq[u] = fmax3(mq[u], __uint_as_float(rs[e + 2 * u]), __uint_as_float(rs[e + 2 * u + 1]));
                 mpart = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3])) * a.scale_log2;   // the scale is positive
+                if (fx) {
+                    // the folded tile's columns: the same mask, its own key base
+                    const int gtx = last - 1;
+                    const bool blk_x = gtx >= n_ctx;
+                    const int kbx = (blk_x ? (gtx - n_ctx) * kNk : gtx * kNk) + cx0;
+                    if (blk_x || kbx + kCX > t) {
+                        const bool tree_x = kTree && blk_x;
+                        const int limx = !blk_x ? t - kbx : (j + 1 < a.R ? j + 1 : a.R) - kbx;
+#pragma unroll
+                        for (int e = 0; e < kCX; ++e) {
+                            const bool vis = tree_x ? ((winx >> e) & 1u) != 0u : e < limx;
+                            rx[e] = vis ? rx[e] : __float_as_uint(-INFINITY);
+                        }
+                    }
+                    float mxx = -INFINITY;
+#pragma unroll
+                    for (int e = 0; e < kCX; e += 2)
+                        mxx = fmax3(mxx, __uint_as_float(rx[e]), __uint_as_float(rx[e + 1]));
+                    mpart = fmaxf(mpart, mxx * a.scale_log2);
+                }
             }
             float mt;
             if constexpr (kHalf) {
@@ -527,6 +589,7 @@ __global__ void __launch_bounds__(Roles<kHalf, kHW>::kThreads, 1)
             // one ex2; a row with no visible key yet (m = -inf) has every score
             // -inf, and exp2(-inf - 0) = 0.
             uint32_t pk[kCols / 2];
+            uint32_t pkx[kCX / 2];
             float ps0 = 0.f, ps1 = 0.f;
             if (work) {
                 const float nm = m_new == -INFINITY ? 0.f : -m_new;
@@ -538,6 +601,17 @@ __global__ void __launch_bounds__(Roles<kHalf, kHW>::kThreads, 1)
                     ps1 += p1;
                     const __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
                     pk[e / 2] = *reinterpret_cast<const uint32_t*>(&pb);
+                }
+                if (fx) {
+#pragma unroll
+                    for (int e = 0; e < kCX; e += 2) {
+                        const float p0 = fast_exp2(fmaf(__uint_as_float(rx[e]), a.scale_log2, nm));
+                        const float p1 = fast_exp2(fmaf(__uint_as_float(rx[e + 1]), a.scale_log2, nm));
+                        ps0 += p0;
+                        ps1 += p1;
+                        const __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
+                        pkx[e / 2] = *reinterpret_cast<const uint32_t*>(&pb);
+                    }
                 }
             }
             lsum = lsum * corr + (ps0 + ps1);
@@ -586,6 +660,20 @@ __global__ void __launch_bounds__(Roles<kHalf, kHW>::kThreads, 1)
                 }
                 tmem_st_wait();
             }
+            if constexpr (kHalf && kHW == 2) {
+                if (fx) {
+                    // the folded tile's P into the other P buffer once the P V of
+                    // step st - 1 has read it: P columns 16 sub + 8 cgp ..
+                    if (st >= 1) {
+                        mbar_wait(&o_done[sb ^ 1], ((st - 1) >> 1) & 1, a.err);
+                        tc_fence_after();
+                    }
+                    if (work) {
+                        tmem_st8_h<kNk / 4>(tP(sb ^ 1) + lane_off + cgp * (kCX / 2), pkx);
+                        tmem_st_wait();
+                    }
+                }
+            }
             {
                 // V rows of cache positions >= t in the last, partial context
                 // tile: P is 0 there, but 0 * a non-finite cache entry is NaN in
@@ -601,13 +689,24 @@ __global__ void __launch_bounds__(Roles<kHalf, kHW>::kThreads, 1)
                     }
                     fence_proxy_async_smem();
                 }
+                if (fx && (t & (kNk - 1)) != 0 && last - 1 == n_ctx - 1) {
+                    // ... and the folded tile when it is that tile (ring step st + 1)
+                    uint8_t* vt = smem + Ly::kOffRing + ((st + 1) % kStages) * kStageBytes + 2 * kRegion;
+                    const int r0 = t & (kNk - 1);
+                    for (int x = threadIdx.x; x < (kNk - r0) * 16; x += 32 * kSoftWarps) {
+                        const int row = r0 + (x >> 4), c = x & 15;
+                        *reinterpret_cast<uint4*>(vt + (c >> 3) * kRegion + row * 128 + (c & 7) * 16) =
+                            make_uint4(0u, 0u, 0u, 0u);
+                    }
+                    fence_proxy_async_smem();
+                }
             }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&p_full[sb]);
         }
-        if (nsteps > 0) {
-            mbar_wait(&o_done[(nsteps - 1) & 1], ((nsteps - 1) >> 1) & 1, a.err);
+        if (nsoft > 0) {
+            mbar_wait(&o_done[(nsoft - 1) & 1], ((nsoft - 1) >> 1) & 1, a.err);
             tc_fence_after();
         }
         // row sum across the row's threads -> this CTA's partial record, kept
