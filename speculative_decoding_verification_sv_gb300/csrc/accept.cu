@@ -26,6 +26,8 @@
 #include <limits.h>
 #include <stdlib.h>
 
+#include <type_traits>
+
 #include "sv_device.cuh"
 #include "sv_internal.h"
 
@@ -323,18 +325,63 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads)
 }
 
 // Many rows (B*R large): persistent CTAs, one per SM, each taking whole rows
-// (row blockIdx.x, + gridDim.x, ...), no cluster and no staging.  Pass 1
-// takes the exact maximum of z = l / T from HBM; pass 2 re-reads the row and
-// builds the same canonical tree: chunk sums of exp(z - M) over 128 leaves (4
-// per lane), block sums over 32 chunks, then the 64 zero-padded block sums.
-// One row in flight per SM keeps the re-read in L2 (152 x 600 KB < 126 MB).
+// (row blockIdx.x, + gridDim.x, ...), no cluster and no staging.  A row needs
+// two passes: the exact maximum of z = l / T, then the canonical tree over
+// exp(z - M) -- chunk sums over 128 leaves (4 per lane), block sums over 32
+// chunks, then the 64 zero-padded block sums.  The two are software
+// pipelined across the CTA's rows: one loop over the chunks re-reads row i
+// (from L2, where its own max pass left it) for the exponential sums and
+// reads row i + 1 from HBM for its maximum, so the DRAM stream of the next
+// row runs under the issue-bound exponentials of the current one.  The
+// re-read carries an evict-first L2 policy: a chunk is dead once summed, so
+// the lines of row i that are still to be read outlive it, and the two rows
+// in flight per SM (2 x 152 x 600 KB) need only about one row's worth of L2.
 #ifndef SV_ROW_THREADS
 #define SV_ROW_THREADS 1024
+#endif
+#ifndef SV_ROW_FUSE
+#define SV_ROW_FUSE 4
+#endif
+#ifndef SV_ROW_PIPE
+#define SV_ROW_PIPE 0
 #endif
 constexpr int kRowThreads = SV_ROW_THREADS;       // one CTA of 32 warps per SM (latency hiding)
 constexpr int kRowCtasPerSm = kRowThreads >= 512 ? 1 : 512 / kRowThreads;
 constexpr int kRowWarps = kRowThreads / 32;
+constexpr int kRowFuse = SV_ROW_FUSE;             // chunks in flight per warp and row
+static_assert(kRowFuse == 2 || kRowFuse == 4, "two or four chunks per warp and row");
 
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+__device__ __forceinline__ float4 ldg_policy(const float* p, uint64_t pol) {
+    float4 v;
+    asm("ld.global.nc.L2::cache_hint.v4.f32 {%0,%1,%2,%3}, [%4], %5;"
+        : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+        : "l"(p), "l"(pol));
+    return v;
+}
+
+// z = l / T of four leaves (kUnitT: T = 1, the logits themselves)
+template <bool kUnitT>
+__device__ __forceinline__ float4 scaled(float4 z, float T) {
+    if constexpr (!kUnitT)
+        z = make_float4(__fdiv_rn(z.x, T), __fdiv_rn(z.y, T), __fdiv_rn(z.z, T), __fdiv_rn(z.w, T));
+    return z;
+}
+
+// Running maximum of four z values (NaN-ignoring: the row's M is the largest
+// number), and a running NaN-propagating minimum: the row holds a non-finite
+// z iff that minimum ends NaN or -inf, or the maximum +inf.
+__device__ __forceinline__ void max_leaves(float4 z, float& m, float& mn) {
+    m = fmax3(m, fmax3(z.x, z.y, z.z), z.w);
+    mn = fmin3_nan(mn, fmin3_nan(z.x, z.y, z.z), z.w);
+}
+
+template <bool kUnitT>
 __global__ void __launch_bounds__(kRowThreads, kRowCtasPerSm) sample_stats_row_kernel(const float* __restrict__ logits, int V,
                                                                          float T, int nblk, int nrows,
                                                                          float2* __restrict__ stats,
@@ -345,86 +392,167 @@ __global__ void __launch_bounds__(kRowThreads, kRowCtasPerSm) sample_stats_row_k
     __shared__ float bsum[kMaxBlocks];
     __shared__ float wred[kRowWarps];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int nvec = V / 4;
-  for (int row = blockIdx.x; row < nrows; row += gridDim.x) {
-    const float* L = logits + static_cast<size_t>(row) * V;
-
-    // pass 1: max, eight loads in flight per thread
-    float m = -INFINITY;
-    // stay 0 unless some z is NaN or infinite (z * 0 is then NaN); one
-    // accumulator per component keeps the dependency chains short
-    float4 nf = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int i0 = tid; i0 < nvec; i0 += 8 * kRowThreads) {
-        float4 x[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            const int i = i0 + u * kRowThreads;
-            x[u] = i < nvec ? __ldg(reinterpret_cast<const float4*>(L) + i) : make_float4(-INFINITY, -INFINITY,
-                                                                                           -INFINITY, -INFINITY);
-        }
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            if (i0 + u * kRowThreads >= nvec) continue;
-            float4 z = x[u];
-            if (T != 1.0f) z = make_float4(__fdiv_rn(z.x, T), __fdiv_rn(z.y, T), __fdiv_rn(z.z, T), __fdiv_rn(z.w, T));
-            nf.x = __fmaf_rn(z.x, 0.0f, nf.x);
-            nf.y = __fmaf_rn(z.y, 0.0f, nf.y);
-            nf.z = __fmaf_rn(z.z, 0.0f, nf.z);
-            nf.w = __fmaf_rn(z.w, 0.0f, nf.w);
-            m = fmax3(m, fmax3(z.x, z.y, z.z), z.w);
-        }
-    }
-    if (__fadd_rn(__fadd_rn(nf.x, nf.y), __fadd_rn(nf.z, nf.w)) != 0.0f) raise_error(err, SV_DEVERR_NONFINITE);
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-    if (lane == 0) wred[warp] = m;
-    __syncthreads();
-    float M = -INFINITY;
-#pragma unroll
-    for (int w = 0; w < kRowWarps; ++w) M = fmaxf(M, wred[w]);
-
-    // pass 2: chunk sums (level 7), four chunks' loads in flight per warp
     const int nch = nblk * kChunksPerBlk;
-    for (int c0 = warp; c0 < nch; c0 += 4 * kRowWarps) {
-        float4 x[4];
+    const int nfull = V / kChunk;   // chunks whose 128 leaves all lie below V
+    const float4 ninf4 = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+    // the warp's chunks c0 + u * kRowWarps; lane holds leaves 4 lane .. of each
+    auto leaf = [&](int c) { return c * kChunk + 4 * lane; };
+    // CTA-wide maximum of the per-thread m (every thread gets it); flags non-finite z
+    auto finish_max = [&](float m, float mn) {
+        if (!(mn > -INFINITY)) raise_error(err, SV_DEVERR_NONFINITE);   // NaN or -inf
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const int v = (c0 + u * kRowWarps) * kChunk + 4 * lane;
-            x[u] = (c0 + u * kRowWarps < nch && v < V) ? __ldg(reinterpret_cast<const float4*>(L + v))
-                                                       : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
+        for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+        if (lane == 0) wred[warp] = m;
+        __syncthreads();
+        float M = -INFINITY;
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const int c = c0 + u * kRowWarps;
-            const int v = c * kChunk + 4 * lane;
-            float4 e = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (c < nch && v < V) {
-                float4 z = x[u];
-                if (T != 1.0f)
-                    z = make_float4(__fdiv_rn(z.x, T), __fdiv_rn(z.y, T), __fdiv_rn(z.z, T), __fdiv_rn(z.w, T));
-                e = make_float4(sv_exp_nb(__fsub_rn(z.x, M)), sv_exp_nb(__fsub_rn(z.y, M)), sv_exp_nb(__fsub_rn(z.z, M)),
-                                sv_exp_nb(__fsub_rn(z.w, M)));
+        for (int w = 0; w < kRowWarps; ++w) M = fmaxf(M, wred[w]);
+        if (tid == 0 && M == INFINITY) raise_error(err, SV_DEVERR_NONFINITE);
+        return M;
+    };
+
+    int row = blockIdx.x;
+    if (row >= nrows) return;
+    float M;
+    {
+        // prologue: the first row's maximum alone, twice the loads in flight
+        const float* L = logits + static_cast<size_t>(row) * V;
+        float m = -INFINITY, mn = INFINITY;
+        for (int c0 = warp; c0 < nch; c0 += 2 * kRowFuse * kRowWarps) {
+            float4 y[2 * kRowFuse];
+#pragma unroll
+            for (int u = 0; u < 2 * kRowFuse; ++u) {
+                const int c = c0 + u * kRowWarps, v = leaf(c);
+                y[u] = (c < nch && v < V) ? __ldg(reinterpret_cast<const float4*>(L + v)) : ninf4;
             }
-            const float cs = warp_tree_sum(quad_sum(e));
-            if (lane == 0 && c < nch) csum[c] = cs;
+#pragma unroll
+            for (int u = 0; u < 2 * kRowFuse; ++u)
+                if (c0 + u * kRowWarps < nch && leaf(c0 + u * kRowWarps) < V)
+                    max_leaves(scaled<kUnitT>(y[u], T), m, mn);
         }
+        M = finish_max(m, mn);
     }
-    __syncthreads();
-    // block sums (level 12); blocks beyond the vocab are zero
-    for (int bk = warp; bk < kMaxBlocks; bk += kRowWarps) {
-        const float bs = bk < nblk ? warp_tree_sum(csum[bk * kChunksPerBlk + lane]) : 0.0f;
-        if (lane == 0) bsum[bk] = bs;
-    }
-    __syncthreads();
-    if (warp == 0) {
-        const float Z = warp_tree_sum(__fadd_rn(bsum[2 * lane], bsum[2 * lane + 1]));   // level 13 -> 18
-        if (lane == 0) {
-            if (!(Z > 0.0f) || !isfinite(Z)) raise_error(err, SV_DEVERR_NONFINITE);
-            stats[row] = make_float2(M, Z);
+    const uint64_t pol = l2_evict_first_policy();
+    for (; row < nrows; row += gridDim.x) {
+        const int nxt = row + gridDim.x;
+        const bool more = nxt < nrows;   // CTA-uniform
+        const float* L = logits + static_cast<size_t>(row) * V;
+        const float* Ln = logits + static_cast<size_t>(more ? nxt : row) * V;
+        float m = -INFINITY, mn = INFINITY;
+        // chunks c0 + u * kRowWarps, u < kRowFuse: row i's leaves (x) and row
+        // i + 1's (y); kFull: all of them lie below V (no per-leaf test)
+        auto load = [&](auto full, int c0, float4 (&x)[kRowFuse], float4 (&y)[kRowFuse]) {
+            constexpr bool kFull = decltype(full)::value;
+#pragma unroll
+            for (int u = 0; u < kRowFuse; ++u) {
+                const int c = c0 + u * kRowWarps, v = leaf(c);
+                x[u] = (kFull || (c < nch && v < V)) ? ldg_policy(L + v, pol) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+            if (more) {
+#pragma unroll
+                for (int u = 0; u < kRowFuse; ++u) {
+                    const int c = c0 + u * kRowWarps, v = leaf(c);
+                    y[u] = (kFull || (c < nch && v < V)) ? __ldg(reinterpret_cast<const float4*>(Ln + v)) : ninf4;
+                }
+            }
+        };
+        auto work = [&](auto full, const float4 (&x)[kRowFuse], const float4 (&y)[kRowFuse], int c0) {
+            constexpr bool kFull = decltype(full)::value;
+            // row i: chunk sums (level 7) of e = exp(z - M), zero beyond V.
+            // Lane l's node over its 4 leaves of each chunk, then the 32
+            // lanes' tree for all the chunks at once: at each of the first
+            // levels a lane keeps half of its chunks and trades the other
+            // half with its partner, so every lane ends with one chunk's sum
+            // (chunk l % kRowFuse).  Each node is still its two children's
+            // sum, so the values are those of the plain per-chunk tree.
+            float q[kRowFuse];
+#pragma unroll
+            for (int u = 0; u < kRowFuse; ++u) {
+                const int c = c0 + u * kRowWarps, v = leaf(c);
+                float4 e = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (kFull || (c < nch && v < V)) {
+                    const float4 z = scaled<kUnitT>(x[u], T);
+                    e = make_float4(sv_exp_nb(__fsub_rn(z.x, M)), sv_exp_nb(__fsub_rn(z.y, M)),
+                                    sv_exp_nb(__fsub_rn(z.z, M)), sv_exp_nb(__fsub_rn(z.w, M)));
+                }
+                q[u] = quad_sum(e);
+            }
+            float w;
+            const bool hi1 = (lane & 1) != 0;
+            if constexpr (kRowFuse == 4) {
+                const bool hi2 = (lane & 2) != 0;
+                const float s0 = __shfl_xor_sync(0xffffffffu, hi1 ? q[0] : q[1], 1);
+                const float s1 = __shfl_xor_sync(0xffffffffu, hi1 ? q[2] : q[3], 1);
+                const float v0 = __fadd_rn(hi1 ? q[1] : q[0], s0);   // chunk (lane & 1)
+                const float v1 = __fadd_rn(hi1 ? q[3] : q[2], s1);   // chunk 2 + (lane & 1)
+                w = __fadd_rn(hi2 ? v1 : v0, __shfl_xor_sync(0xffffffffu, hi2 ? v0 : v1, 2));
+#pragma unroll
+                for (int off = 4; off < 32; off <<= 1) w = __fadd_rn(w, __shfl_xor_sync(0xffffffffu, w, off));
+            } else {
+                w = __fadd_rn(hi1 ? q[1] : q[0], __shfl_xor_sync(0xffffffffu, hi1 ? q[0] : q[1], 1));
+#pragma unroll
+                for (int off = 2; off < 32; off <<= 1) w = __fadd_rn(w, __shfl_xor_sync(0xffffffffu, w, off));
+            }
+            {
+                const int c = c0 + (lane % kRowFuse) * kRowWarps;
+                if (lane < kRowFuse && (kFull || c < nch)) csum[c] = w;
+            }
+            // row i + 1: its maximum
+            if (more) {
+#pragma unroll
+                for (int u = 0; u < kRowFuse; ++u)
+                    if (kFull || (c0 + u * kRowWarps < nch && leaf(c0 + u * kRowWarps) < V))
+                        max_leaves(scaled<kUnitT>(y[u], T), m, mn);
+            }
+        };
+        constexpr int kStep = kRowFuse * kRowWarps;
+        using Full = std::true_type;
+        using Edge = std::false_type;
+        int c0 = warp;
+#if SV_ROW_PIPE
+        // two register sets: the loads of the next chunks go out before the
+        // current ones are summed, so each has a whole iteration to land
+        float4 xa[kRowFuse], ya[kRowFuse], xb[kRowFuse], yb[kRowFuse];
+        load(Edge{}, c0, xa, ya);
+        while (true) {
+            load(Edge{}, c0 + kStep, xb, yb);
+            work(Edge{}, xa, ya, c0);
+            c0 += kStep;
+            if (c0 >= nch) break;
+            load(Edge{}, c0 + kStep, xa, ya);
+            work(Edge{}, xb, yb, c0);
+            c0 += kStep;
+            if (c0 >= nch) break;
         }
+#else
+        for (; c0 + (kRowFuse - 1) * kRowWarps < nfull; c0 += kStep) {
+            float4 x[kRowFuse], y[kRowFuse];
+            load(Full{}, c0, x, y);
+            work(Full{}, x, y, c0);
+        }
+        for (; c0 < nch; c0 += kStep) {
+            float4 x[kRowFuse], y[kRowFuse];
+            load(Edge{}, c0, x, y);
+            work(Edge{}, x, y, c0);
+        }
+#endif
+        __syncthreads();   // csum complete; wred of this row's M no longer read
+        // block sums (level 12); blocks beyond the vocab are zero
+        for (int bk = warp; bk < kMaxBlocks; bk += kRowWarps) {
+            const float bs = bk < nblk ? warp_tree_sum(csum[bk * kChunksPerBlk + lane]) : 0.0f;
+            if (lane == 0) bsum[bk] = bs;
+        }
+        __syncthreads();
+        if (warp == 0) {
+            const float Z = warp_tree_sum(__fadd_rn(bsum[2 * lane], bsum[2 * lane + 1]));   // level 13 -> 18
+            if (lane == 0) {
+                if (!(Z > 0.0f) || !isfinite(Z)) raise_error(err, SV_DEVERR_NONFINITE);
+                stats[row] = make_float2(M, Z);
+            }
+        }
+        if (more) M = finish_max(m, mn);   // its barrier also orders bsum's reuse
+        __syncthreads();                   // wred, csum and bsum are reused by the next row
     }
-    __syncthreads();   // wred, csum and bsum are reused by the next row
-  }
 }
 
 // ==========================================================================
@@ -1021,8 +1149,11 @@ cudaError_t launch_accept_sample(const float* logits, const float* q, int Vq, co
     {
         const int slots = device_sm_count() * kRowCtasPerSm;
         const int nrows = B * R, grid = nrows < slots ? nrows : slots;
-        e = launch_pdl(sample_stats_row_kernel, dim3(grid), dim3(kRowThreads), 0, st, logits, V, temperature, nblk, nrows,
-                       stats, err);
+        e = temperature == 1.0f
+                ? launch_pdl(sample_stats_row_kernel<true>, dim3(grid), dim3(kRowThreads), 0, st, logits, V, temperature,
+                             nblk, nrows, stats, err)
+                : launch_pdl(sample_stats_row_kernel<false>, dim3(grid), dim3(kRowThreads), 0, st, logits, V,
+                             temperature, nblk, nrows, stats, err);
         if (e != cudaSuccess) return e;
     }
     else

@@ -157,6 +157,14 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
     return r;
 }
 
+// Three-input minimum that is NaN if any input is NaN (max.f32 and min.f32
+// without .NaN return the other operand instead).
+__device__ __forceinline__ float fmin3_nan(float a, float b, float c) {
+    float r;
+    asm("min.NaN.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
 __device__ __forceinline__ void prefetch_tmap(const void* tmap) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
 }

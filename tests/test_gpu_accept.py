@@ -125,6 +125,31 @@ def test_sample_chain_injected_uniforms(sv):
         assert_same(got, exp, "sample chain uniforms")
 
 
+@pytest.mark.parametrize("B,k,V,T", [(48, 8, 4100, 0.7), (40, 7, 151936, 1.0), (33, 8, 20000, 1.3)])
+def test_sample_many_rows_pipelined(sv, B, k, V, T):
+    """Enough rows that the statistics CTAs take several rows each (the next
+    row's maximum is read in the loop over the current row's sums): a ragged
+    last chunk, temperatures other than 1, row counts that leave some CTAs a
+    row short."""
+    si = _sample_case(B, k, V, seed=B + k, std=2.0)
+    got = sv.accept_sample(si.logits.cuda(), si.q.cuda(), si.tok.cuda(), temperature=T, seed=77, step=3)
+    exp = oracle.accept_sample(si.logits.numpy(), si.q.numpy(), si.tok.numpy(), temperature=T, seed=77, step=3)
+    assert_same(got, exp, "sample many rows")
+    assert sv.get_device_error() == 0
+
+
+def test_sample_many_rows_nonfinite_flagged(sv):
+    # a non-finite logit in a row whose maximum is taken ahead, under the
+    # previous row's sums (rows past the first wave of CTAs)
+    B, k, V = 40, 8, 4096
+    si = _sample_case(B, k, V, seed=61)
+    for bad in (float("nan"), float("inf")):
+        logits = si.logits.clone()
+        logits[35, 4, 1000] = bad   # row 35 * 9 + 4 = 319
+        sv.accept_sample(logits.cuda(), si.q.cuda(), si.tok.cuda(), seed=1)
+        assert sv.get_device_error() & 0x1
+
+
 def test_sample_full_size_b64_k8(sv):
     """The sampled-acceptance workload at full size: 64 sequences, k = 8,
     vocab 151936, T = 1, target logits ~ N(0, 3^2)."""
