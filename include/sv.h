@@ -295,8 +295,9 @@ SV_API sv_status sv_kv_commit(uint16_t* k_cache, uint16_t* v_cache, const uint16
 /* ------------------------------------------------------------------------ */
 
 /* y[i] = the device exponential used by sv_accept_sample, for n inputs; where
- * the branch-free form of it used by the softmax passes (defined for x <= 0)
- * differs from it in any bit, y[i] = 12345 instead. */
+ * one of the two faster forms of it used by the softmax passes -- the
+ * branch-free one (defined for x <= 0) and the normal-range one (defined for
+ * -86.5 < x <= 0) -- differs from it in any bit, y[i] = 12345 instead. */
 SV_API sv_status sv_diag_exp(const float* x, float* y, int64_t n, void* stream);
 
 /* out[i][0..3] = Philox4x32-10(counter = ctr[i][0..3], key = key[i][0..1]). */

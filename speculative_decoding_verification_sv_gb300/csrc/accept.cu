@@ -342,12 +342,10 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads)
 #ifndef SV_ROW_FUSE
 #define SV_ROW_FUSE 4
 #endif
-#ifndef SV_ROW_PIPE
-#define SV_ROW_PIPE 0
-#endif
 constexpr int kRowThreads = SV_ROW_THREADS;       // one CTA of 32 warps per SM (latency hiding)
 constexpr int kRowCtasPerSm = kRowThreads >= 512 ? 1 : 512 / kRowThreads;
 constexpr int kRowWarps = kRowThreads / 32;
+static_assert(kRowWarps <= 32, "one warp's lanes reduce the CTA's warps");
 constexpr int kRowFuse = SV_ROW_FUSE;             // chunks in flight per warp and row
 static_assert(kRowFuse == 2 || kRowFuse == 4, "two or four chunks per warp and row");
 
@@ -391,29 +389,44 @@ __global__ void __launch_bounds__(kRowThreads, kRowCtasPerSm) sample_stats_row_k
     __shared__ float csum[kMaxBlocks * kChunksPerBlk];
     __shared__ float bsum[kMaxBlocks];
     __shared__ float wred[kRowWarps];
+    __shared__ float wmin[kRowWarps];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int nch = nblk * kChunksPerBlk;
     const int nfull = V / kChunk;   // chunks whose 128 leaves all lie below V
     const float4 ninf4 = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
     // the warp's chunks c0 + u * kRowWarps; lane holds leaves 4 lane .. of each
     auto leaf = [&](int c) { return c * kChunk + 4 * lane; };
-    // CTA-wide maximum of the per-thread m (every thread gets it); flags non-finite z
-    auto finish_max = [&](float m, float mn) {
-        if (!(mn > -INFINITY)) raise_error(err, SV_DEVERR_NONFINITE);   // NaN or -inf
+    // CTA-wide maximum of the per-thread m (every thread gets it); flags
+    // non-finite z; nrm: every z - M of the row lies where sv_exp_nrm applies
+    auto finish_max = [&](float m, float mn, bool& nrm) {
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-        if (lane == 0) wred[warp] = m;
+        for (int off = 16; off > 0; off >>= 1) {
+            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+            mn = fmin_nan(mn, __shfl_xor_sync(0xffffffffu, mn, off));
+        }
+        if (lane == 0) {
+            wred[warp] = m;
+            wmin[warp] = mn;
+        }
         __syncthreads();
-        float M = -INFINITY;
+        // every warp reduces the warps' values itself: lane l takes warp l's
+        float M = lane < kRowWarps ? wred[lane] : -INFINITY;
+        float zmin = lane < kRowWarps ? wmin[lane] : INFINITY;
 #pragma unroll
-        for (int w = 0; w < kRowWarps; ++w) M = fmaxf(M, wred[w]);
-        if (tid == 0 && M == INFINITY) raise_error(err, SV_DEVERR_NONFINITE);
+        for (int off = 16; off > 0; off >>= 1) {
+            M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+            zmin = fmin_nan(zmin, __shfl_xor_sync(0xffffffffu, zmin, off));
+        }
+        if (tid == 0 && (M == INFINITY || !(zmin > -INFINITY))) raise_error(err, SV_DEVERR_NONFINITE);
+        // z - M >= zmin - M for every z (rounding is monotonic); false for NaN
+        nrm = __fsub_rn(zmin, M) > kExpNormalMin;
         return M;
     };
 
     int row = blockIdx.x;
     if (row >= nrows) return;
     float M;
+    bool nrm;
     {
         // prologue: the first row's maximum alone, twice the loads in flight
         const float* L = logits + static_cast<size_t>(row) * V;
@@ -430,7 +443,7 @@ __global__ void __launch_bounds__(kRowThreads, kRowCtasPerSm) sample_stats_row_k
                 if (c0 + u * kRowWarps < nch && leaf(c0 + u * kRowWarps) < V)
                     max_leaves(scaled<kUnitT>(y[u], T), m, mn);
         }
-        M = finish_max(m, mn);
+        M = finish_max(m, mn, nrm);
     }
     const uint64_t pol = l2_evict_first_policy();
     for (; row < nrows; row += gridDim.x) {
@@ -472,8 +485,12 @@ __global__ void __launch_bounds__(kRowThreads, kRowCtasPerSm) sample_stats_row_k
                 float4 e = make_float4(0.f, 0.f, 0.f, 0.f);
                 if (kFull || (c < nch && v < V)) {
                     const float4 z = scaled<kUnitT>(x[u], T);
-                    e = make_float4(sv_exp_nb(__fsub_rn(z.x, M)), sv_exp_nb(__fsub_rn(z.y, M)),
-                                    sv_exp_nb(__fsub_rn(z.z, M)), sv_exp_nb(__fsub_rn(z.w, M)));
+                    const float4 d = make_float4(__fsub_rn(z.x, M), __fsub_rn(z.y, M), __fsub_rn(z.z, M),
+                                                 __fsub_rn(z.w, M));
+                    if (nrm)   // CTA-uniform: the row's exponentials are all normal
+                        e = make_float4(sv_exp_nrm(d.x), sv_exp_nrm(d.y), sv_exp_nrm(d.z), sv_exp_nrm(d.w));
+                    else
+                        e = make_float4(sv_exp_nb(d.x), sv_exp_nb(d.y), sv_exp_nb(d.z), sv_exp_nb(d.w));
                 }
                 q[u] = quad_sum(e);
             }
@@ -509,22 +526,6 @@ __global__ void __launch_bounds__(kRowThreads, kRowCtasPerSm) sample_stats_row_k
         using Full = std::true_type;
         using Edge = std::false_type;
         int c0 = warp;
-#if SV_ROW_PIPE
-        // two register sets: the loads of the next chunks go out before the
-        // current ones are summed, so each has a whole iteration to land
-        float4 xa[kRowFuse], ya[kRowFuse], xb[kRowFuse], yb[kRowFuse];
-        load(Edge{}, c0, xa, ya);
-        while (true) {
-            load(Edge{}, c0 + kStep, xb, yb);
-            work(Edge{}, xa, ya, c0);
-            c0 += kStep;
-            if (c0 >= nch) break;
-            load(Edge{}, c0 + kStep, xa, ya);
-            work(Edge{}, xb, yb, c0);
-            c0 += kStep;
-            if (c0 >= nch) break;
-        }
-#else
         for (; c0 + (kRowFuse - 1) * kRowWarps < nfull; c0 += kStep) {
             float4 x[kRowFuse], y[kRowFuse];
             load(Full{}, c0, x, y);
@@ -535,7 +536,6 @@ __global__ void __launch_bounds__(kRowThreads, kRowCtasPerSm) sample_stats_row_k
             load(Edge{}, c0, x, y);
             work(Edge{}, x, y, c0);
         }
-#endif
         __syncthreads();   // csum complete; wred of this row's M no longer read
         // block sums (level 12); blocks beyond the vocab are zero
         for (int bk = warp; bk < kMaxBlocks; bk += kRowWarps) {
@@ -550,7 +550,7 @@ __global__ void __launch_bounds__(kRowThreads, kRowCtasPerSm) sample_stats_row_k
                 stats[row] = make_float2(M, Z);
             }
         }
-        if (more) M = finish_max(m, mn);   // its barrier also orders bsum's reuse
+        if (more) M = finish_max(m, mn, nrm);   // its barrier also orders bsum's reuse
         __syncthreads();                   // wred, csum and bsum are reused by the next row
     }
 }
@@ -1063,11 +1063,15 @@ __global__ void diag_exp_kernel(const float* x, float* y, int64_t n) {
     for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
          i += static_cast<int64_t>(gridDim.x) * blockDim.x)
     {
-        // the branch-free form used by the softmax passes must agree bit for
-        // bit wherever it is defined; a disagreement shows up as 12345
+        // the branch-free and the normal-range forms used by the softmax
+        // passes must agree bit for bit wherever each is defined; a
+        // disagreement shows up as 12345
         const float e = sv_exp(x[i]);
         const bool defined = !(x[i] != x[i]) && x[i] <= 0.0f;
-        y[i] = (defined && __float_as_uint(sv_exp_nb(x[i])) != __float_as_uint(e)) ? 12345.0f : e;
+        const bool normal = defined && x[i] > kExpNormalMin;
+        const bool bad = (defined && __float_as_uint(sv_exp_nb(x[i])) != __float_as_uint(e)) ||
+                         (normal && __float_as_uint(sv_exp_nrm(x[i])) != __float_as_uint(e));
+        y[i] = bad ? 12345.0f : e;
     }
 }
 

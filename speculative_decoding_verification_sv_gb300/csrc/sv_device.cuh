@@ -491,6 +491,43 @@ __device__ __forceinline__ float sv_exp_nb(float x) {
     return __fmul_rn(__fmul_rn(s, __int_as_float((k + 64 + 127) << 23)), __int_as_float((127 - 64) << 23));
 }
 
+// sv_exp for -86.5 < x <= 0, where every result is a normal number: the same
+// reduction and polynomial, then s * 2^k as an addition of k to the exponent
+// field of s.  There, k >= -125 and s lies in [0.707, 1.415], so s * 2^k is
+// normal and the multiplication by 2^k is exact: the field addition gives the
+// same bits as sv_exp's rounded product, without the clamp and the two
+// multiplies of sv_exp_nb.
+__device__ __forceinline__ float sv_exp_nrm(float x) {
+    const float kInvLn2 = 1.44269504088896340736f;
+    const float kLn2Head = 0.693145751953125f;
+    const float kLn2Tail = 1.428606820309417232e-06f;
+    const float kRound = 12582912.0f;   // as in sv_exp
+    const float t = __fadd_rn(__fmul_rn(x, kInvLn2), kRound);
+    const float n = __fsub_rn(t, kRound);
+    float r = __fmaf_rn(-n, kLn2Head, x);
+    r = __fmaf_rn(-n, kLn2Tail, r);
+    float s = 1.0f / 5040.0f;
+    s = __fmaf_rn(s, r, 1.0f / 720.0f);
+    s = __fmaf_rn(s, r, 1.0f / 120.0f);
+    s = __fmaf_rn(s, r, 1.0f / 24.0f);
+    s = __fmaf_rn(s, r, 1.0f / 6.0f);
+    s = __fmaf_rn(s, r, 0.5f);
+    s = __fmaf_rn(s, r, 1.0f);
+    s = __fmaf_rn(s, r, 1.0f);
+    const uint32_t k = __float_as_uint(t) - __float_as_uint(kRound);   // two's complement of k
+    return __uint_as_float(__float_as_uint(s) + (k << 23));
+}
+
+// Lower bound of the arguments sv_exp_nrm takes.
+constexpr float kExpNormalMin = -86.5f;
+
+// Two-input minimum that is NaN if either input is NaN.
+__device__ __forceinline__ float fmin_nan(float a, float b) {
+    float r;
+    asm("min.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+    return r;
+}
+
 // --------------------------------------------------------------------------
 // Philox4x32-10
 // --------------------------------------------------------------------------

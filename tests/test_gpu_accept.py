@@ -138,6 +138,26 @@ def test_sample_many_rows_pipelined(sv, B, k, V, T):
     assert sv.get_device_error() == 0
 
 
+@pytest.mark.parametrize("T", [1.0, 0.8])
+def test_sample_many_rows_wide_and_narrow(sv, T):
+    """Rows whose z - M all lie above -86.5 (every exp(z - M) a normal number)
+    and rows spanning far more, interleaved over the statistics CTAs: both
+    forms of the exponential must give the oracle's bits."""
+    B, k, V = 40, 8, 20000
+    rng = np.random.default_rng(17)
+    logits = rng.standard_normal((B, k + 1, V)).astype(np.float32) * 2
+    wide = (np.arange(B * (k + 1)).reshape(B, k + 1) % 3) == 0
+    logits[wide] *= 25                     # std 50: spans a few hundred
+    logits[1, 2, :5] = -90.0               # just past the normal range, one row
+    logits[2, 3, 7] = -80.0                # inside it
+    lg = torch.from_numpy(logits)
+    si = synth.sample_inputs(B, k, V, wid=130, logits=lg, logit_std=2.0)
+    got = sv.accept_sample(lg.cuda(), si.q.cuda(), si.tok.cuda(), temperature=T, seed=5, step=1)
+    exp = oracle.accept_sample(logits, si.q.numpy(), si.tok.numpy(), temperature=T, seed=5, step=1)
+    assert_same(got, exp, "sample wide and narrow rows")
+    assert sv.get_device_error() == 0
+
+
 def test_sample_many_rows_nonfinite_flagged(sv):
     # a non-finite logit in a row whose maximum is taken ahead, under the
     # previous row's sums (rows past the first wave of CTAs)

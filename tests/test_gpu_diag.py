@@ -24,6 +24,9 @@ def test_exp_bit_exact_dense(sv):
         rng.uniform(-104.0, 0.0, 2_000_000).astype(np.float32),
         -np.abs(rng.standard_normal(500_000).astype(np.float32)) * 1e-3,
         np.array([0.0, -0.0, -1e-30, -87.3, -88.0, -103.99, -104.0, -104.01, -np.inf, np.nan], np.float32),
+        # around the lower end of the normal-range form (-86.5) and its k = -125
+        np.nextafter(np.float32(-86.5), np.float32(0), dtype=np.float32)[None],
+        np.array([-86.5, -86.49, -86.0, -86.64, -86.65, -86.99, -87.0], np.float32),
     ])
     got = sv.diag_exp(torch.from_numpy(xs).cuda()).cpu().numpy()
     ref = oracle.exp32_array(xs)
