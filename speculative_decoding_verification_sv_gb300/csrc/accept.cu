@@ -26,6 +26,7 @@
 #include <limits.h>
 #include <stdlib.h>
 
+#include <mutex>
 #include <type_traits>
 
 #include "sv_device.cuh"
@@ -324,30 +325,33 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads)
     }
 }
 
-// Many rows (B*R large): persistent CTAs, one per SM, each taking whole rows
-// (row blockIdx.x, + gridDim.x, ...), no cluster and no staging.  A row needs
-// two passes: the exact maximum of z = l / T, then the canonical tree over
-// exp(z - M) -- chunk sums over 128 leaves (4 per lane), block sums over 32
-// chunks, then the 64 zero-padded block sums.  The two are software
-// pipelined across the CTA's rows: one loop over the chunks re-reads row i
-// (from L2, where its own max pass left it) for the exponential sums and
-// reads row i + 1 from HBM for its maximum, so the DRAM stream of the next
-// row runs under the issue-bound exponentials of the current one.  The
-// re-read carries an evict-first L2 policy: a chunk is dead once summed, so
-// the lines of row i that are still to be read outlive it, and the two rows
-// in flight per SM (2 x 152 x 600 KB) need only about one row's worth of L2.
+// Many rows (B*R large): persistent pairs of CTAs (2-CTA clusters), each pair
+// taking whole rows (row = cluster, + clusters, ...), each CTA one half of the
+// row's 4096-leaf blocks.  A row needs two passes: the exact maximum of
+// z = l / T, then the canonical tree over exp(z - M) -- chunk sums over 128
+// leaves (4 per lane), block sums over 32 chunks, then the 64 zero-padded
+// block sums.  The two are software pipelined across the pair's rows: one
+// loop over the chunks re-reads row i (from L2, where its own max pass left
+// it) for the exponential sums and reads row i + 1 from HBM for its maximum,
+// so the DRAM stream of the next row runs under the issue-bound
+// exponentials of the current one.  Splitting each row over two SMs halves
+// the rows in flight (about 2 x 76 x 600 KB), so the re-read stays in L2; the
+// halves' block sums and maxima meet through distributed shared memory, one
+// cluster barrier per row.  The re-read carries an evict-first L2 policy (a
+// summed chunk is dead).
 #ifndef SV_ROW_THREADS
-#define SV_ROW_THREADS 1024
+#define SV_ROW_THREADS 768
 #endif
 #ifndef SV_ROW_FUSE
 #define SV_ROW_FUSE 4
 #endif
-constexpr int kRowThreads = SV_ROW_THREADS;       // one CTA of 32 warps per SM (latency hiding)
+constexpr int kRowThreads = SV_ROW_THREADS;       // one CTA of 24 warps per SM (80 registers: no spills)
 constexpr int kRowCtasPerSm = kRowThreads >= 512 ? 1 : 512 / kRowThreads;
 constexpr int kRowWarps = kRowThreads / 32;
 static_assert(kRowWarps <= 32, "one warp's lanes reduce the CTA's warps");
 constexpr int kRowFuse = SV_ROW_FUSE;             // chunks in flight per warp and row
 static_assert(kRowFuse == 2 || kRowFuse == 4, "two or four chunks per warp and row");
+constexpr int kRowPair = 2;                       // CTAs per row
 
 __device__ __forceinline__ uint64_t l2_evict_first_policy() {
     uint64_t pol;
@@ -380,25 +384,34 @@ __device__ __forceinline__ void max_leaves(float4 z, float& m, float& mn) {
 }
 
 template <bool kUnitT>
-__global__ void __launch_bounds__(kRowThreads, kRowCtasPerSm) sample_stats_row_kernel(const float* __restrict__ logits, int V,
-                                                                         float T, int nblk, int nrows,
-                                                                         float2* __restrict__ stats,
-                                                                         unsigned int* err) {
-    pdl_wait();   // inputs come from the kernels before this one
+__global__ void __cluster_dims__(kRowPair, 1, 1) __launch_bounds__(kRowThreads, kRowCtasPerSm)
+    sample_stats_row_kernel(const float* __restrict__ logits, int V, float T, int nblk, int nrows,
+                            float2* __restrict__ stats, unsigned int* err) {
+    cluster_arrive_relaxed();   // the partner's shared memory is written only after it has started
+    pdl_wait();                 // inputs come from the kernels before this one
     pdl_launch_dependents();
     __shared__ float csum[kMaxBlocks * kChunksPerBlk];
-    __shared__ float bsum[kMaxBlocks];
+    __shared__ float bsum[2][kMaxBlocks];    // rank 0: the row's block sums, by row parity
+    __shared__ float2 xch[2][kRowPair];      // (max, NaN-propagating min) of each half, by parity
     __shared__ float wred[kRowWarps];
     __shared__ float wmin[kRowWarps];
+    cg::cluster_group cluster = cg::this_cluster();
+    const int rank = static_cast<int>(cluster.block_rank());
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int nch = nblk * kChunksPerBlk;
-    const int nfull = V / kChunk;   // chunks whose 128 leaves all lie below V
+    // this CTA's blocks [b0, b1) and chunks [cb0, cb1); chunks below cfull
+    // have all 128 leaves below V
+    const int hb = (nblk + 1) / 2;
+    const int b0 = min(nblk, rank * hb), b1 = min(nblk, b0 + hb);
+    const int cb0 = b0 * kChunksPerBlk, cb1 = b1 * kChunksPerBlk;
+    const int cfull = min(cb1, V / kChunk);
     const float4 ninf4 = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+    if (rank == 0)
+        for (int i = tid; i < 2 * kMaxBlocks; i += kRowThreads) bsum[i / kMaxBlocks][i % kMaxBlocks] = 0.0f;
     // the warp's chunks c0 + u * kRowWarps; lane holds leaves 4 lane .. of each
     auto leaf = [&](int c) { return c * kChunk + 4 * lane; };
-    // CTA-wide maximum of the per-thread m (every thread gets it); flags
-    // non-finite z; nrm: every z - M of the row lies where sv_exp_nrm applies
-    auto finish_max = [&](float m, float mn, bool& nrm) {
+    // the CTA's (max, min) of the next row by warp 0 and lane 0 of each warp
+    // (after the barrier that follows), then into both CTAs' slot `rank`
+    auto warp_minmax = [&](float m, float mn) {
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) {
             m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
@@ -408,47 +421,61 @@ __global__ void __launch_bounds__(kRowThreads, kRowCtasPerSm) sample_stats_row_k
             wred[warp] = m;
             wmin[warp] = mn;
         }
-        __syncthreads();
-        // every warp reduces the warps' values itself: lane l takes warp l's
-        float M = lane < kRowWarps ? wred[lane] : -INFINITY;
-        float zmin = lane < kRowWarps ? wmin[lane] : INFINITY;
+    };
+    auto publish_minmax = [&](int p) {   // warp 0, after a barrier over the warps' values
+        float m = lane < kRowWarps ? wred[lane] : -INFINITY;
+        float mn = lane < kRowWarps ? wmin[lane] : INFINITY;
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) {
-            M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-            zmin = fmin_nan(zmin, __shfl_xor_sync(0xffffffffu, zmin, off));
+            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+            mn = fmin_nan(mn, __shfl_xor_sync(0xffffffffu, mn, off));
         }
-        if (tid == 0 && (M == INFINITY || !(zmin > -INFINITY))) raise_error(err, SV_DEVERR_NONFINITE);
+        if (lane < kRowPair) *cluster.map_shared_rank(&xch[p][rank], lane) = make_float2(m, mn);
+    };
+    // the row's M after the cluster barrier; flags non-finite z; nrm: every
+    // z - M of the row lies where sv_exp_nrm applies
+    auto take_max = [&](int p, bool& nrm) {
+        const float2 h0 = xch[p][0], h1 = xch[p][1];
+        const float M = fmaxf(h0.x, h1.x), zmin = fmin_nan(h0.y, h1.y);
+        if (tid == 0 && rank == 0 && (M == INFINITY || !(zmin > -INFINITY))) raise_error(err, SV_DEVERR_NONFINITE);
         // z - M >= zmin - M for every z (rounding is monotonic); false for NaN
         nrm = __fsub_rn(zmin, M) > kExpNormalMin;
         return M;
     };
 
-    int row = blockIdx.x;
-    if (row >= nrows) return;
+    const int ncl = static_cast<int>(gridDim.x) / kRowPair;
+    int row = static_cast<int>(blockIdx.x) / kRowPair;
+    cluster_wait();
+    if (row >= nrows) return;   // both CTAs of the pair
     float M;
     bool nrm;
     {
         // prologue: the first row's maximum alone, twice the loads in flight
         const float* L = logits + static_cast<size_t>(row) * V;
         float m = -INFINITY, mn = INFINITY;
-        for (int c0 = warp; c0 < nch; c0 += 2 * kRowFuse * kRowWarps) {
+        for (int c0 = cb0 + warp; c0 < cb1; c0 += 2 * kRowFuse * kRowWarps) {
             float4 y[2 * kRowFuse];
 #pragma unroll
             for (int u = 0; u < 2 * kRowFuse; ++u) {
                 const int c = c0 + u * kRowWarps, v = leaf(c);
-                y[u] = (c < nch && v < V) ? __ldg(reinterpret_cast<const float4*>(L + v)) : ninf4;
+                y[u] = (c < cb1 && v < V) ? __ldg(reinterpret_cast<const float4*>(L + v)) : ninf4;
             }
 #pragma unroll
             for (int u = 0; u < 2 * kRowFuse; ++u)
-                if (c0 + u * kRowWarps < nch && leaf(c0 + u * kRowWarps) < V)
+                if (c0 + u * kRowWarps < cb1 && leaf(c0 + u * kRowWarps) < V)
                     max_leaves(scaled<kUnitT>(y[u], T), m, mn);
         }
-        M = finish_max(m, mn, nrm);
+        warp_minmax(m, mn);
+        __syncthreads();
+        if (warp == 0) publish_minmax(1);
+        cluster.sync();
+        M = take_max(1, nrm);
     }
     const uint64_t pol = l2_evict_first_policy();
-    for (; row < nrows; row += gridDim.x) {
-        const int nxt = row + gridDim.x;
-        const bool more = nxt < nrows;   // CTA-uniform
+    for (int it = 0; row < nrows; row += ncl, ++it) {
+        const int p = it & 1;
+        const int nxt = row + ncl;
+        const bool more = nxt < nrows;   // uniform over the pair
         const float* L = logits + static_cast<size_t>(row) * V;
         const float* Ln = logits + static_cast<size_t>(more ? nxt : row) * V;
         float m = -INFINITY, mn = INFINITY;
@@ -459,13 +486,13 @@ __global__ void __launch_bounds__(kRowThreads, kRowCtasPerSm) sample_stats_row_k
 #pragma unroll
             for (int u = 0; u < kRowFuse; ++u) {
                 const int c = c0 + u * kRowWarps, v = leaf(c);
-                x[u] = (kFull || (c < nch && v < V)) ? ldg_policy(L + v, pol) : make_float4(0.f, 0.f, 0.f, 0.f);
+                x[u] = (kFull || (c < cb1 && v < V)) ? ldg_policy(L + v, pol) : make_float4(0.f, 0.f, 0.f, 0.f);
             }
             if (more) {
 #pragma unroll
                 for (int u = 0; u < kRowFuse; ++u) {
                     const int c = c0 + u * kRowWarps, v = leaf(c);
-                    y[u] = (kFull || (c < nch && v < V)) ? __ldg(reinterpret_cast<const float4*>(Ln + v)) : ninf4;
+                    y[u] = (kFull || (c < cb1 && v < V)) ? __ldg(reinterpret_cast<const float4*>(Ln + v)) : ninf4;
                 }
             }
         };
@@ -483,11 +510,11 @@ __global__ void __launch_bounds__(kRowThreads, kRowCtasPerSm) sample_stats_row_k
             for (int u = 0; u < kRowFuse; ++u) {
                 const int c = c0 + u * kRowWarps, v = leaf(c);
                 float4 e = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (kFull || (c < nch && v < V)) {
+                if (kFull || (c < cb1 && v < V)) {
                     const float4 z = scaled<kUnitT>(x[u], T);
                     const float4 d = make_float4(__fsub_rn(z.x, M), __fsub_rn(z.y, M), __fsub_rn(z.z, M),
                                                  __fsub_rn(z.w, M));
-                    if (nrm)   // CTA-uniform: the row's exponentials are all normal
+                    if (nrm)   // uniform: the row's exponentials are all normal
                         e = make_float4(sv_exp_nrm(d.x), sv_exp_nrm(d.y), sv_exp_nrm(d.z), sv_exp_nrm(d.w));
                     else
                         e = make_float4(sv_exp_nb(d.x), sv_exp_nb(d.y), sv_exp_nb(d.z), sv_exp_nb(d.w));
@@ -512,46 +539,48 @@ __global__ void __launch_bounds__(kRowThreads, kRowCtasPerSm) sample_stats_row_k
             }
             {
                 const int c = c0 + (lane % kRowFuse) * kRowWarps;
-                if (lane < kRowFuse && (kFull || c < nch)) csum[c] = w;
+                if (lane < kRowFuse && (kFull || c < cb1)) csum[c] = w;
             }
             // row i + 1: its maximum
             if (more) {
 #pragma unroll
                 for (int u = 0; u < kRowFuse; ++u)
-                    if (kFull || (c0 + u * kRowWarps < nch && leaf(c0 + u * kRowWarps) < V))
+                    if (kFull || (c0 + u * kRowWarps < cb1 && leaf(c0 + u * kRowWarps) < V))
                         max_leaves(scaled<kUnitT>(y[u], T), m, mn);
             }
         };
         constexpr int kStep = kRowFuse * kRowWarps;
         using Full = std::true_type;
         using Edge = std::false_type;
-        int c0 = warp;
-        for (; c0 + (kRowFuse - 1) * kRowWarps < nfull; c0 += kStep) {
+        int c0 = cb0 + warp;
+        for (; c0 + (kRowFuse - 1) * kRowWarps < cfull; c0 += kStep) {
             float4 x[kRowFuse], y[kRowFuse];
             load(Full{}, c0, x, y);
             work(Full{}, x, y, c0);
         }
-        for (; c0 < nch; c0 += kStep) {
+        for (; c0 < cb1; c0 += kStep) {
             float4 x[kRowFuse], y[kRowFuse];
             load(Edge{}, c0, x, y);
             work(Edge{}, x, y, c0);
         }
-        __syncthreads();   // csum complete; wred of this row's M no longer read
-        // block sums (level 12); blocks beyond the vocab are zero
-        for (int bk = warp; bk < kMaxBlocks; bk += kRowWarps) {
-            const float bs = bk < nblk ? warp_tree_sum(csum[bk * kChunksPerBlk + lane]) : 0.0f;
-            if (lane == 0) bsum[bk] = bs;
+        if (more) warp_minmax(m, mn);
+        __syncthreads();   // csum, wred and wmin complete
+        // this half's block sums (level 12) into rank 0's; blocks beyond the
+        // vocab stay zero
+        for (int bk = b0 + warp; bk < b1; bk += kRowWarps) {
+            const float bs = warp_tree_sum(csum[bk * kChunksPerBlk + lane]);
+            if (lane == 0) *cluster.map_shared_rank(&bsum[p][bk], 0) = bs;   // rank 0's
         }
-        __syncthreads();
-        if (warp == 0) {
-            const float Z = warp_tree_sum(__fadd_rn(bsum[2 * lane], bsum[2 * lane + 1]));   // level 13 -> 18
+        if (more && warp == 0) publish_minmax(p);
+        cluster.sync();    // both halves' block sums and next-row maxima are in place
+        if (rank == 0 && warp == 0) {
+            const float Z = warp_tree_sum(__fadd_rn(bsum[p][2 * lane], bsum[p][2 * lane + 1]));   // level 13 -> 18
             if (lane == 0) {
                 if (!(Z > 0.0f) || !isfinite(Z)) raise_error(err, SV_DEVERR_NONFINITE);
                 stats[row] = make_float2(M, Z);
             }
         }
-        if (more) M = finish_max(m, mn, nrm);   // its barrier also orders bsum's reuse
-        __syncthreads();                   // wred, csum and bsum are reused by the next row
+        if (more) M = take_max(p, nrm);
     }
 }
 
@@ -1103,6 +1132,31 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads)
 
 int blocks_for(int V) { return (V + kBlk - 1) / kBlk; }
 
+// Pairs of statistics CTAs that can be resident at once (a cluster sits in
+// one GPC); SMs / 2 when the query fails.
+int row_pairs() {
+    static std::mutex mu;
+    static int cache[64] = {};
+    int dev = 0;
+    const int fallback = device_sm_count() * kRowCtasPerSm / kRowPair > 0 ? device_sm_count() * kRowCtasPerSm / kRowPair
+                                                                            : 1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+        cudaGetLastError();
+        return fallback;
+    }
+    std::lock_guard<std::mutex> lk(mu);
+    if (cache[dev]) return cache[dev];
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(kRowPair, 1, 1);
+    cfg.blockDim = dim3(kRowThreads, 1, 1);
+    cfg.dynamicSmemBytes = 0;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, sample_stats_row_kernel<true>, &cfg) != cudaSuccess) n = 0;
+    cudaGetLastError();
+    cache[dev] = n > 0 ? n : fallback;
+    return cache[dev];
+}
+
 }  // namespace
 
 size_t greedy_workspace(int B, int R, int V) {
@@ -1151,8 +1205,8 @@ cudaError_t launch_accept_sample(const float* logits, const float* q, int Vq, co
     // rows: one CTA per row keeps every SM busy without cluster waves.
     if (static_cast<int64_t>(B) * R >= kRowStatsMinRows)
     {
-        const int slots = device_sm_count() * kRowCtasPerSm;
-        const int nrows = B * R, grid = nrows < slots ? nrows : slots;
+        const int slots = row_pairs();
+        const int nrows = B * R, grid = kRowPair * (nrows < slots ? nrows : slots);
         e = temperature == 1.0f
                 ? launch_pdl(sample_stats_row_kernel<true>, dim3(grid), dim3(kRowThreads), 0, st, logits, V, temperature,
                              nblk, nrows, stats, err)
