@@ -1007,32 +1007,69 @@ __global__ void __launch_bounds__(kThreads) chain_sums_kernel(SampleArgs a, Chai
     float* sp = sr + kSumFloats;
     __shared__ float cr[kChunksPerBlk], cp[kChunksPerBlk];
     constexpr int kPer = kChunksPerBlk / kWarps;   // chunks per warp
+    static_assert(kPer == 4, "four chunks per warp: eight sums per lane");
     typename RowValues::Raw raw[kPer];
 #pragma unroll
     for (int i = 0; i < kPer; ++i) {
         const int v = blk * kBlk + (warp * kPer + i) * kChunk + 4 * lane;
-        if (v < V) raw[i] = rv.load4(v);
+        raw[i] = v < V ? rv.load4(v)
+                       : typename RowValues::Raw{make_float4(0.f, 0.f, 0.f, 0.f), make_float4(0.f, 0.f, 0.f, 0.f)};
     }
+    // d = z - M of the warp's 16 leaves per lane; the normal-range form of the
+    // exponential when all of them allow it (uniform over the warp; NaN: no)
+    float4 d[kPer];
+    float dmin = INFINITY;
 #pragma unroll
     for (int i = 0; i < kPer; ++i) {
-        const int c = warp * kPer + i;
-        const int v = blk * kBlk + c * kChunk + 4 * lane;
+        const int v = blk * kBlk + (warp * kPer + i) * kChunk + 4 * lane;
+        const float4 l = raw[i].l;
+        const float4 z = a.T == 1.0f ? l : make_float4(__fdiv_rn(l.x, a.T), __fdiv_rn(l.y, a.T), __fdiv_rn(l.z, a.T),
+                                                         __fdiv_rn(l.w, a.T));
+        d[i] = make_float4(__fsub_rn(z.x, ms.x), __fsub_rn(z.y, ms.x), __fsub_rn(z.z, ms.x), __fsub_rn(z.w, ms.x));
+        if (v < V) dmin = fmin_nan(dmin, fmin3_nan(d[i].x, d[i].y, fmin_nan(d[i].z, d[i].w)));
+    }
+    const bool nrm = __all_sync(0xffffffffu, dmin > kExpNormalMin);
+    // p = exp(z - M) / Z and the residual max(0, p - q) (the same operations
+    // as RowValues::one without sibling steps), then each lane's node over its
+    // 4 leaves of each chunk: sums 0-3 the residual's chunks, 4-7 p's
+    float sv8[2 * kPer];
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+        const int v = blk * kBlk + (warp * kPer + i) * kChunk + 4 * lane;
         float4 p = make_float4(0.f, 0.f, 0.f, 0.f), r = p;
         if (v < V) {
-            rv.residual = false;
-            p = rv.eval4(raw[i]);
+            auto ex = [&](float x) { return nrm ? sv_exp_nrm(x) : sv_exp_nb(x); };
+            p = make_float4(__fdiv_rn(ex(d[i].x), ms.y), __fdiv_rn(ex(d[i].y), ms.y), __fdiv_rn(ex(d[i].z), ms.y),
+                            __fdiv_rn(ex(d[i].w), ms.y));
             auto res = [](float w, float qv) {   // RowValues::one with residual: max(0, w - q)
-                const float d = __fsub_rn(w, qv);
-                return d > 0.0f ? d : 0.0f;
+                const float dd = __fsub_rn(w, qv);
+                return dd > 0.0f ? dd : 0.0f;
             };
             r = make_float4(res(p.x, raw[i].q.x), res(p.y, raw[i].q.y), res(p.z, raw[i].q.z), res(p.w, raw[i].q.w));
         }
-        const float csr = warp_tree_sum(quad_sum(r)), csp = warp_tree_sum(quad_sum(p));
-        if (lane == 0) {
-            cr[c] = csr;
-            cp[c] = csp;
-        }
+        sv8[i] = quad_sum(r);
+        sv8[kPer + i] = quad_sum(p);
     }
+    // the 32 lanes' trees of all eight sums at once: at each of the first
+    // three levels a lane keeps half of its sums and trades the other half
+    // with its partner (lanes l ^ 1, l ^ 2, l ^ 4), so lane l ends with sum
+    // l % 8; every node is still its two children's sum
+    const bool h1 = (lane & 1) != 0, h2 = (lane & 2) != 0, h4 = (lane & 4) != 0;
+    float w4[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+        w4[j] = __fadd_rn(h1 ? sv8[2 * j + 1] : sv8[2 * j],
+                          __shfl_xor_sync(0xffffffffu, h1 ? sv8[2 * j] : sv8[2 * j + 1], 1));
+    float w2[2];
+#pragma unroll
+    for (int j = 0; j < 2; ++j)
+        w2[j] = __fadd_rn(h2 ? w4[2 * j + 1] : w4[2 * j],
+                          __shfl_xor_sync(0xffffffffu, h2 ? w4[2 * j] : w4[2 * j + 1], 2));
+    float t = __fadd_rn(h4 ? w2[1] : w2[0], __shfl_xor_sync(0xffffffffu, h4 ? w2[0] : w2[1], 4));
+    t = __fadd_rn(t, __shfl_xor_sync(0xffffffffu, t, 8));
+    t = __fadd_rn(t, __shfl_xor_sync(0xffffffffu, t, 16));
+    if (lane < kPer) cr[warp * kPer + lane] = t;
+    else if (lane < 2 * kPer) cp[warp * kPer + lane - kPer] = t;
     __syncthreads();
     if (warp == 0) {
         const float br = warp_tree_sum(cr[lane]), bp = warp_tree_sum(cp[lane]);
