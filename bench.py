@@ -50,14 +50,14 @@ TRAFFIC = {
     # ncu --set full, 28-layer 1.5B round, LM head N=5 H=1536 V=151936
     ("1", "lm_head"): {"bytes": 466809856 + 5381632, "src": "lm_head.cu", "src_hash": "f74183b9259d0f09"},
     # ncu --set full, 7B batch-16 layer (2-layer case, same per-layer launch)
-    ("3b16", "verify_attn"): {"bytes": 269842432 + 3261696, "src": "verify_attn.cu",
-                              "src_hash": "b81f585a7d44226b"},
-    ("3b16s", "verify_attn"): {"bytes": 269842432 + 3261696, "src": "verify_attn.cu",
-                               "src_hash": "b81f585a7d44226b"},
-    # ncu --set full, sampled B64 k8: statistics pass + chain residual pass (the
-    # walk and draw launches move < 0.1 MB and were not captured)
-    ("2", "accept_sampled"): {"bytes": 381219840 + 3627520 + 77820672 + 1609984, "src": "accept.cu",
-                              "src_hash": "a1b4dfc0598b8c78"},
+    ("3b16", "verify_attn"): {"bytes": 269856256 + 3631360, "src": "verify_attn.cu",
+                              "src_hash": "450f22856ba2c178"},
+    ("3b16s", "verify_attn"): {"bytes": 269856256 + 3631360, "src": "verify_attn.cu",
+                               "src_hash": "450f22856ba2c178"},
+    # ncu --set full, sampled B64 k8: the four launches of one acceptance
+    # (statistics, walk, residual pass, draw)
+    ("2", "accept_sampled"): {"bytes": 350172160 + 3333376 + 146688 + 77825024 + 1473536 + 126464,
+                              "src": "accept.cu", "src_hash": "1d83bc8614be787a"},
 }
 
 
