@@ -125,12 +125,14 @@ def test_sample_chain_injected_uniforms(sv):
         assert_same(got, exp, "sample chain uniforms")
 
 
-@pytest.mark.parametrize("B,k,V,T", [(48, 8, 4100, 0.7), (40, 7, 151936, 1.0), (33, 8, 20000, 1.3)])
+@pytest.mark.parametrize("B,k,V,T", [(48, 8, 4100, 0.7), (40, 7, 151936, 1.0), (33, 8, 20000, 1.3),
+                                     (20, 8, 4096, 1.0), (24, 8, 1000, 0.9)])
 def test_sample_many_rows_pipelined(sv, B, k, V, T):
-    """Enough rows that the statistics CTAs take several rows each (the next
-    row's maximum is read in the loop over the current row's sums): a ragged
-    last chunk, temperatures other than 1, row counts that leave some CTAs a
-    row short."""
+    """Enough rows that the statistics CTA pairs take several rows each (the
+    next row's maximum is read in the loop over the current row's sums): a
+    ragged last chunk, temperatures other than 1, row counts that leave some
+    pairs a row short, and one-block rows (V <= 4096: the pair's second CTA
+    holds no chunk)."""
     si = _sample_case(B, k, V, seed=B + k, std=2.0)
     got = sv.accept_sample(si.logits.cuda(), si.q.cuda(), si.tok.cuda(), temperature=T, seed=77, step=3)
     exp = oracle.accept_sample(si.logits.numpy(), si.q.numpy(), si.tok.numpy(), temperature=T, seed=77, step=3)
