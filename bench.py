@@ -57,7 +57,7 @@ TRAFFIC = {
     # ncu --set full, sampled B64 k8: the four launches of one acceptance
     # (statistics, walk, residual pass, draw)
     ("2", "accept_sampled"): {"bytes": 350172160 + 3333376 + 146688 + 77825024 + 1473536 + 126464,
-                              "src": "accept.cu", "src_hash": "1d83bc8614be787a"},
+                              "src": "accept.cu", "src_hash": "23c8a8c8211445b1"},
 }
 
 

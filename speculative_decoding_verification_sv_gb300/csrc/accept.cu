@@ -345,7 +345,7 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads)
 #ifndef SV_ROW_FUSE
 #define SV_ROW_FUSE 4
 #endif
-constexpr int kRowThreads = SV_ROW_THREADS;       // one CTA of 24 warps per SM (80 registers: no spills)
+constexpr int kRowThreads = SV_ROW_THREADS;       // one CTA of 24 warps per SM (80 registers)
 constexpr int kRowCtasPerSm = kRowThreads >= 512 ? 1 : 512 / kRowThreads;
 constexpr int kRowWarps = kRowThreads / 32;
 static_assert(kRowWarps <= 32, "one warp's lanes reduce the CTA's warps");
