@@ -204,6 +204,25 @@ SV_API sv_status sv_accept_greedy(const float* logits, const int32_t* tok, const
                            void* ws, size_t ws_bytes, void* stream);
 
 /* ------------------------------------------------------------------------ */
+/* Relaxed, lossy acceptance ([SCS] sec. 7.2: the Delta-logit relaxation).   */
+/* ------------------------------------------------------------------------ */
+
+/* As sv_accept_greedy, but a draft passes when the gap between its parent
+ * row's top-1 logit and its own logit, one float32 subtraction
+ * fsub_rn(top1, logits[b][u][d]), is <= delta.  The walk, out_tok (the top-1
+ * of the row the walk stops at, lowest index on ties) and path are those of
+ * sv_accept_greedy; delta = 0 with a unique row maximum is greedy acceptance.
+ * LOSSY: the tokens no longer follow the target model exactly ([SCS] sec.
+ * 7.2 measured higher acceptance rates at that cost).
+ *   delta >= 0 (NaN or negative: SV_ERR_ARG); other arguments, the workspace
+ *   (from sv_accept_greedy_relaxed_workspace, caller-owned, any contents) and
+ *   the error flags as for sv_accept_greedy. */
+SV_API size_t sv_accept_greedy_relaxed_workspace(int32_t B, int32_t R, int32_t V);
+SV_API sv_status sv_accept_greedy_relaxed(const float* logits, const int32_t* tok, const int32_t* parent, int32_t B,
+                                   int32_t R, int32_t V, float delta, int32_t* n_acc, int32_t* out_tok,
+                                   int32_t* path, void* ws, size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------------------ */
 /* Modified rejection sampling ([TUT] sec. 2.2; [MINI] "Modified Rejection   */
 /* Sampling"; trees: [SUB] sec. 4.2).                                        */
 /* ------------------------------------------------------------------------ */

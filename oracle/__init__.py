@@ -66,6 +66,8 @@ def lib():
             L.orc_softmax.argtypes = [P, i32, f32, P]
             L.orc_accept_greedy.argtypes = [P, P, P, i32, i32, i32, P, P, P]
             L.orc_accept_greedy.restype = i32
+            L.orc_accept_greedy_relaxed.argtypes = [P, P, P, i32, i32, i32, f32, P, P, P]
+            L.orc_accept_greedy_relaxed.restype = i32
             L.orc_accept_sample.argtypes = [P, P, i32, P, P, i32, i32, i32, f32, u64, u64, P, P, P, P]
             L.orc_accept_sample.restype = i32
             L.orc_kv_commit.argtypes = [P, P, P, P, i32, i32, i32, i32, i32, i32, P, P, P]
@@ -156,6 +158,23 @@ def accept_greedy(logits, tok, parent=None):
     rc = lib().orc_accept_greedy(_p(logits), _p(tok), _p(parent), B, R, V, _p(n_acc), _p(out_tok), _p(path))
     if rc != 0:
         raise OracleError("orc_accept_greedy rejected its inputs")
+    return n_acc, out_tok, path
+
+
+def accept_greedy_relaxed(logits, tok, parent=None, delta=0.0):
+    """Lossy Delta-logit acceptance ([SCS] sec. 7.2): draft passes iff
+    top1 logit - draft logit <= delta (float32).  Shapes as accept_greedy."""
+    logits = _c(logits, np.float32)
+    B, R, V = logits.shape
+    tok = _c(tok, np.int32)
+    parent = _c(parent, np.int32)
+    n_acc = np.zeros(B, np.int32)
+    out_tok = np.zeros(B, np.int32)
+    path = np.zeros((B, R), np.int32)
+    rc = lib().orc_accept_greedy_relaxed(_p(logits), _p(tok), _p(parent), B, R, V, float(delta), _p(n_acc),
+                                         _p(out_tok), _p(path))
+    if rc != 0:
+        raise OracleError("orc_accept_greedy_relaxed rejected its inputs")
     return n_acc, out_tok, path
 
 

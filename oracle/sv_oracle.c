@@ -324,6 +324,54 @@ int orc_accept_greedy(const float* logits, const int32_t* tok, const int32_t* pa
 }
 
 /* ------------------------------------------------------------------------ */
+/* Relaxed, lossy acceptance ([SCS] sec. 7.2, the Delta-logit relaxation): a */
+/* draft passes when the target's top-1 logit exceeds the draft token's      */
+/* logit by at most delta.  The walk, the output token (the top-1 of the     */
+/* row the walk stops at) and the path are those of greedy acceptance; the   */
+/* output no longer follows the target model exactly.  The gap is one        */
+/* float32 subtraction.                                                      */
+/* ------------------------------------------------------------------------ */
+
+static int within_delta(const float* row, int top, int d, float delta) {
+    float gap = row[top] - row[d];
+    return gap <= delta;
+}
+
+int orc_accept_greedy_relaxed(const float* logits, const int32_t* tok, const int32_t* parent,
+                              int B, int R, int V, float delta, int32_t* n_acc, int32_t* out_tok,
+                              int32_t* path) {
+    if (B < 0 || R < 1 || V < 1 || !(delta >= 0.0f)) return ORC_ERR;
+    for (int b = 0; b < B; ++b) {
+        const float* L = logits + (size_t)b * R * V;
+        const int32_t* tk = tok + (size_t)b * R;
+        int32_t* pth = path + (size_t)b * R;
+        for (int j = 0; j < R; ++j) pth[j] = -1;
+        for (int j = 1; j < R; ++j)
+            if (tk[j] < 0 || tk[j] >= V) return ORC_ERR;
+        if (parent != NULL && check_tree(parent + (size_t)b * R, R) != ORC_OK) return ORC_ERR;
+        /* from the root (row 0), into the first child in index order that
+         * passes the test against its parent's row */
+        int u = 0, depth = 0;
+        pth[0] = 0;
+        for (;;) {
+            const float* row = L + (size_t)u * V;
+            int top = argmax_lowest(row, V);
+            int next = -1;
+            for (int c = u + 1; c < R; ++c) {
+                int child = parent == NULL ? (c == u + 1) : (parent[(size_t)b * R + c] == u);
+                if (child && within_delta(row, top, tk[c], delta)) { next = c; break; }
+            }
+            if (next < 0) break;
+            u = next;
+            pth[++depth] = u;
+        }
+        n_acc[b] = depth;
+        out_tok[b] = argmax_lowest(L + (size_t)u * V, V);
+    }
+    return ORC_OK;
+}
+
+/* ------------------------------------------------------------------------ */
 /* Modified rejection sampling ([TUT] sec. 2.2; [MINI] "Modified Rejection   */
 /* Sampling").                                                               */
 /* ------------------------------------------------------------------------ */

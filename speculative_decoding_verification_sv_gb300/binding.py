@@ -52,6 +52,9 @@ def _load():
     L.sv_accept_greedy_workspace.argtypes = [_I32, _I32, _I32]
     L.sv_accept_greedy_workspace.restype = _SZ
     L.sv_accept_greedy.argtypes = [_P, _P, _P, _I32, _I32, _I32, _P, _P, _P, _P, _SZ, _P]
+    L.sv_accept_greedy_relaxed_workspace.argtypes = [_I32, _I32, _I32]
+    L.sv_accept_greedy_relaxed_workspace.restype = _SZ
+    L.sv_accept_greedy_relaxed.argtypes = [_P, _P, _P, _I32, _I32, _I32, ctypes.c_float, _P, _P, _P, _P, _SZ, _P]
     L.sv_accept_sample_workspace.argtypes = [_I32, _I32, _I32]
     L.sv_accept_sample_workspace.restype = _SZ
     L.sv_accept_sample.argtypes = [_P, _P, _I32, _P, _P, _I32, _I32, _I32, _F32, _U64, _U64, _P, _P, _P, _P, _P,
@@ -62,7 +65,8 @@ def _load():
     L.sv_diag_exp.argtypes = [_P, _P, _I64, _P]
     L.sv_diag_philox.argtypes = [_P, _P, _P, _I64, _P]
     L.sv_diag_canon.argtypes = [_P, _I32, _I32, _P, _P, _P, _P]
-    for fn in ("sv_verify_attn", "sv_verify_attn_ex", "sv_lm_head", "sv_lm_head_ex", "sv_accept_greedy", "sv_accept_sample",
+    for fn in ("sv_verify_attn", "sv_verify_attn_ex", "sv_lm_head", "sv_lm_head_ex", "sv_accept_greedy",
+               "sv_accept_greedy_relaxed", "sv_accept_sample",
                "sv_accept_sample_noalloc", "sv_kv_commit",
                "sv_diag_exp", "sv_diag_philox", "sv_diag_canon", "sv_get_device_error"):
         getattr(L, fn).restype = ctypes.c_int
@@ -181,6 +185,21 @@ def accept_greedy(logits, tok, parent=None, n_acc=None, out_tok=None, path=None,
     _check("sv_accept_greedy", lib.sv_accept_greedy(
         _ptr(logits, torch.float32, "logits"), _ptr(tok, i32, "tok"), _ptr(parent, i32, "parent"), B, R, V,
         _ptr(n_acc, i32), _ptr(out_tok, i32), _ptr(path, i32), _ptr(ws), nbytes, _stream(stream)))
+    return n_acc, out_tok, path
+
+
+def accept_greedy_relaxed(logits, tok, parent=None, delta=0.0, n_acc=None, out_tok=None, path=None, ws=None,
+                          stream=None):
+    """Lossy Delta-logit acceptance: as accept_greedy, but a draft passes when
+    its parent row's top-1 logit exceeds its logit by at most delta."""
+    B, R, V = logits.shape
+    n_acc, out_tok, path = _accept_outputs(B, R, logits.device, n_acc, out_tok, path)
+    nbytes = int(lib.sv_accept_greedy_relaxed_workspace(B, R, V))
+    ws = _ws(nbytes, logits.device, ws)
+    i32 = torch.int32
+    _check("sv_accept_greedy_relaxed", lib.sv_accept_greedy_relaxed(
+        _ptr(logits, torch.float32, "logits"), _ptr(tok, i32, "tok"), _ptr(parent, i32, "parent"), B, R, V,
+        float(delta), _ptr(n_acc, i32), _ptr(out_tok, i32), _ptr(path, i32), _ptr(ws), nbytes, _stream(stream)))
     return n_acc, out_tok, path
 
 

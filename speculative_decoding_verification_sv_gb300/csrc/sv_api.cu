@@ -196,6 +196,23 @@ sv_status sv_accept_greedy(const float* logits, const int32_t* tok, const int32_
         sv::launch_accept_greedy(logits, tok, parent, B, R, V, n_acc, out_tok, path, ws, as_stream(stream)));
 }
 
+size_t sv_accept_greedy_relaxed_workspace(int32_t B, int32_t R, int32_t V) {
+    if (B < 1 || R < 1 || V < 1) return 0;
+    return sv::relaxed_workspace(B, R, V);
+}
+
+sv_status sv_accept_greedy_relaxed(const float* logits, const int32_t* tok, const int32_t* parent, int32_t B,
+                                   int32_t R, int32_t V, float delta, int32_t* n_acc, int32_t* out_tok,
+                                   int32_t* path, void* ws, size_t ws_bytes, void* stream) {
+    if (!logits || !tok || !n_acc || !out_tok || !path || !ws) return SV_ERR_ARG;
+    if (!(delta >= 0.0f)) return SV_ERR_ARG;   // negative or NaN
+    if (!aligned16(ws)) return SV_ERR_ARG;
+    if (B < 1 || R < 1 || R > 128 || V < 1 || static_cast<int64_t>(B) * R > 65535) return SV_ERR_SHAPE;
+    if (ws_bytes < sv::relaxed_workspace(B, R, V)) return SV_ERR_WORKSPACE;
+    return launch_status(sv::launch_accept_relaxed(logits, tok, parent, B, R, V, delta, n_acc, out_tok, path, ws,
+                                                   as_stream(stream)));
+}
+
 size_t sv_accept_sample_workspace(int32_t B, int32_t R, int32_t V) {
     if (B < 1 || R < 1 || V < 1) return 0;
     return sv::sample_workspace(B, R, V);

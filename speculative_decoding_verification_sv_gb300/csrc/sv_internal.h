@@ -39,6 +39,12 @@ size_t greedy_workspace(int B, int R, int V);
 cudaError_t launch_accept_greedy(const float* logits, const int32_t* tok, const int32_t* parent, int B, int R,
                                  int V, int32_t* n_acc, int32_t* out_tok, int32_t* path, void* ws,
                                  cudaStream_t st);
+// accept_relaxed.cu
+size_t relaxed_workspace(int B, int R, int V);
+cudaError_t launch_accept_relaxed(const float* logits, const int32_t* tok, const int32_t* parent, int B, int R, int V,
+                                  float delta, int32_t* n_acc, int32_t* out_tok, int32_t* path, void* ws,
+                                  cudaStream_t st);
+// accept.cu (sampled)
 size_t sample_workspace(int B, int R, int V);
 cudaError_t launch_accept_sample(const float* logits, const float* q, int Vq, const int32_t* tok,
                                  const int32_t* parent, int B, int R, int V, float temperature, uint64_t seed,

@@ -90,6 +90,12 @@ def test_host_validation_rejects_before_launch(lib):
     assert L.sv_accept_sample(*args) == 2
     # commit: R above 128
     assert L.sv_kv_commit(fake, fake, fake, fake, 28, 1, 2, 128, 4224, 200, fake, fake, fake, None) == 2
+    # relaxed acceptance: delta must be >= 0 and not NaN; short workspace
+    for bad in (-0.5, float("nan")):
+        assert L.sv_accept_greedy_relaxed(fake, fake, None, 1, 5, 151936, ctypes.c_float(bad), fake, fake, fake,
+                                          fake, 1 << 20, None) == 1
+    assert L.sv_accept_greedy_relaxed(fake, fake, None, 1, 5, 151936, ctypes.c_float(1.0), fake, fake, fake, fake,
+                                      8, None) == 4
 
 
 def test_workspace_queries(lib):

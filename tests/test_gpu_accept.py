@@ -238,3 +238,60 @@ def test_sample_errors_flagged(sv):
     sv.accept_sample(logits.cuda(), si.q.cuda(), tok.cuda(), seed=1)
     word = sv.get_device_error()
     assert word & 0x2 and word & 0x1
+
+
+# ----------------------------------------------------------------------------
+# relaxed (lossy Delta-logit) acceptance
+# ----------------------------------------------------------------------------
+
+def _relaxed_inputs(B, R, V, seed, quantise=False):
+    """Drafts among the verifying row's three best tokens and random ids, so
+    gaps fall on both sides of the thresholds."""
+    rng = np.random.default_rng(seed)
+    logits = (rng.standard_normal((B, R, V)) * 2).astype(np.float32)
+    if quantise:   # many exact ties, gaps in steps of 0.5
+        logits = np.round(logits * 2).astype(np.float32) / 2
+    top3 = np.argsort(-logits, axis=-1, kind="stable")[..., :3]
+    pick = rng.integers(0, 4, size=(B, R))
+    rnd = rng.integers(0, V, size=(B, R))
+    cand = np.where(pick < 3, np.take_along_axis(top3, np.minimum(pick, 2)[..., None], -1)[..., 0], rnd)
+    tok = rng.integers(0, V, size=(B, R)).astype(np.int32)
+    tok[:, 1:] = cand[:, :-1]
+    return logits, tok
+
+
+@pytest.mark.parametrize("B,R,V", [(1, 5, 151936), (16, 9, 152064), (7, 3, 1000), (64, 9, 8192)])
+@pytest.mark.parametrize("delta", [0.0, 0.25, 1.0, 4.0, float("inf")])
+def test_relaxed_chain(sv, B, R, V, delta):
+    logits, tok = _relaxed_inputs(B, R, V, seed=B * 100 + R)
+    got = sv.accept_greedy_relaxed(torch.from_numpy(logits).cuda(), torch.from_numpy(tok).cuda(), delta=delta)
+    assert_same(got, oracle.accept_greedy_relaxed(logits, tok, delta=delta), f"relaxed chain delta {delta}")
+    assert sv.get_device_error() == 0
+
+
+@pytest.mark.parametrize("delta", [0.0, 0.5, 1.5])
+def test_relaxed_ties_and_tree(sv, delta):
+    B, V = 12, 3000
+    par = _tree(40, 6, 3)
+    R = len(par)
+    logits, tok = _relaxed_inputs(B, R, V, seed=77, quantise=True)
+    parent = np.tile(par, (B, 1)).astype(np.int32)
+    for p in (None, parent):
+        pt = None if p is None else torch.from_numpy(p).cuda()
+        got = sv.accept_greedy_relaxed(torch.from_numpy(logits).cuda(), torch.from_numpy(tok).cuda(), pt, delta=delta)
+        assert_same(got, oracle.accept_greedy_relaxed(logits, tok, p, delta=delta), f"relaxed tree={p is not None}")
+
+
+def test_relaxed_zero_delta_equals_greedy_on_gpu(sv):
+    logits, tok = _greedy_inputs(8, 9, 20000, seed=5)
+    a = sv.accept_greedy(torch.from_numpy(logits).cuda(), torch.from_numpy(tok).cuda())
+    b = sv.accept_greedy_relaxed(torch.from_numpy(logits).cuda(), torch.from_numpy(tok).cuda(), delta=0.0)
+    for x, y in zip(a, b):
+        assert torch.equal(x, y)
+
+
+def test_relaxed_bad_token_flagged(sv):
+    logits, tok = _relaxed_inputs(2, 4, 500, seed=9)
+    tok[1, 2] = 600
+    sv.accept_greedy_relaxed(torch.from_numpy(logits).cuda(), torch.from_numpy(tok).cuda(), delta=1.0)
+    assert sv.get_device_error() & 0x2

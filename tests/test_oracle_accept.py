@@ -30,6 +30,105 @@ U_MAX = np.float32(1.0 - 2.0 ** -24)
 # greedy
 # ----------------------------------------------------------------------------
 
+
+# Relaxed, lossy acceptance ([SpecDec-Context-Scaling guide, sec. 7.2], the
+# Delta-logit relaxation): pinned by a hand-worked case, by its reductions to
+# greedy acceptance (delta = 0 with distinct maxima) and to "accept everything"
+# (delta = inf), by monotonicity in delta, and by the tie case where it and
+# greedy must differ.
+
+def test_relaxed_hand_worked_case():
+    # row 0: top-1 5.0 at id 0; draft 1 has 4.5, a gap of exactly 0.5.
+    # row 1: top-1 3.0 at id 2; draft 2 is id 3 with float32(2.9), gap
+    #        3.0 - 2.9000000953674316 = 0.0999999046325684 (exact).
+    # row 2: top-1 9 at id 3 (the bonus row).
+    logits = np.array([[[5.0, 4.5, 1.0, 0.0], [0.0, 2.0, 3.0, 2.9], [1.0, 1.0, 1.0, 9.0]]], np.float32)
+    tok = np.array([[0, 1, 3]], np.int32)
+    cases = {
+        0.4: (0, 0, [0, -1, -1]),      # gap 0.5 > 0.4: reject d_1, replacement = top-1 of row 0
+        0.5: (2, 3, [0, 1, 2]),        # 0.5 <= 0.5 and 0.09999990 <= 0.5: all pass, bonus from row 2
+        0.0999999: (0, 0, [0, -1, -1]),
+    }
+    for delta, (m, out, path) in cases.items():
+        n_acc, out_tok, pth = oracle.accept_greedy_relaxed(logits, tok, delta=delta)
+        assert (int(n_acc[0]), int(out_tok[0]), pth[0].tolist()) == (m, out, path), delta
+    # gap of row 1 against delta just below and at it
+    logits2 = logits.copy()
+    logits2[0, 0, 1] = 5.0          # draft 1 is now tied with the top-1 (gap 0)
+    gap1 = np.float32(3.0) - np.float32(2.9)
+    n_acc, out_tok, _ = oracle.accept_greedy_relaxed(logits2, tok, delta=float(np.nextafter(gap1, np.float32(0))))
+    assert (int(n_acc[0]), int(out_tok[0])) == (1, 2)   # d_1 passes at gap 0, d_2 fails: replacement id 2
+    n_acc, out_tok, _ = oracle.accept_greedy_relaxed(logits2, tok, delta=float(gap1))
+    assert (int(n_acc[0]), int(out_tok[0])) == (2, 3)
+
+
+def test_relaxed_zero_delta_is_greedy_when_maxima_are_unique():
+    rng = np.random.default_rng(31)
+    B, R, V = 24, 9, 500
+    logits = rng.standard_normal((B, R, V)).astype(np.float32)
+    g = logits.argmax(-1)
+    tok = rng.integers(0, V, size=(B, R)).astype(np.int32)
+    plant = rng.random((B, R)) < 0.7
+    tok[:, 1:] = np.where(plant[:, 1:], g[:, :-1], tok[:, 1:])
+    for got, exp in zip(oracle.accept_greedy_relaxed(logits, tok, delta=0.0), oracle.accept_greedy(logits, tok)):
+        assert np.array_equal(got, exp)
+    par = np.array([-1, 0, 0, 1, 1, 2, 3, 3, 5], np.int32)
+    parent = np.tile(par, (B, 1))
+    for got, exp in zip(oracle.accept_greedy_relaxed(logits, tok, parent, delta=0.0),
+                        oracle.accept_greedy(logits, tok, parent)):
+        assert np.array_equal(got, exp)
+
+
+def test_relaxed_infinite_delta_accepts_every_draft():
+    rng = np.random.default_rng(32)
+    B, R, V = 6, 7, 300
+    logits = (rng.standard_normal((B, R, V)) * 10).astype(np.float32)
+    tok = rng.integers(0, V, size=(B, R)).astype(np.int32)
+    n_acc, out_tok, path = oracle.accept_greedy_relaxed(logits, tok, delta=float("inf"))
+    assert (n_acc == R - 1).all()
+    assert (path == np.arange(R)).all()
+    assert (out_tok == logits[:, R - 1].argmax(-1)).all()     # the bonus row's top-1
+    # a tree: the walk takes the first child (index order) at every node
+    par = np.array([-1, 0, 0, 1, 1, 3, 2], np.int32)
+    n_acc, _, path = oracle.accept_greedy_relaxed(logits, tok, np.tile(par, (B, 1)), delta=float("inf"))
+    assert (n_acc == 3).all() and (path[:, :4] == [0, 1, 3, 5]).all() and (path[:, 4:] == -1).all()
+
+
+def test_relaxed_accepts_more_as_delta_grows():
+    rng = np.random.default_rng(33)
+    B, R, V = 32, 9, 200
+    logits = (rng.standard_normal((B, R, V)) * 2).astype(np.float32)
+    tok = rng.integers(0, V, size=(B, R)).astype(np.int32)
+    prev = None
+    for delta in (0.0, 0.5, 1.0, 2.0, 4.0, 8.0, 1e9):
+        n_acc, _, _ = oracle.accept_greedy_relaxed(logits, tok, delta=delta)
+        if prev is not None:
+            assert (n_acc >= prev).all()
+        prev = n_acc
+    assert prev.min() == R - 1
+
+
+def test_relaxed_zero_delta_accepts_any_tied_maximum():
+    # ids 1 and 3 tie for row 0's maximum: greedy wants id 1 (lowest index),
+    # the relaxed test only the gap, which is 0 for either
+    logits = np.zeros((1, 2, 5), np.float32)
+    logits[0, 0, 1] = logits[0, 0, 3] = 2.0
+    logits[0, 1, 4] = 1.0
+    tok = np.array([[0, 3]], np.int32)
+    assert int(oracle.accept_greedy(logits, tok)[0][0]) == 0
+    n_acc, out_tok, path = oracle.accept_greedy_relaxed(logits, tok, delta=0.0)
+    assert (int(n_acc[0]), int(out_tok[0]), path[0].tolist()) == (1, 4, [0, 1])
+
+
+def test_relaxed_rejects_bad_inputs():
+    logits = np.zeros((1, 3, 4), np.float32)
+    tok = np.array([[0, 1, 1]], np.int32)
+    for bad in (-0.1, float("nan")):
+        with pytest.raises(oracle.OracleError):
+            oracle.accept_greedy_relaxed(logits, tok, delta=bad)
+    with pytest.raises(oracle.OracleError):
+        oracle.accept_greedy_relaxed(logits, np.array([[0, 9, 0]], np.int32), delta=1.0)
+
 def test_greedy_alignment_golden():
     g = json.load(open(os.path.join(GOLDEN, "alignment.json")))
     for case in g["cases"]:
