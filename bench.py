@@ -49,11 +49,12 @@ FALLBACK_HBM_GBS = 6800.0
 TRAFFIC = {
     # ncu --set full, 28-layer 1.5B round, LM head N=5 H=1536 V=151936
     ("1", "lm_head"): {"bytes": 466809856 + 5381632, "src": "lm_head.cu", "src_hash": "f74183b9259d0f09"},
-    # ncu --set full, 7B batch-16 layer (2-layer case, same per-layer launch)
-    ("3b16", "verify_attn"): {"bytes": 269856256 + 3631360, "src": "verify_attn.cu",
-                              "src_hash": "450f22856ba2c178"},
-    ("3b16s", "verify_attn"): {"bytes": 269856256 + 3631360, "src": "verify_attn.cu",
-                               "src_hash": "450f22856ba2c178"},
+    # ncu (dram__bytes_read.sum, dram__bytes_write.sum), 7B batch-16 layer
+    # (2-layer case, same per-layer launch)
+    ("3b16", "verify_attn"): {"bytes": 269838080 + 2997760, "src": "verify_attn.cu",
+                              "src_hash": "bb3e32f58ed56bd8"},
+    ("3b16s", "verify_attn"): {"bytes": 269838080 + 2997760, "src": "verify_attn.cu",
+                               "src_hash": "bb3e32f58ed56bd8"},
     # ncu --set full, sampled B64 k8: the four launches of one acceptance
     # (statistics, walk, residual pass, draw)
     ("2", "accept_sampled"): {"bytes": 350172160 + 3333376 + 146688 + 77825024 + 1473536 + 126464,

@@ -85,6 +85,7 @@ typedef enum sv_status {
 #define SV_DEVERR_TREE        0x10u  /* parent[b][0] != -1 or parent[b][j] not in [0, j) */
 #define SV_DEVERR_PATH        0x20u  /* commit: n_acc outside [0, R) or path entry outside [0, R) */
 #define SV_DEVERR_TIMEOUT     0x40u  /* an internal bounded wait gave up (should never happen) */
+#define SV_DEVERR_PAGE        0x80u  /* paged KV: a page-table entry outside [0, num_pages) */
 
 /* Library version, e.g. 100 for 0.1.0. */
 SV_API int sv_version(void);
@@ -158,6 +159,25 @@ SV_API sv_status sv_verify_attn_ex(const sv_attn_shape* shape, const uint16_t* q
                                    const uint16_t* v_cache, const int32_t* len, const uint16_t* k_blk,
                                    const uint16_t* v_blk, const int32_t* parent, float scale, uint16_t* out,
                                    void* ws, size_t ws_bytes, uint32_t flags, void* stream);
+
+/* Paged KV cache ([MINI] implementation architecture: the committed KV lives
+ * in a block tensor addressed through each request's block table, and only
+ * accepted tokens are written into it).  The cache of one layer is a pool of
+ * pages of SV_KV_PAGE (64) positions,
+ *     k_pool, v_pool  [num_pages][Hkv][64][D] bf16,
+ * and position p of sequence b lives in page page_table[b][p / 64], row
+ * p % 64.  page_table [B][max_pages] int32, caller-owned; the pool's pages
+ * are the caller's to allocate (several sequences may not share a page they
+ * both commit into).  shape->T_cap must equal max_pages * 64.
+ * Otherwise as sv_verify_attn_ex (same flags, workspace, numerics).  A page
+ * entry the attention reaches that lies outside [0, num_pages) sets
+ * SV_DEVERR_PAGE and reads as zeros. */
+#define SV_KV_PAGE 64
+SV_API sv_status sv_verify_attn_paged(const sv_attn_shape* shape, const uint16_t* q, const uint16_t* k_pool,
+                                      const uint16_t* v_pool, int32_t num_pages, const int32_t* page_table,
+                                      int32_t max_pages, const int32_t* len, const uint16_t* k_blk,
+                                      const uint16_t* v_blk, const int32_t* parent, float scale, uint16_t* out,
+                                      void* ws, size_t ws_bytes, uint32_t flags, void* stream);
 
 /* ------------------------------------------------------------------------ */
 /* LM head ([SCS] sec. 3: the target's block forward yields one logits row   */
@@ -306,6 +326,19 @@ SV_API sv_status sv_accept_sample_noalloc(const float* logits, const float* q, i
 SV_API sv_status sv_kv_commit(uint16_t* k_cache, uint16_t* v_cache, const uint16_t* k_blk, const uint16_t* v_blk,
                        int32_t L, int32_t B, int32_t Hkv, int32_t D, int32_t T_cap, int32_t R,
                        const int32_t* path, const int32_t* n_acc, int32_t* len, void* stream);
+
+/* sv_kv_commit into paged caches (see sv_verify_attn_paged): position
+ * len[b] + i goes to page page_table[b][(len[b] + i) / 64], row
+ * (len[b] + i) % 64, of every layer's pool.
+ *   k_pool, v_pool [L][num_pages][Hkv][64][D] bf16 (the layers' pools, stacked)
+ *   page_table [B][max_pages] int32 (shared by the layers); capacity max_pages * 64
+ * A sequence whose new rows would reach a page entry outside [0, num_pages)
+ * is left untouched and sets SV_DEVERR_PAGE; length and path errors as for
+ * sv_kv_commit. */
+SV_API sv_status sv_kv_commit_paged(uint16_t* k_pool, uint16_t* v_pool, int32_t num_pages, const int32_t* page_table,
+                                    int32_t max_pages, const uint16_t* k_blk, const uint16_t* v_blk, int32_t L,
+                                    int32_t B, int32_t Hkv, int32_t D, int32_t R, const int32_t* path,
+                                    const int32_t* n_acc, int32_t* len, void* stream);
 
 /* ------------------------------------------------------------------------ */
 /* Diagnostics: the device building blocks of sv_accept_sample, exposed so    */

@@ -216,6 +216,34 @@ def kv_commit(k_cache, v_cache, k_blk, v_blk, path, n_acc, length):
     return kc, vc, ln
 
 
+def gather_pages(pool, page_table, page=64):
+    """The contiguous cache a paged one stands for ([MINI] implementation
+    architecture: KV in a block tensor addressed through the block table):
+    pool [..., P, Hkv, page, D], page_table [B, max_pages] ->
+    [..., B, Hkv, max_pages * page, D], where position p of sequence b is row
+    p % page of page page_table[b][p // page].  A plain re-layout (numpy
+    indexing), no arithmetic."""
+    pool = np.asarray(pool)
+    tab = np.asarray(page_table, np.int64)
+    B, M = tab.shape
+    g = pool[..., tab, :, :, :]                       # [..., B, M, Hkv, page, D]
+    g = np.moveaxis(g, -3, -4)                        # [..., B, Hkv, M, page, D]
+    return np.ascontiguousarray(g.reshape(g.shape[:-3] + (M * page, g.shape[-1])))
+
+
+def scatter_pages(pool, page_table, cache, page=64):
+    """Inverse of gather_pages for the pages the table names (each named
+    once): returns a copy of pool with those pages taken from cache."""
+    out = np.array(pool, copy=True)
+    tab = np.asarray(page_table, np.int64)
+    B, M = tab.shape
+    c = np.asarray(cache)
+    c = c.reshape(c.shape[:-2] + (M, page, c.shape[-1]))   # [..., B, Hkv, M, page, D]
+    c = np.moveaxis(c, -3, -4)                              # [..., B, M, Hkv, page, D]
+    out[..., tab, :, :, :] = c
+    return out
+
+
 def verify_attn(q, k_cache, v_cache, length, k_blk, v_blk, parent=None, scale=None):
     """q [B, R, Hq, D] uint16; cache [B, Hkv, T_cap, D]; block [B, Hkv, R, D];
     returns float64 [B, R, Hq, D]."""

@@ -62,12 +62,15 @@ def _load():
     L.sv_accept_sample_noalloc.argtypes = [_P, _P, _I32, _P, _P, _I32, _I32, _I32, _F32, _U64, _U64, _P, _P, _P,
                                            _P, _P]
     L.sv_kv_commit.argtypes = [_P, _P, _P, _P, _I32, _I32, _I32, _I32, _I32, _I32, _P, _P, _P, _P]
+    L.sv_kv_commit_paged.argtypes = [_P, _P, _I32, _P, _I32, _P, _P, _I32, _I32, _I32, _I32, _I32, _P, _P, _P, _P]
+    L.sv_verify_attn_paged.argtypes = [_P, _P, _P, _P, _I32, _P, _I32, _P, _P, _P, _P, ctypes.c_float, _P, _P, _SZ,
+                                       ctypes.c_uint32, _P]
     L.sv_diag_exp.argtypes = [_P, _P, _I64, _P]
     L.sv_diag_philox.argtypes = [_P, _P, _P, _I64, _P]
     L.sv_diag_canon.argtypes = [_P, _I32, _I32, _P, _P, _P, _P]
     for fn in ("sv_verify_attn", "sv_verify_attn_ex", "sv_lm_head", "sv_lm_head_ex", "sv_accept_greedy",
                "sv_accept_greedy_relaxed", "sv_accept_sample",
-               "sv_accept_sample_noalloc", "sv_kv_commit",
+               "sv_accept_sample_noalloc", "sv_kv_commit", "sv_kv_commit_paged", "sv_verify_attn_paged",
                "sv_diag_exp", "sv_diag_philox", "sv_diag_canon", "sv_get_device_error"):
         getattr(L, fn).restype = ctypes.c_int
     return L
@@ -144,6 +147,35 @@ def verify_attn(q, k_cache, v_cache, length, k_blk, v_blk, parent=None, scale=No
         ctypes.byref(s), _ptr(q, bf, "q"), _ptr(k_cache, bf, "k_cache"), _ptr(v_cache, bf, "v_cache"),
         _ptr(length, torch.int32, "len"), _ptr(k_blk, bf, "k_blk"), _ptr(v_blk, bf, "v_blk"),
         _ptr(parent, torch.int32, "parent"), float(scale), _ptr(out, bf, "out"), _ptr(ws), nbytes,
+        ATTN_CACHE_READY if cache_ready else 0, _stream(stream)))
+    return out
+
+
+KV_PAGE = 64   # positions per page of a paged cache (SV_KV_PAGE)
+
+
+def verify_attn_paged(q, k_pool, v_pool, page_table, length, k_blk, v_blk, parent=None, scale=None, out=None,
+                      ws=None, stream=None, cache_ready=False):
+    """Paged cache: pools [num_pages,Hkv,64,D] bf16, page_table [B,max_pages] int32
+    (position p of sequence b = row p % 64 of page page_table[b][p // 64]);
+    other arguments as verify_attn.  Returns out [B,R,Hq,D] bf16."""
+    B, R, Hq, D = q.shape
+    num_pages, Hkv = k_pool.shape[0], k_pool.shape[1]
+    max_pages = page_table.shape[1]
+    s = _AttnShape(B, R, Hq, Hkv, D, max_pages * KV_PAGE)
+    if scale is None:
+        scale = D ** -0.5
+    if out is None:
+        out = torch.empty_like(q)
+    nbytes = int(lib.sv_verify_attn_workspace(ctypes.byref(s)))
+    if ws is None and nbytes > 0:
+        ws = torch.zeros(nbytes, dtype=torch.uint8, device=q.device)   # ticket words start at zero
+    ws = _ws(nbytes, q.device, ws)
+    bf, i32 = torch.bfloat16, torch.int32
+    _check("sv_verify_attn_paged", lib.sv_verify_attn_paged(
+        ctypes.byref(s), _ptr(q, bf, "q"), _ptr(k_pool, bf, "k_pool"), _ptr(v_pool, bf, "v_pool"), num_pages,
+        _ptr(page_table, i32, "page_table"), max_pages, _ptr(length, i32, "len"), _ptr(k_blk, bf, "k_blk"),
+        _ptr(v_blk, bf, "v_blk"), _ptr(parent, i32, "parent"), float(scale), _ptr(out, bf, "out"), _ptr(ws), nbytes,
         ATTN_CACHE_READY if cache_ready else 0, _stream(stream)))
     return out
 
@@ -247,6 +279,18 @@ def kv_commit(k_cache, v_cache, k_blk, v_blk, path, n_acc, length, stream=None):
         _ptr(k_cache, bf, "k_cache"), _ptr(v_cache, bf, "v_cache"), _ptr(k_blk, bf, "k_blk"),
         _ptr(v_blk, bf, "v_blk"), L, B, Hkv, D, T_cap, R, _ptr(path, i32, "path"), _ptr(n_acc, i32, "n_acc"),
         _ptr(length, i32, "len"), _stream(stream)))
+
+
+def kv_commit_paged(k_pool, v_pool, page_table, k_blk, v_blk, path, n_acc, length, stream=None):
+    """pools [L,num_pages,Hkv,64,D]; page_table [B,max_pages]; blocks [L,B,Hkv,R,D] (bf16);
+    path [B,R], n_acc [B], length [B] int32 (length updated in place)."""
+    L, num_pages, Hkv, _, D = k_pool.shape
+    B, R = k_blk.shape[1], k_blk.shape[3]
+    bf, i32 = torch.bfloat16, torch.int32
+    _check("sv_kv_commit_paged", lib.sv_kv_commit_paged(
+        _ptr(k_pool, bf, "k_pool"), _ptr(v_pool, bf, "v_pool"), num_pages, _ptr(page_table, i32, "page_table"),
+        page_table.shape[1], _ptr(k_blk, bf, "k_blk"), _ptr(v_blk, bf, "v_blk"), L, B, Hkv, D, R,
+        _ptr(path, i32, "path"), _ptr(n_acc, i32, "n_acc"), _ptr(length, i32, "len"), _stream(stream)))
 
 
 def get_device_error(stream=None) -> int:

@@ -162,7 +162,32 @@ sv_status sv_verify_attn_ex(const sv_attn_shape* shape, const uint16_t* q, const
     if (!(scale > 0.0f)) return SV_ERR_ARG;
     if (ws_bytes < sv::attn_workspace(*shape)) return SV_ERR_WORKSPACE;
     return launch_status(sv::launch_verify_attn(*shape, q, k_cache, v_cache, len, k_blk, v_blk, parent, scale, out,
-                                                ws, (flags & SV_ATTN_CACHE_READY) != 0, as_stream(stream)));
+                                                ws, (flags & SV_ATTN_CACHE_READY) != 0, nullptr, 0, 0,
+                                                as_stream(stream)));
+}
+
+sv_status sv_verify_attn_paged(const sv_attn_shape* shape, const uint16_t* q, const uint16_t* k_pool,
+                               const uint16_t* v_pool, int32_t num_pages, const int32_t* page_table,
+                               int32_t max_pages, const int32_t* len, const uint16_t* k_blk, const uint16_t* v_blk,
+                               const int32_t* parent, float scale, uint16_t* out, void* ws, size_t ws_bytes,
+                               uint32_t flags, void* stream) {
+    if (flags & ~SV_ATTN_CACHE_READY) return SV_ERR_ARG;
+    const sv_status st = check_attn_shape(shape);
+    if (st != SV_OK) return st;
+    if (!q || !k_pool || !v_pool || !page_table || !len || !k_blk || !v_blk || !out) return SV_ERR_ARG;
+    if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) || !aligned16(k_blk) || !aligned16(v_blk) ||
+        !aligned16(out) || (ws && !aligned16(ws)))
+        return SV_ERR_ARG;
+    if (num_pages < 1 || max_pages < 1) return SV_ERR_SHAPE;
+    if (static_cast<int64_t>(max_pages) * SV_KV_PAGE != shape->T_cap) return SV_ERR_SHAPE;
+    // tensor-map rows of the pool, and the out-of-pool row used for a bad entry
+    if ((static_cast<int64_t>(num_pages) + 1) * shape->Hkv * SV_KV_PAGE >= (int64_t(1) << 31)) return SV_ERR_SHAPE;
+    if (!ws && sv::attn_workspace(*shape) > 0) return SV_ERR_ARG;
+    if (!(scale > 0.0f)) return SV_ERR_ARG;
+    if (ws_bytes < sv::attn_workspace(*shape)) return SV_ERR_WORKSPACE;
+    return launch_status(sv::launch_verify_attn(*shape, q, k_pool, v_pool, len, k_blk, v_blk, parent, scale, out, ws,
+                                                (flags & SV_ATTN_CACHE_READY) != 0, page_table, max_pages,
+                                                num_pages, as_stream(stream)));
 }
 
 sv_status sv_lm_head(const uint16_t* hid, const uint16_t* W, float* logits, int32_t N, int32_t H, int32_t V,
@@ -245,6 +270,21 @@ sv_status sv_kv_commit(uint16_t* k_cache, uint16_t* v_cache, const uint16_t* k_b
     if (L < 1 || B < 1 || Hkv < 1 || D < 8 || D % 8 || T_cap < 1 || R < 1 || R > 128) return SV_ERR_SHAPE;
     if (static_cast<int64_t>(B) * 8 > 2147483647) return SV_ERR_SHAPE;
     return launch_status(sv::launch_kv_commit(k_cache, v_cache, k_blk, v_blk, L, B, Hkv, D, T_cap, R, path, n_acc, len,
+                                              nullptr, 0, 0, as_stream(stream)));
+}
+
+sv_status sv_kv_commit_paged(uint16_t* k_pool, uint16_t* v_pool, int32_t num_pages, const int32_t* page_table,
+                             int32_t max_pages, const uint16_t* k_blk, const uint16_t* v_blk, int32_t L, int32_t B,
+                             int32_t Hkv, int32_t D, int32_t R, const int32_t* path, const int32_t* n_acc, int32_t* len,
+                             void* stream) {
+    if (!k_pool || !v_pool || !page_table || !k_blk || !v_blk || !path || !n_acc || !len) return SV_ERR_ARG;
+    if (!aligned16(k_pool) || !aligned16(v_pool) || !aligned16(k_blk) || !aligned16(v_blk)) return SV_ERR_ARG;
+    if (L < 1 || B < 1 || Hkv < 1 || D < 8 || D % 8 || R < 1 || R > 128 || num_pages < 1 || max_pages < 1)
+        return SV_ERR_SHAPE;
+    if (static_cast<int64_t>(max_pages) * SV_KV_PAGE > 2147483647 || static_cast<int64_t>(B) * 8 > 2147483647)
+        return SV_ERR_SHAPE;
+    return launch_status(sv::launch_kv_commit(k_pool, v_pool, k_blk, v_blk, L, B, Hkv, D, max_pages * SV_KV_PAGE, R,
+                                              path, n_acc, len, page_table, max_pages, num_pages,
                                               as_stream(stream)));
 }
 

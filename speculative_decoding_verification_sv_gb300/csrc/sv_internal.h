@@ -57,9 +57,13 @@ cudaError_t launch_diag_canon(const float* x, int n, int m, const float* u, floa
                               cudaStream_t st);
 
 // kv_commit.cu
+// pages != nullptr: the caches are page pools [L][num_pages][Hkv][64][D] and
+// pages [B][max_pages] maps each 64-position tile to its page (T_cap =
+// max_pages * 64)
 cudaError_t launch_kv_commit(uint16_t* k_cache, uint16_t* v_cache, const uint16_t* k_blk, const uint16_t* v_blk,
                              int L, int B, int Hkv, int D, int T_cap, int R, const int32_t* path,
-                             const int32_t* n_acc, int32_t* len, cudaStream_t st);
+                             const int32_t* n_acc, int32_t* len, const int32_t* pages, int max_pages,
+                             int num_pages, cudaStream_t st);
 
 // lm_head.cu
 cudaError_t launch_lm_head(const uint16_t* hid, const uint16_t* W, float* logits, int N, int H, int V,
@@ -82,10 +86,13 @@ struct AttnPlan {
 };
 AttnPlan attn_plan(const sv_attn_shape& s);
 size_t attn_workspace(const sv_attn_shape& s);
+// pages != nullptr: k_cache / v_cache are page pools [num_pages][Hkv][64][D]
+// and pages [B][max_pages] maps each 64-position tile to its page
 cudaError_t launch_verify_attn(const sv_attn_shape& s, const uint16_t* q, const uint16_t* k_cache,
                                const uint16_t* v_cache, const int32_t* len, const uint16_t* k_blk,
                                const uint16_t* v_blk, const int32_t* parent, float scale, uint16_t* out,
-                               void* ws, bool cache_ready, cudaStream_t st);
+                               void* ws, bool cache_ready, const int32_t* pages, int max_pages, int num_pages,
+                               cudaStream_t st);
 
 // TMA descriptor encoding (driver entry point fetched through the runtime).
 bool encode_tmap_2d_bf16(void* tmap, const void* base, uint64_t inner, uint64_t outer, uint64_t row_stride_bytes,

@@ -148,6 +148,8 @@ struct AttnArgs {
     int part_rows;           // rows of a partial record block: min(rows, rows per row tile)
     float scale_log2;
     int cache_ready;         // len and the cache are final before the preceding kernel runs
+    const int32_t* pages;    // paged cache: [B][max_pages] page of each 64-position tile (nullptr: contiguous)
+    int max_pages, num_pages;
 };
 
 // TMEM lane that holds row gr of (b, g): full tiles lane = gr - 128 * rt;
@@ -294,6 +296,18 @@ __global__ void __launch_bounds__(Roles<kHalf, kHW>::kThreads, 1)
 
     if (warp == kTmaWarp) {
         // ---------------- TMA producer ----------------
+        // first row of context tile gt in the K/V tensor maps: the contiguous
+        // cache [B][Hkv][T_cap][D], or the tile's page of a [pages][Hkv][64][D]
+        // pool (a page outside the pool reads as zeros and is flagged)
+        auto ctx_row = [&](int gt) {
+            if (a.pages == nullptr) return hg * a.T_cap + gt * kNk;
+            int pg = __ldg(a.pages + static_cast<size_t>(b) * a.max_pages + gt);
+            if (pg < 0 || pg >= a.num_pages) {
+                raise_error(a.err, SV_DEVERR_PAGE);
+                pg = a.num_pages;
+            }
+            return (pg * a.Hkv + g) * kNk;
+        };
         auto load_step = [&](int i) {
             const int s = i % kStages;
             mbar_wait(&kv_empty[s], ((i / kStages) & 1) ^ 1, a.err);
@@ -304,7 +318,7 @@ __global__ void __launch_bounds__(Roles<kHalf, kHW>::kThreads, 1)
                 const int gt = t0 + h;
                 const void* tk = gt < n_ctx ? static_cast<const void*>(&tmK) : static_cast<const void*>(&tmKb);
                 const void* tv = gt < n_ctx ? static_cast<const void*>(&tmV) : static_cast<const void*>(&tmVb);
-                const int y = gt < n_ctx ? hg * a.T_cap + gt * kNk : hg * a.R + (gt - n_ctx) * kNk;
+                const int y = gt < n_ctx ? ctx_row(gt) : hg * a.R + (gt - n_ctx) * kNk;
                 tma_load_2d(st + h * kHalfBytes, tk, 0, y, &kv_full[s]);
                 tma_load_2d(st + kRegion + h * kHalfBytes, tk, 64, y, &kv_full[s]);
                 tma_load_2d(st + 2 * kRegion + h * kHalfBytes, tv, 0, y, &kv_full[s]);
@@ -1104,11 +1118,14 @@ size_t attn_workspace(const sv_attn_shape& s) {
 cudaError_t launch_verify_attn(const sv_attn_shape& s, const uint16_t* q, const uint16_t* k_cache,
                                const uint16_t* v_cache, const int32_t* len, const uint16_t* k_blk,
                                const uint16_t* v_blk, const int32_t* parent, float scale, uint16_t* out,
-                               void* ws, bool cache_ready, cudaStream_t st) {
+                               void* ws, bool cache_ready, const int32_t* pages, int max_pages, int num_pages,
+                               cudaStream_t st) {
     const AttnPlan p = attn_plan(s);
     if (p.clusters > 1 && ws == nullptr) return cudaErrorInvalidValue;
     alignas(64) uint8_t tK[128], tV[128], tKb[128], tVb[128];
-    const uint64_t ctx_rows = static_cast<uint64_t>(s.B) * s.Hkv * s.T_cap;
+    // rows of the context tensor maps: the caches, or the page pool
+    const uint64_t ctx_rows = pages ? static_cast<uint64_t>(num_pages) * s.Hkv * kNk
+                                    : static_cast<uint64_t>(s.B) * s.Hkv * s.T_cap;
     const uint64_t blk_rows = static_cast<uint64_t>(s.B) * s.Hkv * s.R;
     if (!encode_tmap_2d_bf16(tK, k_cache, kD, ctx_rows, kD * 2, 64, kNk) ||
         !encode_tmap_2d_bf16(tV, v_cache, kD, ctx_rows, kD * 2, 64, kNk) ||
@@ -1137,6 +1154,9 @@ cudaError_t launch_verify_attn(const sv_attn_shape& s, const uint16_t* q, const 
     a.part_rows = p.rows < tile_rows ? p.rows : tile_rows;
     a.scale_log2 = scale * 1.4426950408889634f;
     a.cache_ready = cache_ready ? 1 : 0;
+    a.pages = pages;
+    a.max_pages = max_pages;
+    a.num_pages = num_pages;
     if (parent != nullptr)
         return !p.half ? launch_mode<false, true, 2>(p, s, tK, tV, tKb, tVb, a, st)
                : p.hw4 ? launch_mode<true, true, 4>(p, s, tK, tV, tKb, tVb, a, st)

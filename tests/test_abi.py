@@ -90,6 +90,14 @@ def test_host_validation_rejects_before_launch(lib):
     assert L.sv_accept_sample(*args) == 2
     # commit: R above 128
     assert L.sv_kv_commit(fake, fake, fake, fake, 28, 1, 2, 128, 4224, 200, fake, fake, fake, None) == 2
+    # paged attention: T_cap must be max_pages * 64; a page table is required
+    s = b._AttnShape(1, 5, 12, 2, 128, 4224)
+    assert L.sv_verify_attn_paged(ctypes.byref(s), fake, fake, fake, 100, fake, 65, fake, fake, fake, None,
+                                  ctypes.c_float(0.1), fake, fake, 1 << 30, 0, None) == 2
+    assert L.sv_verify_attn_paged(ctypes.byref(s), fake, fake, fake, 100, None, 66, fake, fake, fake, None,
+                                  ctypes.c_float(0.1), fake, fake, 1 << 30, 0, None) == 1
+    assert L.sv_kv_commit_paged(fake, fake, 0, fake, 4, fake, fake, 28, 1, 2, 128, 5, fake, fake, fake, None) == 2
+    assert L.sv_kv_commit_paged(fake, fake, 8, None, 4, fake, fake, 28, 1, 2, 128, 5, fake, fake, fake, None) == 1
     # relaxed acceptance: delta must be >= 0 and not NaN; short workspace
     for bad in (-0.5, float("nan")):
         assert L.sv_accept_greedy_relaxed(fake, fake, None, 1, 5, 151936, ctypes.c_float(bad), fake, fake, fake,

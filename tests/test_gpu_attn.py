@@ -240,3 +240,69 @@ def test_attn_workspace_tickets_reset(sv):
     ok, err, bound = within_tol(shared.float().cpu().numpy(), ref)
     assert ok, (err, bound)
     assert sv.get_device_error() == 0
+
+
+# ----------------------------------------------------------------------------
+# paged cache: the pool's pages in a shuffled order, a page table per
+# sequence; the oracle attends over the contiguous cache the table stands for
+# ----------------------------------------------------------------------------
+
+def _paged_case(B, R, Hq, Hkv, max_pages, lengths, seed, spare=3, poison=False):
+    D, PG = 128, 64
+    g = torch.Generator().manual_seed(seed)
+    mk = lambda *s: torch.randn(*s, generator=g).to(torch.bfloat16)
+    P = B * max_pages + spare
+    kp, vp = mk(P, Hkv, PG, D), mk(P, Hkv, PG, D)
+    table = torch.randperm(P, generator=g)[:B * max_pages].reshape(B, max_pages).to(torch.int32)
+    if poison:   # positions at or past len hold NaN (K) and +inf (V) bits
+        for b, t in enumerate(lengths):
+            for p in range(t, max_pages * PG):
+                kp[table[b, p // PG], :, p % PG] = float("nan")
+                vp[table[b, p // PG], :, p % PG] = float("inf")
+    q, kb, vb = mk(B, R, Hq, D), mk(B, Hkv, R, D), mk(B, Hkv, R, D)
+    return q, kp, vp, table, torch.tensor(lengths, dtype=torch.int32), kb, vb
+
+
+@pytest.mark.parametrize("B,R,Hq,Hkv,max_pages,lengths,tree,poison", [
+    (1, 5, 12, 2, 33, [2048], False, False),               # 1.5B layout over 33 pages
+    (3, 9, 28, 4, 5, [63, 64, 300], False, True),           # tile edges, NaN/+inf past len
+    (4, 9, 28, 4, 18, [1000, 513, 1024, 0], False, False),  # ragged, empty context
+    (2, 65, 28, 4, 9, [513, 300], True, True),              # tree, two block tiles
+])
+def test_attn_paged(sv, B, R, Hq, Hkv, max_pages, lengths, tree, poison):
+    q, kp, vp, table, ln, kb, vb = _paged_case(B, R, Hq, Hkv, max_pages, lengths, seed=B + R, poison=poison)
+    par = None
+    if tree:
+        par = np.tile(synth.random_tree(R - 1, 8, 3, 4), (B, 1)).astype(np.int32)
+    out = sv.verify_attn_paged(q.cuda(), kp.cuda(), vp.cuda(), table.cuda(), ln.cuda(), kb.cuda(), vb.cuda(),
+                               None if par is None else torch.from_numpy(par).cuda())
+    kc = oracle.gather_pages(bits(kp), table.numpy())
+    vc = oracle.gather_pages(bits(vp), table.numpy())
+    ref = oracle.verify_attn(bits(q), kc, vc, ln.numpy(), bits(kb), bits(vb), par)
+    ok, err, bound = within_tol(out.float().cpu().numpy(), ref)
+    assert ok, (err, bound)
+    assert sv.get_device_error() == 0
+    # the same with the cache-ready launch flag: bit for bit
+    out2 = sv.verify_attn_paged(q.cuda(), kp.cuda(), vp.cuda(), table.cuda(), ln.cuda(), kb.cuda(), vb.cuda(),
+                                None if par is None else torch.from_numpy(par).cuda(), cache_ready=True)
+    assert torch.equal(out.view(torch.int16), out2.view(torch.int16))
+
+
+def test_attn_paged_equals_contiguous(sv):
+    """A table that maps sequence b's tile j to page b * max_pages + j makes the
+    pool the contiguous cache: both entry points give the same bits."""
+    B, R, Hq, Hkv, M = 2, 9, 28, 4, 6
+    q, kp, vp, _, ln, kb, vb = _paged_case(B, R, Hq, Hkv, M, [300, 129], seed=3, spare=0)
+    table = torch.arange(B * M, dtype=torch.int32).reshape(B, M)
+    paged = sv.verify_attn_paged(q.cuda(), kp.cuda(), vp.cuda(), table.cuda(), ln.cuda(), kb.cuda(), vb.cuda())
+    kc = kp.reshape(B, M, Hkv, 64, 128).transpose(1, 2).reshape(B, Hkv, M * 64, 128).contiguous()
+    vc = vp.reshape(B, M, Hkv, 64, 128).transpose(1, 2).reshape(B, Hkv, M * 64, 128).contiguous()
+    flat = sv.verify_attn(q.cuda(), kc.cuda(), vc.cuda(), ln.cuda(), kb.cuda(), vb.cuda())
+    assert torch.equal(paged.view(torch.int16), flat.view(torch.int16))
+
+
+def test_attn_paged_bad_page_flagged(sv):
+    q, kp, vp, table, ln, kb, vb = _paged_case(1, 5, 12, 2, 4, [200], seed=8)
+    table[0, 1] = kp.shape[0] + 5          # a page the context reaches, outside the pool
+    sv.verify_attn_paged(q.cuda(), kp.cuda(), vp.cuda(), table.cuda(), ln.cuda(), kb.cuda(), vb.cuda())
+    assert sv.get_device_error() & 0x80

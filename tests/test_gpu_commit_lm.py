@@ -145,3 +145,63 @@ def test_lm_head_weights_ready_same_result(sv, N, H, V):
     torch.cuda.synchronize()
     for a, b in zip(out, ref):
         assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("L,B,Hkv,max_pages,R,tree", [(3, 5, 2, 3, 5, False), (28, 4, 4, 4, 9, False),
+                                                      (2, 3, 4, 5, 65, True)])
+def test_commit_paged(sv, L, B, Hkv, max_pages, R, tree):
+    """Paged commit equals the oracle's commit on the contiguous cache the page
+    table stands for, scattered back; pages no table names are untouched."""
+    D, PG = 128, 64
+    rng = np.random.default_rng(L * 10 + B)
+    P = B * max_pages + 4
+    kp = rng.integers(0, 65535, size=(L, P, Hkv, PG, D), dtype=np.uint16)
+    vp = rng.integers(0, 65535, size=(L, P, Hkv, PG, D), dtype=np.uint16)
+    table = rng.permutation(P)[:B * max_pages].reshape(B, max_pages).astype(np.int32)
+    kb = rng.integers(0, 65535, size=(L, B, Hkv, R, D), dtype=np.uint16)
+    vb = rng.integers(0, 65535, size=(L, B, Hkv, R, D), dtype=np.uint16)
+    T_cap = max_pages * PG
+    t = rng.integers(0, T_cap - R + 1, size=B).astype(np.int32)
+    t[0] = T_cap - R
+    n_acc = rng.integers(0, R, size=B).astype(np.int32)
+    path = np.full((B, R), -1, np.int32)
+    for b in range(B):
+        if tree:   # a strictly increasing node path, as a tree walk produces
+            path[b, :n_acc[b] + 1] = np.concatenate([[0], np.sort(rng.choice(np.arange(1, R), n_acc[b], False))])
+        else:
+            path[b, :n_acc[b] + 1] = np.arange(n_acc[b] + 1)
+    kc_ref, vc_ref, ln_ref = oracle.kv_commit(oracle.gather_pages(kp, table), oracle.gather_pages(vp, table), kb, vb,
+                                              path, n_acc, t)
+    kp_ref = oracle.scatter_pages(kp, table, kc_ref)
+    vp_ref = oracle.scatter_pages(vp, table, vc_ref)
+    kpt, vpt = _bf16_from_bits(kp).cuda(), _bf16_from_bits(vp).cuda()
+    ln = torch.from_numpy(t.copy()).cuda()
+    sv.kv_commit_paged(kpt, vpt, torch.from_numpy(table).cuda(), _bf16_from_bits(kb).cuda(),
+                       _bf16_from_bits(vb).cuda(), torch.from_numpy(path).cuda(), torch.from_numpy(n_acc).cuda(), ln)
+    assert np.array_equal(bits(kpt), kp_ref)
+    assert np.array_equal(bits(vpt), vp_ref)
+    assert np.array_equal(ln.cpu().numpy(), ln_ref)
+    assert sv.get_device_error() == 0
+
+
+def test_commit_paged_bad_page_flagged_and_untouched(sv):
+    D, PG, L, B, Hkv, M, R = 128, 64, 2, 2, 2, 2, 5
+    rng = np.random.default_rng(5)
+    P = B * M
+    kp = rng.integers(0, 65535, size=(L, P, Hkv, PG, D), dtype=np.uint16)
+    table = np.arange(P, dtype=np.int32).reshape(B, M)
+    table[0, 1] = P + 7                       # sequence 0's rows 62.. land on a page outside the pool
+    kb = rng.integers(0, 65535, size=(L, B, Hkv, R, D), dtype=np.uint16)
+    t = np.array([62, 10], np.int32)
+    n_acc = np.array([3, 2], np.int32)
+    path = np.array([[0, 1, 2, 3, -1], [0, 1, 2, -1, -1]], np.int32)
+    kpt = _bf16_from_bits(kp).cuda()
+    vpt = _bf16_from_bits(kp).cuda()
+    ln = torch.from_numpy(t.copy()).cuda()
+    sv.kv_commit_paged(kpt, vpt, torch.from_numpy(table).cuda(), _bf16_from_bits(kb).cuda(), _bf16_from_bits(kb).cuda(),
+                       torch.from_numpy(path).cuda(), torch.from_numpy(n_acc).cuda(), ln)
+    assert sv.get_device_error() & 0x80
+    got = bits(kpt)
+    assert np.array_equal(got[:, 0], kp[:, 0])            # sequence 0 untouched (its page 0 too)
+    assert int(ln[0]) == 62 and int(ln[1]) == 13           # sequence 1 committed
+    assert np.array_equal(got[:, 2, :, 10:13], kb[:, 1, :, 0:3])
