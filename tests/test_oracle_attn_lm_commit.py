@@ -202,3 +202,29 @@ def test_commit_capacity_overflow_is_an_error():
     with pytest.raises(oracle.OracleError):
         oracle.kv_commit(kc, kc, kb, kb, np.array([[0, 1, 2, 3]], np.int32), np.array([3], np.int32),
                          np.array([5], np.int32))
+
+
+def test_gather_and_scatter_pages_brute_force():
+    """The paged cache's re-layout against its definition ([mini-infer Phase 11],
+    block tensor and block table): position p of sequence b is row p % page of
+    page table[b][p // page], checked element by element on a tiny pool."""
+    rng = np.random.default_rng(12)
+    L, P, H, page, D, B, M = 2, 9, 3, 4, 5, 2, 3
+    pool = rng.integers(0, 60000, size=(L, P, H, page, D)).astype(np.uint16)
+    table = np.array([[7, 0, 4], [2, 8, 5]], np.int32)
+    c = oracle.gather_pages(pool, table, page=page)
+    assert c.shape == (L, B, H, M * page, D)
+    for l in range(L):
+        for b in range(B):
+            for h in range(H):
+                for p in range(M * page):
+                    assert np.array_equal(c[l, b, h, p], pool[l, table[b, p // page], h, p % page])
+    # scatter writes back exactly the named pages
+    c2 = c.copy()
+    c2[:, 1, :, 5] = 1                                   # sequence 1, position 5: page 8, row 1
+    back = oracle.scatter_pages(pool, table, c2, page=page)
+    changed = np.argwhere(back != pool)
+    assert set(map(tuple, changed[:, [1, 3]])) <= {(8, 1)}
+    assert np.array_equal(back[:, 8, :, 1], np.ones_like(back[:, 8, :, 1]))
+    for unnamed in (1, 3, 6):
+        assert np.array_equal(back[:, unnamed], pool[:, unnamed])
