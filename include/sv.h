@@ -86,6 +86,8 @@ typedef enum sv_status {
 #define SV_DEVERR_PATH        0x20u  /* commit: n_acc outside [0, R) or path entry outside [0, R) */
 #define SV_DEVERR_TIMEOUT     0x40u  /* an internal bounded wait gave up (should never happen) */
 #define SV_DEVERR_PAGE        0x80u  /* paged KV: a page-table entry outside [0, num_pages) */
+/* (A library built with -DSV_DEBUG also reports failed internal self-checks,
+ * as bit 31 plus a check code in bits 8..23.) */
 
 /* Library version, e.g. 100 for 0.1.0. */
 SV_API int sv_version(void);

@@ -33,12 +33,13 @@ __device__ __forceinline__ void raise_error(unsigned int* err, unsigned int bit)
     if (err) atomicOr(err, bit);
 }
 
-// Self-checks compiled in with -DSV_DEBUG: a failed check sets bit 0x80 and
-// the check's code (bits 8..) in the error word, and the guarded access is
-// skipped.  Without SV_DEBUG the checks vanish.
+// Self-checks compiled in with -DSV_DEBUG: a failed check sets bit 31 and
+// the check's code (bits 8..23) in the error word -- above the public
+// SV_DEVERR_* bits -- and the guarded access is skipped.  Without SV_DEBUG
+// the checks vanish.
 #ifdef SV_DEBUG
 __device__ __forceinline__ bool sv_check(bool ok, unsigned int* err, unsigned int code) {
-    if (!ok) raise_error(err, 0x80u | (1u << (8 + (code & 23))));
+    if (!ok) raise_error(err, 0x80000000u | (1u << (8 + (code & 15))));
     return ok;
 }
 #define SV_CHECK(cond, err, code) ::sv::sv_check((cond), (err), (code))
