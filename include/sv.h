@@ -171,9 +171,11 @@ SV_API sv_status sv_verify_attn_ex(const sv_attn_shape* shape, const uint16_t* q
  * p % 64.  page_table [B][max_pages] int32, caller-owned; the pool's pages
  * are the caller's to allocate (several sequences may not share a page they
  * both commit into).  shape->T_cap must equal max_pages * 64.
- * Otherwise as sv_verify_attn_ex (same flags, workspace, numerics).  A page
- * entry the attention reaches that lies outside [0, num_pages) sets
- * SV_DEVERR_PAGE and reads as zeros. */
+ * Otherwise as sv_verify_attn_ex (same flags, workspace, numerics); with
+ * SV_ATTN_CACHE_READY the promise covers page_table too (it is read, like
+ * len, before the preceding kernel has finished).  A page entry the
+ * attention reaches that lies outside [0, num_pages) sets SV_DEVERR_PAGE and
+ * reads as zeros. */
 #define SV_KV_PAGE 64
 SV_API sv_status sv_verify_attn_paged(const sv_attn_shape* shape, const uint16_t* q, const uint16_t* k_pool,
                                       const uint16_t* v_pool, int32_t num_pages, const int32_t* page_table,
