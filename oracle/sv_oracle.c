@@ -11,7 +11,8 @@
  *   [SCS]  "SpecDec-Context-Scaling project guide" (richardf123.github.io):
  *          sec. 3 (block verification, longest accepted prefix, replacement and
  *          bonus token), sec. 3.1 (logits-row alignment), sec. 3.2 (cache length
- *          equals committed-token count).
+ *          equals committed-token count), sec. 7.2 (the lossy Delta-logit
+ *          relaxation of the acceptance test).
  *   [TUT]  wmrh.cn speculative-decoding tutorial: sec. 2.2 (accept with
  *          min(1, p/q), otherwise resample from norm(max(0, p - q))), sec. 3.2
  *          (one target forward over the gamma drafts, drop rejected KV),
@@ -21,7 +22,10 @@
  *          "Modified Rejection Sampling" (test, resample, stop, bonus from the
  *          last verify row), section on cross-device tensor alignment (draft
  *          probabilities zero-padded from 151936 to 152064), section on the
- *          hidden KV position bug (the pending token's KV must be committed).
+ *          hidden KV position bug (the pending token's KV must be committed),
+ *          implementation architecture (the KV in a block tensor behind a
+ *          block table: the paged cache, which the tests gather into the
+ *          contiguous one this oracle takes).
  *   [SUB]  "SubSpec (NeurIPS'25)" summary: sec. 4.2 (draft token trees verified
  *          by the target in one pass).
  *
