@@ -9,12 +9,16 @@ than the 129 MB L2 (the KV cache of all layers plus the LM-head weights), so
 no L2 flush is needed between steps.
 
 Default workload: the 28-layer Qwen2.5-1.5B-shaped round (t = 4096, k = 4,
-batch 1, greedy).  `--workload` selects another (0, 1, 2, 3, 3b16, 3s, 3b16s, 4 = draft tree).
+batch 1, greedy).  `--workload` selects another (0, 1, 2, 3, 3b16, 3s, 3b16s,
+4 = draft tree greedy, 4s = draft tree sampled).  The line's `workloads`
+object summarises other workloads (`--side`, default the 7B batch-16 round
+and the B = 64 sampled acceptance), timed the same way.
 
 Timing: the step is captured into a CUDA graph through the library's C ABI;
-the timed region replays a graph of `chunk` steps (K steps in total) between
-CUDA events on the launching stream; per-kernel durations come from event
-nodes captured inside that graph (the last replay of the timed region).
+the timed region replays a graph of `chunk` steps (K steps in total, no
+event nodes in it) between CUDA events on the launching stream.  Per-kernel
+durations come from one replay, after the timed region, of the same chunk
+captured with event nodes around each kernel class.
 
 `--impl reference` times the CPU oracle instead (a bounded sample of the
 same workload on the host cores).  Multi-GPU (torchrun): independent replicas,
@@ -71,7 +75,7 @@ def workload_from_name(name: str):
         "0": (0, {}, "greedy"), "1": (1, {}, "greedy"), "2": (2, {}, "sampled"),
         "3": (3, {}, "greedy"), "3s": (3, {}, "sampled"),
         "3b16": (3, {"B": 16}, "greedy"), "3b16s": (3, {"B": 16}, "sampled"),
-        "4": (4, {}, "greedy"),
+        "4": (4, {}, "greedy"), "4s": (4, {}, "sampled"),
     }
     wid, over, mode = table[name]
     return synth.workload(wid, **over), mode
@@ -97,8 +101,25 @@ def greedy_bytes(w) -> int:
     return w.B * w.R * w.V * 4
 
 
+def argmax_key_bytes(w) -> int:
+    """The LM head's greedy argmax keys: one uint64 per row and 128 columns."""
+    return w.B * w.R * ((w.V + 127) // 128) * 8
+
+
+def lm_argmax_bytes(w) -> int:
+    """LM head with the argmax in its epilogue and no logits written."""
+    N = w.B * w.R
+    return w.H * w.V * 2 + N * w.H * 2 + argmax_key_bytes(w)
+
+
 def sample_bytes(w, n_acc: np.ndarray) -> int:
+    """Chain: every row's logits once, the q row of the rejecting row, the
+    ratio test's p and q entries.  Tree: every row's logits once plus one q
+    row per sequence (a lower bound: each rejected sibling's node reads its q
+    row once more)."""
     k = w.R - 1
+    if w.tree:
+        return w.B * w.R * w.V * 4 + w.B * w.draft_vocab * 4
     rejected = int(np.sum(n_acc < k))
     return w.B * w.R * w.V * 4 + rejected * w.draft_vocab * 4 + w.B * k * 8
 
@@ -131,9 +152,12 @@ def load_peaks():
 class Round:
     """Device buffers and the sequence of C-ABI calls of one verify round."""
 
-    def __init__(self, w, mode, device):
+    def __init__(self, w, mode, device, fused=True):
         from speculative_decoding_verification_sv_gb300 import binding as sv
         self.sv, self.w, self.mode, self.dev = sv, w, mode, device
+        # greedy rounds: argmax keys from the LM head's epilogue, then acceptance
+        # and commit in one launch (no logits written)
+        self.fused = fused and mode == "greedy" and w.L > 0
         B, R, V = w.B, w.R, w.V
         self.has_model = w.L > 0
         if self.has_model:
@@ -159,8 +183,14 @@ class Round:
             else:
                 # draft distributions around the round's actual target logits
                 sv.lm_head(self.hid, self.W, logits=self.logits)
-                si = synth.sample_inputs(B, R - 1, V, wid=w.wid, device=device,
-                                         logits=self.logits.reshape(B, R, V).clone())
+                if w.tree:
+                    # sample_inputs draws the children of one shared tree
+                    assert B == 1 or bool((par == par[0]).all())
+                    si = synth.sample_inputs(B, R - 1, V, wid=w.wid, device=device, Vq=w.draft_vocab,
+                                             logits=self.logits.reshape(B, R, V).clone(), parent=par[0])
+                else:
+                    si = synth.sample_inputs(B, R - 1, V, wid=w.wid, device=device, Vq=w.draft_vocab,
+                                             logits=self.logits.reshape(B, R, V).clone())
                 self.q_draft, self.tok = si.q, si.tok
         else:
             self.parent = None
@@ -172,7 +202,10 @@ class Round:
         self.n_acc = self.out_buf[:B]
         self.out_tok = self.out_buf[B:2 * B]
         self.path = self.out_buf[2 * B:].view(B, R)
-        if mode == "greedy":
+        if self.fused:
+            self.amax = torch.empty(B * R, (V + 127) // 128, dtype=torch.int64, device=device)
+            self.acc_ws = None
+        elif mode == "greedy":
             self.acc_ws = torch.empty(sv.lib.sv_accept_greedy_workspace(B, R, V), dtype=torch.uint8, device=device)
         else:
             self.acc_ws = torch.empty(sv.lib.sv_accept_sample_workspace(B, R, V), dtype=torch.uint8, device=device)
@@ -186,7 +219,11 @@ class Round:
             N = self.w.B * self.w.R                  # LM head: <= 16 rows per 64-row pass, else 256
             n += (N + 63) // 64 if N <= 16 else (N + 255) // 256
             n += 1                                   # commit
-        n += 2 if self.mode == "greedy" else 4      # accept: greedy two kernels; sampled chain: stats + three
+        if self.fused:
+            return n   # acceptance and commit: the one launch counted above
+        # accept: greedy two kernels; sampled chain: statistics + three; sampled
+        # tree: statistics + one cluster walk
+        n += 2 if self.mode == "greedy" else (2 if self.w.tree else 4)
         return n
 
     def step(self, ev=None):
@@ -204,6 +241,15 @@ class Round:
                                parent=self.parent, out=self.attn_out[l], ws=self.attn_ws, cache_ready=l > 0)
             rec("attn1")
             # the weights are never written by the kernel before
+            if self.fused:
+                sv.lm_head_argmax(self.hid, self.W, argmax=self.amax, write_logits=False, weights_ready=True)
+                rec("lm1")
+                sv.accept_greedy_commit(self.amax, self.tok, w.V, parent=self.parent, n_acc=self.n_acc,
+                                        out_tok=self.out_tok, path=self.path, k_cache=self.kc, v_cache=self.vc,
+                                        k_blk=self.kb, v_blk=self.vb, length=self.length)
+                rec("acc1")
+                rec("commit1")
+                return
             sv.lm_head(self.hid, self.W, logits=self.logits, weights_ready=True)
             rec("lm1")
         else:
@@ -351,7 +397,9 @@ class OracleRound:
         if mode == "greedy":
             self.tok = np.zeros((B, R), np.int32)
         else:
-            si = synth.sample_inputs(B, R - 1, V, wid=w.wid, logits=torch.from_numpy(self.logits))
+            par = getattr(self, "parent", None)
+            si = synth.sample_inputs(B, R - 1, V, wid=w.wid, logits=torch.from_numpy(self.logits),
+                                     parent=None if par is None else par[0])
             self.qd, self.tok = si.q.numpy(), si.tok.numpy()
         self.units = len(self.attn_units)
 
@@ -385,7 +433,8 @@ class OracleRound:
         if self.mode == "greedy":
             n_acc, _, path = o.accept_greedy(self.logits, self.tok, getattr(self, "parent", None))
         else:
-            n_acc, _, path = o.accept_sample(self.logits, self.qd, self.tok, seed=0x5EED)
+            n_acc, _, path = o.accept_sample(self.logits, self.qd, self.tok, getattr(self, "parent", None),
+                                             seed=0x5EED)
         # commit of every layer: the same per-layer copy, done L times
         for _ in range(w.L):
             o.kv_commit(self.kc[None], self.vc[None], self.kb[None], self.vb[None], path, n_acc,
@@ -448,11 +497,11 @@ def max_over_ranks(x: float, ws: int, device) -> float:
     return float(t.item())
 
 
-def config_dict(w, mode, ws, chunk):
+def config_dict(w, mode, ws):
     return {"workload": w.name if mode == "greedy" or w.L == 0 else w.name.replace("greedy", "sampled"),
             "layers": w.L, "batch": w.B, "k": w.R - 1, "context": w.t, "q_heads": w.Hq, "kv_heads": w.Hkv,
             "head_dim": w.D, "hidden": w.H, "vocab": w.V, "acceptance": mode, "parallelism": f"replicas{ws}",
-            "l2": "inputs larger than L2 every step (no flush)", "graph_chunk": chunk}
+            "l2": "inputs larger than L2 every step (no flush)"}
 
 
 def run_reference(args, ws, rank):
@@ -480,12 +529,160 @@ def run_reference(args, ws, rank):
     line = {"metric": "verify steps/s", "value": value, "unit": "steps/s", "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": 1000.0 * dt / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64 attention/LM head, f32 acceptance",
-            "data": "synthetic", "impl": "reference", "config": config_dict(w, mode, ws, 0),
+            "data": "synthetic", "impl": "reference", "config": config_dict(w, mode, ws),
             "draft_tokens_per_s": value * w.B * (w.R - 1),
             "cpu_baseline": {"value": value, "unit": "steps/s", "cores": orc.oracle.num_threads(),
                              "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": "steps/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
+
+
+KINDS = ["attn0", "attn1", "lm1", "acc1", "commit1"]
+
+
+def chunk_for(K: int) -> int:
+    """Steps per captured graph: the largest divisor of K up to 100."""
+    return max(d for d in range(1, min(100, K) + 1) if K % d == 0)
+
+
+def capture_round(rnd, chunk, stream):
+    """Captures one step (g1), `chunk` steps without event nodes (gC, the
+    timed graph), and the same `chunk` steps with external event nodes
+    around each kernel class (gE, replayed once after the timed region for
+    the per-kernel durations)."""
+    torch.cuda.synchronize()
+    # eager warm-up (library attributes, tensor-map driver entry point)
+    with torch.cuda.stream(stream):
+        rnd.step()
+    torch.cuda.synchronize()
+    g1 = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g1, stream=stream):
+        rnd.step()
+    try:
+        evs = [{k: torch.cuda.Event(enable_timing=True, external=True) for k in KINDS} for _ in range(chunk)]
+        in_graph = True
+    except TypeError:   # torch without external (graph-node) events
+        evs = [{k: torch.cuda.Event(enable_timing=True) for k in KINDS} for _ in range(chunk)]
+        in_graph = False
+    gC = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gC, stream=stream):
+        for _ in range(chunk):
+            rnd.step()
+    gE = None
+    if in_graph:
+        gE = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gE, stream=stream):
+            for i in range(chunk):
+                rnd.step(evs[i])
+    torch.cuda.synchronize()
+    return g1, gC, gE, evs, in_graph
+
+
+def per_kernel_times(rnd, gE, evs, in_graph, chunk, stream):
+    """Average seconds per step of each kernel class, from one replay of the
+    event graph (or, without graph-node events, `chunk` eager rounds)."""
+    with torch.cuda.stream(stream):
+        if in_graph:
+            gE.replay()
+        else:
+            for i in range(chunk):
+                rnd.step(evs[i])
+    torch.cuda.synchronize()
+
+    def avg(a, b):
+        return statistics.mean(evs[i][a].elapsed_time(evs[i][b]) for i in range(chunk)) / 1000.0
+    return avg("attn0", "attn1"), avg("attn1", "lm1"), avg("lm1", "acc1"), avg("acc1", "commit1")
+
+
+def kernel_table(w, mode, times, n_acc, hbm, fused=False):
+    t_attn, t_lm, t_acc, t_commit = times
+    kern = {}
+    if fused:
+        kern["verify_attn"] = {"launches_per_step": w.L, "bytes_per_launch": attn_bytes(w),
+                               "us_per_launch": 1e6 * t_attn / w.L,
+                               "gbs": attn_bytes(w) * w.L / t_attn / 1e9}
+        kern["lm_head_argmax"] = {"launches_per_step": 1, "bytes_per_launch": lm_argmax_bytes(w),
+                                  "us_per_launch": 1e6 * t_lm, "gbs": lm_argmax_bytes(w) / t_lm / 1e9}
+        ab = argmax_key_bytes(w) + commit_bytes(w, n_acc)
+        kern["accept_greedy_commit"] = {"launches_per_step": 1, "bytes_per_launch": ab, "us_per_launch": 1e6 * t_acc,
+                                        "gbs": ab / t_acc / 1e9}
+        for v in kern.values():
+            v["us_per_step"] = v["us_per_launch"] * v["launches_per_step"]
+            v["frac_of_peak"] = v["gbs"] / hbm
+        return kern
+    if w.L > 0:
+        kern["verify_attn"] = {"launches_per_step": w.L, "bytes_per_launch": attn_bytes(w),
+                               "us_per_launch": 1e6 * t_attn / w.L,
+                               "gbs": attn_bytes(w) * w.L / t_attn / 1e9}
+        kern["lm_head"] = {"launches_per_step": 1, "bytes_per_launch": lm_bytes(w), "us_per_launch": 1e6 * t_lm,
+                           "gbs": lm_bytes(w) / t_lm / 1e9}
+        kern["kv_commit"] = {"launches_per_step": 1, "bytes_per_launch": commit_bytes(w, n_acc),
+                             "us_per_launch": 1e6 * t_commit, "gbs": commit_bytes(w, n_acc) / t_commit / 1e9}
+    ab = greedy_bytes(w) if mode == "greedy" else sample_bytes(w, n_acc)
+    kern["accept_" + mode] = {"launches_per_step": 1, "bytes_per_launch": ab, "us_per_launch": 1e6 * t_acc,
+                              "gbs": ab / t_acc / 1e9}
+    for v in kern.values():
+        v["us_per_step"] = v["us_per_launch"] * v["launches_per_step"]
+        v["frac_of_peak"] = v["gbs"] / hbm
+    return kern
+
+
+def step_bytes(kern) -> int:
+    return sum(v["bytes_per_launch"] * v["launches_per_step"] for v in kern.values())
+
+
+def time_round(rnd, K, warmup, ws, stream, clocks=None):
+    """Times exactly K steps of the event-free graph between CUDA events on
+    the launching stream (barrier and synchronise on both sides, max over
+    ranks), then replays the event graph once, outside the timed region, for
+    the per-kernel durations.  Returns (ms_total, chunk, times, g1, clk)."""
+    chunk = chunk_for(K)
+    g1, gC, gE, evs, in_graph = capture_round(rnd, chunk, stream)
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            g1.replay()
+    torch.cuda.synchronize()
+    if clocks is not None:
+        clocks.start()
+        time.sleep(0.3)
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    barrier(ws)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        t_start.record()
+        for _ in range(K // chunk):
+            gC.replay()
+        t_end.record()
+    torch.cuda.synchronize()
+    barrier(ws)
+    clk = clocks.stop() if clocks is not None else None
+    ms_local = t_start.elapsed_time(t_end)
+    times = per_kernel_times(rnd, gE, evs, in_graph, chunk, stream)
+    return ms_local, chunk, times, in_graph, g1, clk
+
+
+def side_workload(name, dev, stream, hbm, steps=40, warmup=5):
+    """A compact record of another workload's round, timed the same way
+    (event-free graph, then one event-graph replay): steps/s, the whole
+    step's fraction of the HBM roofline, and each kernel class's time and
+    fraction."""
+    w, mode = workload_from_name(name)
+    rnd = Round(w, mode, dev)
+    ms, chunk, times, _, _, _ = time_round(rnd, steps, warmup, 1, stream)
+    n_acc = rnd.n_acc.cpu().numpy()
+    kern = kernel_table(w, mode, times, n_acc, hbm, fused=rnd.fused)
+    ms_step = ms / steps
+    rec = {"workload": w.name if mode == "greedy" or w.L == 0 else w.name.replace("greedy", "sampled"),
+           "steps_per_s": 1000.0 / ms_step, "ms_per_step": ms_step, "steps": steps,
+           "step_frac": step_bytes(kern) / (ms_step / 1000.0) / 1e9 / hbm,
+           "kernels": {k: {"us_per_launch": round(v["us_per_launch"], 3),
+                           "launches_per_step": v["launches_per_step"],
+                           "frac_of_peak": round(v["frac_of_peak"], 4)} for k, v in kern.items()}}
+    del rnd
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return rec
 
 
 def main():
@@ -500,6 +697,10 @@ def main():
     ap.add_argument("--layers", type=int, default=None, help="override the layer count (small profiling cases)")
     ap.add_argument("--ref-seconds", type=float, default=150.0,
                     help="host-time budget of the reference (oracle) arm's timed steps")
+    ap.add_argument("--unfused", action="store_true",
+                    help="greedy rounds: LM head logits, then argmax, finish and commit as separate launches")
+    ap.add_argument("--side", default="3b16,2",
+                    help="other workloads summarised in the line's `workloads` object ('' for none)")
     args = ap.parse_args()
     ws, rank, local = dist_setup()
     if args.impl == "reference":
@@ -515,103 +716,34 @@ def main():
     if args.layers is not None:
         from dataclasses import replace
         w = replace(w, L=args.layers, name=w.name.replace("28-layer", f"{args.layers}-layer"))
-    rnd = Round(w, mode, dev)
+    rnd = Round(w, mode, dev, fused=not args.unfused)
     rnd.pack_inputs()
 
     K = args.steps
-    chunk = max(d for d in range(1, min(100, K) + 1) if K % d == 0)
     stream = torch.cuda.Stream(device=dev)
-    kinds = ["attn0", "attn1", "lm1", "acc1", "commit1"]
-    torch.cuda.synchronize()
-    # eager warm-up (library attributes, tensor-map driver entry point)
-    with torch.cuda.stream(stream):
-        rnd.step()
-    torch.cuda.synchronize()
-    g1 = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g1, stream=stream):
-        rnd.step()
-    try:
-        evs = [{k: torch.cuda.Event(enable_timing=True, external=True) for k in kinds} for _ in range(chunk)]
-        in_graph_events = True
-    except TypeError:   # torch without external (graph-node) events
-        evs = [{k: torch.cuda.Event(enable_timing=True) for k in kinds} for _ in range(chunk)]
-        in_graph_events = False
-    gC = torch.cuda.CUDAGraph()          # chunk rounds, no events
-    with torch.cuda.graph(gC, stream=stream):
-        for i in range(chunk):
-            rnd.step()
-    gE = gC
-    if in_graph_events:                  # the same chunk with event nodes (last replay only)
-        gE = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(gE, stream=stream):
-            for i in range(chunk):
-                rnd.step(evs[i])
-    torch.cuda.synchronize()
-
-    with torch.cuda.stream(stream):
-        for _ in range(args.warmup):
-            g1.replay()
-    torch.cuda.synchronize()
-
     clocks = ClockSampler(device_uuid(dev))
-    clocks.start()
-    time.sleep(0.3)
-    t_start = torch.cuda.Event(enable_timing=True)
-    t_end = torch.cuda.Event(enable_timing=True)
-    barrier(ws)
-    torch.cuda.synchronize()
-    with torch.cuda.stream(stream):
-        t_start.record()
-        for _ in range(K // chunk - 1):
-            gC.replay()
-        gE.replay()
-        t_end.record()
-    torch.cuda.synchronize()
-    barrier(ws)
-    clk = clocks.stop()
-    ms_local = t_start.elapsed_time(t_end)
+    ms_local, chunk, times, in_graph, g1, clk = time_round(rnd, K, args.warmup, ws, stream, clocks)
     ms_total = max_over_ranks(ms_local, ws, dev)
     ms_per_step = ms_total / K
     value = ws * K / (ms_total / 1000.0)
 
-    # per-kernel durations from the event nodes of the last replay (or, without
-    # graph-node events, from `chunk` eager rounds timed the same way)
-    if not in_graph_events:
-        with torch.cuda.stream(stream):
-            for i in range(chunk):
-                rnd.step(evs[i])
-        torch.cuda.synchronize()
-
-    def avg(a, b):
-        return statistics.mean(evs[i][a].elapsed_time(evs[i][b]) for i in range(chunk)) / 1000.0
-    t_attn = avg("attn0", "attn1")
-    t_lm = avg("attn1", "lm1")
-    t_acc = avg("lm1", "acc1")
-    t_commit = avg("acc1", "commit1")
     n_acc = rnd.n_acc.cpu().numpy()
     hbm, peak_kind = load_peaks()
-    kern = {}
-    if w.L > 0:
-        kern["verify_attn"] = {"launches_per_step": w.L, "bytes_per_launch": attn_bytes(w),
-                               "us_per_launch": 1e6 * t_attn / w.L,
-                               "gbs": attn_bytes(w) * w.L / t_attn / 1e9}
-        kern["lm_head"] = {"launches_per_step": 1, "bytes_per_launch": lm_bytes(w), "us_per_launch": 1e6 * t_lm,
-                           "gbs": lm_bytes(w) / t_lm / 1e9}
-        kern["kv_commit"] = {"launches_per_step": 1, "bytes_per_launch": commit_bytes(w, n_acc),
-                             "us_per_launch": 1e6 * t_commit, "gbs": commit_bytes(w, n_acc) / t_commit / 1e9}
-    ab = greedy_bytes(w) if mode == "greedy" else sample_bytes(w, n_acc)
-    kern["accept_" + mode] = {"launches_per_step": 1, "bytes_per_launch": ab, "us_per_launch": 1e6 * t_acc,
-                              "gbs": ab / t_acc / 1e9}
-    for v in kern.values():
-        v["frac_of_peak"] = v["gbs"] / hbm
-    dom = max(kern, key=lambda k: kern[k]["bytes_per_launch"] * kern[k]["launches_per_step"])
+    kern = kernel_table(w, mode, times, n_acc, hbm, fused=rnd.fused)
+    # the roofline block describes the kernel class that takes the most time
+    # per step (not the one that moves the most bytes)
+    dom = max(kern, key=lambda k: kern[k]["us_per_step"])
     dk = kern[dom]
     tr = TRAFFIC.get((args.workload, dom))
     traffic = tr["bytes"] if tr and tr["src_hash"] == src_hash(tr["src"]) else None
+    sb = step_bytes(kern)
     roofline = {"kernel": dom, "bound": "hbm", "achieved": dk["gbs"], "peak": hbm, "unit": "GB/s",
                 "frac": dk["gbs"] / hbm, "traffic": traffic, "peak_source": f"hbm_gbs of {peak_kind}",
                 "bytes_per_launch": dk["bytes_per_launch"], "us_per_launch": dk["us_per_launch"],
-                "timing": "CUDA-event nodes inside the timed graph" if in_graph_events else "eager rounds with events"}
+                "share_of_step": dk["us_per_step"] / (1000.0 * ms_per_step),
+                "step_bytes": sb, "step_frac": sb / (ms_per_step / 1000.0) / 1e9 / hbm,
+                "timing": ("CUDA-event nodes in one replay of the round graph after the timed region"
+                           if in_graph else "eager rounds with events after the timed region")}
 
     # end to end through the public API: pinned H2D of the round's inputs, one
     # replay of the captured round, D2H of the accepted tokens, host sync
@@ -668,21 +800,34 @@ def main():
     # top-1 / top-2 margin is below 1e-2 max|logit| (counted, not failed)
     near_ties = None
     if mode == "greedy":
+        if rnd.fused:   # the timed rounds write no logits: one LM head for them here
+            rnd.sv.lm_head(rnd.hid, rnd.W, logits=rnd.logits)
         lg = rnd.logits.float()
         top2 = torch.topk(lg, 2, dim=-1).values
         bound = 1e-2 * float(lg.abs().max())
         near_ties = {"rows": int(lg.shape[0]), "below_bound": int(((top2[:, 0] - top2[:, 1]) < bound).sum()),
                      "bound": bound}
+    launches = rnd.launches_per_step()
+    del rnd, gX, g1
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+
+    # the other workloads the metric is quoted at (7B batch 16; sampled B = 64)
+    side = {}
+    for name in [n for n in args.side.split(",") if n and n != args.workload]:
+        side[name] = side_workload(name, dev, stream, hbm)
 
     line = {"metric": "verify steps/s", "value": value, "unit": "steps/s", "n_gpus": ws, "steps": K,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16 (fp32 accumulate; fp32 acceptance)",
             "data": "synthetic (seeded, Qwen2.5-shaped, random weights)",
-            "config": config_dict(w, mode, ws, chunk),
+            "config": config_dict(w, mode, ws), "graph_chunk": chunk,
             "draft_tokens_per_s": value * w.B * (w.R - 1),
             "mean_accepted": float(np.mean(n_acc)),
             "roofline": roofline, "kernels": kern, "e2e": e2e, "clocks": clk, "greedy_near_ties": near_ties,
-            "gpu_launches": rnd.launches_per_step() * K}
+            "gpu_launches": launches * K}
+    if side:
+        line["workloads"] = side
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, mode)
     if rank == 0:

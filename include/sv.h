@@ -208,6 +208,30 @@ SV_API sv_status sv_lm_head(const uint16_t* hid, const uint16_t* W, float* logit
 SV_API sv_status sv_lm_head_ex(const uint16_t* hid, const uint16_t* W, float* logits, int32_t N, int32_t H,
                                int32_t V, uint32_t flags, void* stream);
 
+/* The LM head with the greedy argmax folded into its epilogue ([SCS] sec. 3:
+ * greedy verification needs only each row's top-1 token; [SCS] sec. 7.1:
+ * the round's control plane -- syncs, token movement, launches after the
+ * target forward -- is worth trimming).  As sv_lm_head_ex, and in addition,
+ * for every row n and 128-column slab s (S = ceil(V / 128) slabs):
+ *     argmax[n][s] = the largest key(logits[n][v]) over v in slab s,
+ *     key(x, v) = (okey(x) << 32) | (~v & 0xffffffff)  (uint64),
+ * where okey(NaN) = 0 and, for every other x, okey(x) is x's bit pattern
+ * (with -0 taken as +0) mapped to an unsigned word in the order of the floats
+ * (sign bit set: all bits flipped; else the sign bit set).  The row's greedy
+ * token -- largest logit, NaN skipped, lowest column on ties, as
+ * sv_accept_greedy takes it -- is the complement of the low word of the
+ * row's largest key (column 0 when that key's high word is 0: only NaN).
+ *   logits  [N][V] fp32, or NULL: the logits are then not written (a greedy
+ *           round that needs only the tokens)
+ *   argmax  [N][S] uint64, caller-owned, at least sv_lm_head_argmax_bytes
+ *           (N, V) bytes (else SV_ERR_WORKSPACE)
+ * NaN logits set SV_DEVERR_NONFINITE.  Other arguments, flags and errors as
+ * for sv_lm_head_ex. */
+#define SV_ARGMAX_SLAB 128
+SV_API size_t sv_lm_head_argmax_bytes(int32_t N, int32_t V);
+SV_API sv_status sv_lm_head_argmax(const uint16_t* hid, const uint16_t* W, float* logits, int32_t N, int32_t H,
+                                   int32_t V, uint64_t* argmax, size_t argmax_bytes, uint32_t flags, void* stream);
+
 /* ------------------------------------------------------------------------ */
 /* Greedy acceptance ([SCS] sec. 3 and 3.1).                                 */
 /* ------------------------------------------------------------------------ */
@@ -226,6 +250,26 @@ SV_API size_t sv_accept_greedy_workspace(int32_t B, int32_t R, int32_t V);
 SV_API sv_status sv_accept_greedy(const float* logits, const int32_t* tok, const int32_t* parent, int32_t B,
                            int32_t R, int32_t V, int32_t* n_acc, int32_t* out_tok, int32_t* path,
                            void* ws, size_t ws_bytes, void* stream);
+
+/* Greedy acceptance and the KV commit in one launch, from the argmax keys
+ * of sv_lm_head_argmax ([SCS] sec. 3 and 3.1 for the acceptance; [SCS] sec.
+ * 3.2, [TUT] sec. 3.2 and [SUB] sec. 4.2 for the commit; [SCS] sec. 7.1: one
+ * launch instead of three after the target forward).  The result is that of
+ * sv_accept_greedy on the same logits followed by sv_kv_commit:
+ *   argmax [B*R][ceil(V/128)] uint64 keys (row b*R + j is sequence b's block
+ *          row j), as written by sv_lm_head_argmax;
+ *   tok, parent, n_acc, out_tok, path as for sv_accept_greedy;
+ *   k_cache, v_cache, k_blk, v_blk, L, Hkv, D, T_cap, len as for
+ *          sv_kv_commit (len updated in place).
+ * k_cache == NULL (with v_cache, k_blk, v_blk NULL; L, Hkv, D, T_cap, len
+ * ignored) gives greedy acceptance alone.  Errors: those of the two calls
+ * (a sequence whose commit would pass T_cap still gets its acceptance
+ * outputs, and its cache and length are left untouched, SV_DEVERR_LENGTH). */
+SV_API sv_status sv_accept_greedy_commit(const uint64_t* argmax, const int32_t* tok, const int32_t* parent,
+                                         int32_t B, int32_t R, int32_t V, int32_t* n_acc, int32_t* out_tok,
+                                         int32_t* path, uint16_t* k_cache, uint16_t* v_cache, const uint16_t* k_blk,
+                                         const uint16_t* v_blk, int32_t L, int32_t Hkv, int32_t D, int32_t T_cap,
+                                         int32_t* len, void* stream);
 
 /* ------------------------------------------------------------------------ */
 /* Relaxed, lossy acceptance ([SCS] sec. 7.2: the Delta-logit relaxation).   */
@@ -303,7 +347,14 @@ SV_API sv_status sv_accept_sample(const float* logits, const float* q, int32_t V
  *     entry needs to start at zero); calls that overlap on the GPU race on it,
  *     so order them on one stream or with events;
  *   - the first call on a device looks up the array's device address and
- *     caches it; make that first call before any stream capture.
+ *     caches it; make that first call before any stream capture.  A device
+ *     reset (cudaDeviceReset) loads the library's device code anew, so the
+ *     first call after it looks the address up again (make that call, too,
+ *     outside any capture);
+ *   - chains and trees alike are walked by one thread-block cluster per
+ *     sequence (the path sv_accept_sample takes for trees), since the array
+ *     holds only the row statistics; the results are those of
+ *     sv_accept_sample bit for bit.
  * No cudaMalloc, cudaFree or other allocating call is made. */
 SV_API sv_status sv_accept_sample_noalloc(const float* logits, const float* q, int32_t Vq, const int32_t* tok,
                                           const int32_t* parent, int32_t B, int32_t R, int32_t V,

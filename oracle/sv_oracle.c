@@ -29,7 +29,7 @@
  *   [SUB]  "SubSpec (NeurIPS'25)" summary: sec. 4.2 (draft token trees verified
  *          by the target in one pass).
  *
- * Readings adopted where the pages are silent (each also listed in the design doc):
+ * Readings adopted where the pages are silent:
  *   - the verify block has R = k+1 rows: row 0 is the pending committed token
  *     c, rows 1..k the drafts; row j is [SCS] sec. 3.1's rows[j-1] and row 0 is
  *     its saved_next;

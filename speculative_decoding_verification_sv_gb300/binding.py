@@ -65,13 +65,19 @@ def _load():
     L.sv_kv_commit_paged.argtypes = [_P, _P, _I32, _P, _I32, _P, _P, _I32, _I32, _I32, _I32, _I32, _P, _P, _P, _P]
     L.sv_verify_attn_paged.argtypes = [_P, _P, _P, _P, _I32, _P, _I32, _P, _P, _P, _P, ctypes.c_float, _P, _P, _SZ,
                                        ctypes.c_uint32, _P]
+    L.sv_lm_head_argmax_bytes.argtypes = [_I32, _I32]
+    L.sv_lm_head_argmax_bytes.restype = _SZ
+    L.sv_lm_head_argmax.argtypes = [_P, _P, _P, _I32, _I32, _I32, _P, _SZ, ctypes.c_uint32, _P]
+    L.sv_accept_greedy_commit.argtypes = [_P, _P, _P, _I32, _I32, _I32, _P, _P, _P, _P, _P, _P, _P, _I32, _I32, _I32,
+                                          _I32, _P, _P]
     L.sv_diag_exp.argtypes = [_P, _P, _I64, _P]
     L.sv_diag_philox.argtypes = [_P, _P, _P, _I64, _P]
     L.sv_diag_canon.argtypes = [_P, _I32, _I32, _P, _P, _P, _P]
     for fn in ("sv_verify_attn", "sv_verify_attn_ex", "sv_lm_head", "sv_lm_head_ex", "sv_accept_greedy",
                "sv_accept_greedy_relaxed", "sv_accept_sample",
                "sv_accept_sample_noalloc", "sv_kv_commit", "sv_kv_commit_paged", "sv_verify_attn_paged",
-               "sv_diag_exp", "sv_diag_philox", "sv_diag_canon", "sv_get_device_error"):
+               "sv_diag_exp", "sv_diag_philox", "sv_diag_canon", "sv_get_device_error", "sv_lm_head_argmax",
+               "sv_accept_greedy_commit"):
         getattr(L, fn).restype = ctypes.c_int
     return L
 
@@ -195,6 +201,52 @@ def lm_head(hid, W, logits=None, stream=None, weights_ready=False):
                                               _ptr(logits, torch.float32, "logits"), N, H, V,
                                               LM_WEIGHTS_READY if weights_ready else 0, _stream(stream)))
     return logits
+
+
+ARGMAX_SLAB = 128   # vocab columns summarised by one argmax key (SV_ARGMAX_SLAB)
+
+
+def lm_head_argmax(hid, W, logits=None, argmax=None, stream=None, weights_ready=False, write_logits=True):
+    """hid [N,H] bf16; W [H,V] bf16 -> (logits [N,V] fp32 or None, argmax keys
+    [N, ceil(V/128)] int64 holding the uint64 keys of sv_lm_head_argmax).
+    write_logits=False passes NULL: only the keys are written."""
+    N, H = hid.shape
+    V = W.shape[1]
+    if write_logits and logits is None:
+        logits = torch.empty(N, V, dtype=torch.float32, device=hid.device)
+    if not write_logits:
+        logits = None
+    S = (V + ARGMAX_SLAB - 1) // ARGMAX_SLAB
+    if argmax is None:
+        argmax = torch.empty(N, S, dtype=torch.int64, device=hid.device)
+    nbytes = int(lib.sv_lm_head_argmax_bytes(N, V))
+    if argmax.numel() * argmax.element_size() < nbytes:
+        raise ValueError("argmax buffer too small")
+    _check("sv_lm_head_argmax", lib.sv_lm_head_argmax(
+        _ptr(hid, torch.bfloat16, "hid"), _ptr(W, torch.bfloat16, "W"), _ptr(logits, torch.float32, "logits"), N, H,
+        V, _ptr(argmax, torch.int64, "argmax"), nbytes, LM_WEIGHTS_READY if weights_ready else 0, _stream(stream)))
+    return logits, argmax
+
+
+def accept_greedy_commit(argmax, tok, V, parent=None, n_acc=None, out_tok=None, path=None, k_cache=None,
+                         v_cache=None, k_blk=None, v_blk=None, length=None, stream=None):
+    """Greedy acceptance from lm_head_argmax's keys [B*R, S] and, when the
+    caches are given (caches [L,B,Hkv,T_cap,D], blocks [L,B,Hkv,R,D] bf16,
+    length [B] int32 updated in place), the KV commit, in one launch.
+    Returns (n_acc [B], out_tok [B], path [B,R])."""
+    B, R = tok.shape
+    n_acc, out_tok, path = _accept_outputs(B, R, tok.device, n_acc, out_tok, path)
+    bf, i32 = torch.bfloat16, torch.int32
+    if k_cache is not None:
+        L, _, Hkv, T_cap, D = k_cache.shape
+    else:
+        L = Hkv = T_cap = D = 0
+    _check("sv_accept_greedy_commit", lib.sv_accept_greedy_commit(
+        _ptr(argmax, torch.int64, "argmax"), _ptr(tok, i32, "tok"), _ptr(parent, i32, "parent"), B, R, V,
+        _ptr(n_acc, i32), _ptr(out_tok, i32), _ptr(path, i32), _ptr(k_cache, bf, "k_cache"),
+        _ptr(v_cache, bf, "v_cache"), _ptr(k_blk, bf, "k_blk"), _ptr(v_blk, bf, "v_blk"), L, Hkv, D, T_cap,
+        _ptr(length, i32, "len"), _stream(stream)))
+    return n_acc, out_tok, path
 
 
 def _accept_outputs(B, R, device, n_acc, out_tok, path):

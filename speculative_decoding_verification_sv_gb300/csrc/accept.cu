@@ -142,32 +142,6 @@ __global__ void __launch_bounds__(kGreedyThreads) greedy_partial_kernel(const fl
     }
 }
 
-// Children of node u in index order, for a chain (parent == nullptr: the only
-// child of u is u+1) or a tree.
-__device__ __forceinline__ int next_child(const int* par, int R, int u, int after) {
-    if (par == nullptr) return (after < 0 && u + 1 < R) ? u + 1 : -1;
-    for (int c = (after < 0 ? u + 1 : after + 1); c < R; ++c)
-        if (par[c] == u) return c;
-    return -1;
-}
-
-// Loads and validates the tree of sequence b into shared memory; returns
-// false (and raises SV_DEVERR_TREE) if it is malformed.
-__device__ bool load_tree(const int32_t* parent, int b, int R, int* par_s, unsigned int* err) {
-    __shared__ int bad;
-    if (threadIdx.x == 0) bad = 0;
-    __syncthreads();
-    for (int j = threadIdx.x; j < R; j += blockDim.x) {
-        const int p = parent[static_cast<size_t>(b) * R + j];
-        par_s[j] = p;
-        if ((j == 0 && p != -1) || (j > 0 && (p < 0 || p >= j))) bad = 1;
-    }
-    __syncthreads();
-    const bool ok = bad == 0;
-    if (!ok && threadIdx.x == 0) raise_error(err, SV_DEVERR_TREE);
-    return ok;
-}
-
 __global__ void __launch_bounds__(128) greedy_finish_kernel(const int2* __restrict__ part, int nchunk,
                                                              const int32_t* __restrict__ tok,
                                                              const int32_t* __restrict__ parent, int R, int V,
@@ -1230,13 +1204,12 @@ cudaError_t launch_accept_sample(const float* logits, const float* q, int Vq, co
     const int nlocal = (nblk + kCluster - 1) / kCluster;
     const size_t smem = static_cast<size_t>(nlocal) * kBlk * sizeof(float);
     cudaError_t e = cudaSuccess;
-    static bool attr_set = false;   // once per process: the largest row (2^18 entries) fits
-    if (!attr_set) {
-        e = cudaFuncSetAttribute(sample_stats_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 kMaxLocalBlocks * kBlk * static_cast<int>(sizeof(float)));
-        if (e != cudaSuccess) return e;
-        attr_set = true;
-    }
+    static PerDeviceOnce attr_once;   // per device: the largest row (2^18 entries) fits
+    e = attr_once.run([]() {
+        return cudaFuncSetAttribute(sample_stats_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    kMaxLocalBlocks * kBlk * static_cast<int>(sizeof(float)));
+    });
+    if (e != cudaSuccess) return e;
     float2* stats = static_cast<float2*>(ws);
     // Few rows: an 8-CTA cluster per row keeps each row's latency short.  Many
     // rows: one CTA per row keeps every SM busy without cluster waves.

@@ -30,25 +30,27 @@
 namespace {
 
 constexpr int kNoAllocMaxRows = 8192;
-constexpr int kMaxDevices = 64;
+using sv::kMaxDevices;
 
 static __device__ __align__(256) float2 g_noalloc_stats[kNoAllocMaxRows];
 
-std::mutex g_noalloc_mu;
+sv::PerDeviceOnce g_noalloc_once;
 void* g_noalloc_addr[kMaxDevices] = {};
 
-// Device address of g_noalloc_stats on the current device (looked up once per
-// device); nullptr if the lookup fails.
+// Device address of g_noalloc_stats on the current device, looked up once per
+// device and again if the device's context has been replaced (after
+// cudaDeviceReset the module is loaded anew and the array may move); nullptr
+// if the lookup fails.
 void* noalloc_scratch() {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-    std::lock_guard<std::mutex> lk(g_noalloc_mu);
-    if (!g_noalloc_addr[dev]) {
+    const cudaError_t e = g_noalloc_once.run([dev]() {
         void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_noalloc_stats) != cudaSuccess) return nullptr;
-        g_noalloc_addr[dev] = p;
-    }
-    return g_noalloc_addr[dev];
+        const cudaError_t r = cudaGetSymbolAddress(&p, g_noalloc_stats);
+        g_noalloc_addr[dev] = r == cudaSuccess ? p : nullptr;
+        return r;
+    });
+    return e == cudaSuccess ? g_noalloc_addr[dev] : nullptr;
 }
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -71,9 +73,11 @@ extern "C" sv_status sv_accept_sample_noalloc(const float* logits, const float* 
     if (static_cast<int64_t>(B) * R > kNoAllocMaxRows) return SV_ERR_SHAPE;
     void* scratch = noalloc_scratch();
     if (!scratch) return SV_ERR_CUDA;
+    // Only the statistics' bytes are offered, so chains and trees alike take
+    // the one-cluster-per-sequence walk, which needs no other scratch.
+    const size_t stats = (static_cast<size_t>(B) * R * sizeof(float2) + 255) / 256 * 256;
     const cudaError_t e = sv::launch_accept_sample(logits, q, Vq, tok, parent, B, R, V, temperature, seed, step,
-                                                   uniforms, n_acc, out_tok, path, scratch,
-                                                   static_cast<size_t>(kNoAllocMaxRows) * sizeof(float2),
+                                                   uniforms, n_acc, out_tok, path, scratch, stats,
                                                    static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? SV_OK : SV_ERR_CUDA;
 }

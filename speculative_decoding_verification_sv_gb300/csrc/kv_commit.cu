@@ -34,6 +34,51 @@ constexpr int kThreads = 256;
 constexpr int kMaxR = 128;         // block rows (the ABI's bound)
 constexpr int kPage = 64;          // positions per page of a paged cache
 
+// Copies this CTA's share of the accepted rows (layers rank, rank + 8, ...)
+// of sequence b: block row path_s[i] -> cache slot t + i, for K and V, in
+// 16-byte pieces, eight loads in flight per thread before their stores.
+__device__ __forceinline__ void copy_accepted_rows(uint16_t* __restrict__ k_cache, uint16_t* __restrict__ v_cache,
+                                                   const uint16_t* __restrict__ k_blk,
+                                                   const uint16_t* __restrict__ v_blk, int L, int B, int Hkv, int D,
+                                                   int T_cap, int R, int b, int t, int m, int rank,
+                                                   const int* path_s, const int* page_s, bool paged, int num_pages) {
+    const int vec = D / 8;                    // 16-byte pieces per row
+    const int rows = m + 1;
+    const int per_layer = 2 * Hkv * rows * vec;
+    const int nl = rank < L ? (L - 1 - rank) / kCluster + 1 : 0;   // layers rank, rank + 8, ...
+    const int total = nl * per_layer;
+    constexpr int kBatch = 8;
+    for (int w0 = threadIdx.x; w0 < total; w0 += kBatch * kThreads) {
+        uint4 v[kBatch];
+        uint4* dst[kBatch];
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+            const int w = w0 + u * kThreads;
+            dst[u] = nullptr;
+            if (w >= total) continue;
+            int x = w % per_layer;
+            const int l = rank + (w / per_layer) * kCluster;
+            const int c = x % vec;
+            x /= vec;
+            const int i = x % rows;
+            x /= rows;
+            const int g = x % Hkv;
+            const int is_v = x / Hkv;
+            const size_t lbg = (static_cast<size_t>(l) * B + b) * Hkv + g;
+            const uint4* src = reinterpret_cast<const uint4*>((is_v ? v_blk : k_blk) +
+                                                              (lbg * R + static_cast<size_t>(path_s[i])) * D) + c;
+            const size_t drow =
+                paged ? ((static_cast<size_t>(l) * num_pages + page_s[i]) * Hkv + g) * kPage + (t + i) % kPage
+                      : lbg * T_cap + static_cast<size_t>(t + i);
+            dst[u] = reinterpret_cast<uint4*>((is_v ? v_cache : k_cache) + drow * D) + c;
+            v[u] = __ldg(src);
+        }
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u)
+            if (dst[u]) *dst[u] = v[u];
+    }
+}
+
 __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads)
     kv_commit_kernel(uint16_t* __restrict__ k_cache, uint16_t* __restrict__ v_cache,
                      const uint16_t* __restrict__ k_blk, const uint16_t* __restrict__ v_blk, int L, int B, int Hkv,
@@ -75,42 +120,142 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads)
                                    : SV_DEVERR_PAGE);
         return;
     }
-    const int vec = D / 8;                    // 16-byte pieces per row
-    const int rows = m + 1;
-    const int per_layer = 2 * Hkv * rows * vec;
-    const int nl = rank < L ? (L - 1 - rank) / kCluster + 1 : 0;   // layers rank, rank + 8, ...
-    const int total = nl * per_layer;
-    // eight pieces per thread in flight: all loads, then all stores
-    constexpr int kBatch = 8;
-    for (int w0 = threadIdx.x; w0 < total; w0 += kBatch * kThreads) {
-        uint4 v[kBatch];
-        uint4* dst[kBatch];
-#pragma unroll
-        for (int u = 0; u < kBatch; ++u) {
-            const int w = w0 + u * kThreads;
-            dst[u] = nullptr;
-            if (w >= total) continue;
-            int x = w % per_layer;
-            const int l = rank + (w / per_layer) * kCluster;
-            const int c = x % vec;
-            x /= vec;
-            const int i = x % rows;
-            x /= rows;
-            const int g = x % Hkv;
-            const int is_v = x / Hkv;
-            const size_t lbg = (static_cast<size_t>(l) * B + b) * Hkv + g;
-            const uint4* src = reinterpret_cast<const uint4*>((is_v ? v_blk : k_blk) +
-                                                              (lbg * R + static_cast<size_t>(path_s[i])) * D) + c;
-            const size_t drow =
-                pages ? ((static_cast<size_t>(l) * num_pages + page_s[i]) * Hkv + g) * kPage + (t + i) % kPage
-                      : lbg * T_cap + static_cast<size_t>(t + i);
-            dst[u] = reinterpret_cast<uint4*>((is_v ? v_cache : k_cache) + drow * D) + c;
-            v[u] = __ldg(src);
-        }
-#pragma unroll
-        for (int u = 0; u < kBatch; ++u)
-            if (dst[u]) *dst[u] = v[u];
+    copy_accepted_rows(k_cache, v_cache, k_blk, v_blk, L, B, Hkv, D, T_cap, R, b, t, m, rank, path_s, page_s,
+                       pages != nullptr, num_pages);
+    cluster.sync();   // every CTA has read len[b]
+    if (rank == 0 && threadIdx.x == 0) len[b] = t + m + 1;
+}
+
+// Greedy acceptance from the LM head's argmax keys, then the commit, in one
+// launch: one 8-CTA cluster per sequence.
+//   1. The R rows' keys (nslab per row) are split into pieces over the
+//      cluster's 64 warps; each warp reduces its piece and pushes the result
+//      into every CTA's shared memory; after a cluster barrier each CTA
+//      holds every row's greedy token g_j.
+//   2. Draft c matches when tok[c] == g_parent(c); the first matching child
+//      of each node (lowest index) comes from one shared-memory atomicMin
+//      per matching draft, and the walk from the root follows those links --
+//      the same walk in every CTA, so every CTA knows the path.
+//   3. The commit as in kv_commit_kernel: each CTA copies its layers' share
+//      of the accepted rows; after a second cluster barrier rank 0 advances
+//      len[b] (rank 0 also writes n_acc, out_tok and path).
+// Without caches (k_cache == nullptr) it is greedy acceptance alone.
+__global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads)
+    greedy_commit_kernel(const uint64_t* __restrict__ amax, int nslab, const int32_t* __restrict__ tok,
+                         const int32_t* __restrict__ parent, int R, int V, int32_t* n_acc, int32_t* out_tok,
+                         int32_t* path, uint16_t* __restrict__ k_cache, uint16_t* __restrict__ v_cache,
+                         const uint16_t* __restrict__ k_blk, const uint16_t* __restrict__ v_blk, int L, int B,
+                         int Hkv, int D, int T_cap, int32_t* len, unsigned int* err) {
+    constexpr int kWarpsPerCta = kThreads / 32;
+    constexpr int kClusterWarps = kCluster * kWarpsPerCta;
+    constexpr int kPieces = 2 * kClusterWarps;   // (row, piece) items: at most two per warp
+    static_assert(kPieces >= kMaxR, "every row gets at least one piece");
+    __shared__ uint64_t piece_s[kPieces];
+    __shared__ int g_s[kMaxR];
+    __shared__ int tok_s[kMaxR];
+    __shared__ int par_s[kMaxR];
+    __shared__ int fmc_s[kMaxR];    // first matching child of each node (R: none)
+    __shared__ int path_s[kMaxR];
+    __shared__ int m_s, t_s, bad_s;
+    cg::cluster_group cluster = cg::this_cluster();
+    const int rank = static_cast<int>(cluster.block_rank());
+    const int b = blockIdx.x / kCluster;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    cluster_arrive_relaxed();   // this CTA has started (remote stores below wait for all)
+    pdl_wait();                 // the keys, tokens and block rows come from the kernels before this one
+    pdl_launch_dependents();
+
+    // the sequence's tokens, tree and length, loaded in parallel
+    if (threadIdx.x == 0) {
+        bad_s = 0;
+        t_s = k_cache ? len[b] : 0;
     }
+    __syncthreads();
+    for (int j = threadIdx.x; j < R; j += kThreads) {
+        const int tk = tok[static_cast<size_t>(b) * R + j];
+        const int p = parent ? parent[static_cast<size_t>(b) * R + j] : j - 1;
+        tok_s[j] = tk;
+        par_s[j] = p;
+        fmc_s[j] = R;
+        if (j > 0 && (tk < 0 || tk >= V)) atomicOr(&bad_s, 1);
+        if ((j == 0 && p != -1) || (j > 0 && (p < 0 || p >= j))) atomicOr(&bad_s, 2);
+    }
+
+    // 1. row argmax: P pieces per row, items (row, piece) over the cluster's warps
+    const int P = kPieces / R;
+    const int items = R * P;
+    const int gw = rank * kWarpsPerCta + warp;
+    uint64_t res[2] = {0, 0};
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+        const int it = gw + r * kClusterWarps;
+        if (it >= items) break;
+        const int j = it / P, p = it % P;
+        const int s0 = static_cast<int>(static_cast<int64_t>(nslab) * p / P);
+        const int s1 = static_cast<int>(static_cast<int64_t>(nslab) * (p + 1) / P);
+        const uint64_t* row = amax + (static_cast<size_t>(b) * R + j) * nslab;
+        uint64_t best = 0;
+#pragma unroll 8
+        for (int s = s0 + lane; s < s1; s += 32) {
+            const uint64_t k = __ldg(row + s);
+            best = k > best ? k : best;
+        }
+        res[r] = warp_max_key(best);
+    }
+    cluster_wait();   // every CTA of the cluster has started
+    if (lane == 0) {
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+            const int it = gw + r * kClusterWarps;
+            if (it >= items) break;
+            for (int dst = 0; dst < kCluster; ++dst) *cluster.map_shared_rank(&piece_s[it], dst) = res[r];
+        }
+    }
+    cluster.sync();   // every piece pushed into every CTA (and tok_s, par_s, t_s visible in the CTA)
+    for (int j = threadIdx.x; j < R; j += kThreads) {
+        uint64_t k = 0;
+        for (int p = 0; p < P; ++p) k = piece_s[j * P + p] > k ? piece_s[j * P + p] : k;
+        g_s[j] = argmax_col(k);
+    }
+    __syncthreads();
+
+    // 2. first matching child of every node, then the walk
+    const bool tree_ok = (bad_s & 2) == 0;
+    if (tree_ok)
+        for (int c = 1 + threadIdx.x; c < R; c += kThreads)
+            if (tok_s[c] == g_s[par_s[c]]) atomicMin(&fmc_s[par_s[c]], c);
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        if (rank == 0) {
+            if (bad_s & 1) raise_error(err, SV_DEVERR_TOKEN);
+            if (parent && !tree_ok) raise_error(err, SV_DEVERR_TREE);
+        }
+        int u = 0, depth = 0;
+        path_s[0] = 0;
+        for (int guard = 0; tree_ok && guard < R && fmc_s[u] < R; ++guard) {
+            u = fmc_s[u];
+            path_s[++depth] = u;
+        }
+        m_s = depth;
+        if (rank == 0) {
+            n_acc[b] = depth;
+            out_tok[b] = g_s[u];
+        }
+    }
+    __syncthreads();
+    const int m = m_s;
+    if (rank == 0)
+        for (int j = threadIdx.x; j < R; j += kThreads) path[static_cast<size_t>(b) * R + j] = j <= m ? path_s[j] : -1;
+    if (k_cache == nullptr) return;
+
+    // 3. the commit
+    const int t = t_s;
+    if (t < 0 || t + m + 1 > T_cap) {   // uniform across the cluster: nobody copies, nobody waits
+        if (rank == 0 && threadIdx.x == 0) raise_error(err, SV_DEVERR_LENGTH);
+        return;
+    }
+    copy_accepted_rows(k_cache, v_cache, k_blk, v_blk, L, B, Hkv, D, T_cap, R, b, t, m, rank, path_s, nullptr, false,
+                       0);
     cluster.sync();   // every CTA has read len[b]
     if (rank == 0 && threadIdx.x == 0) len[b] = t + m + 1;
 }
@@ -123,6 +268,16 @@ cudaError_t launch_kv_commit(uint16_t* k_cache, uint16_t* v_cache, const uint16_
                              int num_pages, cudaStream_t st) {
     return launch_pdl(kv_commit_kernel, dim3(B * kCluster), dim3(kThreads), 0, st, k_cache, v_cache, k_blk, v_blk, L,
                       B, Hkv, D, T_cap, R, path, n_acc, len, pages, max_pages, num_pages, device_error_word());
+}
+
+cudaError_t launch_accept_greedy_commit(const uint64_t* amax, const int32_t* tok, const int32_t* parent, int B, int R,
+                                        int V, int32_t* n_acc, int32_t* out_tok, int32_t* path, uint16_t* k_cache,
+                                        uint16_t* v_cache, const uint16_t* k_blk, const uint16_t* v_blk, int L,
+                                        int Hkv, int D, int T_cap, int32_t* len, cudaStream_t st) {
+    const int nslab = (V + kArgmaxSlab - 1) / kArgmaxSlab;
+    return launch_pdl(greedy_commit_kernel, dim3(B * kCluster), dim3(kThreads), 0, st, amax, nslab, tok, parent, R,
+                      V, n_acc, out_tok, path, k_cache, v_cache, k_blk, v_blk, L, B, Hkv, D, T_cap, len,
+                      device_error_word());
 }
 
 }  // namespace sv

@@ -13,7 +13,12 @@
 //     vocab dimension fills the 16-row M side and tiny row counts waste no
 //     MMA work;
 //   * the epilogue transposes the fp32 tile through shared memory and writes
-//     each logits row with coalesced 16-byte stores.
+//     each logits row with coalesced 16-byte stores;
+//   * optionally the epilogue also summarises each row of the slab by its
+//     greedy argmax key (largest logit, lowest column; one 64-bit word per
+//     row and slab), so greedy acceptance ([SpecDec-Context-Scaling guide,
+//     sec. 3]) needs neither a second pass over the logits nor, when only
+//     tokens are wanted, the logits at all.
 #include "sv_device.cuh"
 #include "sv_internal.h"
 
@@ -39,8 +44,9 @@ struct LmSmem {
 template <int NT>
 __global__ void __launch_bounds__(kThreads) lm_head_kernel(const __grid_constant__ CUtensorMap tmW,
                                                           const __grid_constant__ CUtensorMap tmH,
-                                                          float* __restrict__ logits, int N, int H, int V, int n0,
-                                                          int nslab, int w_ready, unsigned int* err) {
+                                                          float* __restrict__ logits, uint64_t* __restrict__ amax,
+                                                          int N, int H, int V, int n0, int nslab, int w_ready,
+                                                          unsigned int* err) {
     using S = LmSmem<NT>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -148,49 +154,71 @@ __global__ void __launch_bounds__(kThreads) lm_head_kernel(const __grid_constant
         __syncthreads();
         const int vbase = slab * kVT;
         const int nrows = min(S::NP, N - n0);
-        for (int x = tid; x < nrows * (kVT / 4); x += kThreads) {
-            const int n = x / (kVT / 4), c = (x % (kVT / 4)) * 4;
-            if (vbase + c < V) {
-                const float4 val = *reinterpret_cast<const float4*>(out_s + n * kOutPitch + c);
-                *reinterpret_cast<float4*>(logits + static_cast<size_t>(n0 + n) * V + vbase + c) = val;
+        if (amax) {
+            // argmax key of each row over the slab: warp w takes rows w, w+4,
+            // ...; lane l holds columns 4l..4l+3 (V % 4 == 0: all or none valid)
+            bool nan_seen = false;
+            for (int n = warp; n < nrows; n += kThreads / 32) {
+                const int c = 4 * lane;
+                uint64_t best = 0;
+                if (vbase + c < V) {
+                    const float4 x = *reinterpret_cast<const float4*>(out_s + n * kOutPitch + c);
+                    const float xs[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        nan_seen |= xs[e] != xs[e];
+                        const uint64_t k = argmax_key(argmax_okey(xs[e]), vbase + c + e);
+                        best = k > best ? k : best;
+                    }
+                }
+                best = warp_max_key(best);
+                if (lane == 0) amax[static_cast<size_t>(n0 + n) * nslab + slab] = best;
             }
+            if (__any_sync(0xffffffffu, nan_seen) && lane == 0) raise_error(err, SV_DEVERR_NONFINITE);
         }
+        if (logits)
+            for (int x = tid; x < nrows * (kVT / 4); x += kThreads) {
+                const int n = x / (kVT / 4), c = (x % (kVT / 4)) * 4;
+                if (vbase + c < V) {
+                    const float4 val = *reinterpret_cast<const float4*>(out_s + n * kOutPitch + c);
+                    *reinterpret_cast<float4*>(logits + static_cast<size_t>(n0 + n) * V + vbase + c) = val;
+                }
+            }
         __syncthreads();
     }
 }
 
 template <int NT>
-cudaError_t launch_nt(const uint16_t* hid, const uint16_t* W, float* logits, int N, int H, int V, int n0,
-                      bool w_ready, cudaStream_t st) {
+cudaError_t launch_nt(const uint16_t* hid, const uint16_t* W, float* logits, uint64_t* amax, int N, int H, int V,
+                      int n0, bool w_ready, cudaStream_t st) {
     using S = LmSmem<NT>;
     alignas(64) uint8_t tmW[128], tmH[128];
     if (!encode_tmap_2d_bf16(tmW, W, V, H, static_cast<uint64_t>(V) * 2, 64, kHK)) return cudaErrorInvalidValue;
     if (!encode_tmap_2d_bf16(tmH, hid, H, N, static_cast<uint64_t>(H) * 2, kHK, S::NP)) return cudaErrorInvalidValue;
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(lm_head_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kTotal);
-        if (e != cudaSuccess) return e;
-        attr_set = true;
-    }
+    static PerDeviceOnce attr_once;
+    const cudaError_t ea = attr_once.run([]() {
+        return cudaFuncSetAttribute(lm_head_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kTotal);
+    });
+    if (ea != cudaSuccess) return ea;
     const int nslab = (V + kVT - 1) / kVT;
     const int per_sm = S::kTotal <= 110 * 1024 ? 2 : 1;
     int grid = device_sm_count() * per_sm;
     if (grid > nslab) grid = nslab;
     return launch_pdl(lm_head_kernel<NT>, dim3(grid), dim3(kThreads), S::kTotal, st,
-                      *reinterpret_cast<const CUtensorMap*>(tmW), *reinterpret_cast<const CUtensorMap*>(tmH), logits, N,
-                      H, V, n0, nslab, w_ready ? 1 : 0, device_error_word());
+                      *reinterpret_cast<const CUtensorMap*>(tmW), *reinterpret_cast<const CUtensorMap*>(tmH), logits, amax,
+                      N, H, V, n0, nslab, w_ready ? 1 : 0, device_error_word());
 }
 
 }  // namespace
 
-cudaError_t launch_lm_head(const uint16_t* hid, const uint16_t* W, float* logits, int N, int H, int V,
-                           bool w_ready, cudaStream_t st) {
+cudaError_t launch_lm_head(const uint16_t* hid, const uint16_t* W, float* logits, uint64_t* amax, int N, int H,
+                           int V, bool w_ready, cudaStream_t st) {
     // Beyond 16 rows the product is a real dense contraction: tcgen05, up to
     // 256 rows per pass over W.
     if (N > 16) {
         for (int n0 = 0; n0 < N; n0 += 256) {
             const int rows = N - n0 < 256 ? N - n0 : 256;
-            const cudaError_t e = launch_lm_head_tc(hid, W, logits, N, H, V, n0, rows, w_ready, st);
+            const cudaError_t e = launch_lm_head_tc(hid, W, logits, amax, N, H, V, n0, rows, w_ready, st);
             if (e != cudaSuccess) return e;
         }
         return cudaSuccess;
@@ -200,14 +228,14 @@ cudaError_t launch_lm_head(const uint16_t* hid, const uint16_t* W, float* logits
         const int nt = (rows + 7) / 8;
         cudaError_t e;
         switch (nt) {
-            case 1: e = launch_nt<1>(hid, W, logits, N, H, V, n0, w_ready, st); break;
-            case 2: e = launch_nt<2>(hid, W, logits, N, H, V, n0, w_ready, st); break;
-            case 3: e = launch_nt<3>(hid, W, logits, N, H, V, n0, w_ready, st); break;
-            case 4: e = launch_nt<4>(hid, W, logits, N, H, V, n0, w_ready, st); break;
-            case 5: e = launch_nt<5>(hid, W, logits, N, H, V, n0, w_ready, st); break;
-            case 6: e = launch_nt<6>(hid, W, logits, N, H, V, n0, w_ready, st); break;
-            case 7: e = launch_nt<7>(hid, W, logits, N, H, V, n0, w_ready, st); break;
-            default: e = launch_nt<8>(hid, W, logits, N, H, V, n0, w_ready, st); break;
+            case 1: e = launch_nt<1>(hid, W, logits, amax, N, H, V, n0, w_ready, st); break;
+            case 2: e = launch_nt<2>(hid, W, logits, amax, N, H, V, n0, w_ready, st); break;
+            case 3: e = launch_nt<3>(hid, W, logits, amax, N, H, V, n0, w_ready, st); break;
+            case 4: e = launch_nt<4>(hid, W, logits, amax, N, H, V, n0, w_ready, st); break;
+            case 5: e = launch_nt<5>(hid, W, logits, amax, N, H, V, n0, w_ready, st); break;
+            case 6: e = launch_nt<6>(hid, W, logits, amax, N, H, V, n0, w_ready, st); break;
+            case 7: e = launch_nt<7>(hid, W, logits, amax, N, H, V, n0, w_ready, st); break;
+            default: e = launch_nt<8>(hid, W, logits, amax, N, H, V, n0, w_ready, st); break;
         }
         if (e != cudaSuccess) return e;
     }

@@ -13,7 +13,11 @@
 //   * warps 0..3 read the accumulator (tcgen05.ld, one vocab column per
 //     thread) and store each logits row with 128-byte coalesced writes;
 //   * two TMEM accumulators alternate so a slab's epilogue overlaps the next
-//     slab's MMAs; CTAs are persistent over 128-column slabs.
+//     slab's MMAs; CTAs are persistent over 128-column slabs;
+//   * optionally the epilogue also writes each row's greedy argmax key over
+//     the slab (two redux steps per row and warp, then the four warps' keys
+//     combined through shared memory), the summary greedy acceptance reads
+//     in place of the logits.
 #include "sv_device.cuh"
 #include "sv_internal.h"
 
@@ -29,16 +33,19 @@ template <int NP>
 struct TcCfg {
     static constexpr int kHBytes = NP * kHK * 2;
     static constexpr int kStageBytes = kWBytes + kHBytes;
-    static constexpr int kStages = (kStageBytes * 6 <= 216 * 1024) ? 6 : 4;
+    static constexpr int kArgBytes = 4 * NP * 8;   // argmax keys: [epilogue warp][row]
+    // six stages where they fit beside the barriers and the argmax keys
+    static constexpr int kStages = (kStageBytes * 6 + 1024 + 256 + kArgBytes <= 232448) ? 6 : 4;
     static constexpr int kAccCols = NP <= 32 ? 32 : NP <= 64 ? 64 : NP <= 128 ? 128 : 256;
     static constexpr int kTmemCols = 2 * kAccCols;
-    static constexpr int kSmem = kStages * kStageBytes + 1024 + 256;
+    static constexpr int kSmem = kStages * kStageBytes + 1024 + 256 + kArgBytes;
 };
 
 template <int NP>
 __global__ void __launch_bounds__(kThreads, 1) lm_head_tc_kernel(const __grid_constant__ CUtensorMap tmW,
                                                                 const __grid_constant__ CUtensorMap tmH,
-                                                                float* __restrict__ logits, int N, int H, int V,
+                                                                float* __restrict__ logits,
+                                                                uint64_t* __restrict__ amax, int N, int H, int V,
                                                                 int n0, int nslab, int w_ready, unsigned int* err) {
     using C = TcCfg<NP>;
     extern __shared__ uint8_t smem_raw[];
@@ -48,6 +55,7 @@ __global__ void __launch_bounds__(kThreads, 1) lm_head_tc_kernel(const __grid_co
     uint64_t* acc_full = empty + C::kStages;
     uint64_t* acc_empty = acc_full + 2;
     uint32_t* tmem_base_s = reinterpret_cast<uint32_t*>(acc_empty + 2);
+    uint64_t* keys_s = reinterpret_cast<uint64_t*>(smem + C::kStages * C::kStageBytes + 256);   // [4][NP]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nk = (H + kHK - 1) / kHK;
@@ -159,20 +167,45 @@ __global__ void __launch_bounds__(kThreads, 1) lm_head_tc_kernel(const __grid_co
             tc_fence_after();
             const int v = slab * kM + warp * 32 + lane;
             const uint32_t taddr = tmem + ((warp * 32) << 16) + a * C::kAccCols;
+            bool nan_seen = false;
 #pragma unroll 1
             for (int c0 = 0; c0 < NP; c0 += 16) {
                 uint32_t r[16];
                 tmem_ld16_sync(taddr + c0, r);
+                if (logits) {
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const int n = c0 + i;
-                    if (n0 + n < N && n < NP && v < V)
-                        logits[static_cast<size_t>(n0 + n) * V + v] = __uint_as_float(r[i]);
+                    for (int i = 0; i < 16; ++i) {
+                        const int n = c0 + i;
+                        if (n0 + n < N && n < NP && v < V)
+                            logits[static_cast<size_t>(n0 + n) * V + v] = __uint_as_float(r[i]);
+                    }
+                }
+                if (amax) {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const float x = __uint_as_float(r[i]);
+                        const bool valid = v < V;
+                        nan_seen |= valid && n0 + c0 + i < N && x != x;
+                        const uint64_t k = warp_max_key(valid ? argmax_key(argmax_okey(x), v) : 0ull);
+                        if (lane == 0) keys_s[warp * NP + c0 + i] = k;
+                    }
                 }
             }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&acc_empty[a]);
+            if (amax) {
+                if (__any_sync(0xffffffffu, nan_seen) && lane == 0) raise_error(err, SV_DEVERR_NONFINITE);
+                named_barrier(1, 128);   // the four epilogue warps' keys are in
+                const int nrows = N - n0 < NP ? N - n0 : NP;
+                for (int n = threadIdx.x; n < nrows; n += 128) {
+                    uint64_t k = keys_s[n];
+#pragma unroll
+                    for (int w = 1; w < 4; ++w) k = keys_s[w * NP + n] > k ? keys_s[w * NP + n] : k;
+                    amax[static_cast<size_t>(n0 + n) * nslab + slab] = k;
+                }
+                named_barrier(1, 128);   // keys read before the next slab writes them
+            }
         }
     }
     tc_fence_before();
@@ -184,19 +217,17 @@ __global__ void __launch_bounds__(kThreads, 1) lm_head_tc_kernel(const __grid_co
 }
 
 template <int NP>
-cudaError_t launch_tc(const uint16_t* hid, const uint16_t* W, float* logits, int N, int H, int V, int n0,
-                      bool w_ready, cudaStream_t st) {
+cudaError_t launch_tc(const uint16_t* hid, const uint16_t* W, float* logits, uint64_t* amax, int N, int H, int V,
+                      int n0, bool w_ready, cudaStream_t st) {
     using C = TcCfg<NP>;
     alignas(64) uint8_t tmW[128], tmH[128];
     if (!encode_tmap_2d_bf16(tmW, W, V, H, static_cast<uint64_t>(V) * 2, 64, kHK)) return cudaErrorInvalidValue;
     if (!encode_tmap_2d_bf16(tmH, hid, H, N, static_cast<uint64_t>(H) * 2, kHK, NP)) return cudaErrorInvalidValue;
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(lm_head_tc_kernel<NP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             C::kSmem);
-        if (e != cudaSuccess) return e;
-        attr_set = true;
-    }
+    static PerDeviceOnce attr_once;
+    const cudaError_t ea = attr_once.run([]() {
+        return cudaFuncSetAttribute(lm_head_tc_kernel<NP>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+    });
+    if (ea != cudaSuccess) return ea;
     const int nslab = (V + kM - 1) / kM;
     int grid = device_sm_count();
     if (grid > nslab) grid = nslab;
@@ -211,33 +242,33 @@ cudaError_t launch_tc(const uint16_t* hid, const uint16_t* W, float* logits, int
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, lm_head_tc_kernel<NP>, *reinterpret_cast<const CUtensorMap*>(tmW),
-                              *reinterpret_cast<const CUtensorMap*>(tmH), logits, N, H, V, n0, nslab,
+                              *reinterpret_cast<const CUtensorMap*>(tmH), logits, amax, N, H, V, n0, nslab,
                               w_ready ? 1 : 0, device_error_word());
 }
 
 }  // namespace
 
 // Rows n0 .. n0+rows-1 of the pass (17 <= rows <= 256 after padding to 16).
-cudaError_t launch_lm_head_tc(const uint16_t* hid, const uint16_t* W, float* logits, int N, int H, int V, int n0,
-                              int rows, bool w_ready, cudaStream_t st) {
+cudaError_t launch_lm_head_tc(const uint16_t* hid, const uint16_t* W, float* logits, uint64_t* amax, int N, int H,
+                              int V, int n0, int rows, bool w_ready, cudaStream_t st) {
     const int np = (rows + 15) / 16 * 16;
     switch (np) {
-        case 16: return launch_tc<16>(hid, W, logits, N, H, V, n0, w_ready, st);
-        case 32: return launch_tc<32>(hid, W, logits, N, H, V, n0, w_ready, st);
-        case 48: return launch_tc<48>(hid, W, logits, N, H, V, n0, w_ready, st);
-        case 64: return launch_tc<64>(hid, W, logits, N, H, V, n0, w_ready, st);
-        case 80: return launch_tc<80>(hid, W, logits, N, H, V, n0, w_ready, st);
-        case 96: return launch_tc<96>(hid, W, logits, N, H, V, n0, w_ready, st);
-        case 112: return launch_tc<112>(hid, W, logits, N, H, V, n0, w_ready, st);
-        case 128: return launch_tc<128>(hid, W, logits, N, H, V, n0, w_ready, st);
-        case 144: return launch_tc<144>(hid, W, logits, N, H, V, n0, w_ready, st);
-        case 160: return launch_tc<160>(hid, W, logits, N, H, V, n0, w_ready, st);
-        case 176: return launch_tc<176>(hid, W, logits, N, H, V, n0, w_ready, st);
-        case 192: return launch_tc<192>(hid, W, logits, N, H, V, n0, w_ready, st);
-        case 208: return launch_tc<208>(hid, W, logits, N, H, V, n0, w_ready, st);
-        case 224: return launch_tc<224>(hid, W, logits, N, H, V, n0, w_ready, st);
-        case 240: return launch_tc<240>(hid, W, logits, N, H, V, n0, w_ready, st);
-        default: return launch_tc<256>(hid, W, logits, N, H, V, n0, w_ready, st);
+        case 16: return launch_tc<16>(hid, W, logits, amax, N, H, V, n0, w_ready, st);
+        case 32: return launch_tc<32>(hid, W, logits, amax, N, H, V, n0, w_ready, st);
+        case 48: return launch_tc<48>(hid, W, logits, amax, N, H, V, n0, w_ready, st);
+        case 64: return launch_tc<64>(hid, W, logits, amax, N, H, V, n0, w_ready, st);
+        case 80: return launch_tc<80>(hid, W, logits, amax, N, H, V, n0, w_ready, st);
+        case 96: return launch_tc<96>(hid, W, logits, amax, N, H, V, n0, w_ready, st);
+        case 112: return launch_tc<112>(hid, W, logits, amax, N, H, V, n0, w_ready, st);
+        case 128: return launch_tc<128>(hid, W, logits, amax, N, H, V, n0, w_ready, st);
+        case 144: return launch_tc<144>(hid, W, logits, amax, N, H, V, n0, w_ready, st);
+        case 160: return launch_tc<160>(hid, W, logits, amax, N, H, V, n0, w_ready, st);
+        case 176: return launch_tc<176>(hid, W, logits, amax, N, H, V, n0, w_ready, st);
+        case 192: return launch_tc<192>(hid, W, logits, amax, N, H, V, n0, w_ready, st);
+        case 208: return launch_tc<208>(hid, W, logits, amax, N, H, V, n0, w_ready, st);
+        case 224: return launch_tc<224>(hid, W, logits, amax, N, H, V, n0, w_ready, st);
+        case 240: return launch_tc<240>(hid, W, logits, amax, N, H, V, n0, w_ready, st);
+        default: return launch_tc<256>(hid, W, logits, amax, N, H, V, n0, w_ready, st);
     }
 }
 

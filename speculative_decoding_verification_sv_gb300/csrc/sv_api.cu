@@ -22,26 +22,60 @@ namespace sv {
 __device__ unsigned int g_error_word;
 
 namespace {
-constexpr int kMaxDevices = 64;
 std::mutex g_mu;
+PerDeviceOnce g_err_once;
 unsigned int* g_err_ptr[kMaxDevices] = {};
 int g_sm_count[kMaxDevices] = {};
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+PFN_cuCtxGetCurrent_v4000 g_ctx_current = nullptr;
+PFN_cuCtxGetId_v12000 g_ctx_id = nullptr;
+bool g_ctx_fns_looked_up = false;
 
 int current_device() {
     int d = 0;
     cudaGetDevice(&d);
     return (d >= 0 && d < kMaxDevices) ? d : 0;
 }
+
+template <typename P>
+P driver_fn(const char* name, int version) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion(name, &fn, version, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    return reinterpret_cast<P>(fn);
+}
 }  // namespace
+
+unsigned long long current_context_id() {
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        if (!g_ctx_fns_looked_up) {
+            g_ctx_current = driver_fn<PFN_cuCtxGetCurrent_v4000>("cuCtxGetCurrent", 4000);
+            g_ctx_id = driver_fn<PFN_cuCtxGetId_v12000>("cuCtxGetId", 12000);
+            g_ctx_fns_looked_up = true;
+        }
+    }
+    if (!g_ctx_current || !g_ctx_id) return 0;
+    CUcontext ctx = nullptr;
+    if (g_ctx_current(&ctx) != CUDA_SUCCESS || !ctx) return 0;
+    unsigned long long id = 0;
+    if (g_ctx_id(ctx, &id) != CUDA_SUCCESS) return 0;
+    return id;
+}
 
 unsigned int* device_error_word() {
     const int d = current_device();
-    std::lock_guard<std::mutex> lk(g_mu);
-    if (!g_err_ptr[d]) {
+    const cudaError_t e = g_err_once.run([d]() {
         void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_error_word) == cudaSuccess) g_err_ptr[d] = static_cast<unsigned int*>(p);
-    }
+        const cudaError_t r = cudaGetSymbolAddress(&p, g_error_word);
+        g_err_ptr[d] = r == cudaSuccess ? static_cast<unsigned int*>(p) : nullptr;
+        return r;
+    });
+    if (e != cudaSuccess) return nullptr;
     return g_err_ptr[d];
 }
 
@@ -201,8 +235,44 @@ sv_status sv_lm_head_ex(const uint16_t* hid, const uint16_t* W, float* logits, i
     if (!hid || !W || !logits) return SV_ERR_ARG;
     if (!aligned16(hid) || !aligned16(W) || !aligned16(logits)) return SV_ERR_ARG;
     if (N < 1 || N > 4096 || H < 8 || V < 8 || H % 8 || V % 8) return SV_ERR_SHAPE;
-    return launch_status(
-        sv::launch_lm_head(hid, W, logits, N, H, V, (flags & SV_LM_WEIGHTS_READY) != 0, as_stream(stream)));
+    return launch_status(sv::launch_lm_head(hid, W, logits, nullptr, N, H, V, (flags & SV_LM_WEIGHTS_READY) != 0,
+                                            as_stream(stream)));
+}
+
+size_t sv_lm_head_argmax_bytes(int32_t N, int32_t V) {
+    if (N < 1 || V < 1) return 0;
+    return static_cast<size_t>(N) * ((V + SV_ARGMAX_SLAB - 1) / SV_ARGMAX_SLAB) * sizeof(uint64_t);
+}
+
+sv_status sv_lm_head_argmax(const uint16_t* hid, const uint16_t* W, float* logits, int32_t N, int32_t H, int32_t V,
+                            uint64_t* argmax, size_t argmax_bytes, uint32_t flags, void* stream) {
+    if (flags & ~SV_LM_WEIGHTS_READY) return SV_ERR_ARG;
+    if (!hid || !W || !argmax) return SV_ERR_ARG;
+    if (!aligned16(hid) || !aligned16(W) || !aligned16(argmax) || (logits && !aligned16(logits))) return SV_ERR_ARG;
+    if (N < 1 || N > 4096 || H < 8 || V < 8 || H % 8 || V % 8) return SV_ERR_SHAPE;
+    if (argmax_bytes < sv_lm_head_argmax_bytes(N, V)) return SV_ERR_WORKSPACE;
+    return launch_status(sv::launch_lm_head(hid, W, logits, argmax, N, H, V, (flags & SV_LM_WEIGHTS_READY) != 0,
+                                            as_stream(stream)));
+}
+
+sv_status sv_accept_greedy_commit(const uint64_t* argmax, const int32_t* tok, const int32_t* parent, int32_t B,
+                                  int32_t R, int32_t V, int32_t* n_acc, int32_t* out_tok, int32_t* path,
+                                  uint16_t* k_cache, uint16_t* v_cache, const uint16_t* k_blk, const uint16_t* v_blk,
+                                  int32_t L, int32_t Hkv, int32_t D, int32_t T_cap, int32_t* len, void* stream) {
+    if (!argmax || !tok || !n_acc || !out_tok || !path) return SV_ERR_ARG;
+    if (!aligned16(argmax)) return SV_ERR_ARG;
+    if (B < 1 || R < 1 || R > 128 || V < 1 || static_cast<int64_t>(B) * 8 > 2147483647) return SV_ERR_SHAPE;
+    const bool commit = k_cache != nullptr;
+    if (commit) {
+        if (!v_cache || !k_blk || !v_blk || !len) return SV_ERR_ARG;
+        if (!aligned16(k_cache) || !aligned16(v_cache) || !aligned16(k_blk) || !aligned16(v_blk)) return SV_ERR_ARG;
+        if (L < 1 || Hkv < 1 || D < 8 || D % 8 || T_cap < 1) return SV_ERR_SHAPE;
+    } else if (v_cache || k_blk || v_blk) {
+        return SV_ERR_ARG;   // a commit needs all four buffers
+    }
+    return launch_status(sv::launch_accept_greedy_commit(argmax, tok, parent, B, R, V, n_acc, out_tok, path,
+                                                         commit ? k_cache : nullptr, v_cache, k_blk, v_blk, L, Hkv, D,
+                                                         T_cap, len, as_stream(stream)));
 }
 
 size_t sv_accept_greedy_workspace(int32_t B, int32_t R, int32_t V) {

@@ -166,6 +166,12 @@ __device__ __forceinline__ float fmin3_nan(float a, float b, float c) {
     return r;
 }
 
+// Bulk prefetch of [p, p + bytes) into L2: a hint that moves no data into
+// the CTA.  p 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
 __device__ __forceinline__ void prefetch_tmap(const void* tmap) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
 }
@@ -582,6 +588,75 @@ __device__ __forceinline__ float warp_tree_sum(float v) {
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, off));
     return v;
+}
+
+// --------------------------------------------------------------------------
+// draft trees
+// --------------------------------------------------------------------------
+
+// Children of node u in index order, for a chain (parent == nullptr: the only
+// child of u is u+1) or a tree.
+__device__ __forceinline__ int next_child(const int* par, int R, int u, int after) {
+    if (par == nullptr) return (after < 0 && u + 1 < R) ? u + 1 : -1;
+    for (int c = (after < 0 ? u + 1 : after + 1); c < R; ++c)
+        if (par[c] == u) return c;
+    return -1;
+}
+
+// Loads and validates the tree of sequence b into shared memory; returns
+// false (and raises SV_DEVERR_TREE) if it is malformed.
+__device__ inline bool load_tree(const int32_t* parent, int b, int R, int* par_s, unsigned int* err) {
+    __shared__ int bad;
+    if (threadIdx.x == 0) bad = 0;
+    __syncthreads();
+    for (int j = threadIdx.x; j < R; j += blockDim.x) {
+        const int p = parent[static_cast<size_t>(b) * R + j];
+        par_s[j] = p;
+        if ((j == 0 && p != -1) || (j > 0 && (p < 0 || p >= j))) bad = 1;
+    }
+    __syncthreads();
+    const bool ok = bad == 0;
+    if (!ok && threadIdx.x == 0) raise_error(err, SV_DEVERR_TREE);
+    return ok;
+}
+
+// --------------------------------------------------------------------------
+// greedy argmax as 64-bit keys
+// --------------------------------------------------------------------------
+// The greedy token of a row is its largest logit, NaN skipped, ties (and
+// -0 == +0) going to the lowest column.  That order is the unsigned order of
+//     key(x, col) = (okey(x) << 32) | ~col,
+// where okey maps every float other than NaN to an unsigned word in the
+// float order (+0 and -0 to the same word) and NaN to 0, below every other
+// word; ~col makes the lower column the larger word on equal values.  A
+// block of columns is then summarised by the largest key of its entries,
+// and the row by the largest key of its blocks' keys.
+
+__device__ __forceinline__ uint32_t argmax_okey(float x) {
+    if (x != x) return 0u;
+    const uint32_t b = __float_as_uint(__fadd_rn(x, 0.0f));   // -0 + 0 = +0
+    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+
+__device__ __forceinline__ uint64_t argmax_key(uint32_t okey, int col) {
+    return (static_cast<uint64_t>(okey) << 32) | static_cast<uint32_t>(~col);
+}
+
+// Column of the largest key: the complement of its low word; a key whose
+// high word is 0 summarises only NaN (or no column), and the row's token is
+// then column 0.
+__device__ __forceinline__ int argmax_col(uint64_t key) {
+    return (key >> 32) == 0 ? 0 : static_cast<int>(~static_cast<uint32_t>(key));
+}
+
+// Largest key over the warp's lanes (every lane gets it): two redux steps,
+// first the high words, then the low words of the lanes that hold the
+// largest high word.
+__device__ __forceinline__ uint64_t warp_max_key(uint64_t k) {
+    const uint32_t hi = static_cast<uint32_t>(k >> 32), lo = static_cast<uint32_t>(k);
+    const uint32_t mhi = __reduce_max_sync(0xffffffffu, hi);
+    const uint32_t mlo = __reduce_max_sync(0xffffffffu, hi == mhi ? lo : 0u);
+    return (static_cast<uint64_t>(mhi) << 32) | mlo;
 }
 
 }  // namespace sv

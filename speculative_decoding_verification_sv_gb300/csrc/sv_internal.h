@@ -6,9 +6,45 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <mutex>
+
 #include "sv.h"
 
 namespace sv {
+
+constexpr int kMaxDevices = 64;
+
+// Identity of the calling thread's current CUDA context (cuCtxGetId); 0 when
+// no context is current or the query is unavailable.  A device reset
+// (cudaDeviceReset) ends the context, and the next one gets another id, so
+// set-up keyed on it is redone on the new context.
+unsigned long long current_context_id();
+
+// One-time set-up per device and context (kernel attributes, symbol
+// addresses): run() calls `f` on the current device the first time it is
+// asked there, and again after that device's context has been replaced.
+// Thread-safe; `f` runs under the object's lock.
+class PerDeviceOnce {
+public:
+    template <typename F>
+    cudaError_t run(F&& f) {
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+        std::lock_guard<std::mutex> lk(mu_);
+        const unsigned long long before = current_context_id();
+        if (done_[dev] && before == ctx_[dev]) return cudaSuccess;
+        const cudaError_t e = f();
+        if (e != cudaSuccess) return e;
+        done_[dev] = true;
+        ctx_[dev] = current_context_id();   // f made the context current if it was not
+        return cudaSuccess;
+    }
+
+private:
+    std::mutex mu_;
+    bool done_[kMaxDevices] = {};
+    unsigned long long ctx_[kMaxDevices] = {};
+};
 
 // Launch with programmatic dependent launch allowed: the kernel may start
 // while the previous kernel on the stream drains, and waits
@@ -65,13 +101,22 @@ cudaError_t launch_kv_commit(uint16_t* k_cache, uint16_t* v_cache, const uint16_
                              const int32_t* n_acc, int32_t* len, const int32_t* pages, int max_pages,
                              int num_pages, cudaStream_t st);
 
-// lm_head.cu
-cudaError_t launch_lm_head(const uint16_t* hid, const uint16_t* W, float* logits, int N, int H, int V,
-                           bool w_ready, cudaStream_t st);
+// kv_commit.cu: greedy acceptance from the LM head's argmax keys [B*R][nslab],
+// then (k_cache != nullptr) the commit, in one launch.
+cudaError_t launch_accept_greedy_commit(const uint64_t* amax, const int32_t* tok, const int32_t* parent, int B, int R,
+                                        int V, int32_t* n_acc, int32_t* out_tok, int32_t* path, uint16_t* k_cache,
+                                        uint16_t* v_cache, const uint16_t* k_blk, const uint16_t* v_blk, int L,
+                                        int Hkv, int D, int T_cap, int32_t* len, cudaStream_t st);
+
+// lm_head.cu.  logits may be nullptr (not written); amax nullptr or
+// [N][ceil(V/128)] greedy argmax keys, one per row and 128-column slab.
+constexpr int kArgmaxSlab = 128;
+cudaError_t launch_lm_head(const uint16_t* hid, const uint16_t* W, float* logits, uint64_t* amax, int N, int H,
+                           int V, bool w_ready, cudaStream_t st);
 
 // lm_head_tc.cu (rows n0 .. n0+rows-1, 1 <= rows <= 256)
-cudaError_t launch_lm_head_tc(const uint16_t* hid, const uint16_t* W, float* logits, int N, int H, int V, int n0,
-                              int rows, bool w_ready, cudaStream_t st);
+cudaError_t launch_lm_head_tc(const uint16_t* hid, const uint16_t* W, float* logits, uint64_t* amax, int N, int H,
+                              int V, int n0, int rows, bool w_ready, cudaStream_t st);
 
 // verify_attn.cu
 struct AttnPlan {

@@ -137,6 +137,8 @@ struct Lay {
 
 struct AttnArgs {
     const uint16_t* q;
+    const uint16_t* k_blk;   // [B][Hkv][R][D] (read through tmKb / tmVb; raw for the L2 prefetch)
+    const uint16_t* v_blk;
     const int32_t* len;
     const int32_t* parent;
     uint16_t* out;
@@ -233,6 +235,22 @@ __global__ void __launch_bounds__(Roles<kHalf, kHW>::kThreads, 1)
     // cache_ready the length and the committed cache rows were final before that
     // kernel started, so they are read first, and the producer issues its
     // context loads before waiting.
+    // Warm L2 with this unit's Q rows (and, in the CTAs that take the block
+    // tiles, the block's K/V rows) while the preceding kernel may still run.
+    // A prefetch only fills L2, the point of coherence, so rows that kernel is
+    // still writing are read fresh by the loads after the wait below; it saves
+    // the DRAM round trip of the Q gather that follows the wait.
+    if (warp == kMmaWarp && lane == 0) {
+        const int gr0 = rt * kTileRows, gr1 = min(a.rows, gr0 + kTileRows) - 1;
+        for (int jq = gr0 / a.G; jq <= gr1 / a.G; ++jq)
+            prefetch_l2(a.q + ((static_cast<size_t>(b) * a.R + jq) * a.Hq + g * a.G) * kD,
+                        static_cast<uint32_t>(a.G * kD * 2));
+        if (static_cast<int>(blockIdx.x) >= static_cast<int>(gridDim.x) - 2) {
+            const size_t off = static_cast<size_t>(hg) * a.R * kD;
+            prefetch_l2(a.k_blk + off, static_cast<uint32_t>(a.R * kD * 2));
+            prefetch_l2(a.v_blk + off, static_cast<uint32_t>(a.R * kD * 2));
+        }
+    }
     const bool early = a.cache_ready != 0;
     int t = early ? a.len[b] : 0;
     if (!early || warp != kTmaWarp) {
@@ -978,17 +996,14 @@ __global__ void __launch_bounds__(Roles<kHalf, kHW>::kThreads, 1)
 
 template <bool kHalf, bool kTree, int kHW>
 cudaError_t prepare_kernel() {
-    static bool done[64] = {};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    if (done[dev]) return cudaSuccess;
-    cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<kHalf, kTree, kHW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         Lay<kHalf>::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(attn_tc_kernel<kHalf, kTree, kHW>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-    if (e != cudaSuccess) return e;
-    done[dev] = true;
-    return cudaSuccess;
+    static PerDeviceOnce attr_once;
+    return attr_once.run([]() {
+        cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<kHalf, kTree, kHW>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, Lay<kHalf>::kSmemBytes);
+        if (e != cudaSuccess) return e;
+        return cudaFuncSetAttribute(attn_tc_kernel<kHalf, kTree, kHW>, cudaFuncAttributeNonPortableClusterSizeAllowed,
+                                    1);
+    });
 }
 
 // Clusters of C CTAs that can be resident at once (a cluster must fit in one
@@ -1134,6 +1149,8 @@ cudaError_t launch_verify_attn(const sv_attn_shape& s, const uint16_t* q, const 
         return cudaErrorInvalidValue;
     AttnArgs a;
     a.q = q;
+    a.k_blk = k_blk;
+    a.v_blk = v_blk;
     a.len = len;
     a.parent = parent;
     a.out = out;

@@ -210,6 +210,73 @@ def test_sample_tree_with_rejected_siblings(sv):
     assert_same(got, exp, "sample tree siblings")
 
 
+# Draft trees of the token-tree workload (64 nodes, depth 8, up to 3 children)
+# at the 7B vocabulary.  Above 32768 columns each CTA of the walking cluster
+# holds several 4096-column blocks, the layout the full vocabulary runs in.
+V_7B, VQ_DRAFT = 152064, 151936
+
+
+def _tree_children(par):
+    kids = [[] for _ in par]
+    for c in range(1, len(par)):
+        kids[int(par[c])].append(c)
+    return kids
+
+
+@pytest.mark.parametrize("Vq", [V_7B, VQ_DRAFT])
+@pytest.mark.parametrize("seed", [0, 1])
+def test_sample_tree_full_vocab_philox(sv, Vq, seed):
+    par = _tree(64, 8, 40 + seed)
+    si = _sample_case(3, len(par) - 1, V_7B, Vq=Vq, seed=60 + seed, std=1.5, parent=par)
+    for step in (0, 9):
+        got = sv.accept_sample(si.logits.cuda(), si.q.cuda(), si.tok.cuda(), si.parent.cuda(), seed=4242, step=step)
+        exp = oracle.accept_sample(si.logits.numpy(), si.q.numpy(), si.tok.numpy(), si.parent.numpy(), seed=4242,
+                                   step=step)
+        assert_same(got, exp, f"sample tree V={V_7B} Vq={Vq} step {step}")
+    assert sv.get_device_error() == 0
+
+
+@pytest.mark.parametrize("Vq", [V_7B, VQ_DRAFT])
+def test_sample_tree_full_vocab_rejected_siblings(sv, Vq):
+    """q far from p (an independent softmax): residual chains of two and
+    three siblings at the full vocabulary.  Trial 0: the first children of
+    every node carry the draft's most likely tokens (q well above p) and
+    uniforms just below 1, so they are rejected, and the last child carries
+    the target's most likely token with uniform 0, so it is accepted against
+    the residual its siblings left.  Trial 1: every child carries one of the
+    draft's top tokens and is rejected, so each walk ends in a resample from
+    the residual of all its siblings.  Trial 2: random tokens and uniforms."""
+    par = _tree(64, 8, 44)
+    R, B = len(par), 4
+    rng = np.random.default_rng(21)
+    logits = torch.from_numpy((rng.standard_normal((B, R, V_7B)) * 2).astype(np.float32))
+    q = torch.softmax(torch.from_numpy(rng.standard_normal((B, R, Vq)).astype(np.float32) * 2), -1).contiguous()
+    parent = torch.from_numpy(np.tile(par, (B, 1)).astype(np.int32))
+    kids = _tree_children(par)
+    assert len(kids[0]) == 3
+    best = logits[:, :, :Vq].argmax(-1).numpy()
+    qtop = torch.topk(q, 3, dim=-1).indices.numpy()
+    reject = 1.0 - 2.0 ** -24
+    for trial in range(3):
+        tok = rng.integers(0, Vq, size=(B, R)).astype(np.int32)
+        uni = (rng.integers(0, 2 ** 24, size=(B, R, 2)) * 2.0 ** -24).astype(np.float32)
+        if trial < 2:
+            for u, ch in enumerate(kids):
+                for i, c in enumerate(ch):
+                    last = i == len(ch) - 1
+                    tok[:, c] = best[:, u] if (trial == 0 and last) else qtop[:, u, i]
+                    uni[:, c, 0] = 0.0 if (trial == 0 and last) else reject
+        got = sv.accept_sample(logits.cuda(), q.cuda(), torch.from_numpy(tok).cuda(), parent.cuda(),
+                               uniforms=torch.from_numpy(uni).cuda())
+        exp = oracle.accept_sample(logits.numpy(), q.numpy(), tok, parent.numpy(), uniforms=uni)
+        assert_same(got, exp, f"sample tree siblings V={V_7B} Vq={Vq} trial {trial}")
+        if trial == 0:   # the root's third child was taken after two rejections
+            assert all(int(exp[2][b, 1]) == kids[0][-1] for b in range(B))
+        if trial == 1:   # all three of the root's children were rejected
+            assert all(int(exp[0][b]) == 0 for b in range(B))
+    assert sv.get_device_error() == 0
+
+
 def test_sample_one_hot_equals_greedy(sv):
     B, R, V = 40, 6, 4096
     rng = np.random.default_rng(9)
