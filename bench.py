@@ -51,18 +51,25 @@ FALLBACK_HBM_GBS = 6800.0
 # ncu capture, keyed by (workload, kernel), with the hash of the source file it
 # was taken on; a different hash (the kernel changed) reports null.
 TRAFFIC = {
-    # ncu --set full, 28-layer 1.5B round, LM head N=5 H=1536 V=151936
-    ("1", "lm_head"): {"bytes": 466809856 + 5381632, "src": "lm_head.cu", "src_hash": "f74183b9259d0f09"},
-    # ncu (dram__bytes_read.sum, dram__bytes_write.sum), 7B batch-16 layer
-    # (2-layer case, same per-layer launch)
-    ("3b16", "verify_attn"): {"bytes": 269838080 + 2997760, "src": "verify_attn.cu",
-                              "src_hash": "bb3e32f58ed56bd8"},
-    ("3b16s", "verify_attn"): {"bytes": 269838080 + 2997760, "src": "verify_attn.cu",
-                               "src_hash": "bb3e32f58ed56bd8"},
-    # ncu --set full, sampled B64 k8: the four launches of one acceptance
-    # (statistics, walk, residual pass, draw)
-    ("2", "accept_sampled"): {"bytes": 350172160 + 3333376 + 146688 + 77825024 + 1473536 + 126464,
-                              "src": "accept.cu", "src_hash": "23c8a8c8211445b1"},
+    # ncu (dram__bytes_read.sum, dram__bytes_write.sum), one 1.5B layer of the
+    # 28-layer round (t=4096, k=4, b=1)
+    ("1", "verify_attn"): {"bytes": 4292608 + 0, "src": "verify_attn.cu", "src_hash": "924edb500f857bc2"},
+    # the same round: the LM head with the argmax keys and no logits (its own
+    # output is 47 KB of keys; the 3 MB written are L2 write-backs of an
+    # earlier torch result that its weight stream evicted)
+    ("1", "lm_head_argmax"): {"bytes": 466801920 + 3028480, "src": "lm_head.cu", "src_hash": "8e935fce0398e19e"},
+    # the same round: acceptance from the keys plus the commit of 28 layers (the
+    # committed rows stay in L2 during the launch)
+    ("1", "accept_greedy_commit"): {"bytes": 217344 + 0, "src": "kv_commit.cu", "src_hash": "138e5cb993652b5f"},
+    # 7B batch-16 layer (2-layer case, same per-layer launch)
+    ("3b16", "verify_attn"): {"bytes": 270134016 + 3071232, "src": "verify_attn.cu",
+                              "src_hash": "924edb500f857bc2"},
+    ("3b16s", "verify_attn"): {"bytes": 270134016 + 3071232, "src": "verify_attn.cu",
+                               "src_hash": "924edb500f857bc2"},
+    # sampled B64 k8: the four launches of one acceptance (statistics, walk,
+    # residual pass, draw); the residual pass re-reads p and q rows from DRAM
+    ("2", "accept_sampled"): {"bytes": 350174720 + 2959360 + 149760 + 77826304 + 109568 + 128000,
+                              "src": "accept.cu", "src_hash": "c39e70aa53b4df22"},
 }
 
 
@@ -700,7 +707,7 @@ def main():
     ap.add_argument("--unfused", action="store_true",
                     help="greedy rounds: LM head logits, then argmax, finish and commit as separate launches")
     ap.add_argument("--side", default="3b16,2",
-                    help="other workloads summarised in the line's `workloads` object ('' for none)")
+                    help="other workloads summarised in the line's `workloads` object ('none' for none)")
     args = ap.parse_args()
     ws, rank, local = dist_setup()
     if args.impl == "reference":
@@ -814,7 +821,7 @@ def main():
 
     # the other workloads the metric is quoted at (7B batch 16; sampled B = 64)
     side = {}
-    for name in [n for n in args.side.split(",") if n and n != args.workload]:
+    for name in [n for n in args.side.split(",") if n and n != "none" and n != args.workload]:
         side[name] = side_workload(name, dev, stream, hbm)
 
     line = {"metric": "verify steps/s", "value": value, "unit": "steps/s", "n_gpus": ws, "steps": K,

@@ -191,8 +191,9 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads)
         const int it = gw + r * kClusterWarps;
         if (it >= items) break;
         const int j = it / P, p = it % P;
-        const int s0 = static_cast<int>(static_cast<int64_t>(nslab) * p / P);
-        const int s1 = static_cast<int>(static_cast<int64_t>(nslab) * (p + 1) / P);
+        // p < P <= 128, so nslab * (p + 1) <= ceil(V / 128) * 128 < 2^32
+        const int s0 = static_cast<int>(static_cast<uint32_t>(nslab) * p / static_cast<uint32_t>(P));
+        const int s1 = static_cast<int>(static_cast<uint32_t>(nslab) * (p + 1) / static_cast<uint32_t>(P));
         const uint64_t* row = amax + (static_cast<size_t>(b) * R + j) * nslab;
         uint64_t best = 0;
 #pragma unroll 8

@@ -154,6 +154,15 @@ struct AttnArgs {
     int max_pages, num_pages;
 };
 
+// floor(n * i / k), the first key tile of split i of k: unsigned 32-bit
+// arithmetic whenever n * i cannot overflow (every realistic cache), instead of
+// the long out-of-line 64-bit division routine.
+__device__ __forceinline__ int split_bound(int n, int i, int k) {
+    if (n <= 65535 && i <= 65535) return static_cast<int>(static_cast<uint32_t>(n) * static_cast<uint32_t>(i) /
+                                                          static_cast<uint32_t>(k));
+    return static_cast<int>((static_cast<int64_t>(n) * i) / k);
+}
+
 // TMEM lane that holds row gr of (b, g): full tiles lane = gr - 128 * rt;
 // half tiles put row gr in lane 32 * (gr % 4) + gr / 4, so every quadrant
 // (SM sub-partition) carries a quarter of the rows.
@@ -268,8 +277,8 @@ __global__ void __launch_bounds__(Roles<kHalf, kHW>::kThreads, 1)
     // this CTA's share of the key tiles: split blockIdx.x of the gridDim.x
     // CTAs (a.clusters clusters of C) working on (b, g, row tile)
     const int split = blockIdx.x, nsplit = gridDim.x;
-    const int first = static_cast<int>((static_cast<int64_t>(n_all) * split) / nsplit);
-    const int last = static_cast<int>((static_cast<int64_t>(n_all) * (split + 1)) / nsplit);
+    const int first = split_bound(n_all, split, nsplit);
+    const int last = split_bound(n_all, split + 1, nsplit);
     const int ntiles = last - first;
     const int nsteps = (ntiles + kT - 1) / kT;   // ring steps (stages of up to kT tiles)
     // Fold (half tiles, two warps per quadrant): an odd last tile joins the step
@@ -292,9 +301,9 @@ __global__ void __launch_bounds__(Roles<kHalf, kHW>::kThreads, 1)
     auto merge_plan = [&](int& need_o, uint32_t& light_o) {
         int st_r = 1 << 30;
         if (lane < C) {
-            const int64_t sr = split - rank + lane;
-            const int f = static_cast<int>((static_cast<int64_t>(n_all) * sr) / nsplit);
-            const int l = static_cast<int>((static_cast<int64_t>(n_all) * (sr + 1)) / nsplit);
+            const int sr = split - rank + lane;
+            const int f = split_bound(n_all, sr, nsplit);
+            const int l = split_bound(n_all, sr + 1, nsplit);
             st_r = (l - f + kT - 1) / kT;
         }
         need_o = 0;
