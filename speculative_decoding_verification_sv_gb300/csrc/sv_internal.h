@@ -125,6 +125,7 @@ struct AttnPlan {
     int row_tiles;  // ceil(rows / rows per tile)
     bool half;      // 64-row tiles (M = 64 MMAs, two key tiles per step), else 128-row tiles
     bool hw4;       // half tiles with four row-owner warps per TMEM quadrant (long loops), else two
+    bool split_kv;  // K and V halves of a ring stage on separate barriers (loops longer than the ring, one row tile)
     int warps;      // warps per CTA
     int splits;     // CTAs per thread-block cluster (split-KV merged through DSMEM)
     int clusters;   // clusters per (sequence, KV head, row tile); > 1 merges in the workspace

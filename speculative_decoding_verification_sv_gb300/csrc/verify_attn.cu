@@ -132,7 +132,7 @@ struct Lay {
     static constexpr int kSmemBytes = kOffLsum + kGroups * kRows * 4 + 1024;
     static_assert((kRows + kMaxCluster - 1) * kRec * 4 <= kRingBytes, "pushed partials reuse the K/V ring");
     static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
-    static_assert((2 * kStages + 9) * 8 + 4 <= 248, "barrier area (the word at +248 is the ticket flag)");
+    static_assert((4 * kStages + 9) * 8 + 4 <= 248, "barrier area (the word at +248 is the ticket flag)");
 };
 
 struct AttnArgs {
@@ -170,7 +170,9 @@ __device__ __forceinline__ int split_bound(int n, int i, int k) {
 // kTree: the launch carries a draft tree (parent != NULL).  Chains compile
 // without any ancestor-mask code: the speculatively evaluated 64-bit window
 // of the tree mask stalled the chain's block-tile step by ~2500 cycles.
-template <bool kHalf, bool kTree, int kHW>
+// kSplit: the K and V halves of a ring stage land and are released on
+// barriers of their own (long loops over tiles no other row tile shares).
+template <bool kHalf, bool kTree, int kHW, bool kSplit>
 __global__ void __launch_bounds__(Roles<kHalf, kHW>::kThreads, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                    const __grid_constant__ CUtensorMap tmKb, const __grid_constant__ CUtensorMap tmVb, AttnArgs a) {
@@ -183,9 +185,14 @@ __global__ void __launch_bounds__(Roles<kHalf, kHW>::kThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Ly::kOffBar);
-    uint64_t* kv_full = bars;                    // [kStages]
-    uint64_t* kv_empty = bars + kStages;         // [kStages]
-    uint64_t* s_full = bars + 2 * kStages;       // [2]
+    // kSplit: the K and V halves of a ring stage land and are released on
+    // barriers of their own; otherwise v_full / v_empty are k_full / k_empty
+    // (one barrier per stage for both halves)
+    uint64_t* k_full = bars;                                     // [kStages]
+    uint64_t* v_full = kSplit ? bars + kStages : k_full;         // [kStages]
+    uint64_t* k_empty = bars + 2 * kStages;                      // [kStages]
+    uint64_t* v_empty = kSplit ? bars + 3 * kStages : k_empty;   // [kStages]
+    uint64_t* s_full = bars + 4 * kStages;       // [2]
     uint64_t* s_empty = s_full + 2;              // [2]
     uint64_t* p_full = s_empty + 2;              // [2], per P buffer
     uint64_t* o_done = p_full + 2;               // [2], per P buffer
@@ -210,10 +217,7 @@ __global__ void __launch_bounds__(Roles<kHalf, kHW>::kThreads, 1)
         prefetch_tmap(&tmV);
         prefetch_tmap(&tmKb);
         prefetch_tmap(&tmVb);
-        for (int s = 0; s < kStages; ++s) {
-            mbar_init(&kv_full[s], 1);
-            mbar_init(&kv_empty[s], 1);
-        }
+        for (int s = 0; s < 4 * kStages; ++s) mbar_init(&bars[s], 1);   // the ring's full / empty barriers
         for (int i = 0; i < 2; ++i) {
             mbar_init(&s_full[i], 1);
             mbar_init(&s_empty[i], kSoftWarps);
@@ -240,7 +244,10 @@ __global__ void __launch_bounds__(Roles<kHalf, kHW>::kThreads, 1)
     auto tP = [tmem](int i) { return tmem + Ly::kColP + static_cast<uint32_t>(i) * Ly::kPCols; };
 
     // Inputs may come from the kernel before this one: every thread waits for
-    // it before touching them (and before letting the next kernel start).  With
+    // it before touching them.  The next kernel is let start only once this
+    // CTA's loop is over (pdl_launch_dependents before the merge): started at
+    // once, the next layer's early cache loads competed with this layer's
+    // own, 1.5B layer 8.34 -> 8.20 us measured.  With
     // cache_ready the length and the committed cache rows were final before that
     // kernel started, so they are read first, and the producer issues its
     // context loads before waiting.
@@ -262,10 +269,7 @@ __global__ void __launch_bounds__(Roles<kHalf, kHW>::kThreads, 1)
     }
     const bool early = a.cache_ready != 0;
     int t = early ? a.len[b] : 0;
-    if (!early || warp != kTmaWarp) {
-        pdl_wait();
-        pdl_launch_dependents();
-    }
+    if (!early || warp != kTmaWarp) pdl_wait();
     if (!early) t = a.len[b];
     if (t < 0 || t > a.T_cap) {
         if (threadIdx.x == 0 && rank == 0 && rt == 0) raise_error(a.err, SV_DEVERR_LENGTH);
@@ -335,38 +339,49 @@ __global__ void __launch_bounds__(Roles<kHalf, kHW>::kThreads, 1)
             }
             return (pg * a.Hkv + g) * kNk;
         };
-        auto load_step = [&](int i) {
+        // kSplit: lane 0 streams the K half of every ring step and lane 1 the
+        // V half, each on its own barriers, so a stage's K region is reloaded
+        // as soon as the step's score MMAs have read it, its V region once the
+        // P V MMAs have; in long loops over tiles no other CTA shares, the K
+        // loads then run ahead of the P V MMAs (7B batch-16 layer 57.3 -> 53.5
+        // us in a probe chain).  Otherwise lane 0 loads whole stages on one
+        // barrier each: where several row tiles share each tile through L2
+        // (the tree) or the loop fits the ring (batch 1) the split measured
+        // slower (27.4 -> 28.4 us, 8.17 -> 8.30 us).
+        auto load_step = [&](int i, bool vp) {
             const int s = i % kStages;
-            mbar_wait(&kv_empty[s], ((i / kStages) & 1) ^ 1, a.err);
+            uint64_t* ful = vp ? &v_full[s] : &k_full[s];
+            mbar_wait(vp ? &v_empty[s] : &k_empty[s], ((i / kStages) & 1) ^ 1, a.err);
             const int t0 = first + i * kT, nt = min(kT, last - t0);
             uint8_t* st = smem + Ly::kOffRing + s * kStageBytes;
-            mbar_arrive_expect_tx(&kv_full[s], static_cast<uint32_t>(nt * kTileBytes));
+            mbar_arrive_expect_tx(ful, static_cast<uint32_t>(nt * (kSplit ? kTileBytes / 2 : kTileBytes)));
             for (int h = 0; h < nt; ++h) {
                 const int gt = t0 + h;
                 const void* tk = gt < n_ctx ? static_cast<const void*>(&tmK) : static_cast<const void*>(&tmKb);
                 const void* tv = gt < n_ctx ? static_cast<const void*>(&tmV) : static_cast<const void*>(&tmVb);
                 const int y = gt < n_ctx ? ctx_row(gt) : hg * a.R + (gt - n_ctx) * kNk;
-                tma_load_2d(st + h * kHalfBytes, tk, 0, y, &kv_full[s]);
-                tma_load_2d(st + kRegion + h * kHalfBytes, tk, 64, y, &kv_full[s]);
-                tma_load_2d(st + 2 * kRegion + h * kHalfBytes, tv, 0, y, &kv_full[s]);
-                tma_load_2d(st + 3 * kRegion + h * kHalfBytes, tv, 64, y, &kv_full[s]);
+                if (!kSplit || !vp) {
+                    tma_load_2d(st + h * kHalfBytes, tk, 0, y, ful);
+                    tma_load_2d(st + kRegion + h * kHalfBytes, tk, 64, y, ful);
+                }
+                if (!kSplit || vp) {
+                    tma_load_2d(st + 2 * kRegion + h * kHalfBytes, tv, 0, y, ful);
+                    tma_load_2d(st + 3 * kRegion + h * kHalfBytes, tv, 64, y, ful);
+                }
             }
         };
-        if (lane == 0) {
+        if (kSplit ? lane < 2 : lane == 0) {
+            const bool vp = kSplit && lane == 1;
             int i = 0;
             if (early) {
                 // the first ring pass of context-only steps, while the preceding
                 // kernel drains (committed rows: no kernel writes them now)
-                for (; i < nsteps && i < kStages && min(first + (i + 1) * kT, last) <= n_ctx; ++i) load_step(i);
+                for (; i < nsteps && i < kStages && min(first + (i + 1) * kT, last) <= n_ctx; ++i) load_step(i, vp);
             }
-            if (early) {
-                pdl_wait();
-                pdl_launch_dependents();
-            }
-            for (; i < nsteps; ++i) load_step(i);
+            if (early) pdl_wait();
+            for (; i < nsteps; ++i) load_step(i, vp);
         } else if (early) {
             pdl_wait();
-            pdl_launch_dependents();
         }
         __syncwarp();
         merge_plan(need, light);
@@ -386,6 +401,8 @@ __global__ void __launch_bounds__(Roles<kHalf, kHW>::kThreads, 1)
                 const int pb = st & 1, s = st % kStages;
                 const int nt = min(kT, ntiles - st * kT);
                 mbar_wait(&p_full[pb], (st >> 1) & 1, a.err);
+                // (one barrier per stage: S already waited for the whole stage)
+                if constexpr (kSplit) mbar_wait(&v_full[s], (st / kStages) & 1, a.err);
                 tc_fence_after();
                 // A = P [M lanes][keys] in TMEM (8 columns per 16 keys); B = V
                 // [keys][128 dims], MN-major: 8-key groups 1024 B apart (keys run
@@ -398,20 +415,22 @@ __global__ void __launch_bounds__(Roles<kHalf, kHW>::kThreads, 1)
                 if (fold && st == nsoft - 1) {
                     // the folded tile: P in the other P buffer, V in ring step st + 1
                     const int sx = (st + 1) % kStages;
+                    if constexpr (kSplit) mbar_wait(&v_full[sx], ((st + 1) / kStages) & 1, a.err);
+                    tc_fence_after();
                     const uint64_t bdx =
                         smem_desc_sw128(smem_u32(smem + Ly::kOffRing + sx * kStageBytes + 2 * kRegion), kRegion, 1024);
                     for (int kc = 0; kc < kNk / 16; ++kc)
                         tc_mma_ts(tO, tP(pb ^ 1) + kc * 8, bdx + kc * (2048 >> 4), idesc_o, 1u);
-                    tc_commit(&kv_empty[sx]);
+                    tc_commit(&v_empty[sx]);
                 }
                 tc_commit(&o_done[pb]);
-                tc_commit(&kv_empty[s]);
+                tc_commit(&v_empty[s]);
             };
             for (int st = 0; st < nsoft; ++st) {
                 const int sb = st & 1, s = st % kStages;
                 const int nt = min(kT, ntiles - st * kT);
                 mbar_wait(&s_empty[sb], ((st >> 1) & 1) ^ 1, a.err);
-                mbar_wait(&kv_full[s], (st / kStages) & 1, a.err);
+                mbar_wait(&k_full[s], (st / kStages) & 1, a.err);
                 tc_fence_after();
                 const uint64_t kd0 = smem_desc_sw128(smem_u32(smem + Ly::kOffRing + s * kStageBytes), 16, 1024);
                 const uint32_t id = nt == kT ? idesc_s : idesc_s1;
@@ -426,7 +445,7 @@ __global__ void __launch_bounds__(Roles<kHalf, kHW>::kThreads, 1)
                     // columns of the other buffer, once step st - 1 has read it
                     const int sx = (st + 1) % kStages;
                     if (st >= 1) mbar_wait(&s_empty[sb ^ 1], ((st - 1) >> 1) & 1, a.err);
-                    mbar_wait(&kv_full[sx], ((st + 1) / kStages) & 1, a.err);
+                    mbar_wait(&k_full[sx], ((st + 1) / kStages) & 1, a.err);
                     tc_fence_after();
                     const uint64_t kdx = smem_desc_sw128(smem_u32(smem + Ly::kOffRing + sx * kStageBytes), 16, 1024);
 #pragma unroll
@@ -435,7 +454,9 @@ __global__ void __launch_bounds__(Roles<kHalf, kHW>::kThreads, 1)
                         tc_mma(tS(sb ^ 1), qd0 + ((half * (kM * 128) + kin) >> 4),
                                kdx + ((half * kRegion + kin) >> 4), idesc_s1, k16 > 0 ? 1u : 0u);
                     }
+                    if constexpr (kSplit) tc_commit(&k_empty[sx]);
                 }
+                if constexpr (kSplit) tc_commit(&k_empty[s]);   // K of this step read once these MMAs are done
                 tc_commit(&s_full[sb]);
                 if (st > 0) pv(st - 1);
             }
@@ -721,6 +742,9 @@ __global__ void __launch_bounds__(Roles<kHalf, kHW>::kThreads, 1)
                 // P V, so they are zeroed before the P V of this step
                 const int tl = n_ctx - 1 - first - st * kT;   // that tile within this step
                 if ((t & (kNk - 1)) != 0 && tl >= 0 && tl < kT && tl < ntiles - st * kT) {
+                    // with split barriers V lands on its own: wait for it before
+                    // zeroing rows (otherwise the score MMAs waited for the stage)
+                    if constexpr (kSplit) mbar_wait(&v_full[st % kStages], (st / kStages) & 1, a.err);
                     uint8_t* vt = smem + Ly::kOffRing + (st % kStages) * kStageBytes + 2 * kRegion + tl * kHalfBytes;
                     const int r0 = t & (kNk - 1);
                     for (int x = threadIdx.x; x < (kNk - r0) * 16; x += 32 * kSoftWarps) {
@@ -732,6 +756,7 @@ __global__ void __launch_bounds__(Roles<kHalf, kHW>::kThreads, 1)
                 }
                 if (fx && (t & (kNk - 1)) != 0 && last - 1 == n_ctx - 1) {
                     // ... and the folded tile when it is that tile (ring step st + 1)
+                    if constexpr (kSplit) mbar_wait(&v_full[(st + 1) % kStages], ((st + 1) / kStages) & 1, a.err);
                     uint8_t* vt = smem + Ly::kOffRing + ((st + 1) % kStages) * kStageBytes + 2 * kRegion;
                     const int r0 = t & (kNk - 1);
                     for (int x = threadIdx.x; x < (kNk - r0) * 16; x += 32 * kSoftWarps) {
@@ -786,6 +811,7 @@ __global__ void __launch_bounds__(Roles<kHalf, kHW>::kThreads, 1)
         }
         tc_fence_before();
         __syncwarp();
+        pdl_launch_dependents();             // see the note at the programmatic-launch wait
         cluster_wait();                      // every CTA of the cluster has started
         if (need == 0) cluster_sync_warp();  // (1) and has drained its ring
         // push the partial record of row prow into slot `rank` of the row's
@@ -815,6 +841,7 @@ __global__ void __launch_bounds__(Roles<kHalf, kHW>::kThreads, 1)
     }
     if (warp >= kSoftWarps) {   // producer and MMA warps, once their lane 0 is done
         __syncwarp();
+        pdl_launch_dependents();
         cluster_wait();
         if (need == 0) cluster_sync_warp();   // (1)
     }
@@ -1003,14 +1030,14 @@ __global__ void __launch_bounds__(Roles<kHalf, kHW>::kThreads, 1)
     }
 }
 
-template <bool kHalf, bool kTree, int kHW>
+template <bool kHalf, bool kTree, int kHW, bool kSplit>
 cudaError_t prepare_kernel() {
     static PerDeviceOnce attr_once;
     return attr_once.run([]() {
-        cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<kHalf, kTree, kHW>,
+        cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<kHalf, kTree, kHW, kSplit>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, Lay<kHalf>::kSmemBytes);
         if (e != cudaSuccess) return e;
-        return cudaFuncSetAttribute(attn_tc_kernel<kHalf, kTree, kHW>, cudaFuncAttributeNonPortableClusterSizeAllowed,
+        return cudaFuncSetAttribute(attn_tc_kernel<kHalf, kTree, kHW, kSplit>, cudaFuncAttributeNonPortableClusterSizeAllowed,
                                     1);
     });
 }
@@ -1030,7 +1057,7 @@ int active_clusters(int C) {
     std::lock_guard<std::mutex> lk(mu);
     if (cache[dev][C]) return cache[dev][C];
     int n = 0;
-    if (prepare_kernel<kHalf, false, 2>() == cudaSuccess) {   // both tree variants use the same resources
+    if (prepare_kernel<kHalf, false, 2, false>() == cudaSuccess) {   // every variant uses the same resources
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(C, 1, 1);
         cfg.blockDim = dim3(Roles<kHalf, 2>::kThreads, 1, 1);
@@ -1042,7 +1069,7 @@ int active_clusters(int C) {
         attr[0].val.clusterDim.z = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        if (cudaOccupancyMaxActiveClusters(&n, attn_tc_kernel<kHalf, false, 2>, &cfg) != cudaSuccess) n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, attn_tc_kernel<kHalf, false, 2, false>, &cfg) != cudaSuccess) n = 0;
     }
     cudaGetLastError();
     if (n <= 0) n = fallback;
@@ -1050,11 +1077,11 @@ int active_clusters(int C) {
     return n;
 }
 
-template <bool kHalf, bool kTree, int kHW>
+template <bool kHalf, bool kTree, int kHW, bool kSplit>
 cudaError_t launch_mode(const AttnPlan& p, const sv_attn_shape& s, const uint8_t* tK, const uint8_t* tV,
                         const uint8_t* tKb, const uint8_t* tVb, const AttnArgs& a, cudaStream_t st) {
     constexpr int kThreads = Roles<kHalf, kHW>::kThreads;
-    cudaError_t e = prepare_kernel<kHalf, kTree, kHW>();
+    cudaError_t e = prepare_kernel<kHalf, kTree, kHW, kSplit>();
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(p.splits * p.clusters, s.B * s.Hkv * p.row_tiles, 1);
@@ -1070,7 +1097,7 @@ cudaError_t launch_mode(const AttnPlan& p, const sv_attn_shape& s, const uint8_t
     attrs[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attrs;
     cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, attn_tc_kernel<kHalf, kTree, kHW>, *reinterpret_cast<const CUtensorMap*>(tK),
+    return cudaLaunchKernelEx(&cfg, attn_tc_kernel<kHalf, kTree, kHW, kSplit>, *reinterpret_cast<const CUtensorMap*>(tK),
                               *reinterpret_cast<const CUtensorMap*>(tV), *reinterpret_cast<const CUtensorMap*>(tKb),
                               *reinterpret_cast<const CUtensorMap*>(tVb), a);
 }
@@ -1120,6 +1147,11 @@ AttnPlan attn_plan(const sv_attn_shape& s) {
         }
     }
     p.hw4 = p.half && (tiles + p.splits * p.clusters - 1) / (p.splits * p.clusters) >= kHw4MinTiles;
+    // separate K and V barriers (chains in half tiles): loops longer than the
+    // ring over tiles no other row tile of the unit shares
+    p.split_kv = p.half && p.row_tiles == 1 &&
+                 ((tiles + p.splits * p.clusters - 1) / (p.splits * p.clusters) + Lay<true>::kT - 1) / Lay<true>::kT >
+                     Lay<true>::kStages;
     p.warps = !p.half ? Roles<false>::kThreads / 32 : p.hw4 ? Roles<true, 4>::kThreads / 32 : Roles<true, 2>::kThreads / 32;
     return p;
 }
@@ -1184,12 +1216,15 @@ cudaError_t launch_verify_attn(const sv_attn_shape& s, const uint16_t* q, const 
     a.max_pages = max_pages;
     a.num_pages = num_pages;
     if (parent != nullptr)
-        return !p.half ? launch_mode<false, true, 2>(p, s, tK, tV, tKb, tVb, a, st)
-               : p.hw4 ? launch_mode<true, true, 4>(p, s, tK, tV, tKb, tVb, a, st)
-                       : launch_mode<true, true, 2>(p, s, tK, tV, tKb, tVb, a, st);
-    return !p.half ? launch_mode<false, false, 2>(p, s, tK, tV, tKb, tVb, a, st)
-           : p.hw4 ? launch_mode<true, false, 4>(p, s, tK, tV, tKb, tVb, a, st)
-                   : launch_mode<true, false, 2>(p, s, tK, tV, tKb, tVb, a, st);
+        return !p.half ? launch_mode<false, true, 2, false>(p, s, tK, tV, tKb, tVb, a, st)
+               : p.hw4 ? launch_mode<true, true, 4, false>(p, s, tK, tV, tKb, tVb, a, st)
+                       : launch_mode<true, true, 2, false>(p, s, tK, tV, tKb, tVb, a, st);
+    if (p.split_kv)
+        return p.hw4 ? launch_mode<true, false, 4, true>(p, s, tK, tV, tKb, tVb, a, st)
+                     : launch_mode<true, false, 2, true>(p, s, tK, tV, tKb, tVb, a, st);
+    return !p.half ? launch_mode<false, false, 2, false>(p, s, tK, tV, tKb, tVb, a, st)
+           : p.hw4 ? launch_mode<true, false, 4, false>(p, s, tK, tV, tKb, tVb, a, st)
+                   : launch_mode<true, false, 2, false>(p, s, tK, tV, tKb, tVb, a, st);
 }
 
 }  // namespace sv
