@@ -53,7 +53,7 @@ FALLBACK_HBM_GBS = 6800.0
 TRAFFIC = {
     # ncu (dram__bytes_read.sum, dram__bytes_write.sum), one 1.5B layer of the
     # 28-layer round (t=4096, k=4, b=1)
-    ("1", "verify_attn"): {"bytes": 4292608 + 0, "src": "verify_attn.cu", "src_hash": "924edb500f857bc2"},
+    ("1", "verify_attn"): {"bytes": 4292608 + 0, "src": "verify_attn.cu", "src_hash": "9f198100f22c2e6a"},
     # the same round: the LM head with the argmax keys and no logits (its own
     # output is 47 KB of keys; the 3 MB written are L2 write-backs of an
     # earlier torch result that its weight stream evicted)
@@ -61,11 +61,11 @@ TRAFFIC = {
     # the same round: acceptance from the keys plus the commit of 28 layers (the
     # committed rows stay in L2 during the launch)
     ("1", "accept_greedy_commit"): {"bytes": 217344 + 0, "src": "kv_commit.cu", "src_hash": "138e5cb993652b5f"},
-    # 7B batch-16 layer (2-layer case, same per-layer launch)
-    ("3b16", "verify_attn"): {"bytes": 270134016 + 3071232, "src": "verify_attn.cu",
-                              "src_hash": "924edb500f857bc2"},
-    ("3b16s", "verify_attn"): {"bytes": 270134016 + 3071232, "src": "verify_attn.cu",
-                               "src_hash": "924edb500f857bc2"},
+    # 7B batch-16 layer (2-layer case, same per-layer launch; split K/V barriers)
+    ("3b16", "verify_attn"): {"bytes": 270134784 + 3001600, "src": "verify_attn.cu",
+                              "src_hash": "9f198100f22c2e6a"},
+    ("3b16s", "verify_attn"): {"bytes": 270134784 + 3001600, "src": "verify_attn.cu",
+                               "src_hash": "9f198100f22c2e6a"},
     # sampled B64 k8: the four launches of one acceptance (statistics, walk,
     # residual pass, draw); the residual pass re-reads p and q rows from DRAM
     ("2", "accept_sampled"): {"bytes": 350174720 + 2959360 + 149760 + 77826304 + 109568 + 128000,
