@@ -271,6 +271,18 @@ SV_API sv_status sv_accept_greedy_commit(const uint64_t* argmax, const int32_t* 
                                          const uint16_t* v_blk, int32_t L, int32_t Hkv, int32_t D, int32_t T_cap,
                                          int32_t* len, void* stream);
 
+/* sv_accept_greedy_commit into paged caches: the acceptance as above, the
+ * commit as sv_kv_commit_paged (pools [L][num_pages][Hkv][64][D], page_table
+ * [B][max_pages], capacity max_pages * 64).  A sequence whose new rows would
+ * reach a page entry outside [0, num_pages) keeps its pages and length and
+ * sets SV_DEVERR_PAGE; it still gets its acceptance outputs. */
+SV_API sv_status sv_accept_greedy_commit_paged(const uint64_t* argmax, const int32_t* tok, const int32_t* parent,
+                                               int32_t B, int32_t R, int32_t V, int32_t* n_acc, int32_t* out_tok,
+                                               int32_t* path, uint16_t* k_pool, uint16_t* v_pool, int32_t num_pages,
+                                               const int32_t* page_table, int32_t max_pages, const uint16_t* k_blk,
+                                               const uint16_t* v_blk, int32_t L, int32_t Hkv, int32_t D, int32_t* len,
+                                               void* stream);
+
 /* ------------------------------------------------------------------------ */
 /* Relaxed, lossy acceptance ([SCS] sec. 7.2: the Delta-logit relaxation).   */
 /* ------------------------------------------------------------------------ */

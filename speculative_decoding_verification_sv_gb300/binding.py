@@ -70,6 +70,8 @@ def _load():
     L.sv_lm_head_argmax.argtypes = [_P, _P, _P, _I32, _I32, _I32, _P, _SZ, ctypes.c_uint32, _P]
     L.sv_accept_greedy_commit.argtypes = [_P, _P, _P, _I32, _I32, _I32, _P, _P, _P, _P, _P, _P, _P, _I32, _I32, _I32,
                                           _I32, _P, _P]
+    L.sv_accept_greedy_commit_paged.argtypes = [_P, _P, _P, _I32, _I32, _I32, _P, _P, _P, _P, _P, _I32, _P, _I32,
+                                                _P, _P, _I32, _I32, _I32, _P, _P]
     L.sv_diag_exp.argtypes = [_P, _P, _I64, _P]
     L.sv_diag_philox.argtypes = [_P, _P, _P, _I64, _P]
     L.sv_diag_canon.argtypes = [_P, _I32, _I32, _P, _P, _P, _P]
@@ -77,7 +79,7 @@ def _load():
                "sv_accept_greedy_relaxed", "sv_accept_sample",
                "sv_accept_sample_noalloc", "sv_kv_commit", "sv_kv_commit_paged", "sv_verify_attn_paged",
                "sv_diag_exp", "sv_diag_philox", "sv_diag_canon", "sv_get_device_error", "sv_lm_head_argmax",
-               "sv_accept_greedy_commit"):
+               "sv_accept_greedy_commit", "sv_accept_greedy_commit_paged"):
         getattr(L, fn).restype = ctypes.c_int
     return L
 
@@ -246,6 +248,23 @@ def accept_greedy_commit(argmax, tok, V, parent=None, n_acc=None, out_tok=None, 
         _ptr(n_acc, i32), _ptr(out_tok, i32), _ptr(path, i32), _ptr(k_cache, bf, "k_cache"),
         _ptr(v_cache, bf, "v_cache"), _ptr(k_blk, bf, "k_blk"), _ptr(v_blk, bf, "v_blk"), L, Hkv, D, T_cap,
         _ptr(length, i32, "len"), _stream(stream)))
+    return n_acc, out_tok, path
+
+
+def accept_greedy_commit_paged(argmax, tok, V, k_pool, v_pool, page_table, k_blk, v_blk, length, parent=None,
+                               n_acc=None, out_tok=None, path=None, stream=None):
+    """accept_greedy_commit into paged caches: pools [L,num_pages,Hkv,64,D] bf16,
+    page_table [B,max_pages] int32, blocks [L,B,Hkv,R,D] bf16, length [B]
+    int32 (updated in place).  Returns (n_acc, out_tok, path)."""
+    B, R = tok.shape
+    n_acc, out_tok, path = _accept_outputs(B, R, tok.device, n_acc, out_tok, path)
+    L, num_pages, Hkv, _, D = k_pool.shape
+    bf, i32 = torch.bfloat16, torch.int32
+    _check("sv_accept_greedy_commit_paged", lib.sv_accept_greedy_commit_paged(
+        _ptr(argmax, torch.int64, "argmax"), _ptr(tok, i32, "tok"), _ptr(parent, i32, "parent"), B, R, V,
+        _ptr(n_acc, i32), _ptr(out_tok, i32), _ptr(path, i32), _ptr(k_pool, bf, "k_pool"), _ptr(v_pool, bf, "v_pool"),
+        num_pages, _ptr(page_table, i32, "page_table"), page_table.shape[1], _ptr(k_blk, bf, "k_blk"),
+        _ptr(v_blk, bf, "v_blk"), L, Hkv, D, _ptr(length, i32, "len"), _stream(stream)))
     return n_acc, out_tok, path
 
 

@@ -137,7 +137,8 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads)
 //      per matching draft, and the walk from the root follows those links --
 //      the same walk in every CTA, so every CTA knows the path.
 //   3. The commit as in kv_commit_kernel: each CTA copies its layers' share
-//      of the accepted rows; after a second cluster barrier rank 0 advances
+//      of the accepted rows (into page pools through the page table when
+//      pages != nullptr); after a second cluster barrier rank 0 advances
 //      len[b] (rank 0 also writes n_acc, out_tok and path).
 // Without caches (k_cache == nullptr) it is greedy acceptance alone.
 __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads)
@@ -145,7 +146,8 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads)
                          const int32_t* __restrict__ parent, int R, int V, int32_t* n_acc, int32_t* out_tok,
                          int32_t* path, uint16_t* __restrict__ k_cache, uint16_t* __restrict__ v_cache,
                          const uint16_t* __restrict__ k_blk, const uint16_t* __restrict__ v_blk, int L, int B,
-                         int Hkv, int D, int T_cap, int32_t* len, unsigned int* err) {
+                         int Hkv, int D, int T_cap, int32_t* len, const int32_t* __restrict__ pages, int max_pages,
+                         int num_pages, unsigned int* err) {
     constexpr int kWarpsPerCta = kThreads / 32;
     constexpr int kClusterWarps = kCluster * kWarpsPerCta;
     constexpr int kPieces = 2 * kClusterWarps;   // (row, piece) items: at most two per warp
@@ -156,7 +158,8 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads)
     __shared__ int par_s[kMaxR];
     __shared__ int fmc_s[kMaxR];    // first matching child of each node (R: none)
     __shared__ int path_s[kMaxR];
-    __shared__ int m_s, t_s, bad_s;
+    __shared__ int page_s[kMaxR];   // paged: the page of slot t + i
+    __shared__ int m_s, t_s, bad_s, page_ok_s;
     cg::cluster_group cluster = cg::this_cluster();
     const int rank = static_cast<int>(cluster.block_rank());
     const int b = blockIdx.x / kCluster;
@@ -255,8 +258,22 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads)
         if (rank == 0 && threadIdx.x == 0) raise_error(err, SV_DEVERR_LENGTH);
         return;
     }
-    copy_accepted_rows(k_cache, v_cache, k_blk, v_blk, L, B, Hkv, D, T_cap, R, b, t, m, rank, path_s, nullptr, false,
-                       0);
+    if (pages) {   // the pages of slots t..t+m, staged and checked first
+        if (threadIdx.x == 0) page_ok_s = 1;
+        __syncthreads();
+        if (threadIdx.x <= m) {
+            const int pg = pages[static_cast<size_t>(b) * max_pages + (t + threadIdx.x) / kPage];
+            page_s[threadIdx.x] = pg;
+            if (pg < 0 || pg >= num_pages) page_ok_s = 0;
+        }
+        __syncthreads();
+        if (!page_ok_s) {   // uniform across the cluster
+            if (rank == 0 && threadIdx.x == 0) raise_error(err, SV_DEVERR_PAGE);
+            return;
+        }
+    }
+    copy_accepted_rows(k_cache, v_cache, k_blk, v_blk, L, B, Hkv, D, T_cap, R, b, t, m, rank, path_s, page_s,
+                       pages != nullptr, num_pages);
     cluster.sync();   // every CTA has read len[b]
     if (rank == 0 && threadIdx.x == 0) len[b] = t + m + 1;
 }
@@ -274,11 +291,12 @@ cudaError_t launch_kv_commit(uint16_t* k_cache, uint16_t* v_cache, const uint16_
 cudaError_t launch_accept_greedy_commit(const uint64_t* amax, const int32_t* tok, const int32_t* parent, int B, int R,
                                         int V, int32_t* n_acc, int32_t* out_tok, int32_t* path, uint16_t* k_cache,
                                         uint16_t* v_cache, const uint16_t* k_blk, const uint16_t* v_blk, int L,
-                                        int Hkv, int D, int T_cap, int32_t* len, cudaStream_t st) {
+                                        int Hkv, int D, int T_cap, int32_t* len, const int32_t* pages, int max_pages,
+                                        int num_pages, cudaStream_t st) {
     const int nslab = (V + kArgmaxSlab - 1) / kArgmaxSlab;
     return launch_pdl(greedy_commit_kernel, dim3(B * kCluster), dim3(kThreads), 0, st, amax, nslab, tok, parent, R,
-                      V, n_acc, out_tok, path, k_cache, v_cache, k_blk, v_blk, L, B, Hkv, D, T_cap, len,
-                      device_error_word());
+                      V, n_acc, out_tok, path, k_cache, v_cache, k_blk, v_blk, L, B, Hkv, D, T_cap, len, pages,
+                      max_pages, num_pages, device_error_word());
 }
 
 }  // namespace sv

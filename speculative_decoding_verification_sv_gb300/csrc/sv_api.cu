@@ -272,7 +272,25 @@ sv_status sv_accept_greedy_commit(const uint64_t* argmax, const int32_t* tok, co
     }
     return launch_status(sv::launch_accept_greedy_commit(argmax, tok, parent, B, R, V, n_acc, out_tok, path,
                                                          commit ? k_cache : nullptr, v_cache, k_blk, v_blk, L, Hkv, D,
-                                                         T_cap, len, as_stream(stream)));
+                                                         T_cap, len, nullptr, 0, 0, as_stream(stream)));
+}
+
+sv_status sv_accept_greedy_commit_paged(const uint64_t* argmax, const int32_t* tok, const int32_t* parent, int32_t B,
+                                        int32_t R, int32_t V, int32_t* n_acc, int32_t* out_tok, int32_t* path,
+                                        uint16_t* k_pool, uint16_t* v_pool, int32_t num_pages,
+                                        const int32_t* page_table, int32_t max_pages, const uint16_t* k_blk,
+                                        const uint16_t* v_blk, int32_t L, int32_t Hkv, int32_t D, int32_t* len,
+                                        void* stream) {
+    if (!argmax || !tok || !n_acc || !out_tok || !path) return SV_ERR_ARG;
+    if (!k_pool || !v_pool || !page_table || !k_blk || !v_blk || !len) return SV_ERR_ARG;
+    if (!aligned16(argmax) || !aligned16(k_pool) || !aligned16(v_pool) || !aligned16(k_blk) || !aligned16(v_blk))
+        return SV_ERR_ARG;
+    if (B < 1 || R < 1 || R > 128 || V < 1 || static_cast<int64_t>(B) * 8 > 2147483647) return SV_ERR_SHAPE;
+    if (L < 1 || Hkv < 1 || D < 8 || D % 8 || num_pages < 1 || max_pages < 1) return SV_ERR_SHAPE;
+    if (static_cast<int64_t>(max_pages) * SV_KV_PAGE > 2147483647) return SV_ERR_SHAPE;
+    return launch_status(sv::launch_accept_greedy_commit(argmax, tok, parent, B, R, V, n_acc, out_tok, path, k_pool,
+                                                         v_pool, k_blk, v_blk, L, Hkv, D, max_pages * SV_KV_PAGE, len,
+                                                         page_table, max_pages, num_pages, as_stream(stream)));
 }
 
 size_t sv_accept_greedy_workspace(int32_t B, int32_t R, int32_t V) {

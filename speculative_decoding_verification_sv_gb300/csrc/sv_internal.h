@@ -102,11 +102,13 @@ cudaError_t launch_kv_commit(uint16_t* k_cache, uint16_t* v_cache, const uint16_
                              int num_pages, cudaStream_t st);
 
 // kv_commit.cu: greedy acceptance from the LM head's argmax keys [B*R][nslab],
-// then (k_cache != nullptr) the commit, in one launch.
+// then (k_cache != nullptr) the commit, in one launch; pages != nullptr: the
+// caches are page pools as for launch_kv_commit
 cudaError_t launch_accept_greedy_commit(const uint64_t* amax, const int32_t* tok, const int32_t* parent, int B, int R,
                                         int V, int32_t* n_acc, int32_t* out_tok, int32_t* path, uint16_t* k_cache,
                                         uint16_t* v_cache, const uint16_t* k_blk, const uint16_t* v_blk, int L,
-                                        int Hkv, int D, int T_cap, int32_t* len, cudaStream_t st);
+                                        int Hkv, int D, int T_cap, int32_t* len, const int32_t* pages, int max_pages,
+                                        int num_pages, cudaStream_t st);
 
 // lm_head.cu.  logits may be nullptr (not written); amax nullptr or
 // [N][ceil(V/128)] greedy argmax keys, one per row and 128-column slab.

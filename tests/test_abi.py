@@ -104,6 +104,25 @@ def test_host_validation_rejects_before_launch(lib):
                                           fake, 1 << 20, None) == 1
     assert L.sv_accept_greedy_relaxed(fake, fake, None, 1, 5, 151936, ctypes.c_float(1.0), fake, fake, fake, fake,
                                       8, None) == 4
+    # LM head with argmax keys: the key buffer is required and sized by the query;
+    # unknown flags rejected; logits may be NULL
+    need = L.sv_lm_head_argmax_bytes(5, 151936)
+    assert need == 5 * 1187 * 8
+    assert L.sv_lm_head_argmax(fake, fake, None, 5, 1536, 151936, None, need, 0, None) == 1
+    assert L.sv_lm_head_argmax(fake, fake, None, 5, 1536, 151936, fake, need - 8, 0, None) == 4
+    assert L.sv_lm_head_argmax(fake, fake, None, 5, 1536, 151936, fake, need, 2, None) == 1
+    assert L.sv_lm_head_argmax(fake, fake, None, 5, 1537, 151936, fake, need, 0, None) == 2
+    # fused acceptance + commit: a commit needs all four cache buffers; R <= 128
+    assert L.sv_accept_greedy_commit(fake, fake, None, 1, 5, 151936, fake, fake, fake, None, fake, None, None, 28, 2,
+                                     128, 4224, fake, None) == 1
+    assert L.sv_accept_greedy_commit(fake, fake, None, 1, 200, 151936, fake, fake, fake, None, None, None, None, 0, 0,
+                                     0, 0, None, None) == 2
+    assert L.sv_accept_greedy_commit(None, fake, None, 1, 5, 151936, fake, fake, fake, None, None, None, None, 0, 0,
+                                     0, 0, None, None) == 1
+    assert L.sv_accept_greedy_commit_paged(fake, fake, None, 1, 5, 151936, fake, fake, fake, fake, fake, 0, fake, 4,
+                                           fake, fake, 28, 2, 128, fake, None) == 2
+    assert L.sv_accept_greedy_commit_paged(fake, fake, None, 1, 5, 151936, fake, fake, fake, fake, fake, 8, None, 4,
+                                           fake, fake, 28, 2, 128, fake, None) == 1
 
 
 def test_workspace_queries(lib):

@@ -216,3 +216,69 @@ def test_fused_nan_and_bad_token_flagged(sv):
     n_acc, _, _ = sv.accept_greedy_commit(keys, tok, V)
     assert sv.get_device_error() & 0x2
     assert int(n_acc[0]) == 0
+
+
+def _paged_case(L, B, Hkv, M, R, seed):
+    rng = np.random.default_rng(seed)
+    P = B * M + 3
+    kp = rng.integers(0, 65535, size=(L, P, Hkv, 64, 128), dtype=np.uint16)
+    vp = rng.integers(0, 65535, size=(L, P, Hkv, 64, 128), dtype=np.uint16)
+    table = rng.permutation(P)[:B * M].reshape(B, M).astype(np.int32)
+    kb = rng.integers(0, 65535, size=(L, B, Hkv, R, 128), dtype=np.uint16)
+    vb = rng.integers(0, 65535, size=(L, B, Hkv, R, 128), dtype=np.uint16)
+    return kp, vp, table, kb, vb
+
+
+@pytest.mark.parametrize("tree", [False, True])
+def test_fused_paged_vs_oracle(sv, tree):
+    """Acceptance from the argmax keys and the commit into paged pools in one
+    launch: the oracle's acceptance, and its commit on the contiguous cache the
+    page table stands for, scattered back."""
+    B, H, V, L, Hkv, M = 3, 128, 20000, 2, 2, 4
+    par = synth.random_tree(64, 8, 3, 61) if tree else None
+    R = len(par) if tree else 5
+    parent = np.tile(par, (B, 1)).astype(np.int32) if tree else None
+    hid, W = _exact_lm(B * R, H, V, seed=90 + R)
+    logits = _oracle_logits(hid, W).reshape(B, R, V)
+    g = logits.argmax(-1)
+    if tree:
+        tok = np.stack([synth.plant_tree_drafts(g[b:b + 1], par[None], 0.8, V, 7 + b)[0] for b in range(B)])
+    else:
+        tok = synth.plant_chain_drafts(g, 0.8, V, seed=3)
+    kp, vp, table, kb, vb = _paged_case(L, B, Hkv, M, R, seed=R)
+    T_cap = M * 64
+    t = np.array([T_cap - 9, 64 - 2, 100], np.int32)   # the last page, a page edge, the middle
+    exp = oracle.accept_greedy(logits, tok, parent)
+    kc_ref, vc_ref, ln_ref = oracle.kv_commit(oracle.gather_pages(kp, table), oracle.gather_pages(vp, table), kb, vb,
+                                              exp[2], exp[0], t)
+    kpt, vpt = _t(kp), _t(vp)
+    ln = torch.from_numpy(t.copy()).cuda()
+    _, keys = sv.lm_head_argmax(hid.cuda(), W.cuda(), write_logits=False)
+    got = sv.accept_greedy_commit_paged(keys, torch.from_numpy(tok).cuda(), V, kpt, vpt, torch.from_numpy(table).cuda(),
+                                        _t(kb), _t(vb), ln, parent=None if parent is None else
+                                        torch.from_numpy(parent).cuda())
+    assert_same(got, exp, "fused paged acceptance")
+    assert np.array_equal(bits(kpt), oracle.scatter_pages(kp, table, kc_ref))
+    assert np.array_equal(bits(vpt), oracle.scatter_pages(vp, table, vc_ref))
+    assert np.array_equal(ln.cpu().numpy(), ln_ref)
+    assert sv.get_device_error() == 0
+
+
+def test_fused_paged_bad_page_flagged(sv):
+    B, H, V, L, Hkv, M, R = 2, 128, 4000, 2, 2, 2, 5
+    hid, W = _exact_lm(B * R, H, V, seed=31)
+    logits = _oracle_logits(hid, W).reshape(B, R, V)
+    tok = synth.plant_chain_drafts(logits.argmax(-1), 1.0, V, seed=2)   # all accepted: 5 rows each
+    kp, vp, table, kb, vb = _paged_case(L, B, Hkv, M, R, seed=8)
+    table[0, 1] = 10 ** 6                     # sequence 0's rows 62.. would land outside the pool
+    t = np.array([62, 10], np.int32)
+    kpt, vpt = _t(kp), _t(vp)
+    ln = torch.from_numpy(t.copy()).cuda()
+    _, keys = sv.lm_head_argmax(hid.cuda(), W.cuda(), write_logits=False)
+    got = sv.accept_greedy_commit_paged(keys, torch.from_numpy(tok).cuda(), V, kpt, vpt, torch.from_numpy(table).cuda(),
+                                        _t(kb), _t(vb), ln)
+    assert_same(got, oracle.accept_greedy(logits, tok), "fused paged acceptance, bad page")
+    assert sv.get_device_error() & 0x80
+    k_got = bits(kpt)
+    assert int(ln[0]) == 62 and np.array_equal(k_got[:, table[0, 0]], kp[:, table[0, 0]])
+    assert int(ln[1]) == 15 and np.array_equal(k_got[:, table[1, 0], :, 10:15], kb[:, 1, :, 0:5])
