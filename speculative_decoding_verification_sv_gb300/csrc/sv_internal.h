@@ -125,9 +125,10 @@ struct AttnPlan {
     int G;          // query heads per KV head
     int rows;       // R * G query rows per (sequence, KV head)
     int row_tiles;  // ceil(rows / rows per tile)
-    bool half;      // 64-row tiles (M = 64 MMAs, two key tiles per step), else 128-row tiles
+    bool half;      // 64-row tiles (M = 64 MMAs), else 128-row tiles (M = 128); two key tiles per step in both
     bool hw4;       // half tiles with four row-owner warps per TMEM quadrant (long loops), else two
-    bool split_kv;  // K and V halves of a ring stage on separate barriers (loops longer than the ring, one row tile)
+    bool split_kv;  // K and V halves of a ring stage on separate barriers (full tiles; half tiles whose loops
+                    // are longer than the ring over one row tile)
     int warps;      // warps per CTA
     int splits;     // CTAs per thread-block cluster (split-KV merged through DSMEM)
     int clusters;   // clusters per (sequence, KV head, row tile); > 1 merges in the workspace

@@ -9,31 +9,31 @@
 //
 // Decomposition.  For every (sequence b, KV head g) the R*G query rows of the
 // G query heads that share g are packed together (row r = j*G + local head),
-// so each K/V tile streamed from HBM serves all of them (GQA); rows are cut
-// into tiles of 128, the MMA's M.  One thread-block cluster of C CTAs (C up
-// to 16) handles one (b, g, row tile): the 64-key tiles -- ceil(t/64) context
-// tiles followed by ceil(R/64) block tiles -- are split evenly over its CTAs
-// (split-KV, sized so the grid fills the SMs).  Inside a CTA, keys are
-// processed one 64-key tile per step:
-//   * warp 16 streams K and V tiles through a TMA ring (cp.async.bulk.tensor,
-//     128-byte swizzle, full/empty mbarriers);
-//   * one thread of warp 17 issues tcgen05.mma: S = Q K^T into one of two
-//     64-column TMEM score buffers (A = Q K-major, B = K tile K-major), and
-//     O += P V into a TMEM accumulator (A = P K-major from one of two shared
-//     P buffers, B = V tile MN-major), releasing stages and buffers with
+// so each K/V tile streamed from HBM serves all of them (GQA).  Rows are cut
+// into row tiles: half tiles of 64 rows (M = 64 MMAs) or full tiles of 128
+// (M = 128), whichever the plan costs lower.  One thread-block cluster of C
+// CTAs (1 <= C <= 16) handles one (b, g, row tile), a unit: its 64-key tiles
+// -- ceil(t/64) context tiles followed by ceil(R/64) block tiles -- are split
+// evenly over the CTAs (split-KV, sized so the grid fills the SMs; several
+// clusters per unit meet in a workspace).  Inside a CTA, keys are processed
+// two 64-key tiles per step:
+//   * one warp streams K and V tiles through a TMA ring (cp.async.bulk.tensor,
+//     128-byte swizzle, full/empty mbarriers; K and V regions on barriers of
+//     their own where the loop outgrows the ring);
+//   * one thread of another warp issues tcgen05.mma: S = Q K^T (N = 128, both
+//     tiles) into one of two TMEM score buffers, and O += P V into a TMEM
+//     accumulator with P read from TMEM, releasing stages and buffers with
 //     tcgen05.commit; S of step st+1 is issued before P V of step st, so the
 //     score MMAs run under the softmax;
-//   * sixteen row-owner warps: warp w reads TMEM lanes 32*(w%4).. (one query
-//     row per thread) and the 16-score column group w/4 of each step; the four
-//     threads of a row exchange their partial maxima through shared memory,
-//     apply the chain/tree/length mask, keep the running max and sum, write P
-//     (bf16) to shared memory, and rescale their part of the row of O in TMEM
-//     only when the max has grown by more than 2^8 since it was last used
-//     (otherwise the stale max keeps every P <= 256, exact in fp32).  Warps
-//     whose 32 rows are all padding skip the arithmetic;
-//   * at the end every CTA leaves its unnormalised partial (max, sum, O row)
-//     in shared memory and the cluster merges the C partials of each row
-//     through distributed shared memory, writing bf16 rows.
+//   * row-owner warps read the scores of their TMEM quadrant, exchange partial
+//     maxima through shared memory, apply the chain/tree/length mask, keep the
+//     running max and sum, write P (bf16) back to TMEM, and rescale their part
+//     of the row of O only when the max has grown by more than 2^8 since it was
+//     last used (otherwise the stale max keeps every P <= 256, exact in fp32).
+//     Warps whose rows are all padding skip the arithmetic;
+//   * at the end every CTA pushes its unnormalised partial (max, sum, O row) of
+//     each row into the shared memory of the row's owner CTA (distributed
+//     shared memory), and the owners merge the C partials, writing bf16 rows.
 // Launch: programmatic dependent launch; everything earlier kernels may have
 // written (lengths, cache rows, Q, block K/V, tree) is read after
 // griddepcontrol.wait.
@@ -60,7 +60,7 @@ constexpr int kRec = kD + 4;              // partial record: m, l, 2 pad, o[128]
 constexpr int kMaxR = 128;
 constexpr int kMaxCluster = 16;
 #ifndef SV_ATTN_MERGE_COST
-#define SV_ATTN_MERGE_COST 6
+#define SV_ATTN_MERGE_COST 7
 #endif
 constexpr int kMergeCost = SV_ATTN_MERGE_COST;   // workspace merge, in key-tile times
 constexpr int kWsMergeBatch = 12;         // workspace partials per unit merged in one round of loads
@@ -68,19 +68,14 @@ constexpr int kGroups = 4;                // full tiles: column groups of a step
 #ifndef SV_ATTN_HALF_MAX_ROWS
 #define SV_ATTN_HALF_MAX_ROWS 64
 #endif
-#ifndef SV_ATTN_HALF_MAX_UNITS
-#define SV_ATTN_HALF_MAX_UNITS 16
-#endif
-// Row tiles: (b, g) groups of at most kHalfMaxRows rows use one half tile (64
-// rows, two key tiles per step); larger groups use half tiles too when there
-// are at most kHalfMaxUnits (b, g) groups (few units: the shorter step per key
-// wins), else full tiles (128 rows, one key tile per step: each K/V tile read
-// once for twice the rows)
+// Row tiles: (b, g) groups of at most kHalfMaxRows rows use one half tile;
+// larger groups use half or full tiles as the plan's cost decides (full tiles
+// serve twice the rows with the same MMAs per key, half tiles make more units
+// for the SMs)
 constexpr int kHalfMaxRows = SV_ATTN_HALF_MAX_ROWS;
-constexpr int kHalfMaxUnits = SV_ATTN_HALF_MAX_UNITS;
 
 // Full tiles (128 rows): 16 row-owner warps, warp w on TMEM quadrant w % 4
-// and column group w / 4.  Half tiles (64 rows): kHW = 2 or 4 row-owner warps
+// and the 32-column group w / 4 of each step.  Half tiles (64 rows): kHW = 2 or 4 row-owner warps
 // per quadrant (= per SM sub-partition, so one hides another's latency), the
 // rows spread over the first 16 lanes of every quadrant, 2 kHW threads per row
 // (two per warp via the 16x32bx2 access, one warp per column slice).
@@ -102,21 +97,23 @@ struct Roles {
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescale = 8.0f;          // log2 of the largest tolerated P
 
-// Shared-memory and TMEM layout.  Full tiles: M = 128 MMAs, 32 KB of Q, one
-// key tile per softmax step, 5 ring stages.  Half tiles: M = 64 MMAs (row m of
-// the tile in TMEM lane 32 * (m / 16) + m % 16), 16 KB of Q, two key tiles per
-// step (S = Q K^T as one N = 128 MMA chain over both: fewer, larger MMAs per
-// key; an M = 64 MMA takes as long as an M = 128 one), 3 stages of two tiles.
+// Shared-memory and TMEM layout.  Both modes take two key tiles per step
+// (S = Q K^T as one N = 128 MMA chain over both: fewer, larger MMAs per key).
+// Full tiles: M = 128 MMAs, 32 KB of Q, 2 ring stages of two tiles (always
+// on split K/V barriers: with two stages the K loads must run ahead of the
+// P V reads).  Half tiles: M = 64 MMAs (row m of the tile in TMEM lane
+// 32 * (m / 16) + m % 16), 16 KB of Q, 3 stages; an M = 64 MMA issues as
+// slowly as an M = 128 one, so full tiles do twice the work per MMA.
 // A stage holds its tiles' boxes region by region: K dims 0-63 of every tile,
 // K dims 64-127, V dims 0-63, V dims 64-127, so keys are contiguous per region.
 template <bool kHalf>
 struct Lay {
     static constexpr int kM = kHalf ? 64 : 128;            // MMA M (rows of the Q tile)
-    static constexpr int kT = kHalf ? 2 : 1;                // key tiles per softmax step
+    static constexpr int kT = 2;                            // key tiles per softmax step
     static constexpr int kStepKeys = kT * kNk;
     static constexpr int kStageBytes = kT * kTileBytes;
     static constexpr int kRegion = kT * kHalfBytes;        // one region of a stage
-    static constexpr int kStages = kHalf ? 3 : 5;           // ring depth in steps
+    static constexpr int kStages = kHalf ? 3 : 2;           // ring depth in steps
     static constexpr int kQBytes = kM * kD * 2;             // two 64-dim halves of kM rows
     static constexpr int kRingBytes = kStages * kStageBytes;
     // TMEM columns: two S buffers, O (128 columns), two P buffers (two bf16 per column)
@@ -267,14 +264,18 @@ __global__ void __launch_bounds__(Roles<kHalf, kHW>::kThreads, 1)
             prefetch_l2(a.v_blk + off, static_cast<uint32_t>(a.R * kD * 2));
         }
     }
+    // Without cache_ready the length may come from the kernel before: every
+    // thread waits first.  With it, the plan below (split bounds, fold, merge
+    // plan) is computed while that kernel drains, and each warp waits only
+    // before its first read of that kernel's outputs (Q, the block K/V, the
+    // tree) or its first global store: reading the parameter block and doing
+    // this set-up after the wait put ~1 us on every batch-1 layer's critical
+    // path.
     const bool early = a.cache_ready != 0;
-    int t = early ? a.len[b] : 0;
-    if (!early || warp != kTmaWarp) pdl_wait();
-    if (!early) t = a.len[b];
-    if (t < 0 || t > a.T_cap) {
-        if (threadIdx.x == 0 && rank == 0 && rt == 0) raise_error(a.err, SV_DEVERR_LENGTH);
-        t = t < 0 ? 0 : a.T_cap;
-    }
+    if (!early) pdl_wait();
+    int t = a.len[b];
+    const bool bad_len = t < 0 || t > a.T_cap;
+    if (bad_len) t = t < 0 ? 0 : a.T_cap;
     const int n_ctx = (t + kNk - 1) / kNk;
     const int n_blk = (a.R + kNk - 1) / kNk;
     const int n_all = n_ctx + n_blk;
@@ -387,7 +388,8 @@ __global__ void __launch_bounds__(Roles<kHalf, kHW>::kThreads, 1)
         merge_plan(need, light);
     } else if (warp == kMmaWarp) {
         // ---------------- MMA issuer ----------------
-        merge_plan(need, light);   // while the Q tile is still on its way
+        merge_plan(need, light);   // before the wait (cache_ready) or while the Q tile is on its way
+        if (early) pdl_wait();
         if (lane == 0 && ntiles > 0) {
             // S = Q K^T over the step's tiles (N = 64 per tile), O += P V
             constexpr uint32_t idesc_s = idesc_bf16_f32(kM, kStepKeys, false, false);
@@ -464,6 +466,11 @@ __global__ void __launch_bounds__(Roles<kHalf, kHW>::kThreads, 1)
         }
     } else {
         // ---------------- row-owner warps ----------------
+        if (early) {
+            merge_plan(need, light);
+            pdl_wait();
+        }
+        if (bad_len && threadIdx.x == 0 && rank == 0 && rt == 0) raise_error(a.err, SV_DEVERR_LENGTH);
         // tree ancestor masks: bit i of anc[jj] set iff block row i is jj or an ancestor
         if (tree) {
             const int32_t* par = a.parent + static_cast<size_t>(b) * a.R;
@@ -507,7 +514,7 @@ __global__ void __launch_bounds__(Roles<kHalf, kHW>::kThreads, 1)
                     *reinterpret_cast<uint4*>(dst) = v;
                 }
             }
-            merge_plan(need, light);   // while the Q copies are in flight
+            if (!early) merge_plan(need, light);   // while the Q copies are in flight
             cp_async_wait_all();
         }
         fence_proxy_async_smem();
@@ -557,20 +564,120 @@ __global__ void __launch_bounds__(Roles<kHalf, kHW>::kThreads, 1)
             mbar_wait(&s_full[sb], (st >> 1) & 1, a.err);
             tc_fence_after();
             const bool work = quarter_live;
+            if constexpr (!kHalf) {
+                // Full tiles: 32 columns per thread, taken as two 16-column
+                // halves that the exponent pass reads from TMEM a second time,
+                // so that only 16 scores are live (32 at once spill at the 96
+                // registers an 18-warp CTA leaves each thread)
+                const int ti = st * kT + tsub;
+                const bool tile_live = ti < ntiles;
+                const int gt = first + ti;
+                const bool is_block = gt >= n_ctx;
+                const int kb = (is_block ? (gt - n_ctx) * kNk : gt * kNk) + ctile;
+                // visibility of this thread's 32 keys as one bit mask, formed once
+                // per step (context: kl < t; chain block: kl <= j and kl < R; no
+                // tile: none; tree block: the ancestor window, read from shared
+                // memory), so that chains and trees run the same per-key code and
+                // unmasked steps skip it; a per-key choice between the tree and the
+                // length test, kept by the compiler in every step, doubled the
+                // tree variant's step time
+                const bool masked = is_block || kb + kCols > t || !tile_live;
+                uint32_t vmask = ~0u;
+                if (masked) {
+                    const int lim = !tile_live ? 0 : !is_block ? t - kb : (j + 1 < a.R ? j + 1 : a.R) - kb;
+                    vmask = lim >= 32 ? ~0u : lim <= 0 ? 0u : (1u << lim) - 1u;
+                    if (kTree && is_block && tile_live) vmask = static_cast<uint32_t>(anc[2 * j + (gt - n_ctx)] >> ctile);
+                }
+                auto load_half = [&](int h, uint32_t (&v)[16]) {
+                    tmem_ld16_sync(tS(sb) + lane_off + col0 + 16 * h, v);
+                    if (vmask != ~0u) {
+#pragma unroll
+                        for (int e = 0; e < 16; ++e)
+                            v[e] = ((vmask >> (16 * h + e)) & 1u) != 0u ? v[e] : __float_as_uint(-INFINITY);
+                    }
+                };
+                float mpart = -INFINITY;
+                if (work) {
+                    float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        uint32_t v[16];
+                        load_half(h, v);
+#pragma unroll
+                        for (int e = 0; e < 16; e += 8)
+#pragma unroll
+                            for (int u = 0; u < 4; ++u)
+                                mq[u] = fmax3(mq[u], __uint_as_float(v[e + 2 * u]), __uint_as_float(v[e + 2 * u + 1]));
+                    }
+                    mpart = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3])) * a.scale_log2;
+                }
+                red[(sb * kGroups + cgp) * kRows + r] = mpart;
+                named_barrier(2, 32 * kSoftWarps);
+                float mt = red[(sb * kGroups + 0) * kRows + r];
+#pragma unroll
+                for (int c2 = 1; c2 < kGroups; ++c2) mt = fmaxf(mt, red[(sb * kGroups + c2) * kRows + r]);
+                float m_new = m_ref, corr = 1.f;
+                if (mt > -INFINITY && (m_ref == -INFINITY || mt > m_ref + kRescale)) {
+                    m_new = mt;
+                    corr = m_ref == -INFINITY ? 0.f : fast_exp2(m_ref - m_new);
+                }
+                // P buffer sb is free once the P V of step st-2 is done; O is
+                // rescaled once the P V of step st-1 has settled it
+                if (st >= 2) {
+                    mbar_wait(&o_done[sb], ((st - 2) >> 1) & 1, a.err);
+                    tc_fence_after();
+                }
+                if (quarter_live && st >= 1 && __any_sync(0xffffffffu, corr != 1.f)) {
+                    mbar_wait(&o_done[sb ^ 1], ((st - 1) >> 1) & 1, a.err);
+                    tc_fence_after();
+#pragma unroll
+                    for (int c0 = 0; c0 < kD / kGroups; c0 += 16) {
+                        const uint32_t ta = tO + lane_off + cgp * (kD / kGroups) + c0;
+                        uint32_t o16[16];
+                        tmem_ld16_sync(ta, o16);
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) o16[e] = __float_as_uint(__uint_as_float(o16[e]) * corr);
+                        tmem_st16(ta, o16);
+                    }
+                    tmem_st_wait();
+                }
+                float ps0 = 0.f, ps1 = 0.f;
+                if (work) {
+                    const float nm = m_new == -INFINITY ? 0.f : -m_new;
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        uint32_t v[16];
+                        load_half(h, v);
+                        uint32_t pk[8];
+#pragma unroll
+                        for (int e = 0; e < 16; e += 2) {
+                            const float p0 = fast_exp2(fmaf(__uint_as_float(v[e]), a.scale_log2, nm));
+                            const float p1 = fast_exp2(fmaf(__uint_as_float(v[e + 1]), a.scale_log2, nm));
+                            ps0 += p0;
+                            ps1 += p1;
+                            const __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
+                            pk[e / 2] = *reinterpret_cast<const uint32_t*>(&pb);
+                        }
+                        tmem_st8(tP(sb) + lane_off + (col0 + 16 * h) / 2, pk);
+                    }
+                    tmem_st_wait();
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&s_empty[sb]);
+                lsum = lsum * corr + (ps0 + ps1);
+                m_ref = m_new;
+            } else {
             uint32_t rs[kCols];
             uint32_t rx[kCX];
             if constexpr (kHalf && kHW == 2) {
                 if (work && fx) tmem_ld16_h_sync<kNk / 2>(tS(sb ^ 1) + lane_off + cgp * kCX, rx);
             }
             if (work) {
-                if constexpr (kHalf) {
-                    // columns 32 cgp .. of the step's first tile (threads 0-15)
-                    // and of its second tile (threads 16-31)
-                    if constexpr (kCols == 32) tmem_ld32_h_sync<kStepKeys / 2>(tS(sb) + lane_off + cgp * kCols, rs);
-                    else tmem_ld16_h_sync<kStepKeys / 2>(tS(sb) + lane_off + cgp * kCols, rs);
-                } else {
-                    tmem_ld16_sync(tS(sb) + lane_off + col0, rs);
-                }
+                // columns 32 cgp .. of the step's first tile (threads 0-15)
+                // and of its second tile (threads 16-31)
+                if constexpr (kCols == 32) tmem_ld32_h_sync<kStepKeys / 2>(tS(sb) + lane_off + cgp * kCols, rs);
+                else tmem_ld16_h_sync<kStepKeys / 2>(tS(sb) + lane_off + cgp * kCols, rs);
             }
             tc_fence_before();
             __syncwarp();
@@ -625,22 +732,13 @@ __global__ void __launch_bounds__(Roles<kHalf, kHW>::kThreads, 1)
                     mpart = fmaxf(mpart, mxx * a.scale_log2);
                 }
             }
-            float mt;
-            if constexpr (kHalf) {
-                // the row's other tile sits 16 lanes away in the same warp, its
-                // other column half in the quadrant's other warp
-                mt = fmaxf(mpart, __shfl_xor_sync(0xffffffffu, mpart, 16));
-                red[(sb * kGroups + cgp) * kRows + r] = mt;
-                named_barrier(3 + q4, 32 * kHalfWarps);
+            // the row's other tile sits 16 lanes away in the same warp, its
+            // other column half in the quadrant's other warp
+            float mt = fmaxf(mpart, __shfl_xor_sync(0xffffffffu, mpart, 16));
+            red[(sb * kGroups + cgp) * kRows + r] = mt;
+            named_barrier(3 + q4, 32 * kHalfWarps);
 #pragma unroll
-                for (int c2 = 0; c2 < kHalfWarps; ++c2) mt = fmaxf(mt, red[(sb * kGroups + c2) * kRows + r]);
-            } else {
-                red[(sb * kGroups + cgp) * kRows + r] = mpart;
-                named_barrier(2, 32 * kSoftWarps);
-                mt = red[(sb * kGroups + 0) * kRows + r];
-#pragma unroll
-                for (int c2 = 1; c2 < kGroups; ++c2) mt = fmaxf(mt, red[(sb * kGroups + c2) * kRows + r]);
-            }
+            for (int c2 = 0; c2 < kHalfWarps; ++c2) mt = fmaxf(mt, red[(sb * kGroups + c2) * kRows + r]);
             float m_new = m_ref, corr = 1.f;
             if (mt > -INFINITY && (m_ref == -INFINITY || mt > m_ref + kRescale)) {
                 m_new = mt;
@@ -687,39 +785,22 @@ __global__ void __launch_bounds__(Roles<kHalf, kHW>::kThreads, 1)
                 // rescale O: wait for the P V of step st-1 to settle it
                 mbar_wait(&o_done[sb ^ 1], ((st - 1) >> 1) & 1, a.err);
                 tc_fence_after();
-                if constexpr (kHalf) {
-                    // O columns 64 sub + (64 / kHalfWarps) cgp .. of the row
+                // O columns 64 sub + (64 / kHalfWarps) cgp .. of the row
 #pragma unroll
-                    for (int c0 = 0; c0 < kD / (2 * kHalfWarps); c0 += 16) {
-                        const uint32_t ta = tO + lane_off + cgp * (kD / (2 * kHalfWarps)) + c0;
-                        uint32_t o16[16];
-                        tmem_ld16_h_sync<kD / 2>(ta, o16);
+                for (int c0 = 0; c0 < kD / (2 * kHalfWarps); c0 += 16) {
+                    const uint32_t ta = tO + lane_off + cgp * (kD / (2 * kHalfWarps)) + c0;
+                    uint32_t o16[16];
+                    tmem_ld16_h_sync<kD / 2>(ta, o16);
 #pragma unroll
-                        for (int e = 0; e < 16; ++e) o16[e] = __float_as_uint(__uint_as_float(o16[e]) * corr);
-                        tmem_st16_h<kD / 2>(ta, o16);
-                    }
-                } else {
-#pragma unroll
-                    for (int c0 = 0; c0 < kD / kGroups; c0 += 16) {
-                        const uint32_t ta = tO + lane_off + cgp * (kD / kGroups) + c0;
-                        uint32_t o16[16];
-                        tmem_ld16_sync(ta, o16);
-#pragma unroll
-                        for (int e = 0; e < 16; ++e) o16[e] = __float_as_uint(__uint_as_float(o16[e]) * corr);
-                        tmem_st16(ta, o16);
-                    }
+                    for (int e = 0; e < 16; ++e) o16[e] = __float_as_uint(__uint_as_float(o16[e]) * corr);
+                    tmem_st16_h<kD / 2>(ta, o16);
                 }
                 tmem_st_wait();
             }
             if (work) {
                 // P of this thread's columns into TMEM buffer sb, two keys per column
-                if constexpr (kHalf) {
-                    // P columns col0/2 .. (two keys per column)
-                    if constexpr (kCols == 32) tmem_st16_h<kStepKeys / 4>(tP(sb) + lane_off + cgp * (kCols / 2), pk);
-                    else tmem_st8_h<kStepKeys / 4>(tP(sb) + lane_off + cgp * (kCols / 2), pk);
-                } else {
-                    tmem_st8(tP(sb) + lane_off + col0 / 2, pk);
-                }
+                if constexpr (kCols == 32) tmem_st16_h<kStepKeys / 4>(tP(sb) + lane_off + cgp * (kCols / 2), pk);
+                else tmem_st8_h<kStepKeys / 4>(tP(sb) + lane_off + cgp * (kCols / 2), pk);
                 tmem_st_wait();
             }
             if constexpr (kHalf && kHW == 2) {
@@ -735,6 +816,7 @@ __global__ void __launch_bounds__(Roles<kHalf, kHW>::kThreads, 1)
                         tmem_st_wait();
                     }
                 }
+            }
             }
             {
                 // V rows of cache positions >= t in the last, partial context
@@ -1057,7 +1139,7 @@ int active_clusters(int C) {
     std::lock_guard<std::mutex> lk(mu);
     if (cache[dev][C]) return cache[dev][C];
     int n = 0;
-    if (prepare_kernel<kHalf, false, 2, false>() == cudaSuccess) {   // every variant uses the same resources
+    if (prepare_kernel<kHalf, false, 2, !kHalf>() == cudaSuccess) {   // every variant uses the same resources
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(C, 1, 1);
         cfg.blockDim = dim3(Roles<kHalf, 2>::kThreads, 1, 1);
@@ -1069,7 +1151,7 @@ int active_clusters(int C) {
         attr[0].val.clusterDim.z = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        if (cudaOccupancyMaxActiveClusters(&n, attn_tc_kernel<kHalf, false, 2, false>, &cfg) != cudaSuccess) n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, attn_tc_kernel<kHalf, false, 2, !kHalf>, &cfg) != cudaSuccess) n = 0;
     }
     cudaGetLastError();
     if (n <= 0) n = fallback;
@@ -1106,52 +1188,69 @@ cudaError_t launch_mode(const AttnPlan& p, const sv_attn_shape& s, const uint8_t
 
 // Split-KV plan.  Every (sequence, KV head, row tile) -- a unit -- gets
 // `clusters` clusters of `splits` CTAs; its key tiles are divided evenly over
-// those CTAs.  Candidates C = 16, 8, 4, 2, 1 take as many clusters per unit as
-// fit in one wave of resident clusters (at most 32, at least one key tile per
-// CTA); the cost counts the key tiles of the busiest CTA plus a fixed start-up
-// of three tiles per wave, and a merge through the workspace as six tiles (its
-// partials cross the L2 in a few dependent round trips, measured at several
-// microseconds) plus the partial bytes each merging SM reads (one SM pulls
-// about 40 KB per tile time).  Ties keep the larger cluster.
+// those CTAs.  For each row-tile mode (half tiles; full tiles when a (b, g)
+// group has more than 64 rows) and each cluster size C = 16 .. 1, one cluster
+// per unit or as many as fit in one wave of resident clusters (at most 32, at
+// least one key tile per CTA) are costed: the key tiles of the busiest CTA
+// plus a fixed start-up of three tiles per wave, and a merge through the
+// workspace as seven tiles (its partials cross the L2 in a few dependent round
+// trips: at 7B batch 1 two clusters per KV head measured 17.4 -> 22.9 us, and
+// on the draft tree's shape 4 x 2 CTAs took 27.6 us against 25.6-26.1 us for
+// one cluster of 6) plus the partial bytes each merging SM reads (one SM
+// pulls about 40 KB per tile time).  A full-tile step takes
+// 9/8 of a half-tile step (measured on the draft tree's shape: ~2650 against
+// ~2360 cycles per two-tile step).  Resident clusters come from the occupancy
+// query, so sizes that leave a unit for a second wave (7, 8 and 9 CTAs fit 15
+// times on the GB300) are costed as such.  Ties keep the larger cluster.
 AttnPlan attn_plan(const sv_attn_shape& s) {
     AttnPlan p;
     p.G = s.Hq / s.Hkv;
     p.rows = s.R * p.G;
-    p.half = p.rows <= kHalfMaxRows || static_cast<int64_t>(s.B) * s.Hkv <= kHalfMaxUnits;
-    const int tile_rows = p.half ? Lay<true>::kM : Lay<false>::kM;
-    p.row_tiles = (p.rows + tile_rows - 1) / tile_rows;
-    p.hw4 = false;
-    const int64_t units = static_cast<int64_t>(s.B) * s.Hkv * p.row_tiles;
     const int64_t tiles = (s.T_cap + kNk - 1) / kNk + (s.R + kNk - 1) / kNk;
     int64_t best = -1;
+    p.half = true;
+    p.row_tiles = (p.rows + Lay<true>::kM - 1) / Lay<true>::kM;
     p.splits = 1;
     p.clusters = 1;
-    for (int C = kMaxCluster; C >= 1; C >>= 1) {
-        if (C > tiles && C > 1) continue;
-        const int64_t cap = p.half ? active_clusters<true>(C) : active_clusters<false>(C);
-        int64_t nc_max = cap / units;
-        if (nc_max > 32) nc_max = 32;
-        if (nc_max > tiles / C) nc_max = tiles / C;
-        if (nc_max < 1) nc_max = 1;
-        for (int64_t nc = 1; nc <= nc_max; nc = nc < nc_max ? nc_max : nc_max + 1) {   // one cluster, or the most
-            const int64_t waves = (units * nc + cap - 1) / cap;
-            const int64_t per_cta = (tiles + C * nc - 1) / (C * nc);
-            const int64_t part_rows = p.rows < tile_rows ? p.rows : tile_rows;
-            const int64_t merge_bytes = nc * part_rows * kRec * 4 / C;   // per SM of the merging cluster
-            const int64_t cost = waves * (3 + per_cta) + (nc > 1 ? kMergeCost + merge_bytes / (40 * 1024) : 0);
-            if (best < 0 || cost < best) {
-                best = cost;
-                p.splits = C;
-                p.clusters = static_cast<int>(nc);
+    for (int mode = 0; mode < 2; ++mode) {
+        const bool half = mode == 0;
+        if (!half && p.rows <= kHalfMaxRows) continue;
+        const int tile_rows = half ? Lay<true>::kM : Lay<false>::kM;
+        const int step_cost = half ? 8 : 9;   // eighths of a half-tile step per tile
+        const int row_tiles = (p.rows + tile_rows - 1) / tile_rows;
+        const int64_t units = static_cast<int64_t>(s.B) * s.Hkv * row_tiles;
+        for (int C = kMaxCluster; C >= 1; --C) {
+            if (C > tiles && C > 1) continue;
+            const int64_t cap = half ? active_clusters<true>(C) : active_clusters<false>(C);
+            int64_t nc_max = cap / units;
+            if (nc_max > 32) nc_max = 32;
+            if (nc_max > tiles / C) nc_max = tiles / C;
+            if (nc_max < 1) nc_max = 1;
+            for (int64_t nc = 1; nc <= nc_max; nc = nc < nc_max ? nc_max : nc_max + 1) {   // one cluster, or the most
+                const int64_t waves = (units * nc + cap - 1) / cap;
+                const int64_t per_cta = (tiles + C * nc - 1) / (C * nc);
+                const int64_t part_rows = p.rows < tile_rows ? p.rows : tile_rows;
+                const int64_t merge_bytes = nc * part_rows * kRec * 4 / C;   // per SM of the merging cluster
+                const int64_t cost = waves * (3 * 8 + step_cost * per_cta) +
+                                     (nc > 1 ? 8 * (kMergeCost + merge_bytes / (40 * 1024)) : 0);
+                if (best < 0 || cost < best) {
+                    best = cost;
+                    p.half = half;
+                    p.row_tiles = row_tiles;
+                    p.splits = C;
+                    p.clusters = static_cast<int>(nc);
+                }
             }
         }
     }
     p.hw4 = p.half && (tiles + p.splits * p.clusters - 1) / (p.splits * p.clusters) >= kHw4MinTiles;
-    // separate K and V barriers (chains in half tiles): loops longer than the
-    // ring over tiles no other row tile of the unit shares
-    p.split_kv = p.half && p.row_tiles == 1 &&
-                 ((tiles + p.splits * p.clusters - 1) / (p.splits * p.clusters) + Lay<true>::kT - 1) / Lay<true>::kT >
-                     Lay<true>::kStages;
+    // separate K and V barriers: always with full tiles (two ring stages), and
+    // for chains in half tiles whose loops are longer than the ring over tiles
+    // no other row tile of the unit shares
+    p.split_kv = !p.half ||
+                 (p.row_tiles == 1 &&
+                  ((tiles + p.splits * p.clusters - 1) / (p.splits * p.clusters) + Lay<true>::kT - 1) / Lay<true>::kT >
+                      Lay<true>::kStages);
     p.warps = !p.half ? Roles<false>::kThreads / 32 : p.hw4 ? Roles<true, 4>::kThreads / 32 : Roles<true, 2>::kThreads / 32;
     return p;
 }
@@ -1216,15 +1315,15 @@ cudaError_t launch_verify_attn(const sv_attn_shape& s, const uint16_t* q, const 
     a.max_pages = max_pages;
     a.num_pages = num_pages;
     if (parent != nullptr)
-        return !p.half ? launch_mode<false, true, 2, false>(p, s, tK, tV, tKb, tVb, a, st)
+        return !p.half ? launch_mode<false, true, 2, true>(p, s, tK, tV, tKb, tVb, a, st)
                : p.hw4 ? launch_mode<true, true, 4, false>(p, s, tK, tV, tKb, tVb, a, st)
                        : launch_mode<true, true, 2, false>(p, s, tK, tV, tKb, tVb, a, st);
+    if (!p.half) return launch_mode<false, false, 2, true>(p, s, tK, tV, tKb, tVb, a, st);   // always split
     if (p.split_kv)
         return p.hw4 ? launch_mode<true, false, 4, true>(p, s, tK, tV, tKb, tVb, a, st)
                      : launch_mode<true, false, 2, true>(p, s, tK, tV, tKb, tVb, a, st);
-    return !p.half ? launch_mode<false, false, 2, false>(p, s, tK, tV, tKb, tVb, a, st)
-           : p.hw4 ? launch_mode<true, false, 4, false>(p, s, tK, tV, tKb, tVb, a, st)
-                   : launch_mode<true, false, 2, false>(p, s, tK, tV, tKb, tVb, a, st);
+    return p.hw4 ? launch_mode<true, false, 4, false>(p, s, tK, tV, tKb, tVb, a, st)
+                 : launch_mode<true, false, 2, false>(p, s, tK, tV, tKb, tVb, a, st);
 }
 
 }  // namespace sv
