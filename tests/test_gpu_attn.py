@@ -125,6 +125,45 @@ def test_attn_tree_65_nodes(sv, seed):
     assert ok, (err, bound)
 
 
+@pytest.mark.parametrize("B,R,Hq,Hkv,lengths,tree", [
+    (8, 17, 16, 4, [600, 1, 64, 65, 300, 0, 511, 700], False),   # 68 rows: quadrants 0-2 live, 4 rows in 2
+    (8, 10, 32, 4, [600, 513, 64, 0, 700, 1, 65, 300], False),   # 80 rows, 8 heads per group
+    (8, 24, 16, 4, [600, 300, 0, 700, 1, 64, 65, 511], False),   # 96 rows: quadrant 3 dead
+    (8, 30, 16, 4, [700, 600, 1, 0, 65, 64, 300, 513], False),   # 120 rows: padding inside quadrant 3
+    (8, 33, 16, 4, [600, 0, 700, 64, 1, 65, 511, 300], False),   # 132 rows: a full tile and a 4-row tile
+    (4, 33, 16, 4, [600, 0, 700, 65], True),                     # the same under a tree mask
+    (2, 65, 28, 4, [700, 513], True),                            # the draft tree at batch 2 (4-CTA clusters)
+])
+def test_attn_full_tile_row_counts(sv, B, R, Hq, Hkv, lengths, tree):
+    """128-row tiles (two key tiles per step, split K/V barriers) with every
+    count of live TMEM quadrants and padding rows inside a live quadrant,
+    chains and trees, against the oracle (the plan takes full tiles for these
+    shapes, in clusters of 4 or 2)."""
+    parent = None
+    if tree:
+        parent = np.tile(synth.random_tree(R - 1, 8, 3, R), (B, 1))
+    got, ref = _run(sv, B, R, Hq, Hkv, 704, lengths, parent=parent, seed=B * 13 + R)
+    ok, err, bound = within_tol(got, ref)
+    assert ok, (err, bound)
+    assert sv.get_device_error() == 0
+
+
+@pytest.mark.parametrize("B,R,Hq,Hkv,T_cap,lengths,tree", [
+    (1, 17, 16, 2, 704, [600], False),                 # half tiles, 12-CTA clusters
+    (1, 33, 16, 4, 704, [650], False),                 # full tiles, 12-CTA clusters
+    (3, 33, 16, 4, 1408, [1300, 1, 700], False),       # full tiles, 5-CTA clusters
+    (1, 65, 28, 4, 1408, [1300], True),                # the draft tree, full tiles, 6-CTA clusters
+])
+def test_attn_cluster_sizes(sv, B, R, Hq, Hkv, T_cap, lengths, tree):
+    """Shapes whose plan picks a cluster size that is not a power of two
+    (split bounds, light owners and the merge over C CTAs)."""
+    parent = np.tile(synth.random_tree(R - 1, 8, 3, 7), (B, 1)) if tree else None
+    got, ref = _run(sv, B, R, Hq, Hkv, T_cap, lengths, parent=parent, seed=B * 17 + R)
+    ok, err, bound = within_tol(got, ref)
+    assert ok, (err, bound)
+    assert sv.get_device_error() == 0
+
+
 @pytest.mark.parametrize("seed", [3, 4])
 def test_attn_tree_small_unit(sv, seed):
     """A 9-node tree with 3 query heads per KV head: 27 query rows per
