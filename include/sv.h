@@ -118,7 +118,8 @@ typedef struct sv_attn_shape {
  * once).  0 when every (sequence, KV head) is handled by one cluster, whose
  * split partials merge on chip; ws may then be NULL.  Otherwise several
  * clusters share a (sequence, KV head): the workspace holds one ticket word per
- * (sequence, KV head, 128-row tile) followed by the clusters' fp32 partials.
+ * (sequence, KV head, row tile of 64 or 128 rows, as the plan picks) followed by
+ * the clusters' fp32 partials.
  * The ticket words must be zero before the first call on a workspace (e.g.
  * cudaMemset to 0 once); every call that completes leaves them zero again, so
  * one workspace serves any number of calls in stream order.  Calls running
