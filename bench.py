@@ -767,18 +767,20 @@ def main():
     E = args.e2e_steps
     done = torch.cuda.Event()
     # the copy in, the round and the copy out as one CUDA graph (how a serving
-    # loop would issue them); if this torch cannot capture host copies, the
-    # three are issued one by one
+    # loop would issue them); the copies are the library's own (sv_copy: the
+    # SMs read the pinned inputs and write the pinned result over the host
+    # link, inside the round's launch chain); if this torch cannot capture the
+    # round, the three are issued one by one
     gX = None
     try:
         torch.cuda.synchronize()
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
             for d, h in zip(ins, h_in):
-                d.copy_(h, non_blocking=True)
+                rnd.sv.copy(d, h, stream=stream)
             rnd.step()
             for h, d in zip(h_out, outs):
-                h.copy_(d, non_blocking=True)
+                rnd.sv.copy(h, d, stream=stream)
         gX = g
     except Exception:
         torch.cuda.synchronize()
@@ -792,20 +794,22 @@ def main():
                     gX.replay()
                 else:
                     for d, h in zip(ins, h_in):
-                        d.copy_(h, non_blocking=True)
+                        rnd.sv.copy(d, h, stream=stream)
                     g1.replay()
                     for h, d in zip(h_out, outs):
-                        h.copy_(d, non_blocking=True)
+                        rnd.sv.copy(h, d, stream=stream)
                 done.record()
             done.synchronize()
         e2e_s = time.perf_counter() - t0
     e2e_s = max_over_ranks(e2e_s, ws, dev)
     e2e = {"value": ws * E / e2e_s, "unit": "steps/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-           "steps": E, "how": ("one CUDA graph per step: pinned H2D of the round's inputs (one buffer), the "
-                               "C-ABI calls, D2H of n_acc/out_tok/path (one buffer); host sync every step"
+           "steps": E, "how": ("one CUDA graph per step: H2D of the round's inputs from pinned host memory "
+                               "(one buffer), the C-ABI calls, D2H of n_acc/out_tok/path into pinned host memory "
+                               "(one buffer), both copies by sv_copy (the SMs read and write host memory over "
+                               "the host link); host sync every step"
                                if gX is not None else
-                               "pinned H2D of the round's inputs + CUDA-graph replay of the C-ABI calls + "
-                               "D2H of n_acc/out_tok/path + host sync, every step")}
+                               "sv_copy H2D of the round's inputs from pinned host memory + CUDA-graph replay of "
+                               "the C-ABI calls + sv_copy D2H of n_acc/out_tok/path + host sync, every step")}
 
     # greedy decisions too close to call within the logits tolerance: rows whose
     # top-1 / top-2 margin is below 1e-2 max|logit| (counted, not failed)

@@ -14,7 +14,7 @@
  *                     update (cache length == committed-token count).
  *
  * Sources, cited by page title and section:
- *   [SCS]  "SpecDec-Context-Scaling project guide", sec. 3, 3.1, 3.2
+ *   [SCS]  "SpecDec-Context-Scaling project guide", sec. 3, 3.1, 3.2, 7.1
  *   [TUT]  wmrh.cn speculative-decoding tutorial, sec. 2.2, 3.2, 3.3
  *   [MINI] "mini-infer Phase 11: Speculative Decoding", sections "Modified
  *          Rejection Sampling", cross-device tensor alignment, hidden KV
@@ -407,6 +407,27 @@ SV_API sv_status sv_kv_commit_paged(uint16_t* k_pool, uint16_t* v_pool, int32_t 
                                     int32_t max_pages, const uint16_t* k_blk, const uint16_t* v_blk, int32_t L,
                                     int32_t B, int32_t Hkv, int32_t D, int32_t R, const int32_t* path,
                                     const int32_t* n_acc, int32_t* len, void* stream);
+
+/* Moving a round's inputs in and its results out ([SCS] sec. 7.1: the control
+ * plane of a round first -- fewer synchronisations and no host-to-device
+ * copies between its kernels).  dst[0..bytes) = src[0..bytes), copied by a
+ * kernel on `stream` (programmatic dependent launch, like every kernel here)
+ * whose SMs load and store the bytes themselves: either side may be device
+ * memory or page-locked host memory (cudaHostAlloc / cudaHostRegister;
+ * reached through unified addressing -- on GB300 over the coherent
+ * NVLink-C2C link), so a round's inputs and outputs cross the host link inside
+ * the round's own kernel chain instead of as copy-engine operations.  The host
+ * may read host-side dst once the copy has completed in stream order (an
+ * event or a stream synchronisation).
+ *   dst, src: non-NULL when bytes > 0, each device or page-locked host memory
+ *             (checked with cudaPointerGetAttributes: anything else, e.g.
+ *             pageable host memory, returns SV_ERR_ARG before any launch); both
+ *             ranges [p, p + bytes) must lie inside their allocations and must
+ *             not overlap.  Any alignment; 16-byte aligned pointers move 16
+ *             bytes per access.
+ *   bytes == 0: SV_OK, nothing launched.
+ * Ownership: the caller's; the library keeps nothing. */
+SV_API sv_status sv_copy(void* dst, const void* src, size_t bytes, void* stream);
 
 /* ------------------------------------------------------------------------ */
 /* Diagnostics: the device building blocks of sv_accept_sample, exposed so    */

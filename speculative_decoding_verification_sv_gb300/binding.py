@@ -72,6 +72,7 @@ def _load():
                                           _I32, _P, _P]
     L.sv_accept_greedy_commit_paged.argtypes = [_P, _P, _P, _I32, _I32, _I32, _P, _P, _P, _P, _P, _I32, _P, _I32,
                                                 _P, _P, _I32, _I32, _I32, _P, _P]
+    L.sv_copy.argtypes = [_P, _P, _SZ, _P]
     L.sv_diag_exp.argtypes = [_P, _P, _I64, _P]
     L.sv_diag_philox.argtypes = [_P, _P, _P, _I64, _P]
     L.sv_diag_canon.argtypes = [_P, _I32, _I32, _P, _P, _P, _P]
@@ -79,7 +80,7 @@ def _load():
                "sv_accept_greedy_relaxed", "sv_accept_sample",
                "sv_accept_sample_noalloc", "sv_kv_commit", "sv_kv_commit_paged", "sv_verify_attn_paged",
                "sv_diag_exp", "sv_diag_philox", "sv_diag_canon", "sv_get_device_error", "sv_lm_head_argmax",
-               "sv_accept_greedy_commit", "sv_accept_greedy_commit_paged"):
+               "sv_accept_greedy_commit", "sv_accept_greedy_commit_paged", "sv_copy"):
         getattr(L, fn).restype = ctypes.c_int
     return L
 
@@ -362,6 +363,22 @@ def kv_commit_paged(k_pool, v_pool, page_table, k_blk, v_blk, path, n_acc, lengt
         _ptr(k_pool, bf, "k_pool"), _ptr(v_pool, bf, "v_pool"), num_pages, _ptr(page_table, i32, "page_table"),
         page_table.shape[1], _ptr(k_blk, bf, "k_blk"), _ptr(v_blk, bf, "v_blk"), L, B, Hkv, D, R,
         _ptr(path, i32, "path"), _ptr(n_acc, i32, "n_acc"), _ptr(length, i32, "len"), _stream(stream)))
+
+
+def copy(dst: torch.Tensor, src: torch.Tensor, stream=None) -> torch.Tensor:
+    """dst <- src (same byte count, contiguous) by sv_copy: each side a CUDA
+    tensor or a pinned CPU tensor; the copy is a kernel on the stream."""
+    for name, t in (("dst", dst), ("src", src)):
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+        if not t.is_cuda and not t.is_pinned():
+            raise ValueError(f"{name} must be a CUDA tensor or pinned host memory")
+    nbytes = dst.numel() * dst.element_size()
+    if src.numel() * src.element_size() != nbytes:
+        raise ValueError("dst and src must hold the same number of bytes")
+    _check("sv_copy", lib.sv_copy(ctypes.c_void_p(dst.data_ptr()), ctypes.c_void_p(src.data_ptr()), nbytes,
+                                  _stream(stream)))
+    return dst
 
 
 def get_device_error(stream=None) -> int:

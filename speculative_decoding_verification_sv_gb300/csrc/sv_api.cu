@@ -376,6 +376,27 @@ sv_status sv_kv_commit_paged(uint16_t* k_pool, uint16_t* v_pool, int32_t num_pag
                                               as_stream(stream)));
 }
 
+// Device or page-locked host memory (the kernel reaches both through unified
+// addressing); pageable or unknown pointers are refused.
+static bool gpu_reachable(const void* p) {
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    if (a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged) return true;
+    return a.type == cudaMemoryTypeHost && a.devicePointer == p;
+}
+
+sv_status sv_copy(void* dst, const void* src, size_t bytes, void* stream) {
+    if (bytes == 0) return SV_OK;
+    if (!dst || !src) return SV_ERR_ARG;
+    if (!gpu_reachable(dst) || !gpu_reachable(src)) return SV_ERR_ARG;
+    const uintptr_t d = reinterpret_cast<uintptr_t>(dst), s = reinterpret_cast<uintptr_t>(src);
+    if (d < s + bytes && s < d + bytes) return SV_ERR_ARG;   // overlapping ranges
+    return launch_status(sv::launch_stage_copy(dst, src, bytes, as_stream(stream)));
+}
+
 sv_status sv_diag_exp(const float* x, float* y, int64_t n, void* stream) {
     if (n < 0 || (n > 0 && (!x || !y))) return SV_ERR_ARG;
     if (n == 0) return SV_OK;

@@ -86,6 +86,8 @@ cudaError_t launch_accept_sample(const float* logits, const float* q, int Vq, co
                                  const int32_t* parent, int B, int R, int V, float temperature, uint64_t seed,
                                  uint64_t step, const float* uniforms, int32_t* n_acc, int32_t* out_tok,
                                  int32_t* path, void* ws, size_t ws_bytes, cudaStream_t st);
+// stage.cu
+cudaError_t launch_stage_copy(void* dst, const void* src, size_t bytes, cudaStream_t st);
 cudaError_t launch_diag_exp(const float* x, float* y, int64_t n, cudaStream_t st);
 cudaError_t launch_diag_philox(const uint32_t* ctr, const uint32_t* key, uint32_t* out, int64_t n,
                                cudaStream_t st);

@@ -125,6 +125,21 @@ def test_host_validation_rejects_before_launch(lib):
                                            fake, fake, 28, 2, 128, fake, None) == 1
 
 
+def test_copy_host_validation(lib):
+    """sv_copy: nothing to do is OK; NULLs, overlapping ranges and pageable
+    host memory are refused before any launch."""
+    from speculative_decoding_verification_sv_gb300 import binding as b
+    L = b.lib
+    fake = ctypes.c_void_p(0x10000)
+    assert L.sv_copy(None, None, 0, None) == 0
+    assert L.sv_copy(None, fake, 16, None) == 1
+    assert L.sv_copy(fake, None, 16, None) == 1
+    buf = ctypes.create_string_buffer(64)   # pageable host memory
+    base = ctypes.addressof(buf)
+    assert L.sv_copy(ctypes.c_void_p(base + 32), ctypes.c_void_p(base), 16, None) == 1
+    assert L.sv_copy(ctypes.c_void_p(base + 8), ctypes.c_void_p(base), 16, None) == 1   # overlapping
+
+
 def test_workspace_queries(lib):
     from speculative_decoding_verification_sv_gb300 import binding as b
     assert b.lib.sv_accept_greedy_workspace(16, 9, 152064) == 16 * 9 * 19 * 8
