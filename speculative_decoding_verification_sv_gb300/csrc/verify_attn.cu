@@ -399,70 +399,168 @@ __global__ void __launch_bounds__(Roles<kHalf, kHW>::kThreads, 1)
             // both S operands K-major; the two 64-dim halves are separate boxes
             const uint64_t qd0 = smem_desc_sw128(sq, 16, 1024);
             mbar_wait(q_ready, 0, a.err);
-            auto pv = [&](int st) {
-                const int pb = st & 1, s = st % kStages;
-                const int nt = min(kT, ntiles - st * kT);
-                mbar_wait(&p_full[pb], (st >> 1) & 1, a.err);
-                // (one barrier per stage: S already waited for the whole stage)
-                if constexpr (kSplit) mbar_wait(&v_full[s], (st / kStages) & 1, a.err);
-                tc_fence_after();
-                // A = P [M lanes][keys] in TMEM (8 columns per 16 keys); B = V
-                // [keys][128 dims], MN-major: 8-key groups 1024 B apart (keys run
-                // on across the step's tiles), the two 64-dim halves one region
-                // apart, 16 keys = 2048 B (descriptor units of 16 B)
-                const uint32_t sv = smem_u32(smem + Ly::kOffRing + s * kStageBytes + 2 * kRegion);
-                const uint64_t bd0 = smem_desc_sw128(sv, kRegion, 1024);
-                for (int kc = 0; kc < nt * (kNk / 16); ++kc)
-                    tc_mma_ts(tO, tP(pb) + kc * 8, bd0 + kc * (2048 >> 4), idesc_o, (st > 0 || kc > 0) ? 1u : 0u);
-                if (fold && st == nsoft - 1) {
-                    // the folded tile: P in the other P buffer, V in ring step st + 1
-                    const int sx = (st + 1) % kStages;
-                    if constexpr (kSplit) mbar_wait(&v_full[sx], ((st + 1) / kStages) & 1, a.err);
+            if constexpr (!(kHalf && kHW == 2)) {
+                // Long loops (four row-owner warps per quadrant, or full tiles): every
+                // step but the last takes kT tiles, so its MMA chains are issued with
+                // compile-time trip counts (a run-time count cost the single issuing
+                // thread ~12-40 cycles per MMA in a probe, against ~65 for the MMA
+                // itself; the tree layer 24.7 -> 23.8 us).  The last step picks its
+                // variant once.  Short loops (batch 1: two or three steps, two warps
+                // per quadrant, the only ones that fold an odd tile) keep the single
+                // loop below: there the separate variants' code, run once per CTA,
+                // cost more than the chains saved (1.5B layer 8.12 -> 8.34 us).
+                using NtFull = std::integral_constant<int, kT>;
+                using NtOne = std::integral_constant<int, 1>;
+                using NoFold = std::false_type;
+                using Fold = std::true_type;
+                auto pv = [&](int st, auto nt_c, auto fold_c) {
+                    constexpr int NT = decltype(nt_c)::value;
+                    constexpr bool FOLD = decltype(fold_c)::value;
+                    const int pb = st & 1, s = st % kStages;
+                    mbar_wait(&p_full[pb], (st >> 1) & 1, a.err);
+                    // (one barrier per stage: S already waited for the whole stage)
+                    if constexpr (kSplit) mbar_wait(&v_full[s], (st / kStages) & 1, a.err);
                     tc_fence_after();
-                    const uint64_t bdx =
-                        smem_desc_sw128(smem_u32(smem + Ly::kOffRing + sx * kStageBytes + 2 * kRegion), kRegion, 1024);
-                    for (int kc = 0; kc < kNk / 16; ++kc)
-                        tc_mma_ts(tO, tP(pb ^ 1) + kc * 8, bdx + kc * (2048 >> 4), idesc_o, 1u);
-                    tc_commit(&v_empty[sx]);
-                }
-                tc_commit(&o_done[pb]);
-                tc_commit(&v_empty[s]);
-            };
-            for (int st = 0; st < nsoft; ++st) {
-                const int sb = st & 1, s = st % kStages;
-                const int nt = min(kT, ntiles - st * kT);
-                mbar_wait(&s_empty[sb], ((st >> 1) & 1) ^ 1, a.err);
-                mbar_wait(&k_full[s], (st / kStages) & 1, a.err);
-                tc_fence_after();
-                const uint64_t kd0 = smem_desc_sw128(smem_u32(smem + Ly::kOffRing + s * kStageBytes), 16, 1024);
-                const uint32_t id = nt == kT ? idesc_s : idesc_s1;
-#pragma unroll
-                for (int k16 = 0; k16 < kD / 16; ++k16) {
-                    const uint32_t half = k16 >> 2, kin = (k16 & 3) * 32;
-                    tc_mma(tS(sb), qd0 + ((half * (kM * 128) + kin) >> 4), kd0 + ((half * kRegion + kin) >> 4), id,
-                           k16 > 0 ? 1u : 0u);
-                }
-                if (fold && st == nsoft - 1) {
-                    // the folded tile (ring step st + 1): scores into the first 64
-                    // columns of the other buffer, once step st - 1 has read it
-                    const int sx = (st + 1) % kStages;
-                    if (st >= 1) mbar_wait(&s_empty[sb ^ 1], ((st - 1) >> 1) & 1, a.err);
-                    mbar_wait(&k_full[sx], ((st + 1) / kStages) & 1, a.err);
+                    // A = P [M lanes][keys] in TMEM (8 columns per 16 keys); B = V
+                    // [keys][128 dims], MN-major: 8-key groups 1024 B apart (keys run
+                    // on across the step's tiles), the two 64-dim halves one region
+                    // apart, 16 keys = 2048 B (descriptor units of 16 B)
+                    const uint32_t sv = smem_u32(smem + Ly::kOffRing + s * kStageBytes + 2 * kRegion);
+                    const uint64_t bd0 = smem_desc_sw128(sv, kRegion, 1024);
+                    const uint32_t acc0 = st > 0 ? 1u : 0u;
+    #pragma unroll
+                    for (int kc = 0; kc < NT * (kNk / 16); ++kc)
+                        tc_mma_ts(tO, tP(pb) + kc * 8, bd0 + kc * (2048 >> 4), idesc_o, kc > 0 ? 1u : acc0);
+                    if constexpr (FOLD) {
+                        // the folded tile: P in the other P buffer, V in ring step st + 1
+                        const int sx = (st + 1) % kStages;
+                        if constexpr (kSplit) mbar_wait(&v_full[sx], ((st + 1) / kStages) & 1, a.err);
+                        tc_fence_after();
+                        const uint64_t bdx =
+                            smem_desc_sw128(smem_u32(smem + Ly::kOffRing + sx * kStageBytes + 2 * kRegion), kRegion, 1024);
+    #pragma unroll
+                        for (int kc = 0; kc < kNk / 16; ++kc)
+                            tc_mma_ts(tO, tP(pb ^ 1) + kc * 8, bdx + kc * (2048 >> 4), idesc_o, 1u);
+                        tc_commit(&v_empty[sx]);
+                    }
+                    tc_commit(&o_done[pb]);
+                    tc_commit(&v_empty[s]);
+                };
+                auto scores = [&](int st, auto nt_c, auto fold_c) {
+                    constexpr int NT = decltype(nt_c)::value;
+                    constexpr bool FOLD = decltype(fold_c)::value;
+                    const int sb = st & 1, s = st % kStages;
+                    mbar_wait(&s_empty[sb], ((st >> 1) & 1) ^ 1, a.err);
+                    mbar_wait(&k_full[s], (st / kStages) & 1, a.err);
                     tc_fence_after();
-                    const uint64_t kdx = smem_desc_sw128(smem_u32(smem + Ly::kOffRing + sx * kStageBytes), 16, 1024);
-#pragma unroll
+                    const uint64_t kd0 = smem_desc_sw128(smem_u32(smem + Ly::kOffRing + s * kStageBytes), 16, 1024);
+                    constexpr uint32_t id = NT == kT ? idesc_s : idesc_s1;
+    #pragma unroll
                     for (int k16 = 0; k16 < kD / 16; ++k16) {
                         const uint32_t half = k16 >> 2, kin = (k16 & 3) * 32;
-                        tc_mma(tS(sb ^ 1), qd0 + ((half * (kM * 128) + kin) >> 4),
-                               kdx + ((half * kRegion + kin) >> 4), idesc_s1, k16 > 0 ? 1u : 0u);
+                        tc_mma(tS(sb), qd0 + ((half * (kM * 128) + kin) >> 4), kd0 + ((half * kRegion + kin) >> 4), id,
+                               k16 > 0 ? 1u : 0u);
                     }
-                    if constexpr (kSplit) tc_commit(&k_empty[sx]);
+                    if constexpr (FOLD) {
+                        // the folded tile (ring step st + 1): scores into the first 64
+                        // columns of the other buffer, once step st - 1 has read it
+                        const int sx = (st + 1) % kStages;
+                        if (st >= 1) mbar_wait(&s_empty[sb ^ 1], ((st - 1) >> 1) & 1, a.err);
+                        mbar_wait(&k_full[sx], ((st + 1) / kStages) & 1, a.err);
+                        tc_fence_after();
+                        const uint64_t kdx = smem_desc_sw128(smem_u32(smem + Ly::kOffRing + sx * kStageBytes), 16, 1024);
+    #pragma unroll
+                        for (int k16 = 0; k16 < kD / 16; ++k16) {
+                            const uint32_t half = k16 >> 2, kin = (k16 & 3) * 32;
+                            tc_mma(tS(sb ^ 1), qd0 + ((half * (kM * 128) + kin) >> 4),
+                                   kdx + ((half * kRegion + kin) >> 4), idesc_s1, k16 > 0 ? 1u : 0u);
+                        }
+                        if constexpr (kSplit) tc_commit(&k_empty[sx]);
+                    }
+                    if constexpr (kSplit) tc_commit(&k_empty[s]);   // K of this step read once these MMAs are done
+                    tc_commit(&s_full[sb]);
+                };
+                const int last = nsoft - 1;
+                for (int st = 0; st < last; ++st) {
+                    scores(st, NtFull{}, NoFold{});
+                    if (st > 0) pv(st - 1, NtFull{}, NoFold{});
                 }
-                if constexpr (kSplit) tc_commit(&k_empty[s]);   // K of this step read once these MMAs are done
-                tc_commit(&s_full[sb]);
-                if (st > 0) pv(st - 1);
+                // the last step: kT tiles or one tile
+                if (ntiles - last * kT >= kT) {
+                    scores(last, NtFull{}, NoFold{});
+                    if (last > 0) pv(last - 1, NtFull{}, NoFold{});
+                    pv(last, NtFull{}, NoFold{});
+                } else {
+                    scores(last, NtOne{}, NoFold{});
+                    if (last > 0) pv(last - 1, NtFull{}, NoFold{});
+                    pv(last, NtOne{}, NoFold{});
+                }
+            } else {
+                auto pv = [&](int st) {
+                    const int pb = st & 1, s = st % kStages;
+                    const int nt = min(kT, ntiles - st * kT);
+                    mbar_wait(&p_full[pb], (st >> 1) & 1, a.err);
+                    // (one barrier per stage: S already waited for the whole stage)
+                    if constexpr (kSplit) mbar_wait(&v_full[s], (st / kStages) & 1, a.err);
+                    tc_fence_after();
+                    // A = P [M lanes][keys] in TMEM (8 columns per 16 keys); B = V
+                    // [keys][128 dims], MN-major: 8-key groups 1024 B apart (keys run
+                    // on across the step's tiles), the two 64-dim halves one region
+                    // apart, 16 keys = 2048 B (descriptor units of 16 B)
+                    const uint32_t sv = smem_u32(smem + Ly::kOffRing + s * kStageBytes + 2 * kRegion);
+                    const uint64_t bd0 = smem_desc_sw128(sv, kRegion, 1024);
+                    for (int kc = 0; kc < nt * (kNk / 16); ++kc)
+                        tc_mma_ts(tO, tP(pb) + kc * 8, bd0 + kc * (2048 >> 4), idesc_o, (st > 0 || kc > 0) ? 1u : 0u);
+                    if (fold && st == nsoft - 1) {
+                        // the folded tile: P in the other P buffer, V in ring step st + 1
+                        const int sx = (st + 1) % kStages;
+                        if constexpr (kSplit) mbar_wait(&v_full[sx], ((st + 1) / kStages) & 1, a.err);
+                        tc_fence_after();
+                        const uint64_t bdx =
+                            smem_desc_sw128(smem_u32(smem + Ly::kOffRing + sx * kStageBytes + 2 * kRegion), kRegion, 1024);
+                        for (int kc = 0; kc < kNk / 16; ++kc)
+                            tc_mma_ts(tO, tP(pb ^ 1) + kc * 8, bdx + kc * (2048 >> 4), idesc_o, 1u);
+                        tc_commit(&v_empty[sx]);
+                    }
+                    tc_commit(&o_done[pb]);
+                    tc_commit(&v_empty[s]);
+                };
+                for (int st = 0; st < nsoft; ++st) {
+                    const int sb = st & 1, s = st % kStages;
+                    const int nt = min(kT, ntiles - st * kT);
+                    mbar_wait(&s_empty[sb], ((st >> 1) & 1) ^ 1, a.err);
+                    mbar_wait(&k_full[s], (st / kStages) & 1, a.err);
+                    tc_fence_after();
+                    const uint64_t kd0 = smem_desc_sw128(smem_u32(smem + Ly::kOffRing + s * kStageBytes), 16, 1024);
+                    const uint32_t id = nt == kT ? idesc_s : idesc_s1;
+    #pragma unroll
+                    for (int k16 = 0; k16 < kD / 16; ++k16) {
+                        const uint32_t half = k16 >> 2, kin = (k16 & 3) * 32;
+                        tc_mma(tS(sb), qd0 + ((half * (kM * 128) + kin) >> 4), kd0 + ((half * kRegion + kin) >> 4), id,
+                               k16 > 0 ? 1u : 0u);
+                    }
+                    if (fold && st == nsoft - 1) {
+                        // the folded tile (ring step st + 1): scores into the first 64
+                        // columns of the other buffer, once step st - 1 has read it
+                        const int sx = (st + 1) % kStages;
+                        if (st >= 1) mbar_wait(&s_empty[sb ^ 1], ((st - 1) >> 1) & 1, a.err);
+                        mbar_wait(&k_full[sx], ((st + 1) / kStages) & 1, a.err);
+                        tc_fence_after();
+                        const uint64_t kdx = smem_desc_sw128(smem_u32(smem + Ly::kOffRing + sx * kStageBytes), 16, 1024);
+    #pragma unroll
+                        for (int k16 = 0; k16 < kD / 16; ++k16) {
+                            const uint32_t half = k16 >> 2, kin = (k16 & 3) * 32;
+                            tc_mma(tS(sb ^ 1), qd0 + ((half * (kM * 128) + kin) >> 4),
+                                   kdx + ((half * kRegion + kin) >> 4), idesc_s1, k16 > 0 ? 1u : 0u);
+                        }
+                        if constexpr (kSplit) tc_commit(&k_empty[sx]);
+                    }
+                    if constexpr (kSplit) tc_commit(&k_empty[s]);   // K of this step read once these MMAs are done
+                    tc_commit(&s_full[sb]);
+                    if (st > 0) pv(st - 1);
+                }
+                pv(nsoft - 1);
             }
-            pv(nsoft - 1);
         }
     } else {
         // ---------------- row-owner warps ----------------
