@@ -663,10 +663,12 @@ __global__ void __launch_bounds__(Roles<kHalf, kHW>::kThreads, 1)
             tc_fence_after();
             const bool work = quarter_live;
             if constexpr (!kHalf) {
-                // Full tiles: 32 columns per thread, taken as two 16-column
-                // halves that the exponent pass reads from TMEM a second time,
-                // so that only 16 scores are live (32 at once spill at the 96
-                // registers an 18-warp CTA leaves each thread)
+                // Full tiles: 32 columns per thread.  The max pass and the
+                // exponent pass each read them from TMEM in one 32-column load
+                // (one round trip each); P goes back in two 16-column stores, so
+                // the exponent pass holds 32 scores and 8 packed P words at most
+                // (holding all 16 P words besides spilled at the 96 registers an
+                // 18-warp CTA leaves each thread)
                 const int ti = st * kT + tsub;
                 const bool tile_live = ti < ntiles;
                 const int gt = first + ti;
@@ -686,31 +688,31 @@ __global__ void __launch_bounds__(Roles<kHalf, kHW>::kThreads, 1)
                     vmask = lim >= 32 ? ~0u : lim <= 0 ? 0u : (1u << lim) - 1u;
                     if (kTree && is_block && tile_live) vmask = static_cast<uint32_t>(anc[2 * j + (gt - n_ctx)] >> ctile);
                 }
-                auto load_half = [&](int h, uint32_t (&v)[16]) {
-                    tmem_ld16_sync(tS(sb) + lane_off + col0 + 16 * h, v);
+                // all 32 columns in one TMEM round trip per pass
+                auto load_all = [&](uint32_t (&v)[32]) {
+                    tmem_ld32_sync(tS(sb) + lane_off + col0, v);
                     if (vmask != ~0u) {
 #pragma unroll
-                        for (int e = 0; e < 16; ++e)
-                            v[e] = ((vmask >> (16 * h + e)) & 1u) != 0u ? v[e] : __float_as_uint(-INFINITY);
+                        for (int e = 0; e < 32; ++e)
+                            v[e] = ((vmask >> e) & 1u) != 0u ? v[e] : __float_as_uint(-INFINITY);
                     }
                 };
                 float mpart = -INFINITY;
                 if (work) {
+                    uint32_t v[32];
+                    load_all(v);
                     float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        uint32_t v[16];
-                        load_half(h, v);
+                    for (int e = 0; e < 32; e += 8)
 #pragma unroll
-                        for (int e = 0; e < 16; e += 8)
-#pragma unroll
-                            for (int u = 0; u < 4; ++u)
-                                mq[u] = fmax3(mq[u], __uint_as_float(v[e + 2 * u]), __uint_as_float(v[e + 2 * u + 1]));
-                    }
+                        for (int u = 0; u < 4; ++u)
+                            mq[u] = fmax3(mq[u], __uint_as_float(v[e + 2 * u]), __uint_as_float(v[e + 2 * u + 1]));
                     mpart = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3])) * a.scale_log2;
                 }
+                // a row's four column groups are the quadrant's four warps:
+                // one 128-thread barrier per quadrant
                 red[(sb * kGroups + cgp) * kRows + r] = mpart;
-                named_barrier(2, 32 * kSoftWarps);
+                named_barrier(3 + q4, 128);
                 float mt = red[(sb * kGroups + 0) * kRows + r];
 #pragma unroll
                 for (int c2 = 1; c2 < kGroups; ++c2) mt = fmaxf(mt, red[(sb * kGroups + c2) * kRows + r]);
@@ -742,15 +744,15 @@ __global__ void __launch_bounds__(Roles<kHalf, kHW>::kThreads, 1)
                 float ps0 = 0.f, ps1 = 0.f;
                 if (work) {
                     const float nm = m_new == -INFINITY ? 0.f : -m_new;
+                    uint32_t v[32];
+                    load_all(v);
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
-                        uint32_t v[16];
-                        load_half(h, v);
                         uint32_t pk[8];
 #pragma unroll
                         for (int e = 0; e < 16; e += 2) {
-                            const float p0 = fast_exp2(fmaf(__uint_as_float(v[e]), a.scale_log2, nm));
-                            const float p1 = fast_exp2(fmaf(__uint_as_float(v[e + 1]), a.scale_log2, nm));
+                            const float p0 = fast_exp2(fmaf(__uint_as_float(v[16 * h + e]), a.scale_log2, nm));
+                            const float p1 = fast_exp2(fmaf(__uint_as_float(v[16 * h + e + 1]), a.scale_log2, nm));
                             ps0 += p0;
                             ps1 += p1;
                             const __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
@@ -967,7 +969,7 @@ __global__ void __launch_bounds__(Roles<kHalf, kHW>::kThreads, 1)
             for (int c2 = 0; c2 < kHalfWarps; ++c2) lt += lsx[c2 * kRows + r];
         } else {
             lsx[cgp * kRows + r] = lsum;
-            named_barrier(2, 32 * kSoftWarps);
+            named_barrier(3 + q4, 128);   // the row's four column groups: the quadrant's warps
             lt = 0.f;
 #pragma unroll
             for (int c2 = 0; c2 < kGroups; ++c2) lt += lsx[c2 * kRows + r];
