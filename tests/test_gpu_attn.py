@@ -233,9 +233,10 @@ def test_attn_full_tree_layer(sv):
 
 
 def test_attn_workspace_multi_row_tiles(sv):
-    """72 query rows per KV head (two half tiles) over a 32K context: several
-    clusters per (KV head, row tile) meet in the workspace; the merged rows of
-    both row tiles match the oracle and the tickets end at zero."""
+    """72 query rows per KV head over a 32K context (one 128-row tile or two
+    half tiles, as the plan costs them): several clusters per (KV head, row
+    tile) meet in the workspace; the merged rows match the oracle and the
+    tickets end at zero."""
     B, R, Hq, Hkv, T_cap = 1, 9, 8, 1, 32832
     nbytes = sv.verify_attn_workspace(B, R, Hq, Hkv, 128, T_cap)
     assert nbytes > 0
@@ -250,6 +251,20 @@ def test_attn_workspace_multi_row_tiles(sv):
     assert int(ws[:256].view(torch.int32).abs().sum()) == 0
     ref = oracle.verify_attn(bits(q), bits(kc), bits(vc), ln.numpy(), bits(kb), bits(vb))
     ok, err, bound = within_tol(out.float().cpu().numpy(), ref)
+    assert ok, (err, bound)
+    assert sv.get_device_error() == 0
+
+
+def test_attn_workspace_full_tile_tree(sv):
+    """A 64-node draft tree with 7 query heads on one KV head (455 rows: four
+    128-row tiles) over a 16K context: the plan splits each tile over several
+    clusters of a size that is not a power of two, which meet in the workspace
+    under the tree mask."""
+    B, R, Hq, Hkv, T_cap = 1, 65, 7, 1, 16448
+    assert sv.verify_attn_workspace(B, R, Hq, Hkv, 128, T_cap) > 0   # several clusters per tile
+    par = synth.random_tree(R - 1, 8, 3, 21)[None, :]
+    got, ref = _run(sv, B, R, Hq, Hkv, T_cap, [16300], parent=par, seed=29)
+    ok, err, bound = within_tol(got, ref)
     assert ok, (err, bound)
     assert sv.get_device_error() == 0
 
