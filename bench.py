@@ -270,8 +270,8 @@ class Round:
             sv.accept_greedy(lg, self.tok, parent=self.parent, n_acc=self.n_acc, out_tok=self.out_tok,
                              path=self.path, ws=self.acc_ws)
         else:
-            sv.accept_sample(lg, self.q_draft, self.tok, temperature=w.temperature, seed=0x5EED, step=0,
-                             n_acc=self.n_acc, out_tok=self.out_tok, path=self.path, ws=self.acc_ws)
+            sv.accept_sample(lg, self.q_draft, self.tok, parent=self.parent, temperature=w.temperature, seed=0x5EED,
+                             step=0, n_acc=self.n_acc, out_tok=self.out_tok, path=self.path, ws=self.acc_ws)
         rec("acc1")
         if self.has_model:
             sv.kv_commit(self.kc, self.vc, self.kb, self.vb, self.path, self.n_acc, self.length)

@@ -307,10 +307,26 @@ def accept_greedy_relaxed(logits, tok, parent=None, delta=0.0, n_acc=None, out_t
     return n_acc, out_tok, path
 
 
+def _check_sample_shapes(logits, q, tok, parent):
+    """q holds one draft distribution per chain position (R - 1 rows) or per
+    tree node (R rows); the C ABI cannot see its row count, so it is checked
+    here."""
+    B, R, _ = logits.shape
+    rq = R if parent is not None else R - 1
+    if q.dim() != 3 or q.shape[0] != B or q.shape[1] != rq:
+        raise ValueError(f"q must be [B, {rq}, Vq] for a {'tree' if parent is not None else 'chain'} of R = {R} "
+                         f"rows, got {tuple(q.shape)}")
+    if tuple(tok.shape) != (B, R):
+        raise ValueError(f"tok must be [B, R] = [{B}, {R}], got {tuple(tok.shape)}")
+    if parent is not None and tuple(parent.shape) != (B, R):
+        raise ValueError(f"parent must be [B, R] = [{B}, {R}], got {tuple(parent.shape)}")
+
+
 def accept_sample(logits, q, tok, parent=None, temperature=1.0, seed=0, step=0, uniforms=None, n_acc=None,
                   out_tok=None, path=None, ws=None, stream=None):
     """logits [B,R,V] fp32; q [B,R-1 (chain) or R (tree),Vq] fp32; tok [B,R] int32;
     uniforms None (Philox) or [B,R,2] fp32."""
+    _check_sample_shapes(logits, q, tok, parent)
     B, R, V = logits.shape
     Vq = q.shape[-1]
     n_acc, out_tok, path = _accept_outputs(B, R, logits.device, n_acc, out_tok, path)
@@ -330,6 +346,7 @@ def accept_sample_noalloc(logits, q, tok, parent=None, temperature=1.0, seed=0, 
     """accept_sample for callers that cannot allocate device memory: the
     library's fixed scratch array replaces the workspace (B*R <= 8192; calls
     overlapping on the GPU race on it)."""
+    _check_sample_shapes(logits, q, tok, parent)
     B, R, V = logits.shape
     Vq = q.shape[-1]
     n_acc, out_tok, path = _accept_outputs(B, R, logits.device, n_acc, out_tok, path)

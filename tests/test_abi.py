@@ -146,3 +146,19 @@ def test_workspace_queries(lib):
     # row statistics, then the chain path's per-sequence records and sums
     assert b.lib.sv_accept_sample_workspace(64, 9, 151936) == 64 * 9 * 8 + 64 * 16 + 64 * 2 * (64 * 32 + 64) * 4
     assert b.verify_attn_workspace(16, 9, 28, 4, 128, 8320) == 0
+
+
+def test_sample_shapes_checked(lib):
+    """The binding refuses a q whose row count does not match the mode (R - 1
+    rows for a chain, R for a tree): the C ABI cannot see it."""
+    import torch
+    from speculative_decoding_verification_sv_gb300 import binding as b
+    lg = torch.zeros(1, 5, 16)
+    tok = torch.zeros(1, 5, dtype=torch.int32)
+    par = torch.tensor([[-1, 0, 0, 1, 1]], dtype=torch.int32)
+    with pytest.raises(ValueError):
+        b.accept_sample(lg, torch.zeros(1, 5, 16), tok)          # a chain wants 4 rows of q
+    with pytest.raises(ValueError):
+        b.accept_sample(lg, torch.zeros(1, 4, 16), tok, par)     # a tree wants 5
+    with pytest.raises(ValueError):
+        b.accept_sample_noalloc(lg, torch.zeros(1, 4, 16), tok, par)
