@@ -10,8 +10,9 @@
 //      into shared memory with bulk copies, reduces the max of l/T across the
 //      cluster through distributed shared memory, and forms the canonical
 //      sum Z of exp(l/T - max).  The row is read from HBM exactly once.
-//   2. sample_finish_kernel: one 8-CTA cluster per sequence runs the
-//      acceptance walk (element-wise ratio tests from the row statistics),
+//   2. sample_finish_kernel: one cluster per sequence (16 CTAs for a few
+//      sequences, else 8) runs the acceptance walk (element-wise ratio tests
+//      from the row statistics),
 //      and the full-vocab passes it needs: the residual max(0, w - q) and its
 //      canonical sum, then inverse-CDF sampling by descending the summation
 //      tree (block level across the cluster, chunk level in shared memory,
@@ -686,28 +687,29 @@ __device__ __forceinline__ int descend_levels(const float* tree, int n, float ta
 // Full pass over the vocab: chunk sums into csum (this CTA's blocks), block
 // sums into every CTA's bsum; returns the canonical total (identical in every
 // CTA).  All threads of all CTAs of the cluster must call it.
-template <class Vals>
+template <int kC, int kW, class Vals>
 __device__ float full_pass(const Vals& vals, int V, int nblk, PassSmem& sm, cg::cluster_group& cluster) {
+    static_assert(kC <= 32 && kMaxBlocks / kC <= kMaxLocalBlocks && kW >= kMaxBlocks / kC, "cluster shape");
     const int rank = static_cast<int>(cluster.block_rank());
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int nlocal = rank < nblk ? (nblk - rank + kCluster - 1) / kCluster : 0;
+    const int nlocal = rank < nblk ? (nblk - rank + kC - 1) / kC : 0;
     cluster.sync();   // all CTAs started (first pass) / previous pass fully consumed everywhere
     const int nch = nlocal * kChunksPerBlk;
     constexpr int kBatch = 2;   // chunks whose loads a warp keeps in flight
-    for (int cid0 = warp; cid0 < nch; cid0 += kBatch * kWarps) {
+    for (int cid0 = warp; cid0 < nch; cid0 += kBatch * kW) {
         typename Vals::Raw raw[kBatch];
         bool live[kBatch];
 #pragma unroll
         for (int u = 0; u < kBatch; ++u) {
-            const int cid = cid0 + u * kWarps;
+            const int cid = cid0 + u * kW;
             const int lb = cid / kChunksPerBlk, c = cid % kChunksPerBlk;
-            const int v = (rank + lb * kCluster) * kBlk + c * kChunk + 4 * lane;
+            const int v = (rank + lb * kC) * kBlk + c * kChunk + 4 * lane;
             live[u] = cid < nch && v < V;
             if (live[u]) raw[u] = vals.load4(v);
         }
 #pragma unroll
         for (int u = 0; u < kBatch; ++u) {
-            const int cid = cid0 + u * kWarps;
+            const int cid = cid0 + u * kW;
             const float4 x = live[u] ? vals.eval4(raw[u]) : make_float4(0.f, 0.f, 0.f, 0.f);
             const float cs = warp_tree_sum(quad_sum(x));
             if (lane == 0 && cid < nch) sm.csum[cid] = cs;
@@ -716,7 +718,7 @@ __device__ float full_pass(const Vals& vals, int V, int nblk, PassSmem& sm, cg::
     __syncthreads();
     if (warp < nlocal) {
         const float bs = warp_tree_sum(sm.csum[warp * kChunksPerBlk + lane]);
-        if (lane < kCluster) *cluster.map_shared_rank(&sm.bsum[rank + warp * kCluster], lane) = bs;
+        if (lane < kC) *cluster.map_shared_rank(&sm.bsum[rank + warp * kC], lane) = bs;
     }
     cluster.sync();
     // levels 13 -> 18 over the 64 block sums (lane i: blocks 2i, 2i+1)
@@ -773,7 +775,7 @@ __device__ __forceinline__ int descend_chunk(const Vals& vals, int v0, int V, fl
 
 // Inverse-CDF draw after full_pass(vals): returns the token in the CTA that
 // owns the chosen block (and -1 elsewhere).  All threads of all CTAs call it.
-template <class Vals>
+template <int kC, class Vals>
 __device__ int tree_descent(const Vals& vals, int V, float total, float u, PassSmem& sm,
                             cg::cluster_group& cluster, unsigned int* err) {
     const int rank = static_cast<int>(cluster.block_rank());
@@ -789,8 +791,8 @@ __device__ int tree_descent(const Vals& vals, int V, float total, float u, PassS
     __syncthreads();
     const int blk = sm.node;
     if (!SV_CHECK(blk >= 0 && blk < kMaxBlocks, err, 1)) return -1;
-    if (blk % kCluster != rank) return -1;
-    const int lb = blk / kCluster;
+    if (blk % kC != rank) return -1;
+    const int lb = blk / kC;
     __syncthreads();
     // levels 12 -> 7 over the block's 32 chunk sums
     if ((threadIdx.x >> 5) == 0) build_levels(sm.csum + lb * kChunksPerBlk, kChunksPerBlk, sm.tree);
@@ -813,8 +815,8 @@ __device__ int tree_descent(const Vals& vals, int V, float total, float u, PassS
     return sm.token;
 }
 
-__global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads)
-    sample_finish_kernel(SampleArgs a) {
+template <int kC, int kW>
+__global__ void __launch_bounds__(kW * 32, 1) sample_finish_kernel(SampleArgs a) {
     pdl_wait();   // inputs come from the kernels before this one
     pdl_launch_dependents();
     __shared__ PassSmem sm;
@@ -822,7 +824,7 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads)
     __shared__ float Schain[kMaxR];
     cg::cluster_group cluster = cg::this_cluster();
     const int rank = static_cast<int>(cluster.block_rank());
-    const int b = blockIdx.x / kCluster;
+    const int b = blockIdx.x / kC;
     const int R = a.R, V = a.V, Vq = a.Vq;
     if (threadIdx.x < kMaxBlocks) sm.bsum[threadIdx.x] = 0.0f;
     bool tree_ok = true;
@@ -844,8 +846,9 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads)
         int first = tree_ok ? next_child(par, R, u, -1) : -1;
         if (first < 0) {   // leaf: bonus token from p_u
             rv.Q = nullptr;
-            const float tot = full_pass(rv, V, a.nblk, sm, cluster);
-            token = tree_descent(rv, V, tot, node_uniforms(a.seed, a.step, b, u, a.uniforms, R).y, sm, cluster, a.err);
+            const float tot = full_pass<kC, kW>(rv, V, a.nblk, sm, cluster);
+            token = tree_descent<kC>(rv, V, tot, node_uniforms(a.seed, a.step, b, u, a.uniforms, R).y, sm, cluster,
+                                     a.err);
             break;
         }
         int accepted = -1, nsteps = 0;
@@ -867,15 +870,15 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads)
             const bool last = next_child(par, R, u, c) < 0;
             rv.nsteps = nsteps;
             rv.residual = true;
-            const float S = full_pass(rv, V, a.nblk, sm, cluster);
+            const float S = full_pass<kC, kW>(rv, V, a.nblk, sm, cluster);
             if (last) {
                 const float ur = node_uniforms(a.seed, a.step, b, u, a.uniforms, R).y;
                 if (S > 0.0f) {
-                    token = tree_descent(rv, V, S, ur, sm, cluster, a.err);
+                    token = tree_descent<kC>(rv, V, S, ur, sm, cluster, a.err);
                 } else {
                     rv.residual = false;
-                    const float tot = full_pass(rv, V, a.nblk, sm, cluster);
-                    token = tree_descent(rv, V, tot, ur, sm, cluster, a.err);
+                    const float tot = full_pass<kC, kW>(rv, V, a.nblk, sm, cluster);
+                    token = tree_descent<kC>(rv, V, tot, ur, sm, cluster, a.err);
                 }
                 break;
             }
@@ -1135,8 +1138,8 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads)
     if (threadIdx.x < kMaxBlocks) sm.bsum[threadIdx.x] = 0.0f;
     __syncthreads();
     ArrayValues vals{x + static_cast<size_t>(row) * n};
-    const float tot = full_pass(vals, n, nblk, sm, cluster);
-    const int tok = tree_descent(vals, n, tot, u[row], sm, cluster, nullptr);
+    const float tot = full_pass<kCluster, kWarps>(vals, n, nblk, sm, cluster);
+    const int tok = tree_descent<kCluster>(vals, n, tot, u[row], sm, cluster, nullptr);
     if (threadIdx.x == 0 && cluster.block_rank() == 0) sums[row] = tot;
     if (threadIdx.x == 0 && tok >= 0) draws[row] = tok;
 }
@@ -1192,6 +1195,34 @@ cudaError_t launch_accept_greedy(const float* logits, const int32_t* tok, const 
 
 // Row statistics (B*R float2); then, for the chain path, the per-sequence
 // records and summation-tree sums.
+constexpr int kWideWalkMaxB = 4;   // sequences up to which the walk takes 16-CTA clusters
+
+template <int kC, int kW>
+cudaError_t launch_finish(const SampleArgs& a, int B, cudaStream_t st) {
+    static PerDeviceOnce attr_once;
+    const cudaError_t ea = attr_once.run([]() {
+        return kC > 8 ? cudaFuncSetAttribute(sample_finish_kernel<kC, kW>,
+                                             cudaFuncAttributeNonPortableClusterSizeAllowed, 1)
+                      : cudaSuccess;
+    });
+    if (ea != cudaSuccess) return ea;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(B * kC, 1, 1);
+    cfg.blockDim = dim3(kW * 32, 1, 1);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = st;
+    cudaLaunchAttribute attrs[2];
+    attrs[0].id = cudaLaunchAttributeClusterDimension;
+    attrs[0].val.clusterDim.x = kC;
+    attrs[0].val.clusterDim.y = 1;
+    attrs[0].val.clusterDim.z = 1;
+    attrs[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attrs[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attrs;
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, sample_finish_kernel<kC, kW>, a);
+}
+
 static size_t stats_bytes(int B, int R) { return ((static_cast<size_t>(B) * R * sizeof(float2) + 255) / 256) * 256; }
 size_t sample_workspace(int B, int R, int /*V*/) { return stats_bytes(B, R) + chain_ws_bytes(B); }
 
@@ -1267,8 +1298,13 @@ cudaError_t launch_accept_sample(const float* logits, const float* q, int Vq, co
         if (e != cudaSuccess) return e;
     } else {
         // trees (sibling residuals depend on each other), or a workspace that
-        // only holds the row statistics: one cluster walks each sequence
-        e = launch_pdl(sample_finish_kernel, dim3(B * kCluster), dim3(kThreads), 0, st, a);
+        // only holds the row statistics: one cluster walks each sequence.  Its
+        // passes evaluate the exponential, the division by Z and one division
+        // per rejected sibling for every vocab entry on the cluster's SMs, so a
+        // few sequences take 16-CTA clusters of 768 threads (the 64-node tree's
+        // acceptance 167 -> 86 us against 8 x 256; 512 threads 92 us, 1024
+        // spill); many sequences keep 8 x 256 (more clusters resident at once)
+        e = B <= kWideWalkMaxB ? launch_finish<16, 24>(a, B, st) : launch_finish<kCluster, kWarps>(a, B, st);
         if (e != cudaSuccess) return e;
     }
     if (debug_sync()) {
