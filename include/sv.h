@@ -115,11 +115,16 @@ typedef struct sv_attn_shape {
 
 /* Workspace bytes sv_verify_attn needs for this shape (device-dependent: the
  * split-KV plan follows the SM count and how many thread-block clusters fit at
- * once).  0 when every (sequence, KV head) is handled by one cluster, whose
- * split partials merge on chip; ws may then be NULL.  Otherwise several
- * clusters share a (sequence, KV head): the workspace holds one ticket word per
- * (sequence, KV head, row tile of 64 or 128 rows, as the plan picks) followed by
- * the clusters' fp32 partials.
+ * once).  0 when every (sequence, KV head) is handled by one cluster whose
+ * split partials merge on chip; ws may then be NULL.  Otherwise it holds, in
+ * this order and as the plan needs them:
+ *   - when several clusters share a (sequence, KV head): one ticket word per
+ *     (sequence, KV head, row tile of 64 or 128 rows, as the plan picks), then
+ *     the clusters' fp32 partials;
+ *   - when the plan takes 128-row tiles (more than 64 query rows per
+ *     (sequence, KV head), e.g. a draft tree) in clusters of 2 to 8 CTAs: an
+ *     exchange area, one fp32 block of partial rows per CTA, through which
+ *     the cluster's CTAs merge (any contents before a call).
  * The ticket words must be zero before the first call on a workspace (e.g.
  * cudaMemset to 0 once); every call that completes leaves them zero again, so
  * one workspace serves any number of calls in stream order.  Calls running

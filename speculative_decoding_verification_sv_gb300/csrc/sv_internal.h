@@ -134,6 +134,8 @@ struct AttnPlan {
     int warps;      // warps per CTA
     int splits;     // CTAs per thread-block cluster (split-KV merged through DSMEM)
     int clusters;   // clusters per (sequence, KV head, row tile); > 1 merges in the workspace
+    bool xch;       // the cluster's CTAs exchange their partial rows through L2 (the workspace's
+                    // exchange area) instead of pushing them into the owners' shared memory
 };
 AttnPlan attn_plan(const sv_attn_shape& s);
 size_t attn_workspace(const sv_attn_shape& s);

@@ -64,6 +64,7 @@ constexpr int kMaxCluster = 16;
 #endif
 constexpr int kMergeCost = SV_ATTN_MERGE_COST;   // workspace merge, in key-tile times
 constexpr int kWsMergeBatch = 12;         // workspace partials per unit merged in one round of loads
+constexpr int kXchMaxCluster = 8;         // largest cluster whose partials meet through the L2 exchange
 constexpr int kGroups = 4;                // full tiles: column groups of a step
 #ifndef SV_ATTN_HALF_MAX_ROWS
 #define SV_ATTN_HALF_MAX_ROWS 64
@@ -128,6 +129,10 @@ struct Lay {
     static constexpr int kOffLsum = kOffRed + 2 * kGroups * kRows * 4;  // [kGroups][kRows] partial row sums
     static constexpr int kSmemBytes = kOffLsum + kGroups * kRows * 4 + 1024;
     static_assert((kRows + kMaxCluster - 1) * kRec * 4 <= kRingBytes, "pushed partials reuse the K/V ring");
+    // a CTA's block of the L2 exchange: (max, sum) of each row, then O as
+    // [kD / 4 column chunks][kM rows] float4, so that a warp's 32 rows of one
+    // chunk are one contiguous 512-byte store or load
+    static constexpr int kXchFloats = kM * (2 + kD);
     static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
     static_assert((4 * kStages + 9) * 8 + 4 <= 248, "barrier area (the word at +248 is the ticket flag)");
 };
@@ -141,6 +146,8 @@ struct AttnArgs {
     uint16_t* out;
     unsigned int* err;
     float* ws_part;          // [unit][cluster][part_rows][kRec] cluster partials (clusters > 1)
+    float* xch;              // [grid CTA][Lay::kXchFloats] partial rows exchanged through L2 (nullptr:
+                             // pushed into the owners' shared memory)
     unsigned int* ws_cnt;    // [unit] tickets of clusters done; zero between launches
     int B, R, Hq, Hkv, G, T_cap, rows, row_tiles;
     int clusters;            // clusters per (b, g, row tile); their partials meet in ws_part
@@ -198,6 +205,8 @@ __global__ void __launch_bounds__(Roles<kHalf, kHW>::kThreads, 1)
     uint64_t* anc = reinterpret_cast<uint64_t*>(smem + Ly::kOffAnc);   // [kMaxR][2]
     // after the loop: partial records pushed to this CTA, [row / C][source rank][kRec]
     float* part = reinterpret_cast<float*>(smem + Ly::kOffRing);
+    // the L2 exchange (128-row tiles only: half-tile kernels compile without it)
+    float* const xch = kHalf ? nullptr : a.xch;
 
     cg::cluster_group cluster = cg::this_cluster();
     const int C = static_cast<int>(cluster.num_blocks());
@@ -995,10 +1004,21 @@ __global__ void __launch_bounds__(Roles<kHalf, kHW>::kThreads, 1)
         __syncwarp();
         pdl_launch_dependents();             // see the note at the programmatic-launch wait
         cluster_wait();                      // every CTA of the cluster has started
-        if (need == 0) cluster_sync_warp();  // (1) and has drained its ring
-        // push the partial record of row prow into slot `rank` of the row's
-        // owner: slots [(prow / n_owners) * C + src] of its receive area
-        if (valid) {
+        if (need == 0 && xch == nullptr) cluster_sync_warp();  // (1) and has drained its ring
+        if (valid && xch != nullptr) {
+            // the partial row into this CTA's block of the L2 exchange (a warp's
+            // 32 rows of one column chunk are one contiguous 512-byte store)
+            const int prow = gr - rt * kTileRows;
+            float* xmine = xch + static_cast<size_t>(blockIdx.y * gridDim.x + blockIdx.x) * Ly::kXchFloats;
+            if (cgp == 0 && sub == 0)
+                __stcg(reinterpret_cast<float2*>(xmine) + prow, make_float2(use ? m_ref : -INFINITY, use ? lt : 0.f));
+            uint4* xo = reinterpret_cast<uint4*>(xmine + 2 * kTileRows);
+#pragma unroll
+            for (int e = 0; e < kOCols; e += 4)
+                __stcg(xo + ((ocol0 + e) >> 2) * kTileRows + prow, make_uint4(ov[e], ov[e + 1], ov[e + 2], ov[e + 3]));
+        } else if (valid) {
+            // push the partial record of row prow into slot `rank` of the row's
+            // owner: slots [(prow / n_owners) * C + src] of its receive area
             const int prow = gr - rt * kTileRows;      // < kTileRows for every real row
             int owner, li;
             if (need > 0) {
@@ -1025,10 +1045,10 @@ __global__ void __launch_bounds__(Roles<kHalf, kHW>::kThreads, 1)
         __syncwarp();
         pdl_launch_dependents();
         cluster_wait();
-        if (need == 0) cluster_sync_warp();   // (1)
+        if (need == 0 && xch == nullptr) cluster_sync_warp();   // (1)
     }
     __syncwarp();
-    cluster_sync_warp();   // (2) every record pushed and visible to its owner
+    cluster_sync_warp();   // (2) every record pushed (or stored) and visible to its owner
 
     // merge: this CTA finalises rows rank, rank + C, ... of the row tile (all
     // warps) from the records pushed to it; with one cluster per (b, g, row
@@ -1050,7 +1070,64 @@ __global__ void __launch_bounds__(Roles<kHalf, kHW>::kThreads, 1)
     const int n_owners = need > 0 ? __popc(light) : C;
     const float* recv = need > 0 ? reinterpret_cast<const float*>(smem + Ly::kOffRing + (kStages - need) * kStageBytes)
                                  : part;
-    for (int li = warp; owns && k0 + n_owners * li < nrows; li += kThreads / 32) {
+    if (xch != nullptr) {
+        // merge from the L2 exchange: units of (32-row group, 4-column chunk)
+        // split evenly over the cluster's CTAs and their warps; lane l takes
+        // row 32 * group + l, so each load of a source's partial is one
+        // contiguous 256-byte (max, sum) or 512-byte (O) piece
+        constexpr int kCh = kD / 4;
+        const int nunits = ((nrows + 31) / 32) * kCh;
+        const int per = (nunits + C - 1) / C;
+        const int u1 = min(nunits, (rank + 1) * per);
+        const float* xb = xch + static_cast<size_t>(blockIdx.y * gridDim.x + blockIdx.x - rank) * Ly::kXchFloats;
+        for (int u = rank * per + warp; u < u1; u += kThreads / 32) {
+            const int lr = (u / kCh) * 32 + lane, ch = u % kCh;
+            if (lr >= nrows) continue;
+            float2 ml[kXchMaxCluster];
+            float4 x[kXchMaxCluster];
+#pragma unroll
+            for (int sr = 0; sr < kXchMaxCluster; ++sr) {
+                ml[sr] = make_float2(-INFINITY, 0.f);
+                x[sr] = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (sr < C) {
+                    const float* xs = xb + sr * Ly::kXchFloats;
+                    ml[sr] = __ldcg(reinterpret_cast<const float2*>(xs) + lr);
+                    x[sr] = __ldcg(reinterpret_cast<const float4*>(xs + 2 * kTileRows) + ch * kTileRows + lr);
+                }
+            }
+            float M = -INFINITY;
+#pragma unroll
+            for (int sr = 0; sr < kXchMaxCluster; ++sr) M = fmaxf(M, ml[sr].x);
+            float L = 0.f;
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int sr = 0; sr < kXchMaxCluster; ++sr) {
+                // an empty partial (-inf, 0) and its zero O row weigh nothing
+                const float w = (ml[sr].y > 0.f && M != -INFINITY) ? exp2f(ml[sr].x - M) : 0.f;
+                L += w * ml[sr].y;
+                acc.x += w * x[sr].x;
+                acc.y += w * x[sr].y;
+                acc.z += w * x[sr].z;
+                acc.w += w * x[sr].w;
+            }
+            if (a.clusters == 1) {
+                const float inv = L > 0.f ? 1.0f / L : 0.f;
+                const int row = rt * kTileRows + lr;
+                const int jr = row / a.G, h = g * a.G + row % a.G;
+                uint16_t* dst = a.out + ((static_cast<size_t>(b) * a.R + jr) * a.Hq + h) * kD + 4 * ch;
+                *reinterpret_cast<uint2*>(dst) =
+                    make_uint2(pack_bf16x2(acc.x * inv, acc.y * inv), pack_bf16x2(acc.z * inv, acc.w * inv));
+            } else {
+                float* rec_g = a.ws_part + ((static_cast<size_t>(unit) * a.clusters + ci) * a.part_rows + lr) * kRec;
+                if (ch == 0) {
+                    rec_g[0] = L > 0.f ? M : -INFINITY;
+                    rec_g[1] = L;
+                }
+                *reinterpret_cast<float4*>(rec_g + 4 + 4 * ch) = acc;
+            }
+        }
+    }
+    for (int li = warp; xch == nullptr && owns && k0 + n_owners * li < nrows; li += kThreads / 32) {
         const int lr = k0 + n_owners * li;
         const float* slots = recv + li * C * kRec;
         float ms = -INFINITY, ls = 0.f;
@@ -1352,6 +1429,16 @@ AttnPlan attn_plan(const sv_attn_shape& s) {
                   ((tiles + p.splits * p.clusters - 1) / (p.splits * p.clusters) + Lay<true>::kT - 1) / Lay<true>::kT >
                       Lay<true>::kStages);
     p.warps = !p.half ? Roles<false>::kThreads / 32 : p.hw4 ? Roles<true, 4>::kThreads / 32 : Roles<true, 2>::kThreads / 32;
+    // Clusters of 128-row tiles meet through L2: each CTA stores its partial
+    // rows in coalesced pieces and the owners load them after one cluster
+    // barrier.  Pushed into the owners' shared memory instead, the records
+    // (66 KB per CTA) cross the cluster at the ~20 GB/s per SM that distributed
+    // shared memory gives an all-to-all, after a barrier for every ring to
+    // drain: the draft tree's layer (6-CTA clusters) 23.4 -> 21.6 us.  Half
+    // tiles keep the push: with 2-CTA clusters of 63 rows (7B batch 16) half
+    // of a CTA's records stay in its own shared memory, and the exchange
+    // measured 48.1 -> 50.3 us
+    p.xch = !p.half && p.splits >= 2 && p.splits <= kXchMaxCluster;
     return p;
 }
 
@@ -1361,13 +1448,28 @@ static size_t attn_ticket_bytes(const AttnPlan& p, const sv_attn_shape& s) {
     return (units * 4 + 255) / 256 * 256;
 }
 
-size_t attn_workspace(const sv_attn_shape& s) {
-    const AttnPlan p = attn_plan(s);
+// Bytes of the tickets and cluster partials (0 with one cluster per unit).
+static size_t attn_part_bytes(const AttnPlan& p, const sv_attn_shape& s) {
     if (p.clusters <= 1) return 0;
     const size_t units = static_cast<size_t>(s.B) * s.Hkv * p.row_tiles;
     const int tile_rows = p.half ? Lay<true>::kM : Lay<false>::kM;
     const size_t part_rows = p.rows < tile_rows ? p.rows : tile_rows;
     return attn_ticket_bytes(p, s) + units * p.clusters * part_rows * kRec * sizeof(float);
+}
+
+// Offset and bytes of the L2 exchange area (one block per CTA of the grid).
+static size_t attn_xch_offset(const AttnPlan& p, const sv_attn_shape& s) {
+    return (attn_part_bytes(p, s) + 255) / 256 * 256;
+}
+static size_t attn_xch_bytes(const AttnPlan& p, const sv_attn_shape& s) {
+    if (!p.xch) return 0;
+    const size_t ctas = static_cast<size_t>(p.splits) * p.clusters * s.B * s.Hkv * p.row_tiles;
+    return ctas * (p.half ? Lay<true>::kXchFloats : Lay<false>::kXchFloats) * sizeof(float);
+}
+
+size_t attn_workspace(const sv_attn_shape& s) {
+    const AttnPlan p = attn_plan(s);
+    return p.xch ? attn_xch_offset(p, s) + attn_xch_bytes(p, s) : attn_part_bytes(p, s);
 }
 
 cudaError_t launch_verify_attn(const sv_attn_shape& s, const uint16_t* q, const uint16_t* k_cache,
@@ -1376,7 +1478,7 @@ cudaError_t launch_verify_attn(const sv_attn_shape& s, const uint16_t* q, const 
                                void* ws, bool cache_ready, const int32_t* pages, int max_pages, int num_pages,
                                cudaStream_t st) {
     const AttnPlan p = attn_plan(s);
-    if (p.clusters > 1 && ws == nullptr) return cudaErrorInvalidValue;
+    if ((p.clusters > 1 || p.xch) && ws == nullptr) return cudaErrorInvalidValue;
     alignas(64) uint8_t tK[128], tV[128], tKb[128], tVb[128];
     // rows of the context tensor maps: the caches, or the page pool
     const uint64_t ctx_rows = pages ? static_cast<uint64_t>(num_pages) * s.Hkv * kNk
@@ -1398,6 +1500,7 @@ cudaError_t launch_verify_attn(const sv_attn_shape& s, const uint16_t* q, const 
     a.ws_cnt = p.clusters > 1 ? static_cast<unsigned int*>(ws) : nullptr;
     a.ws_part = p.clusters > 1 ? reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + attn_ticket_bytes(p, s))
                                : nullptr;
+    a.xch = p.xch ? reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + attn_xch_offset(p, s)) : nullptr;
     a.B = s.B;
     a.R = s.R;
     a.Hq = s.Hq;

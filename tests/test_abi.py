@@ -145,6 +145,8 @@ def test_workspace_queries(lib):
     assert b.lib.sv_accept_greedy_workspace(16, 9, 152064) == 16 * 9 * 19 * 8
     # row statistics, then the chain path's per-sequence records and sums
     assert b.lib.sv_accept_sample_workspace(64, 9, 151936) == 64 * 9 * 8 + 64 * 16 + 64 * 2 * (64 * 32 + 64) * 4
+    # 7B batch 16: 63 rows per (sequence, KV head) in 64-row tiles, one cluster
+    # each, merged on chip
     assert b.verify_attn_workspace(16, 9, 28, 4, 128, 8320) == 0
 
 
