@@ -122,7 +122,7 @@ typedef struct sv_attn_shape {
  *     (sequence, KV head, row tile of 64 or 128 rows, as the plan picks), then
  *     the clusters' fp32 partials;
  *   - when the plan takes 128-row tiles (more than 64 query rows per
- *     (sequence, KV head), e.g. a draft tree) in clusters of 2 to 8 CTAs: an
+ *     (sequence, KV head), e.g. a draft tree) in clusters of 2 to 6 CTAs: an
  *     exchange area, one fp32 block of partial rows per CTA, through which
  *     the cluster's CTAs merge (any contents before a call).
  * The ticket words must be zero before the first call on a workspace (e.g.

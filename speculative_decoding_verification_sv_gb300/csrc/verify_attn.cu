@@ -64,7 +64,7 @@ constexpr int kMaxCluster = 16;
 #endif
 constexpr int kMergeCost = SV_ATTN_MERGE_COST;   // workspace merge, in key-tile times
 constexpr int kWsMergeBatch = 12;         // workspace partials per unit merged in one round of loads
-constexpr int kXchMaxCluster = 8;         // largest cluster whose partials meet through the L2 exchange
+constexpr int kXchMaxCluster = 6;         // largest cluster whose partials meet through the L2 exchange
 constexpr int kGroups = 4;                // full tiles: column groups of a step
 #ifndef SV_ATTN_HALF_MAX_ROWS
 #define SV_ATTN_HALF_MAX_ROWS 64
@@ -1072,44 +1072,43 @@ __global__ void __launch_bounds__(Roles<kHalf, kHW>::kThreads, 1)
                                  : part;
     if (xch != nullptr) {
         // merge from the L2 exchange: units of (32-row group, 4-column chunk)
-        // split evenly over the cluster's CTAs and their warps; lane l takes
-        // row 32 * group + l, so each load of a source's partial is one
-        // contiguous 256-byte (max, sum) or 512-byte (O) piece
-        constexpr int kCh = kD / 4;
+        // split evenly over the cluster's CTAs, up to two per warp at a time;
+        // lane l takes row 32 * group + l, so each load of a source's partial
+        // is one contiguous 512-byte (O) or 256-byte (max, sum) piece.  The
+        // rows' weights are formed once per CTA (a warp per row group) while
+        // the first O pieces are in flight, and shared through shared memory
+        // (the drained ring): one round of loads for the whole merge
+        constexpr int kCh = kD / 4, kNW = kThreads / 32, kX = kXchMaxCluster;
         const int nunits = ((nrows + 31) / 32) * kCh;
         const int per = (nunits + C - 1) / C;
-        const int u1 = min(nunits, (rank + 1) * per);
+        const int u0 = min(nunits, rank * per), u1 = min(nunits, u0 + per);
+        const int g0 = u0 / kCh, ng = u1 > u0 ? (u1 - 1) / kCh - g0 + 1 : 0;
         const float* xb = xch + static_cast<size_t>(blockIdx.y * gridDim.x + blockIdx.x - rank) * Ly::kXchFloats;
-        for (int u = rank * per + warp; u < u1; u += kThreads / 32) {
+        float* wsm = reinterpret_cast<float*>(smem + Ly::kOffRing);   // [group][kX weights, M, L][32 rows]
+        auto load_unit = [&](int u, float4 (&x)[kX]) {
             const int lr = (u / kCh) * 32 + lane, ch = u % kCh;
-            if (lr >= nrows) continue;
-            float2 ml[kXchMaxCluster];
-            float4 x[kXchMaxCluster];
 #pragma unroll
-            for (int sr = 0; sr < kXchMaxCluster; ++sr) {
-                ml[sr] = make_float2(-INFINITY, 0.f);
+            for (int sr = 0; sr < kX; ++sr) {
                 x[sr] = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (sr < C) {
-                    const float* xs = xb + sr * Ly::kXchFloats;
-                    ml[sr] = __ldcg(reinterpret_cast<const float2*>(xs) + lr);
-                    x[sr] = __ldcg(reinterpret_cast<const float4*>(xs + 2 * kTileRows) + ch * kTileRows + lr);
-                }
+                if (u < u1 && lr < nrows && sr < C)
+                    x[sr] = __ldcg(reinterpret_cast<const float4*>(xb + sr * Ly::kXchFloats + 2 * kTileRows) +
+                                   ch * kTileRows + lr);
             }
-            float M = -INFINITY;
-#pragma unroll
-            for (int sr = 0; sr < kXchMaxCluster; ++sr) M = fmaxf(M, ml[sr].x);
-            float L = 0.f;
+        };
+        auto finish_unit = [&](int u, const float4 (&x)[kX]) {
+            const int lr = (u / kCh) * 32 + lane, ch = u % kCh;
+            if (u >= u1 || lr >= nrows) return;
+            const float* wr = wsm + (u / kCh - g0) * (kX + 2) * 32 + lane;
             float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-            for (int sr = 0; sr < kXchMaxCluster; ++sr) {
-                // an empty partial (-inf, 0) and its zero O row weigh nothing
-                const float w = (ml[sr].y > 0.f && M != -INFINITY) ? exp2f(ml[sr].x - M) : 0.f;
-                L += w * ml[sr].y;
+            for (int sr = 0; sr < kX; ++sr) {
+                const float w = sr < C ? wr[sr * 32] : 0.f;
                 acc.x += w * x[sr].x;
                 acc.y += w * x[sr].y;
                 acc.z += w * x[sr].z;
                 acc.w += w * x[sr].w;
             }
+            const float M = wr[kX * 32], L = wr[(kX + 1) * 32];
             if (a.clusters == 1) {
                 const float inv = L > 0.f ? 1.0f / L : 0.f;
                 const int row = rt * kTileRows + lr;
@@ -1125,6 +1124,41 @@ __global__ void __launch_bounds__(Roles<kHalf, kHW>::kThreads, 1)
                 }
                 *reinterpret_cast<float4*>(rec_g + 4 + 4 * ch) = acc;
             }
+        };
+        for (int base = u0; base < u1; base += 2 * kNW) {   // CTA-uniform trip count
+            float4 xa[kX], xc[kX];
+            load_unit(base + warp, xa);
+            load_unit(base + kNW + warp, xc);
+            if (base == u0) {
+                if (warp < ng) {
+                    // weights of row 32 (g0 + warp) + lane: exp2(m_s - M) over
+                    // the sources with a non-empty partial, and the merged sum
+                    const int lr = (g0 + warp) * 32 + lane;
+                    float2 ml[kX];
+#pragma unroll
+                    for (int sr = 0; sr < kX; ++sr)
+                        ml[sr] = (lr < nrows && sr < C)
+                                     ? __ldcg(reinterpret_cast<const float2*>(xb + sr * Ly::kXchFloats) + lr)
+                                     : make_float2(-INFINITY, 0.f);
+                    float M = -INFINITY;
+#pragma unroll
+                    for (int sr = 0; sr < kX; ++sr) M = fmaxf(M, ml[sr].x);
+                    float L = 0.f;
+                    float* wr = wsm + warp * (kX + 2) * 32 + lane;
+#pragma unroll
+                    for (int sr = 0; sr < kX; ++sr) {
+                        // an empty partial (-inf, 0) and its zero O row weigh nothing
+                        const float w = (ml[sr].y > 0.f && M != -INFINITY) ? exp2f(ml[sr].x - M) : 0.f;
+                        L += w * ml[sr].y;
+                        wr[sr * 32] = w;
+                    }
+                    wr[kX * 32] = M;
+                    wr[(kX + 1) * 32] = L;
+                }
+                __syncthreads();
+            }
+            finish_unit(base + warp, xa);
+            finish_unit(base + kNW + warp, xc);
         }
     }
     for (int li = warp; xch == nullptr && owns && k0 + n_owners * li < nrows; li += kThreads / 32) {
