@@ -586,7 +586,9 @@ struct RowValues {
     const float* Q;     // q row u (Vq entries); nullptr when no q row exists (a leaf)
     int Vq;
     float T, M, Z;
+    float rZ;           // 1 / Z rounded to nearest (the divisions by Z through div_rn_by)
     const float* S;     // S_1..S_nsteps
+    const float* rS;    // 1 / S_s rounded to nearest, where S_s > 0
     int nsteps;
     bool residual;      // value = max(0, w_nsteps - q) instead of w_nsteps
     int V;
@@ -594,11 +596,11 @@ struct RowValues {
 
     __device__ __forceinline__ float one(float l, float qv) const {
         const float z = (T == 1.0f) ? l : __fdiv_rn(l, T);
-        float w = __fdiv_rn(sv_exp_nb(__fsub_rn(z, M)), Z);
+        float w = div_rn_by(sv_exp_nb(__fsub_rn(z, M)), Z, rZ);
         for (int s = 0; s < nsteps; ++s) {
             const float d = __fsub_rn(w, qv);
             const float rho = d > 0.0f ? d : 0.0f;
-            w = S[s] > 0.0f ? __fdiv_rn(rho, S[s]) : w;
+            w = S[s] > 0.0f ? div_rn_by(rho, S[s], rS[s]) : w;
         }
         if (residual) {
             const float d = __fsub_rn(w, qv);
@@ -822,6 +824,7 @@ __global__ void __launch_bounds__(kW * 32, 1) sample_finish_kernel(SampleArgs a)
     __shared__ PassSmem sm;
     __shared__ int par_s[kMaxR];
     __shared__ float Schain[kMaxR];
+    __shared__ float rSchain[kMaxR];
     cg::cluster_group cluster = cg::this_cluster();
     const int rank = static_cast<int>(cluster.block_rank());
     const int b = blockIdx.x / kC;
@@ -841,8 +844,8 @@ __global__ void __launch_bounds__(kW * 32, 1) sample_finish_kernel(SampleArgs a)
     for (int guard = 0; guard <= R && token < 0; ++guard) {
         if (!SV_CHECK(u >= 0 && u < R, a.err, 7)) break;
         const float2 ms = st[u];
-        RowValues rv{Lb + static_cast<size_t>(u) * V, Qb + static_cast<size_t>(u) * Vq, Vq, a.T, ms.x, ms.y, Schain,
-                     0, false, V, a.err};
+        RowValues rv{Lb + static_cast<size_t>(u) * V, Qb + static_cast<size_t>(u) * Vq, Vq, a.T, ms.x, ms.y,
+                     __frcp_rn(ms.y), Schain, rSchain, 0, false, V, a.err};
         int first = tree_ok ? next_child(par, R, u, -1) : -1;
         if (first < 0) {   // leaf: bonus token from p_u
             rv.Q = nullptr;
@@ -882,7 +885,10 @@ __global__ void __launch_bounds__(kW * 32, 1) sample_finish_kernel(SampleArgs a)
                 }
                 break;
             }
-            if (threadIdx.x == 0 && SV_CHECK(nsteps < kMaxR, a.err, 8)) Schain[nsteps] = S;
+            if (threadIdx.x == 0 && SV_CHECK(nsteps < kMaxR, a.err, 8)) {
+                Schain[nsteps] = S;
+                rSchain[nsteps] = S > 0.0f ? __frcp_rn(S) : 0.0f;
+            }
             __syncthreads();
             ++nsteps;
         }
@@ -938,7 +944,7 @@ __global__ void __launch_bounds__(kMaxR) chain_walk_kernel(SampleArgs a, ChainWs
         const int u = t, d = a.tok[static_cast<size_t>(b) * R + t + 1];
         const float2 ms = a.stats[static_cast<size_t>(b) * R + u];
         RowValues rv{a.logits + (static_cast<size_t>(b) * R + u) * V, a.q + (static_cast<size_t>(b) * (R - 1) + u) * Vq,
-                     Vq, a.T, ms.x, ms.y, nullptr, 0, false, V, a.err};
+                     Vq, a.T, ms.x, ms.y, __frcp_rn(ms.y), nullptr, nullptr, 0, false, V, a.err};
         tok_bad = !(d >= 0 && d < V);
         accept = false;
         if (!tok_bad) {
@@ -978,8 +984,8 @@ __global__ void __launch_bounds__(kThreads) chain_sums_kernel(SampleArgs a, Chai
     const int u = rc.x;
     const float2 ms = a.stats[static_cast<size_t>(b) * R + u];
     const float* Qrow = rc.y == kChainResidual ? a.q + (static_cast<size_t>(b) * (R - 1) + u) * Vq : nullptr;
-    RowValues rv{a.logits + (static_cast<size_t>(b) * R + u) * V, Qrow, Vq, a.T, ms.x, ms.y, nullptr, 0, false, V,
-                 a.err};
+    RowValues rv{a.logits + (static_cast<size_t>(b) * R + u) * V, Qrow, Vq, a.T, ms.x, ms.y, __frcp_rn(ms.y), nullptr,
+                 nullptr, 0, false, V, a.err};
     float* sr = w.sums + static_cast<size_t>(b) * 2 * kSumFloats;
     float* sp = sr + kSumFloats;
     __shared__ float cr[kChunksPerBlk], cp[kChunksPerBlk];
@@ -1016,8 +1022,8 @@ __global__ void __launch_bounds__(kThreads) chain_sums_kernel(SampleArgs a, Chai
         float4 p = make_float4(0.f, 0.f, 0.f, 0.f), r = p;
         if (v < V) {
             auto ex = [&](float x) { return nrm ? sv_exp_nrm(x) : sv_exp_nb(x); };
-            p = make_float4(__fdiv_rn(ex(d[i].x), ms.y), __fdiv_rn(ex(d[i].y), ms.y), __fdiv_rn(ex(d[i].z), ms.y),
-                            __fdiv_rn(ex(d[i].w), ms.y));
+            p = make_float4(div_rn_by(ex(d[i].x), ms.y, rv.rZ), div_rn_by(ex(d[i].y), ms.y, rv.rZ),
+                            div_rn_by(ex(d[i].z), ms.y, rv.rZ), div_rn_by(ex(d[i].w), ms.y, rv.rZ));
             auto res = [](float w, float qv) {   // RowValues::one with residual: max(0, w - q)
                 const float dd = __fsub_rn(w, qv);
                 return dd > 0.0f ? dd : 0.0f;
@@ -1081,8 +1087,8 @@ __global__ void __launch_bounds__(32) chain_draw_kernel(SampleArgs a, ChainWs w)
     const float total = use_r ? Sr : Sp;
     const float2 ms = a.stats[static_cast<size_t>(b) * R + u];
     RowValues rv{a.logits + (static_cast<size_t>(b) * R + u) * V,
-                 use_r ? a.q + (static_cast<size_t>(b) * (R - 1) + u) * Vq : nullptr, Vq, a.T, ms.x, ms.y, nullptr, 0,
-                 use_r, V, a.err};
+                 use_r ? a.q + (static_cast<size_t>(b) * (R - 1) + u) * Vq : nullptr, Vq, a.T, ms.x, ms.y,
+                 __frcp_rn(ms.y), nullptr, nullptr, 0, use_r, V, a.err};
     const float tau = __fmul_rn(node_uniforms(a.seed, a.step, b, u, a.uniforms, R).y, total);
     bs[lane] = block_sum(set, lane);
     bs[lane + 32] = block_sum(set, lane + 32);
