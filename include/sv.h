@@ -446,6 +446,13 @@ SV_API sv_status sv_copy(void* dst, const void* src, size_t bytes, void* stream)
  * -86.5 < x <= 0) -- differs from it in any bit, y[i] = 12345 instead. */
 SV_API sv_status sv_diag_exp(const float* x, float* y, int64_t n, void* stream);
 
+/* q[i] = a[i] / b[i] as sv_accept_sample divides by a row's sum Z or a
+ * sibling residual sum S: from the reciprocal 1/b rounded to nearest by one
+ * Markstein correction step where a and b lie in [2^-60, 2^60], the
+ * correctly rounded division elsewhere.  Either way the result must be the
+ * IEEE quotient rounded to nearest even, bit for bit. */
+SV_API sv_status sv_diag_div(const float* a, const float* b, float* q, int64_t n, void* stream);
+
 /* out[i][0..3] = Philox4x32-10(counter = ctr[i][0..3], key = key[i][0..1]). */
 SV_API sv_status sv_diag_philox(const uint32_t* ctr, const uint32_t* key, uint32_t* out, int64_t n, void* stream);
 

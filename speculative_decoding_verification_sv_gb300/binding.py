@@ -74,12 +74,13 @@ def _load():
                                                 _P, _P, _I32, _I32, _I32, _P, _P]
     L.sv_copy.argtypes = [_P, _P, _SZ, _P]
     L.sv_diag_exp.argtypes = [_P, _P, _I64, _P]
+    L.sv_diag_div.argtypes = [_P, _P, _P, _I64, _P]
     L.sv_diag_philox.argtypes = [_P, _P, _P, _I64, _P]
     L.sv_diag_canon.argtypes = [_P, _I32, _I32, _P, _P, _P, _P]
     for fn in ("sv_verify_attn", "sv_verify_attn_ex", "sv_lm_head", "sv_lm_head_ex", "sv_accept_greedy",
                "sv_accept_greedy_relaxed", "sv_accept_sample",
                "sv_accept_sample_noalloc", "sv_kv_commit", "sv_kv_commit_paged", "sv_verify_attn_paged",
-               "sv_diag_exp", "sv_diag_philox", "sv_diag_canon", "sv_get_device_error", "sv_lm_head_argmax",
+               "sv_diag_exp", "sv_diag_div", "sv_diag_philox", "sv_diag_canon", "sv_get_device_error", "sv_lm_head_argmax",
                "sv_accept_greedy_commit", "sv_accept_greedy_commit_paged", "sv_copy"):
         getattr(L, fn).restype = ctypes.c_int
     return L
@@ -411,6 +412,16 @@ def diag_exp(x: torch.Tensor, stream=None) -> torch.Tensor:
     _check("sv_diag_exp", lib.sv_diag_exp(_ptr(x, torch.float32), _ptr(y, torch.float32), x.numel(),
                                           _stream(stream)))
     return y
+
+
+def diag_div(a: torch.Tensor, b: torch.Tensor, stream=None) -> torch.Tensor:
+    """Elementwise a / b (float32, same shape) through the acceptance's division."""
+    if a.shape != b.shape:
+        raise ValueError("a and b differ in shape")
+    q = torch.empty_like(a)
+    _check("sv_diag_div", lib.sv_diag_div(_ptr(a, torch.float32), _ptr(b, torch.float32), _ptr(q, torch.float32),
+                                          a.numel(), _stream(stream)))
+    return q
 
 
 def diag_philox(ctr: torch.Tensor, key: torch.Tensor, stream=None) -> torch.Tensor:

@@ -1202,6 +1202,10 @@ cudaError_t launch_accept_greedy(const float* logits, const int32_t* tok, const 
 // Row statistics (B*R float2); then, for the chain path, the per-sequence
 // records and summation-tree sums.
 constexpr int kWideWalkMaxB = 4;   // sequences up to which the walk takes 16-CTA clusters
+#ifndef SV_WIDE_WALK_WARPS
+#define SV_WIDE_WALK_WARPS 24
+#endif
+constexpr int kWideWalkWarps = SV_WIDE_WALK_WARPS;   // warps per CTA of those clusters
 
 template <int kC, int kW>
 cudaError_t launch_finish(const SampleArgs& a, int B, cudaStream_t st) {
@@ -1310,13 +1314,26 @@ cudaError_t launch_accept_sample(const float* logits, const float* q, int Vq, co
         // few sequences take 16-CTA clusters of 768 threads (the 64-node tree's
         // acceptance 167 -> 86 us against 8 x 256; 512 threads 92 us, 1024
         // spill); many sequences keep 8 x 256 (more clusters resident at once)
-        e = B <= kWideWalkMaxB ? launch_finish<16, 24>(a, B, st) : launch_finish<kCluster, kWarps>(a, B, st);
+        e = B <= kWideWalkMaxB ? launch_finish<16, kWideWalkWarps>(a, B, st) : launch_finish<kCluster, kWarps>(a, B, st);
         if (e != cudaSuccess) return e;
     }
     if (debug_sync()) {
         e = cudaStreamSynchronize(st);
         if (e != cudaSuccess) return e;
     }
+    return cudaGetLastError();
+}
+
+// the acceptance's division by a per-divisor reciprocal
+__global__ void diag_div_kernel(const float* a, const float* b, float* q, int64_t n) {
+    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x)
+        q[i] = div_rn_by(a[i], b[i], __frcp_rn(b[i]));
+}
+
+cudaError_t launch_diag_div(const float* a, const float* b, float* q, int64_t n, cudaStream_t st) {
+    const int64_t blocks = (n + 255) / 256;
+    diag_div_kernel<<<static_cast<int>(blocks > 65535 ? 65535 : (blocks < 1 ? 1 : blocks)), 256, 0, st>>>(a, b, q, n);
     return cudaGetLastError();
 }
 

@@ -403,6 +403,12 @@ sv_status sv_diag_exp(const float* x, float* y, int64_t n, void* stream) {
     return launch_status(sv::launch_diag_exp(x, y, n, as_stream(stream)));
 }
 
+sv_status sv_diag_div(const float* a, const float* b, float* q, int64_t n, void* stream) {
+    if (n < 0 || (n > 0 && (!a || !b || !q))) return SV_ERR_ARG;
+    if (n == 0) return SV_OK;
+    return launch_status(sv::launch_diag_div(a, b, q, n, as_stream(stream)));
+}
+
 sv_status sv_diag_philox(const uint32_t* ctr, const uint32_t* key, uint32_t* out, int64_t n, void* stream) {
     if (n < 0 || (n > 0 && (!ctr || !key || !out))) return SV_ERR_ARG;
     if (n == 0) return SV_OK;

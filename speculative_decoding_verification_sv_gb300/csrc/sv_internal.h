@@ -89,6 +89,7 @@ cudaError_t launch_accept_sample(const float* logits, const float* q, int Vq, co
 // stage.cu
 cudaError_t launch_stage_copy(void* dst, const void* src, size_t bytes, cudaStream_t st);
 cudaError_t launch_diag_exp(const float* x, float* y, int64_t n, cudaStream_t st);
+cudaError_t launch_diag_div(const float* a, const float* b, float* q, int64_t n, cudaStream_t st);
 cudaError_t launch_diag_philox(const uint32_t* ctr, const uint32_t* key, uint32_t* out, int64_t n,
                                cudaStream_t st);
 cudaError_t launch_diag_canon(const float* x, int n, int m, const float* u, float* sums, int32_t* draws,

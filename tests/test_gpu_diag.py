@@ -34,6 +34,41 @@ def test_exp_bit_exact_dense(sv):
     assert same.all(), xs[~same][:5]
 
 
+def test_division_bit_exact(sv):
+    """The acceptance divides by a row's sum Z (in [1, V]) and by sibling
+    residual sums S (in (0, 1]) through a reciprocal and one correction step;
+    its quotients must be IEEE float32 division rounded to nearest, which
+    numpy computes on the host."""
+    rng = np.random.default_rng(5)
+    n = 4_000_000
+
+    def f32(lo_exp, hi_exp, size):   # random significands, exponents uniform in [lo, hi]
+        e = rng.integers(lo_exp, hi_exp + 1, size=size)
+        m = rng.integers(0, 2 ** 23, size=size)
+        return ((e + 127).astype(np.uint32) << 23 | m.astype(np.uint32)).view(np.float32)
+
+    # divisors with special significands (1, all ones, 1 + ulp, 1.5, ...)
+    sig = np.array([0, 0x7FFFFF, 1, 0x400000, 0x7FFFFE, 0x3FFFFF, 0x555555], np.uint32)
+    bexp = np.array([0, 1, 5, 12, 17, -1, -7, -40], np.int64)
+    bs = ((bexp[:, None] + 127).astype(np.uint32) << 23 | sig[None, :]).view(np.float32).ravel()
+    a_dense = (np.uint32(0x3F000000) | np.arange(0, 2 ** 23, 64, dtype=np.uint32)).view(np.float32)
+    pairs = [
+        (np.tile(a_dense, bs.size), np.repeat(bs, a_dense.size)),
+        (f32(-59, -1, n), f32(0, 17, n)),                          # e / Z
+        (f32(-50, -1, n), f32(-50, -1, n)),                        # rho / S (any order of sizes)
+        (f32(-60, 59, n), f32(-60, 59, n)),                        # the whole fast range
+        (f32(-126, -61, 100_000), f32(0, 17, 100_000)),            # below it: the division itself
+        (np.array([0.0, 1.0, 2.0 ** -60, 2.0 ** -61, 1e-45, 3.0, 1.0], np.float32),
+         np.array([3.0, 3.0, 7.0, 7.0, 3.0, 2.0 ** -61, 2.0 ** 61], np.float32)),
+    ]
+    a = np.concatenate([p[0] for p in pairs]).astype(np.float32)
+    b = np.concatenate([p[1] for p in pairs]).astype(np.float32)
+    got = sv.diag_div(torch.from_numpy(a).cuda(), torch.from_numpy(b).cuda()).cpu().numpy()
+    ref = a / b
+    same = got.view(np.uint32) == ref.view(np.uint32)
+    assert same.all(), (a[~same][:5], b[~same][:5])
+
+
 def test_philox_bit_exact(sv):
     rng = np.random.default_rng(2)
     n = 200_000
