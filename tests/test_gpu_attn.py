@@ -269,6 +269,22 @@ def test_attn_workspace_full_tile_tree(sv):
     assert sv.get_device_error() == 0
 
 
+@pytest.mark.parametrize("B,R,Hq,Hkv,T_cap,lengths,tree", [
+    (1, 65, 7, 1, 32832, [32700], True),          # a 64-node tree on one KV head: 4 tiles x ~7 clusters of 5
+    (2, 33, 7, 1, 32832, [32000, 20013], False),   # 231-row chains: 2 tiles per sequence, several clusters each
+])
+def test_attn_workspace_exchange(sv, B, R, Hq, Hkv, T_cap, lengths, tree):
+    """128-row tiles split over several clusters of at most six CTAs: each
+    cluster's CTAs meet through the L2 exchange area, and the clusters'
+    merged partials through the workspace tickets, in one launch."""
+    assert sv.verify_attn_workspace(B, R, Hq, Hkv, 128, T_cap) > 0
+    parent = np.tile(synth.random_tree(R - 1, 8, 3, 31), (B, 1)) if tree else None
+    got, ref = _run(sv, B, R, Hq, Hkv, T_cap, lengths, parent=parent, seed=B * 41 + R)
+    ok, err, bound = within_tol(got, ref)
+    assert ok, (err, bound)
+    assert sv.get_device_error() == 0
+
+
 def test_attn_workspace_tickets_reset(sv):
     """A batch-1, 32K-context layer splits each KV head over several clusters
     that meet in the workspace through a ticket word; every call must leave
