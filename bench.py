@@ -53,7 +53,7 @@ FALLBACK_HBM_GBS = 6800.0
 TRAFFIC = {
     # ncu (dram__bytes_read.sum, dram__bytes_write.sum), one 1.5B layer of the
     # 28-layer round (t=4096, k=4, b=1)
-    ("1", "verify_attn"): {"bytes": 4295168 + 0, "src": "verify_attn.cu", "src_hash": "30be471da6579ce0"},
+    ("1", "verify_attn"): {"bytes": 4295168 + 0, "src": "verify_attn.cu", "src_hash": "d977ade712ea17dc"},
     # the same round: the LM head with the argmax keys and no logits (its own
     # output is 47 KB of keys; the 3 MB written are L2 write-backs of an
     # earlier torch result that its weight stream evicted)
@@ -63,14 +63,14 @@ TRAFFIC = {
     ("1", "accept_greedy_commit"): {"bytes": 222208 + 0, "src": "kv_commit.cu", "src_hash": "11e3452aa759e99f"},
     # 7B batch-16 layer (2-layer case, same per-layer launch; split K/V barriers)
     ("3b16", "verify_attn"): {"bytes": 270150656 + 3010304, "src": "verify_attn.cu",
-                              "src_hash": "30be471da6579ce0"},
+                              "src_hash": "d977ade712ea17dc"},
     ("3b16s", "verify_attn"): {"bytes": 270150656 + 3010304, "src": "verify_attn.cu",
-                               "src_hash": "30be471da6579ce0"},
+                               "src_hash": "d977ade712ea17dc"},
     # 7B tree layer (64 draft nodes, 455 query rows per KV head in four 128-row
     # tiles sharing each K/V tile through L2; the clusters' partial rows meet
     # in the workspace's exchange area, which stays in L2; 2-layer case)
-    ("4", "verify_attn"): {"bytes": 17501696 + 0, "src": "verify_attn.cu", "src_hash": "30be471da6579ce0"},
-    ("4s", "verify_attn"): {"bytes": 17501696 + 0, "src": "verify_attn.cu", "src_hash": "30be471da6579ce0"},
+    ("4", "verify_attn"): {"bytes": 17501696 + 0, "src": "verify_attn.cu", "src_hash": "d977ade712ea17dc"},
+    ("4s", "verify_attn"): {"bytes": 17501696 + 0, "src": "verify_attn.cu", "src_hash": "d977ade712ea17dc"},
     # sampled B64 k8: the four launches of one acceptance (statistics, walk,
     # residual pass, draw); the residual pass re-reads p and q rows from DRAM
     ("2", "accept_sampled"): {"bytes": 350166016 + 3029760 + 150016 + 77830912 + 116992 + 128000,

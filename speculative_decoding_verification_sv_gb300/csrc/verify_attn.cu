@@ -31,9 +31,9 @@
 //     of the row of O only when the max has grown by more than 2^8 since it was
 //     last used (otherwise the stale max keeps every P <= 256, exact in fp32).
 //     Warps whose rows are all padding skip the arithmetic;
-//   * at the end every CTA pushes its unnormalised partial (max, sum, O row) of
-//     each row into the shared memory of the row's owner CTA (distributed
-//     shared memory), and the owners merge the C partials, writing bf16 rows.
+//   * at the end each CTA's unnormalised partial (max, sum, O row) of every
+//     row reaches the row's owner CTA (pushed into its shared memory, or with
+//     128-row tiles through an L2 exchange area), which writes the bf16 rows.
 // Launch: programmatic dependent launch; everything earlier kernels may have
 // written (lengths, cache rows, Q, block K/V, tree) is read after
 // griddepcontrol.wait.
