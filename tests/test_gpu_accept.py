@@ -236,6 +236,22 @@ def test_sample_tree_full_vocab_philox(sv, Vq, seed):
     assert sv.get_device_error() == 0
 
 
+@pytest.mark.parametrize("T,B", [(0.7, 2), (1.3, 6)])
+def test_sample_tree_full_vocab_temperature(sv, T, B):
+    """The 64-node tree at the 7B vocabulary with a temperature other than 1:
+    every pass divides the logits by T before the row's maximum, exponential
+    and divisions by Z and S; at B = 2 the walk takes 16-CTA clusters, at
+    B = 6 8-CTA ones."""
+    par = _tree(64, 8, 52)
+    si = _sample_case(B, len(par) - 1, V_7B, Vq=VQ_DRAFT, seed=70 + B, std=1.5, parent=par)
+    got = sv.accept_sample(si.logits.cuda(), si.q.cuda(), si.tok.cuda(), si.parent.cuda(), temperature=T,
+                           seed=515, step=7)
+    exp = oracle.accept_sample(si.logits.numpy(), si.q.numpy(), si.tok.numpy(), si.parent.numpy(), temperature=T,
+                               seed=515, step=7)
+    assert_same(got, exp, f"sample tree T={T}")
+    assert sv.get_device_error() == 0
+
+
 @pytest.mark.parametrize("Vq", [V_7B, VQ_DRAFT])
 def test_sample_tree_full_vocab_rejected_siblings(sv, Vq):
     """q far from p (an independent softmax): residual chains of two and
