@@ -188,31 +188,51 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads)
     const int P = kPieces / R;
     const int items = R * P;
     const int gw = rank * kWarpsPerCta + warp;
-    uint64_t res[2] = {0, 0};
-#pragma unroll
-    for (int r = 0; r < 2; ++r) {
-        const int it = gw + r * kClusterWarps;
-        if (it >= items) break;
-        const int j = it / P, p = it % P;
-        // p < P <= 128, so nslab * (p + 1) <= ceil(V / 128) * 128 < 2^32
-        const int s0 = static_cast<int>(static_cast<uint32_t>(nslab) * p / static_cast<uint32_t>(P));
-        const int s1 = static_cast<int>(static_cast<uint32_t>(nslab) * (p + 1) / static_cast<uint32_t>(P));
-        const uint64_t* row = amax + (static_cast<size_t>(b) * R + j) * nslab;
-        uint64_t best = 0;
-#pragma unroll 8
-        for (int s = s0 + lane; s < s1; s += 32) {
-            const uint64_t k = __ldg(row + s);
-            best = k > best ? k : best;
+    // both of a warp's items at once, up to 8 keys per lane and item in
+    // flight per round (one dependent round trip per 256 keys of both items,
+    // not per 256 keys of each item in turn)
+    // keys [p, p + n) of item `it` of this sequence (n = 0 past the last item)
+    auto item_keys = [&](int it, const uint64_t*& p_out, int& n_out) {
+        p_out = amax;
+        n_out = 0;
+        if (it < items) {
+            const int j = it / P, p = it % P;
+            // p < P <= 128, so nslab * (p + 1) <= ceil(V / 128) * 128 < 2^32
+            const int s0 = static_cast<int>(static_cast<uint32_t>(nslab) * p / static_cast<uint32_t>(P));
+            const int s1 = static_cast<int>(static_cast<uint32_t>(nslab) * (p + 1) / static_cast<uint32_t>(P));
+            p_out = amax + (static_cast<size_t>(b) * R + j) * nslab + s0;
+            n_out = s1 - s0;
         }
-        res[r] = warp_max_key(best);
+    };
+    const uint64_t *kp0, *kp1;
+    int kn0, kn1;
+    item_keys(gw, kp0, kn0);
+    item_keys(gw + kClusterWarps, kp1, kn1);
+    uint64_t best0 = 0, best1 = 0;
+    constexpr int kKeysInFlight = 8;
+    for (int base = lane; base < max(kn0, kn1); base += 32 * kKeysInFlight) {
+        uint64_t k0[kKeysInFlight], k1[kKeysInFlight];
+#pragma unroll
+        for (int u = 0; u < kKeysInFlight; ++u) {
+            const int s = base + 32 * u;
+            k0[u] = s < kn0 ? __ldg(kp0 + s) : 0ull;
+            k1[u] = s < kn1 ? __ldg(kp1 + s) : 0ull;
+        }
+#pragma unroll
+        for (int u = 0; u < kKeysInFlight; ++u) {
+            best0 = k0[u] > best0 ? k0[u] : best0;
+            best1 = k1[u] > best1 ? k1[u] : best1;
+        }
     }
+    const uint64_t res0 = warp_max_key(best0), res1 = warp_max_key(best1);
     cluster_wait();   // every CTA of the cluster has started
     if (lane == 0) {
 #pragma unroll
         for (int r = 0; r < 2; ++r) {
             const int it = gw + r * kClusterWarps;
             if (it >= items) break;
-            for (int dst = 0; dst < kCluster; ++dst) *cluster.map_shared_rank(&piece_s[it], dst) = res[r];
+            for (int dst = 0; dst < kCluster; ++dst)
+                *cluster.map_shared_rank(&piece_s[it], dst) = r == 0 ? res0 : res1;
         }
     }
     cluster.sync();   // every piece pushed into every CTA (and tok_s, par_s, t_s visible in the CTA)
