@@ -60,7 +60,7 @@ TRAFFIC = {
     ("1", "lm_head_argmax"): {"bytes": 466801920 + 3028480, "src": "lm_head.cu", "src_hash": "8e935fce0398e19e"},
     # the same round: acceptance from the keys plus the commit of 28 layers (the
     # committed rows stay in L2 during the launch)
-    ("1", "accept_greedy_commit"): {"bytes": 222208 + 0, "src": "kv_commit.cu", "src_hash": "11e3452aa759e99f"},
+    ("1", "accept_greedy_commit"): {"bytes": 220160 + 0, "src": "kv_commit.cu", "src_hash": "29608bdabe574e87"},
     # 7B batch-16 layer (2-layer case, same per-layer launch; split K/V barriers)
     ("3b16", "verify_attn"): {"bytes": 270150656 + 3010304, "src": "verify_attn.cu",
                               "src_hash": "d977ade712ea17dc"},
